@@ -1,0 +1,159 @@
+/*
+ * nfq.h — C ABI of the GB300 (sm_103a) MTP draft-layer tail.
+ *
+ * Two operations, each one asynchronous launch sequence on a caller stream:
+ *
+ *   nfq_mtp_reduce_norm_quant   k BF16 partial sums + residual -> RMSNorm ->
+ *                               (BF16 hidden, packed FP8 activation)
+ *   nfq_lm_head_fp8_argmax      packed FP8 activation x block-scaled FP8 LM
+ *                               head -> greedy draft token per row, via a
+ *                               vocab-sharded argmax; logits are never stored
+ *
+ * Sources (page title, section):
+ *   [R] "[Quant][MTP] Reuse packed FP8 logits inputs" (vLLM pull request 51947),
+ *       Purpose and Dependencies.
+ *   [F] "[Spec Decode][Perf] Fuse the MTP trailing all-reduce; local-argmax
+ *       draft tokens" (vLLM pull request 49793), intro bullets, Benchmarks and
+ *       Accuracy.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers unless stated otherwise; the caller
+ *    owns every buffer.  The library never allocates device memory, never frees
+ *    and never synchronises (except nfq_device_error, which says so).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous on it; results are valid once the stream
+ *    has reached the call.
+ *  - Every argument is validated on the host before anything is launched; the
+ *    first violation is returned and nothing runs.  Launch failures return
+ *    NFQ_ERR_CUDA.  No C++ exception crosses this boundary.
+ *  - Tensor values are not inspected: NaN or infinite inputs give unspecified
+ *    (but memory-safe) results.
+ *  - Row-major layouts throughout; every device pointer must be 16-byte aligned.
+ */
+#ifndef NFQ_H_
+#define NFQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NFQ_OK = 0,
+  NFQ_ERR_NULL = -1,       /* a required pointer is NULL                       */
+  NFQ_ERR_SHAPE = -2,      /* a size is out of range or inconsistent           */
+  NFQ_ERR_ALIGN = -3,      /* a device pointer is not 16-byte aligned          */
+  NFQ_ERR_WORKSPACE = -4,  /* the workspace is missing or too small            */
+  NFQ_ERR_CUDA = -5,       /* a CUDA runtime call or launch failed             */
+  NFQ_ERR_TIMEOUT = -6,    /* a kernel gave up a bounded wait (nfq_device_error) */
+  NFQ_ERR_DEVICE = -7      /* the current device is not sm_103 / sm_100 class  */
+} nfq_status;
+
+/* Packed FP8 QuantizedActivation ([R] Purpose: the draft layer's first output,
+ * consumed by the LM head without unpacking or requantising it).
+ *   codes  : e4m3fn bytes [tokens][hidden]
+ *   scales : fp32 [tokens][hidden / group]; element (t, h) represents
+ *            decode(codes[t][h]) * scales[t][h / group]
+ *   group  : must be 128 (one scale per 1x128 token group)            */
+typedef struct {
+  uint8_t *codes;
+  float *scales;
+  int32_t tokens;
+  int32_t hidden;
+  int32_t group;
+} nfq_quant_act;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *nfq_status_str(int status);
+
+/* ABI version: (major << 16) | minor. */
+int nfq_abi_version(void);
+
+/*
+ * Stage 1 — fused trailing all-reduce + residual + final RMSNorm + packed FP8.
+ * [R] Purpose: the MTP layer's final all-reduce and RMSNorm are fused with
+ * packed FP8 quantisation, and the layer returns two deliberately different
+ * values: the packed activation for the logits projection and the post-norm
+ * BF16 hidden state recycled into the next MTP position.  [F] intro: the
+ * trailing all-reduce is fused into the final RMSNorm.  [F] Accuracy: the fused
+ * kernel accumulates in fp32.
+ *
+ * On one GPU the tensor-parallel partial outputs are k BF16 tensors in HBM and
+ * the all-reduce is their sum.  For every token t and channel h:
+ *   x      = ((p_0 + p_1) + ... + p_{k-1}) + residual      fp32, this order
+ *   hidden = bf16_rne( x * rsqrt(mean_h(x^2) + eps) * w )
+ *   per 128-channel group g: scale = max_g |hidden| / 448  (fp32 division)
+ *   code   = e4m3fn_rne_satfinite(hidden / scale), 0 when scale == 0
+ *
+ *   partials   HOST array of k device pointers, each BF16 [T][H]
+ *   k          1..16
+ *   residual   BF16 [T][H]
+ *   norm_w     BF16 [H]
+ *   eps        added to mean(x^2); must be >= 0 (the MTP layers use 1e-6)
+ *   T, H       T >= 1 (T == 0 is a no-op returning NFQ_OK), H % 128 == 0,
+ *              128 <= H <= 32768
+ *   hidden_out BF16 [T][H]; must not overlap any input
+ *   q_out      host struct; q_out->codes [T][H], q_out->scales [T][H/128];
+ *              q_out->tokens == T, q_out->hidden == H, q_out->group == 128
+ * Bounded waits inside the kernel that expire set the device error word read
+ * by nfq_device_error.
+ */
+int nfq_mtp_reduce_norm_quant(const void *const *partials, int k, const void *residual,
+                              const void *norm_w, float eps, int T, int H, void *hidden_out,
+                              const nfq_quant_act *q_out, void *stream);
+
+/*
+ * Stage 2 — shared LM head on the prequantised activation, greedy draft token.
+ * [R] Dependencies: the LM-head GEMM consumes prequantised activations (block
+ * linear, prequantised-input contract).  [F] intro: greedy draft tokens come
+ * from a vocab-parallel local argmax, skipping the full-vocab all-gather of the
+ * logits; [F] Benchmarks: at 64 tokens that gather is 64 x 151k x 2 bytes per
+ * draft step.  [F] Accuracy: local argmax changes how ties at shard boundaries
+ * are broken; here every tie goes to the lowest global vocab index.
+ *
+ *   L[t][v] = sum_k decode(a.codes[t][k]) * a.scales[t][k/128]
+ *                 * decode(w[v][k]) * w_scales[v/128][k/128]     (fp32 accumulate)
+ * The V vocab rows form S equal shards [s*V/S, (s+1)*V/S).  Outputs:
+ *   tokens_out    int32 [T]    argmax_v L[t][v], lowest index among equal maxima
+ *   max_logit_out fp32 [T]     L at that index, or NULL
+ *   shard_idx_out int32 [S][T] per-shard argmax (global index), or NULL
+ *   shard_val_out fp32 [S][T]  per-shard maximum, or NULL
+ * A -0 logit compares equal to +0 (the value reported is +0).  The full [T][V]
+ * logits are never written to memory.
+ *
+ *   a          host struct describing the activation (group == 128, hidden % 128 == 0)
+ *   w          e4m3fn [V][H], H = a->hidden
+ *   w_scales   fp32 [ceil(V/128)][H/128]
+ *   V, S       V >= 1, 1 <= S <= 64, V % S == 0
+ *   workspace  device scratch of at least nfq_lm_head_workspace_bytes(T, S) bytes.
+ *              It must be zero-filled before its first use (nfq_lm_head_workspace_init);
+ *              every call returns it to all-zero, so one zeroing suffices for
+ *              any number of calls that run one after another on a stream.
+ *              Concurrent calls need separate workspaces.
+ * T = a->tokens may be any size >= 1; rows are processed 256 at a time (each
+ * chunk streams the weights once).
+ */
+size_t nfq_lm_head_workspace_bytes(int T, int S);
+
+int nfq_lm_head_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+int nfq_lm_head_fp8_argmax(const nfq_quant_act *a, const uint8_t *w, const float *w_scales,
+                           int V, int S, int32_t *tokens_out, float *max_logit_out,
+                           int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                           size_t ws_bytes, void *stream);
+
+/*
+ * Reads the current device's error word that kernels set when a bounded wait
+ * expires (bit 0: stage 1, bit 1: stage 2).  SYNCHRONISES the current device.
+ * Returns NFQ_OK when clear, NFQ_ERR_TIMEOUT when set (and clears it when
+ * `clear` != 0), NFQ_ERR_CUDA if the device cannot be read.
+ */
+int nfq_device_error(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NFQ_H_ */

@@ -1,0 +1,204 @@
+"""GB300 (sm_103a) MTP draft-layer tail: Python binding of the C-ABI library.
+
+Thin argument marshalling over libnfq.so (include/nfq.h); every step of the
+path runs in the library's CUDA kernels.  PyTorch only provides device memory
+and the current stream.  There is no fallback: if the library is missing or
+the device is not a compute-capability 10.3 GPU, calls raise.
+
+  mtp_reduce_norm_quant(partials, residual, norm_w, eps=1e-6)
+      -> (hidden bf16 [T][H], codes uint8 [T][H], scales fp32 [T][H/128])
+  lm_head_fp8_argmax(codes, scales, w, w_scales, S, workspace=None)
+      -> draft tokens int32 [T] (optionally max logit and per-shard results)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libnfq.so")
+
+NFQ_OK = 0
+NFQ_ERR_NULL = -1
+NFQ_ERR_SHAPE = -2
+NFQ_ERR_ALIGN = -3
+NFQ_ERR_WORKSPACE = -4
+NFQ_ERR_CUDA = -5
+NFQ_ERR_TIMEOUT = -6
+NFQ_ERR_DEVICE = -7
+
+GROUP = 128
+
+
+class NfqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_str(status)} (status {status})")
+
+
+class QuantAct(ctypes.Structure):
+    """nfq_quant_act: packed FP8 activation descriptor (host struct)."""
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("group", ctypes.c_int32)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+
+
+def load(path: str = LIB_PATH):
+    """Load libnfq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with norm_fp8_quant_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    lib.nfq_status_str.argtypes = [ctypes.c_int]
+    lib.nfq_status_str.restype = ctypes.c_char_p
+    lib.nfq_abi_version.argtypes = []
+    lib.nfq_abi_version.restype = ctypes.c_int
+    lib.nfq_mtp_reduce_norm_quant.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
+                                              ctypes.c_int, ctypes.c_int, _P,
+                                              ctypes.POINTER(QuantAct), _P]
+    lib.nfq_mtp_reduce_norm_quant.restype = ctypes.c_int
+    lib.nfq_lm_head_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.nfq_lm_head_workspace_bytes.restype = ctypes.c_size_t
+    lib.nfq_lm_head_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
+    lib.nfq_lm_head_workspace_init.restype = ctypes.c_int
+    lib.nfq_lm_head_fp8_argmax.argtypes = [ctypes.POINTER(QuantAct), _P, _P, ctypes.c_int,
+                                           ctypes.c_int, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    lib.nfq_lm_head_fp8_argmax.restype = ctypes.c_int
+    lib.nfq_device_error.argtypes = [ctypes.c_int]
+    lib.nfq_device_error.restype = ctypes.c_int
+    lib.nfq_stage1_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_stage1_plan.restype = ctypes.c_int
+    lib.nfq_stage1_tune.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.nfq_stage1_tune.restype = None
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load().nfq_status_str(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != NFQ_OK:
+        raise NfqError(status, what)
+
+
+def _stream_ptr(stream=None):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+# ----------------------------------------------------------------- stage 1 --
+
+def mtp_reduce_norm_quant(partials, residual, norm_w, eps: float = 1e-6,
+                          hidden_out=None, codes_out=None, scales_out=None, stream=None):
+    """Sum k BF16 partials and the residual in fp32, RMSNorm, and emit the BF16
+    hidden plus the packed FP8 activation (e4m3 codes, fp32 scale per 128)."""
+    import torch
+    k = len(partials)
+    T, H = residual.shape
+    _need_cuda(residual, norm_w, *partials)
+    for p in partials:
+        if p.dtype != torch.bfloat16 or p.shape != (T, H):
+            raise ValueError("partials must be bf16 [T][H]")
+    if residual.dtype != torch.bfloat16 or norm_w.dtype != torch.bfloat16:
+        raise ValueError("residual and norm_w must be bf16")
+    dev = residual.device
+    hidden = hidden_out if hidden_out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    codes = codes_out if codes_out is not None else torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = scales_out if scales_out is not None else torch.empty((T, H // GROUP), dtype=torch.float32, device=dev)
+    arr = (ctypes.c_void_p * max(k, 1))(*[p.data_ptr() for p in partials])
+    q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
+    with torch.cuda.device(dev):
+        st = load().nfq_mtp_reduce_norm_quant(arr, k, _ptr(residual), _ptr(norm_w), float(eps),
+                                              T, H, _ptr(hidden), ctypes.byref(q),
+                                              _stream_ptr(stream))
+    _check(st, "nfq_mtp_reduce_norm_quant")
+    return hidden, codes, scales
+
+
+# ----------------------------------------------------------------- stage 2 --
+
+def lm_head_workspace_bytes(T: int, S: int) -> int:
+    return int(load().nfq_lm_head_workspace_bytes(T, S))
+
+
+def lm_head_workspace(T: int, S: int, device, stream=None):
+    """A zero-filled workspace for nfq_lm_head_fp8_argmax (kept zero by every call)."""
+    import torch
+    n = lm_head_workspace_bytes(T, S)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    with torch.cuda.device(ws.device):
+        _check(load().nfq_lm_head_workspace_init(_ptr(ws), n, _stream_ptr(stream)),
+               "nfq_lm_head_workspace_init")
+    return ws
+
+
+def lm_head_fp8_argmax(codes, scales, w, w_scales, S: int, workspace=None,
+                       tokens_out=None, want_max: bool = False, want_shards: bool = False,
+                       stream=None):
+    """Greedy draft token per row of the packed FP8 activation against the
+    block-scaled FP8 LM head, via a vocab-sharded argmax (ties -> lowest id).
+
+    Returns tokens, or (tokens, max_logit, shard_idx, shard_val) with the
+    optional ones None unless requested."""
+    import torch
+    T, H = codes.shape
+    V = w.shape[0]
+    _need_cuda(codes, scales, w, w_scales)
+    if codes.dtype != torch.uint8 or w.dtype != torch.uint8:
+        raise ValueError("codes and w must be uint8 e4m3 patterns")
+    if scales.dtype != torch.float32 or w_scales.dtype != torch.float32:
+        raise ValueError("scales must be float32")
+    dev = codes.device
+    ws = workspace if workspace is not None else lm_head_workspace(T, S, dev, stream)
+    tokens = tokens_out if tokens_out is not None else torch.empty(T, dtype=torch.int32, device=dev)
+    mx = torch.empty(T, dtype=torch.float32, device=dev) if want_max else None
+    sidx = torch.empty((S, T), dtype=torch.int32, device=dev) if want_shards else None
+    sval = torch.empty((S, T), dtype=torch.float32, device=dev) if want_shards else None
+    q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
+    opt = lambda t: ctypes.c_void_p(None) if t is None else _ptr(t)
+    with torch.cuda.device(dev):
+        st = load().nfq_lm_head_fp8_argmax(ctypes.byref(q), _ptr(w), _ptr(w_scales), V, S,
+                                           _ptr(tokens), opt(mx), opt(sidx), opt(sval),
+                                           _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(st, "nfq_lm_head_fp8_argmax")
+    if want_max or want_shards:
+        return tokens, mx, sidx, sval
+    return tokens
+
+
+def device_error(clear: bool = True) -> int:
+    """Synchronise the current device and return its error-word status
+    (NFQ_OK, or NFQ_ERR_TIMEOUT when a kernel gave up a bounded wait)."""
+    return int(load().nfq_device_error(1 if clear else 0))
+
+
+def stage1_plan(T: int, H: int, k: int, num_sms: int = 152):
+    out = (ctypes.c_int * 6)()
+    _check(load().nfq_stage1_plan(T, H, k, num_sms, out), "nfq_stage1_plan")
+    return dict(zip(["cluster", "vpt", "active_threads", "threads", "slots", "smem"], list(out)))
+
+
+def stage1_tune(cluster: int = 0, vpt: int = 0, slots: int = 0):
+    """Override the stage-1 launch plan (0 = automatic); for tuning sweeps."""
+    load().nfq_stage1_tune(cluster, vpt, slots)

@@ -1,0 +1,207 @@
+// C ABI of the MTP draft-layer tail: argument validation, device properties,
+// the device error word and dispatch to the stage kernels.  See include/nfq.h
+// for the contract of every entry point.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/nfq.h"
+#include "nfq_internal.h"
+
+namespace nfq {
+
+// bit 0: a stage-1 wait expired, bit 1: a stage-2 wait expired
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready;
+  bool supported;
+  int num_sms;
+  unsigned *err;   // device address of g_device_error
+};
+
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, looked up once per device (the first call on a device does
+// this set-up; it issues no device work).
+int device_info(DeviceInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NFQ_ERR_CUDA;
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return NFQ_ERR_CUDA;
+    void *err = nullptr;
+    if (cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess) return NFQ_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.err = static_cast<unsigned *>(err);
+    d.ready = true;
+  }
+  if (!d.supported) return NFQ_ERR_DEVICE;
+  *out = &d;
+  return NFQ_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? NFQ_OK : NFQ_ERR_CUDA; }
+
+}  // namespace
+
+}  // namespace nfq
+
+using namespace nfq;
+
+extern "C" {
+
+const char *nfq_status_str(int status) {
+  switch (status) {
+    case NFQ_OK: return "ok";
+    case NFQ_ERR_NULL: return "a required pointer is NULL";
+    case NFQ_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case NFQ_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+    case NFQ_ERR_WORKSPACE: return "the workspace is missing or too small";
+    case NFQ_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case NFQ_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    case NFQ_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
+    default: return "unknown status";
+  }
+}
+
+int nfq_abi_version(void) { return (1 << 16) | 0; }
+
+int nfq_mtp_reduce_norm_quant(const void *const *partials, int k, const void *residual,
+                              const void *norm_w, float eps, int T, int H, void *hidden_out,
+                              const nfq_quant_act *q_out, void *stream) {
+  if (!partials || !residual || !norm_w || !hidden_out || !q_out) return NFQ_ERR_NULL;
+  if (k < 1 || k > kMaxPartials) return NFQ_ERR_SHAPE;
+  for (int i = 0; i < k; ++i)
+    if (!partials[i]) return NFQ_ERR_NULL;
+  if (!q_out->codes || !q_out->scales) return NFQ_ERR_NULL;
+  if (T < 0 || H < 128 || H > 32768 || H % 128 != 0) return NFQ_ERR_SHAPE;
+  if (!(eps >= 0.0f) || eps > 1.0f) return NFQ_ERR_SHAPE;
+  if (q_out->group != 128 || q_out->tokens != T || q_out->hidden != H) return NFQ_ERR_SHAPE;
+  for (int i = 0; i < k; ++i)
+    if (!aligned16(partials[i])) return NFQ_ERR_ALIGN;
+  if (!aligned16(residual) || !aligned16(norm_w) || !aligned16(hidden_out) ||
+      !aligned16(q_out->codes) || !aligned16(q_out->scales))
+    return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  Stage1Params p;
+  std::memset(&p, 0, sizeof(p));
+  for (int i = 0; i < k; ++i) p.partials[i] = partials[i];
+  p.residual = residual;
+  p.norm_w = norm_w;
+  p.hidden = hidden_out;
+  p.codes = q_out->codes;
+  p.scales = q_out->scales;
+  p.err = d->err;
+  p.eps = eps;
+  p.k = k;
+  p.T = T;
+  p.H = H;
+  const cudaError_t e = launch_stage1(p, d->num_sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
+  return map_cuda(e);
+}
+
+size_t nfq_lm_head_workspace_bytes(int T, int S) {
+  (void)T;
+  if (S < 1 || S > 64) return 0;
+  return stage2_workspace_bytes(S);
+}
+
+int nfq_lm_head_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
+  if (!workspace) return NFQ_ERR_NULL;
+  if (!aligned16(workspace)) return NFQ_ERR_ALIGN;
+  return map_cuda(cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_lm_head_fp8_argmax(const nfq_quant_act *a, const uint8_t *w, const float *w_scales,
+                           int V, int S, int32_t *tokens_out, float *max_logit_out,
+                           int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                           size_t ws_bytes, void *stream) {
+  if (!a || !w || !w_scales || !tokens_out) return NFQ_ERR_NULL;
+  if (!a->codes || !a->scales) return NFQ_ERR_NULL;
+  const int T = a->tokens, H = a->hidden;
+  if (a->group != 128 || H < 128 || H > 16384 || H % 128 != 0 || T < 0) return NFQ_ERR_SHAPE;
+  if (V < 1 || S < 1 || S > 64 || V % S != 0) return NFQ_ERR_SHAPE;
+  if (!workspace) return NFQ_ERR_WORKSPACE;
+  if (ws_bytes < stage2_workspace_bytes(S)) return NFQ_ERR_WORKSPACE;
+  if (!aligned16(a->codes) || !aligned16(a->scales) || !aligned16(w) || !aligned16(w_scales) ||
+      !aligned16(tokens_out) || !aligned16(workspace) ||
+      (max_logit_out && !aligned16(max_logit_out)) ||
+      (shard_idx_out && !aligned16(shard_idx_out)) ||
+      (shard_val_out && !aligned16(shard_val_out)))
+    return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  const int G = H / 128;
+  Stage2Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.w_scales = w_scales;
+  p.shard_idx_out = shard_idx_out;
+  p.shard_val_out = shard_val_out;
+  p.keys = static_cast<unsigned long long *>(workspace);
+  p.counter = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(workspace) +
+                                           stage2_workspace_bytes(S) - 16u);
+  p.err = d->err;
+  p.T_total = T;
+  p.H = H;
+  p.G = G;
+  p.V = V;
+  p.S = S;
+  p.shard_width = V / S;
+  p.n_vtiles = (V + 127) / 128;
+  for (int t0 = 0; t0 < T; t0 += 256) {
+    const int Tc = (T - t0) < 256 ? (T - t0) : 256;
+    p.tok0 = t0;
+    p.T = Tc;
+    p.act_codes = a->codes + (size_t)t0 * H;
+    p.act_scales = a->scales + (size_t)t0 * G;
+    p.tokens_out = tokens_out + t0;
+    p.max_logit_out = max_logit_out ? max_logit_out + t0 : nullptr;
+    const cudaError_t e =
+        launch_stage2(p, p.act_codes, w, d->num_sms, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
+    if (e != cudaSuccess) return NFQ_ERR_CUDA;
+  }
+  return NFQ_OK;
+}
+
+int nfq_device_error(int clear) {
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return NFQ_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return NFQ_ERR_CUDA;
+  if (v && clear) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess)
+      return NFQ_ERR_CUDA;
+  }
+  return v ? NFQ_ERR_TIMEOUT : NFQ_OK;
+}
+
+// Launch-plan query and override for the stage-1 kernel (tuning sweeps; 0 = automatic).
+int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out6) {
+  if (!out6) return NFQ_ERR_NULL;
+  if (H < 128 || H % 128 || T < 1 || k < 1 || num_sms < 1) return NFQ_ERR_SHAPE;
+  return stage1_plan(T, H, k, num_sms, out6);
+}
+
+void nfq_stage1_tune(int cluster, int vpt, int slots) { stage1_set_tuning(cluster, vpt, slots); }
+
+}  // extern "C"

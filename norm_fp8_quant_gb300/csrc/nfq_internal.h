@@ -1,0 +1,59 @@
+// Internal interfaces between the C ABI layer (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace nfq {
+
+constexpr int kMaxPartials = 16;
+
+// Stage 1 launch parameters (passed by value to the kernel).
+struct Stage1Params {
+  const void *partials[kMaxPartials];  // k BF16 [T][H]
+  const void *residual;                // BF16 [T][H]
+  const void *norm_w;                  // BF16 [H]
+  void *hidden;                        // BF16 [T][H]
+  uint8_t *codes;                      // e4m3 [T][H]
+  float *scales;                       // fp32 [T][H/128]
+  unsigned *err;                       // device error word
+  float eps;
+  int k, T, H;
+  int C;          // CTAs per cluster (channel split of a row)
+  int E;          // channels per CTA = H / C
+  int nslot;      // shared-memory ring slots of E BF16 values
+  int n_active;   // consumer threads holding data
+};
+
+cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream);
+void stage1_set_tuning(int cluster, int vpt, int slots);
+int stage1_plan(int T, int H, int k, int num_sms, int *out6);
+
+// Stage 2 launch parameters.
+struct Stage2Params {
+  const uint8_t *act_codes;   // e4m3 [T][H]   (this launch's token chunk)
+  const float *act_scales;    // fp32 [T][G]
+  const float *w_scales;      // fp32 [ceil(V/128)][G]
+  int32_t *tokens_out;        // [T]
+  float *max_logit_out;       // [T] or null
+  int32_t *shard_idx_out;     // [S][T_total] or null, column offset tok0
+  float *shard_val_out;       // [S][T_total] or null
+  unsigned long long *keys;   // workspace [S][NPAD] packed (value, index) maxima
+  unsigned *counter;          // workspace: CTAs finished
+  unsigned *err;              // device error word
+  int T;                      // tokens in this chunk (<= 256)
+  int T_total;                // row stride of the per-shard outputs
+  int tok0;                   // first token of this chunk
+  int H, G, V, S;
+  int shard_width;            // V / S
+  int n_vtiles;               // ceil(V / 128)
+};
+
+cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes_base, const void *w,
+                          int num_sms, cudaStream_t stream);
+
+size_t stage2_workspace_bytes(int S);
+
+}  // namespace nfq

@@ -1,0 +1,394 @@
+// Stage 1: fused k-way partial-sum reduction + residual + RMSNorm + packed FP8.
+//
+// "[Quant][MTP] Reuse packed FP8 logits inputs", Purpose: the MTP layer's final
+// all-reduce and RMSNorm are fused with packed FP8 quantisation and the layer
+// returns both the packed activation and the post-norm BF16 hidden state.
+// "[Spec Decode][Perf] Fuse the MTP trailing all-reduce; local-argmax draft
+// tokens", intro and Accuracy: the trailing all-reduce goes into the final
+// RMSNorm and the fused kernel accumulates in fp32.
+//
+// Design (HBM-bound streaming kernel):
+//  * A row of H channels is split over a cluster of C CTAs (C = 1 for long
+//    inputs, up to 8 when there are too few rows to occupy every SM); each CTA
+//    owns E = H / C consecutive channels (whole 128-channel groups).
+//  * Warp 0 is the producer: one thread streams (row, input) chunks of E BF16
+//    values — the k partials, then the residual — into a ring of shared-memory
+//    slots with 1-D TMA bulk copies completing on per-slot mbarriers.
+//  * The consumer warps own fixed 16-byte vectors of the slice: vector j of the
+//    slice is held by thread j mod NA in register slot j / NA, so the 16
+//    vectors of a 128-channel group sit in 16 consecutive lanes.  They add the
+//    inputs in fp32 in input order (no intermediate rounding), square-sum
+//    per warp with shuffles, combine warps in shared memory and, when C > 1,
+//    exchange the CTA partial sums through distributed shared memory.
+//  * Epilogue per vector: y = bf16((x * rsqrt(ms + eps)) * w); the group
+//    maximum |y| is a 16-lane shuffle reduction; scale = amax / 448 (IEEE
+//    division); codes = cvt.rn.satfinite.e4m3x2(y / scale).  Hidden (16 B),
+//    codes (8 B) and scales go straight to global memory, coalesced.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "nfq_internal.h"
+#include "ptx.cuh"
+
+namespace nfq {
+
+namespace {
+
+constexpr int kErrBitStage1 = 1;
+constexpr int kMaxStage1Threads = 288;   // producer warp + up to 256 consumers
+
+struct RowSums {
+  float red[2][32];     // per consumer warp, double-buffered by row parity
+  float cl[2][8];       // per cluster rank, double-buffered by row parity
+};
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel(const Stage1Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int E = p.E;
+  const uint32_t slot_bytes = (uint32_t)E * 2u;
+  uint8_t *ring = smem;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)p.nslot * slot_bytes);
+  uint64_t *empty = full + p.nslot;
+  uint64_t *ss_bar = empty + p.nslot;               // [2], cluster exchange
+  uint64_t *red_bar = ss_bar + 2;                   // [2], consumer warps of this CTA
+  RowSums *sums = reinterpret_cast<RowSums *>(red_bar + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sums + 1);
+
+  const int C = p.C;
+  const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
+  const int cid = (C > 1) ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int ncl = (C > 1) ? (int)nclusters_x() : (int)gridDim.x;
+  const int col0 = (int)rank * E;
+  const int n_cons_warps = (int)(blockDim.x / 32) - 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.nslot; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), (uint32_t)n_cons_warps);
+    }
+    mbar_init(smem_u32(&ss_bar[0]), (uint32_t)C);
+    mbar_init(smem_u32(&ss_bar[1]), (uint32_t)C);
+    mbar_init(smem_u32(&red_bar[0]), (uint32_t)n_cons_warps);
+    mbar_init(smem_u32(&red_bar[1]), (uint32_t)n_cons_warps);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (C > 1) cluster_sync_all();   // peers' barriers exist before any remote arrive
+
+  const int warp = (int)(threadIdx.x / 32);
+  const int lane = (int)(threadIdx.x % 32);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int r = cid; r < p.T && ok; r += ncl) {
+        const size_t off = ((size_t)r * (size_t)p.H + (size_t)col0) * 2u;
+        for (int i = 0; i <= p.k; ++i, ++it) {
+          const uint32_t s = it % (uint32_t)p.nslot;
+          const uint32_t ph = (it / (uint32_t)p.nslot) & 1u;
+          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage1)) {
+            ok = false;
+            break;
+          }
+          const uint8_t *src =
+              static_cast<const uint8_t *>(i < p.k ? p.partials[i] : p.residual) + off;
+          mbar_arrive_expect_tx(smem_u32(&full[s]), slot_bytes);
+          bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes), src, slot_bytes,
+                   smem_u32(&full[s]), pol);
+        }
+      }
+      // every copy issued lands before the CTA can leave
+      const uint32_t issued = it;
+      const uint32_t first = issued > (uint32_t)p.nslot ? issued - (uint32_t)p.nslot : 0u;
+      for (uint32_t j = first; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&full[j % (uint32_t)p.nslot]), (j / (uint32_t)p.nslot) & 1u);
+    }
+  } else {
+    // ----------------------------------------------------------- consumers --
+    const int tc = (int)threadIdx.x - 32;
+    const int cw = warp - 1;
+    const int NA = p.n_active;
+    const bool active = tc < NA;
+
+    uint4 wpk[VPT];   // norm weight, packed BF16 pairs
+    if (active) {
+      const uint4 *wsrc = reinterpret_cast<const uint4 *>(
+          static_cast<const uint8_t *>(p.norm_w) + (size_t)col0 * 2u);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) wpk[v] = __ldg(wsrc + v * NA + tc);
+    }
+
+    uint32_t it = 0;
+    int row_iter = 0;
+    for (int r = cid; r < p.T; r += ncl, ++row_iter) {
+      float x[VPT][8];
+      bool ok = true;
+      for (int i = 0; i <= p.k; ++i, ++it) {
+        const uint32_t s = it % (uint32_t)p.nslot;
+        const uint32_t ph = (it / (uint32_t)p.nslot) & 1u;
+        if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err, kErrBitStage1)) {
+          ok = false;
+          break;
+        }
+        if (active) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(ring + (size_t)s * slot_bytes);
+#pragma unroll
+          for (int v = 0; v < VPT; ++v) {
+            float f[8];
+            unpack_bf16x8(src[v * NA + tc], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[v][e] = (i == 0) ? f[e] : __fadd_rn(x[v][e], f[e]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      }
+      if (!ok) break;
+
+      // sum of squares: thread -> warp -> CTA -> cluster, fixed orders
+      float ss = 0.0f;
+      if (active) {
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ss = fmaf(x[v][e], x[v][e], ss);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const int par = row_iter & 1;
+      const uint32_t pph = (uint32_t)((row_iter >> 1) & 1);
+      if (lane == 0) {
+        sums->red[par][cw] = ss;
+        mbar_arrive(smem_u32(&red_bar[par]));   // release: the store above is visible
+      }
+      if (!mbar_wait(smem_u32(&red_bar[par]), pph, abort_flag, p.err, kErrBitStage1)) break;
+      float tot = 0.0f;
+      for (int q = 0; q < n_cons_warps; ++q) tot += sums->red[par][q];
+      if (C > 1) {
+        if (tc == 0) {
+          const uint32_t slot_addr = smem_u32(&sums->cl[par][rank]);
+          for (int q = 0; q < C; ++q) {
+            st_remote_f32(slot_addr, (uint32_t)q, tot);
+            mbar_arrive_remote(smem_u32(&ss_bar[par]), (uint32_t)q);
+          }
+        }
+        if (!mbar_wait<true>(smem_u32(&ss_bar[par]), pph, abort_flag, p.err, kErrBitStage1))
+          break;
+        tot = 0.0f;
+        for (int q = 0; q < C; ++q) tot += sums->cl[par][q];
+      }
+      const float ms = __fdiv_rn(tot, (float)p.H);
+      const float rr = __frsqrt_rn(__fadd_rn(ms, p.eps));
+
+      if (active) {
+        const size_t rowbase = (size_t)r * (size_t)p.H + (size_t)col0;
+        uint4 *hid = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.hidden) + rowbase * 2u);
+        uint2 *cod = reinterpret_cast<uint2 *>(p.codes + rowbase);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          float wv[8];
+          unpack_bf16x8(wpk[v], wv);
+          float y[8];
+          uint32_t hb[4];
+          float amax = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const __nv_bfloat16 b0 = __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]));
+            const __nv_bfloat16 b1 =
+                __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
+            const uint32_t u0 = __bfloat16_as_ushort(b0), u1 = __bfloat16_as_ushort(b1);
+            hb[e / 2] = u0 | (u1 << 16);
+            y[e] = __uint_as_float(u0 << 16);
+            y[e + 1] = __uint_as_float(u1 << 16);
+            amax = fmaxf(amax, fmaxf(fabsf(y[e]), fabsf(y[e + 1])));
+          }
+          // 16 lanes hold one 128-channel group
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const float scale = __fdiv_rn(amax, 448.0f);
+          uint32_t q[2] = {0u, 0u};
+          if (scale != 0.0f) {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const uint32_t pr =
+                  e4m3x2(__fdiv_rn(y[e], scale), __fdiv_rn(y[e + 1], scale));
+              q[e / 4] |= pr << ((e % 4) * 8);
+            }
+          }
+          const int j = v * NA + tc;
+          hid[j] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+          cod[j] = make_uint2(q[0], q[1]);
+          if ((tc & 15) == 0)
+            p.scales[(size_t)r * (size_t)(p.H / 128) + (size_t)((col0 + j * 8) / 128)] = scale;
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (C > 1) cluster_sync_all();   // no CTA leaves while a peer may still write to it
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------- host --
+
+namespace {
+
+struct Stage1Choice {
+  int C, VPT, NA, threads, nslot;
+  size_t smem;
+};
+
+int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0;
+
+size_t stage1_smem_bytes(int nslot, int E) {
+  return (size_t)nslot * (size_t)E * 2u + (size_t)nslot * 16u + 32u + sizeof(RowSums) + 16u;
+}
+
+// Vectors per consumer thread for a slice of Gc groups: whole warps with 192..256
+// active threads first, then at least 128, then whole warps, then anything.
+int pick_vpt(int Gc) {
+  for (int pass = 0; pass < 4; ++pass)
+    for (int v = 8; v >= 1; --v) {
+      if (Gc % v) continue;
+      const int na = 16 * Gc / v;
+      if (na > kMaxStage1Threads - 32) continue;
+      const bool whole = na % 32 == 0;
+      if (pass == 0 && !(whole && na >= 192)) continue;
+      if (pass == 1 && !(whole && na >= 128)) continue;
+      if (pass == 2 && !whole) continue;
+      return v;
+    }
+  return 0;
+}
+
+Stage1Choice choose_stage1(int T, int H, int k, int num_sms) {
+  const int G = H / 128;
+  Stage1Choice ch{};
+  // cluster split: enough CTAs to cover most SMs when rows are few, and small
+  // enough slices that a CTA of at most 256 consumer threads holds one
+  int C = 0, vpt = 0;
+  const int opts[4] = {1, 2, 4, 8};
+  for (int c : opts) {
+    if (G % c) continue;
+    if (g_tune_C > 0 && c != g_tune_C) continue;
+    const int v = (g_tune_vpt > 0 && (G / c) % g_tune_vpt == 0 &&
+                   16 * (G / c) / g_tune_vpt <= kMaxStage1Threads - 32)
+                      ? g_tune_vpt
+                      : pick_vpt(G / c);
+    if (!v) continue;
+    C = c;
+    vpt = v;
+    if (g_tune_C > 0 || (long)T * c >= (long)num_sms * 3 / 4) break;
+  }
+  if (!C) return ch;   // VPT == 0 signals an unsupported width
+  ch.C = C;
+  ch.VPT = vpt;
+  ch.NA = 16 * (G / C) / vpt;
+  ch.threads = 32 + ((ch.NA + 31) / 32) * 32;
+  const int E = H / C;
+  const size_t budget = 200u * 1024u;
+  int nslot = (int)(budget / ((size_t)E * 2u));
+  // chunks one CTA streams when the grid covers every SM
+  const long clusters = (long)num_sms / C;
+  const long rows_each = (T + clusters - 1) / clusters;
+  const long total_chunks = rows_each * (k + 1);
+  if (nslot > total_chunks) nslot = (int)total_chunks;
+  if (nslot > 64) nslot = 64;
+  if (nslot < 2) nslot = 2;
+  if (g_tune_slots > 0) nslot = g_tune_slots;
+  ch.nslot = nslot;
+  ch.smem = stage1_smem_bytes(nslot, E);
+  return ch;
+}
+
+template <int VPT>
+cudaError_t launch_vpt(const Stage1Params &p, const Stage1Choice &ch, int grid,
+                       cudaStream_t stream) {
+  auto kern = reduce_norm_quant_kernel<VPT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)ch.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)ch.threads);
+  cfg.dynamicSmemBytes = ch.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ch.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+void stage1_set_tuning(int cluster, int vpt, int slots) {
+  g_tune_C = cluster;
+  g_tune_vpt = vpt;
+  g_tune_slots = slots;
+}
+
+int stage1_plan(int T, int H, int k, int num_sms, int *out6) {
+  Stage1Choice ch = choose_stage1(T, H, k, num_sms);
+  out6[0] = ch.C;
+  out6[1] = ch.VPT;
+  out6[2] = ch.NA;
+  out6[3] = ch.threads;
+  out6[4] = ch.nslot;
+  out6[5] = (int)ch.smem;
+  return 0;
+}
+
+cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream) {
+  Stage1Choice ch = choose_stage1(p.T, p.H, p.k, num_sms);
+  if (ch.VPT == 0) return cudaErrorInvalidConfiguration;
+  p.C = ch.C;
+  p.E = p.H / ch.C;
+  p.nslot = ch.nslot;
+  p.n_active = ch.NA;
+  // persistent grid: at most one CTA per SM, whole clusters, no more rows than exist
+  long clusters = num_sms / ch.C;
+  if (clusters > p.T) clusters = p.T;
+  if (clusters < 1) clusters = 1;
+  const int grid = (int)(clusters * ch.C);
+  switch (ch.VPT) {
+    case 1: return launch_vpt<1>(p, ch, grid, stream);
+    case 2: return launch_vpt<2>(p, ch, grid, stream);
+    case 3: return launch_vpt<3>(p, ch, grid, stream);
+    case 4: return launch_vpt<4>(p, ch, grid, stream);
+    case 5: return launch_vpt<5>(p, ch, grid, stream);
+    case 6: return launch_vpt<6>(p, ch, grid, stream);
+    case 7: return launch_vpt<7>(p, ch, grid, stream);
+    case 8: return launch_vpt<8>(p, ch, grid, stream);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+}  // namespace nfq

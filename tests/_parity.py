@@ -1,0 +1,132 @@
+"""Shared helpers of the parity tests: GPU upload, acceptance checks.
+
+Acceptance rules (the method's stated tolerances, with the readings noted):
+  hidden  BF16 within 1 ulp in sign-magnitude order (+0 == -0)
+  scales  within 1e-6 relative in every group whose 128 BF16 hidden values
+          agree exactly with the oracle; elsewhere the GPU scale must equal
+          max|GPU hidden| / 448 in fp32 (self-consistency)
+  codes   bit-exact in groups whose hidden agrees; elsewhere at most one e4m3
+          step apart, and such differences on at most 0.1% of all elements
+  tokens  exact wherever the oracle's top-2 relative gap is >= 1e-3 and for
+          exact ties (gap 0); in between a near tie is counted, and the GPU's
+          pick must still be within the logit tolerance of the maximum
+  logits  |GPU - oracle| <= 2 * gamma_H * sum_k |a_k w_k| (fp32 accumulation
+          bound applied to both sides), gamma_n = n u / (1 - n u), u = 2^-24
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+U = 2.0 ** -24
+
+
+def to_dev_bf16(bits: np.ndarray, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def to_dev(a: np.ndarray, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def bf16_host(t) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _ordered_bf16(bits):
+    b = bits.astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def _ordered_e4m3(codes):
+    c = codes.astype(np.int32)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def check_stage1(hidden, codes, scales, ref, max_code_frac=1e-3):
+    """hidden/codes/scales: host arrays from the GPU; ref: oracle dict.
+    Returns a dict of counts for reporting."""
+    R, H = ref["hidden"].shape
+    G = H // 128
+    dh = np.abs(_ordered_bf16(hidden) - _ordered_bf16(ref["hidden"]))
+    assert dh.max(initial=0) <= 1, f"hidden differs by {dh.max()} bf16 ulps"
+    group_same = (dh.reshape(R, G, 128) == 0).all(axis=2)
+    # scales: rel 1e-6 where the group's hidden agrees
+    so, sg = ref["scales"], scales
+    rel = np.abs(sg.astype(np.float64) - so) / np.maximum(np.abs(so).astype(np.float64), 1e-30)
+    bad = group_same & (rel > 1e-6) & ~((sg == 0) & (so == 0))
+    assert not bad.any(), f"{bad.sum()} scales off in agreeing groups"
+    # self-consistency everywhere
+    yg = np.abs(oracle.bf16_to_f32(hidden).reshape(R, G, 128)).max(axis=2)
+    assert np.array_equal(sg, (yg / np.float32(448)).astype(np.float32)), "scale != amax/448"
+    # codes: identical (zero sign ignored) in agreeing groups
+    cg = np.where((codes & 0x7F) == 0, 0, codes).reshape(R, G, 128)
+    co = np.where((ref["codes"] & 0x7F) == 0, 0, ref["codes"]).reshape(R, G, 128)
+    diff = cg != co
+    assert not (diff & group_same[:, :, None]).any(), "codes differ in a group whose hidden agrees"
+    step = np.abs(_ordered_e4m3(cg) - _ordered_e4m3(co))
+    assert step.max(initial=0) <= 1, f"codes differ by {step.max()} steps"
+    frac = diff.sum() / diff.size
+    assert frac <= max_code_frac, f"{frac:.2e} of codes differ"
+    return {"hidden_ulp_diffs": int((dh > 0).sum()), "groups_differing": int((~group_same).sum()),
+            "codes_differing": int(diff.sum())}
+
+
+def dequant_rows(codes, scales):
+    """fp64 dequantised rows of a [R][H] code block with [R][G] or [Rb][G] scales."""
+    return oracle.e4m3_to_f32(codes.ravel()).reshape(codes.shape).astype(np.float64) * \
+        np.repeat(scales.astype(np.float64), 128, axis=1)
+
+
+def abs_dot(qa_row, sa_row, qw, sw, rows):
+    """sum_k |a_k w_k| for one activation row against weight rows `rows`."""
+    a = np.abs(dequant_rows(qa_row[None, :], sa_row[None, :]))[0]
+    out = []
+    for v in rows:
+        w = np.abs(dequant_rows(qw[v][None, :], sw[v // 128][None, :]))[0]
+        out.append(float(a @ w))
+    return np.array(out)
+
+
+def check_stage2(tokens, qa, sa, qw, sw, S, sample, max_logit=None, shard_idx=None,
+                 shard_val=None, expected=None):
+    """Compare GPU draft tokens (and optional outputs) on the sampled token rows
+    with the oracle's full-vocab logits; expected: {token: id} known by
+    construction.  Returns (#near ties, #checked)."""
+    H = qa.shape[1]
+    gamma = (H + 2) * U / (1 - (H + 2) * U)
+    L = oracle.lm_head_logits(qa, sa, qw, sw, tokens=sample)
+    r = oracle.argmax(L, S)
+    near = 0
+    V = qw.shape[0]
+    width = V // S
+    for i, t in enumerate(sample):
+        gap = r["gap"][i]
+        tol = 2 * gamma * abs_dot(qa[t], sa[t], qw, sw, [int(r["tokens"][i])])[0]
+        if expected is not None and t in expected:
+            assert r["tokens"][i] == expected[t], "oracle misses a planted tie"
+        if gap >= 1e-3 or gap == 0.0:
+            assert tokens[t] == r["tokens"][i], f"token {t}: gpu {tokens[t]} oracle {r['tokens'][i]} gap {gap}"
+        else:
+            near += 1
+            assert L[i, tokens[t]] >= r["values"][i] - 2 * tol
+        if max_logit is not None:
+            assert abs(float(max_logit[t]) - float(r["values"][i])) <= tol + 1e-30
+        if shard_idx is not None:
+            sg = oracle.shard_gaps(L[i:i + 1], S)[0]
+            for s in range(S):
+                oi = int(r["shard_idx"][i, s])
+                gi = int(shard_idx[s, t])
+                assert s * width <= gi < (s + 1) * width
+                stol = 2 * gamma * abs_dot(qa[t], sa[t], qw, sw, [oi])[0]
+                if sg[s] >= 1e-3 or sg[s] == 0.0:
+                    assert gi == oi, f"token {t} shard {s}: gpu {gi} oracle {oi}"
+                else:
+                    assert L[i, gi] >= r["shard_val"][i, s] - 2 * stol
+                if shard_val is not None:
+                    assert abs(float(shard_val[s, t]) - float(r["shard_val"][i, s])) <= stol + 1e-30
+    return near, len(sample)

@@ -1,0 +1,108 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol and
+rejects bad arguments before touching a device (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import norm_fp8_quant_gb300 as nfq
+from norm_fp8_quant_gb300 import build as nfq_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nfq_build.build()
+    return nfq.load()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "nfq.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(nfq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 7
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert lib.nfq_abi_version() >> 16 == 1
+    for st in range(-7, 1):
+        assert nfq.status_str(st) != "unknown status"
+
+
+FAKE = 1 << 20          # aligned fake device addresses: never dereferenced
+MIS = FAKE + 8
+
+
+def _stage1(lib, partials, k=2, residual=FAKE, norm_w=FAKE, eps=1e-6, T=4, H=1024,
+            hidden=FAKE, codes=FAKE, scales=FAKE, tokens=None, hidden_q=None, group=128):
+    arr = (ctypes.c_void_p * max(len(partials), 1))(*partials) if partials is not None else None
+    q = nfq.QuantAct(codes, scales, T if tokens is None else tokens,
+                     H if hidden_q is None else hidden_q, group)
+    return lib.nfq_mtp_reduce_norm_quant(arr, k, residual, norm_w, eps, T, H, hidden,
+                                         ctypes.byref(q), None)
+
+
+def test_stage1_argument_validation(lib):
+    ok = [FAKE, FAKE]
+    assert _stage1(lib, None) == nfq.NFQ_ERR_NULL
+    assert _stage1(lib, [FAKE, 0]) == nfq.NFQ_ERR_NULL
+    assert _stage1(lib, ok, residual=0) == nfq.NFQ_ERR_NULL
+    assert _stage1(lib, ok, codes=0) == nfq.NFQ_ERR_NULL
+    assert _stage1(lib, ok, k=0) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, [FAKE] * 17, k=17) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, H=1000) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, H=0) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, T=-1, tokens=-1) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, eps=-1.0) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, eps=float("nan")) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, group=64) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, tokens=5) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, ok, hidden_q=2048) == nfq.NFQ_ERR_SHAPE
+    assert _stage1(lib, [FAKE, MIS]) == nfq.NFQ_ERR_ALIGN
+    assert _stage1(lib, ok, hidden=MIS) == nfq.NFQ_ERR_ALIGN
+    assert _stage1(lib, ok, scales=MIS) == nfq.NFQ_ERR_ALIGN
+    # an empty batch is a no-op that needs no device
+    assert _stage1(lib, ok, T=0, tokens=0) == nfq.NFQ_OK
+
+
+def _stage2(lib, T=4, H=1024, group=128, codes=FAKE, scales=FAKE, w=FAKE, ws_=FAKE, V=4096,
+            S=2, tokens=FAKE, ws=FAKE, ws_bytes=None, mx=None):
+    q = nfq.QuantAct(codes, scales, T, H, group)
+    if ws_bytes is None:
+        ws_bytes = lib.nfq_lm_head_workspace_bytes(T, S)
+    return lib.nfq_lm_head_fp8_argmax(ctypes.byref(q), w, ws_, V, S, tokens, mx, None, None,
+                                      ws, ws_bytes, None)
+
+
+def test_stage2_argument_validation(lib):
+    assert lib.nfq_lm_head_workspace_bytes(4, 0) == 0
+    assert lib.nfq_lm_head_workspace_bytes(4, 8) >= 8 * 8
+    assert _stage2(lib, codes=0) == nfq.NFQ_ERR_NULL
+    assert _stage2(lib, w=0) == nfq.NFQ_ERR_NULL
+    assert _stage2(lib, tokens=0) == nfq.NFQ_ERR_NULL
+    assert _stage2(lib, V=4095) == nfq.NFQ_ERR_SHAPE        # V % S != 0
+    assert _stage2(lib, S=0) == nfq.NFQ_ERR_SHAPE
+    assert _stage2(lib, S=65, V=65 * 64) == nfq.NFQ_ERR_SHAPE
+    assert _stage2(lib, H=1000) == nfq.NFQ_ERR_SHAPE
+    assert _stage2(lib, H=32768) == nfq.NFQ_ERR_SHAPE
+    assert _stage2(lib, group=32) == nfq.NFQ_ERR_SHAPE
+    assert _stage2(lib, ws=0) == nfq.NFQ_ERR_WORKSPACE
+    assert _stage2(lib, ws_bytes=8) == nfq.NFQ_ERR_WORKSPACE
+    assert _stage2(lib, w=MIS) == nfq.NFQ_ERR_ALIGN
+    assert _stage2(lib, mx=MIS) == nfq.NFQ_ERR_ALIGN
+    assert _stage2(lib, T=0) == nfq.NFQ_OK
+    assert lib.nfq_lm_head_workspace_init(None, 16, None) == nfq.NFQ_ERR_NULL
+
+
+def test_stage1_plans_cover_the_workload_shapes(lib):
+    for (T, H, k) in [(4, 1024, 2), (1, 7168, 8), (64, 6144, 8), (8192, 7168, 8),
+                      (256, 6144, 4), (3, 128, 1), (7, 896, 3), (2, 32768, 16)]:
+        p = nfq.stage1_plan(T, H, k, 152)
+        assert p["vpt"] >= 1 and (H // 128) % (p["cluster"] * p["vpt"]) == 0
+        assert p["active_threads"] * p["vpt"] * 8 * p["cluster"] == H
+        assert p["threads"] <= 288 and p["smem"] <= 227 * 1024

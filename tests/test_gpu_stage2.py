@@ -1,0 +1,138 @@
+"""GPU parity of the FP8 LM head with the fused vocab-sharded argmax against
+the CPU oracle, through the C ABI (via the Python binding)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests._parity import check_stage2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nfq():
+    import norm_fp8_quant_gb300 as m
+    from norm_fp8_quant_gb300 import build
+    build.build()
+    m.load()
+    assert torch.cuda.is_available()
+    return m
+
+
+def stage1_ref(w):
+    inp = synth.stage1_inputs(w)
+    return oracle.reduce_norm_quant(inp["partials"], inp["residual"], inp["norm_w"])
+
+
+def run_gpu(nfq, qa, sa, qw, sw, S, ws=None):
+    out = nfq.lm_head_fp8_argmax(to_dev(qa), to_dev(sa), to_dev(qw), to_dev(sw), S,
+                                 workspace=ws, want_max=True, want_shards=True)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    return [None if x is None else x.cpu().numpy() for x in out]
+
+
+def test_stage2_tiny_all_tokens(nfq):
+    w = synth.workload("tiny")
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, list(range(w.T)),
+                 mx, sidx, sval)
+
+
+def test_stage2_decode_c1_full_vocab(nfq):
+    """T = 1, V = 129280 in 8 shards of 16160 rows: shard boundaries fall inside
+    128-row scale blocks and tiles."""
+    w = synth.workload("decode_c1")
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, [0], mx, sidx, sval)
+
+
+def test_stage2_decode_c64_sampled_tokens(nfq):
+    w = synth.workload("decode_c64")
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    assert tok.shape == (64,) and np.all((0 <= tok) & (tok < w.V))
+    check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, [0, 31, 63], mx, sidx, sval)
+
+
+def test_stage2_tie_stress(nfq):
+    """T = 256, V = 151552, S = 8; 30% of tokens have an exact duplicate maximum
+    on either side of a shard boundary: the lower global index must win."""
+    w = synth.workload("tie_stress")
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    expected = synth.plant_ties(w, qw, sw, ref["codes"])
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    width = w.V // w.S
+    for t, row in expected.items():
+        assert tok[t] == row, f"token {t}: {tok[t]} != {row}"
+        s = row // width
+        assert sidx[s, t] == row and sidx[s + 1, t] == row + 2 * ((s + 1) * width - 1 - row) + 1
+        assert sval[s, t] == sval[s + 1, t] == mx[t]
+    ties = sorted(expected)
+    sample = ties[:2] + [t for t in range(w.T) if t not in expected][:2]
+    check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, sample, mx, sidx, sval,
+                 expected=expected)
+
+
+@pytest.mark.parametrize("T,H,V,S", [(1, 128, 128, 1), (3, 256, 200, 2), (16, 512, 1000, 5),
+                                     (17, 384, 4100, 4), (33, 256, 2048, 64),
+                                     (64, 1024, 3000, 3), (100, 512, 1536, 6),
+                                     (129, 256, 1024, 8), (256, 256, 640, 5),
+                                     (300, 256, 512, 2)])
+def test_stage2_edge_shapes(nfq, T, H, V, S):
+    """Ragged vocab tails, shard widths below a tile or a warp, every token
+    count class (padding inside the MMA N, two warpgroups, 256-token chunks)."""
+    w = synth.workload("tiny", T=T, H=H, k=2, V=V, S=S, seed=T + H + V + S)
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, S)
+    check_stage2(tok, ref["codes"], ref["scales"], qw, sw, S, list(range(T)), mx, sidx, sval)
+
+
+def test_stage2_planted_ties_and_zero_logits(nfq):
+    """Exact duplicates inside one warp, across warps of a tile, across tiles and
+    at the last row; an all-zero activation row makes every logit +-0 and must
+    give token 0."""
+    T, H, V, S = 6, 256, 1024, 4
+    w = synth.workload("tiny", T=T, H=H, k=2, V=V, S=S, seed=5)
+    ref = stage1_ref(w)
+    qa, sa = ref["codes"].copy(), ref["scales"].copy()
+    qw, sw = synth.lm_head_weights(w)
+    sw[:] = sw[0]                      # one scale row: equal codes give equal logits
+    qa[5] = 0
+    sa[5] = 0
+    pairs = {0: (3, 17), 1: (40, 100), 2: (127, 128), 3: (255, 256), 4: (700, 1023)}
+    for t, (a, b) in pairs.items():
+        row = np.where((qa[t] & 0x7F) == 0, 0, np.where(qa[t] & 0x80, 0xFE, 0x7E)).astype(np.uint8)
+        qw[a] = row
+        qw[b] = row
+    tok, mx, sidx, sval = run_gpu(nfq, qa, sa, qw, sw, S)
+    for t, (a, b) in pairs.items():
+        assert tok[t] == a
+    assert tok[5] == 0 and mx[5] == 0.0 and not np.signbit(mx[5])
+    assert list(sidx[:, 5]) == [0, 256, 512, 768]
+    check_stage2(tok, qa, sa, qw, sw, S, list(range(T)), mx, sidx, sval,
+                 expected={t: a for t, (a, b) in pairs.items()})
+
+
+def test_stage2_workspace_stays_zero_across_calls(nfq):
+    w = synth.workload("tiny", T=20, H=512, V=2048, S=4, seed=9)
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    ws = nfq.lm_head_workspace(w.T, w.S, "cuda")
+    first = None
+    for _ in range(3):
+        out = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S, ws=ws)
+        assert torch.count_nonzero(ws).item() == 0
+        if first is None:
+            first = out
+        for a, b in zip(first, out):
+            assert np.array_equal(a, b)
