@@ -1,0 +1,418 @@
+"""Benchmark of the MTP draft-layer tail on GB300.
+
+One step = one pass of the whole hot path over one batch of the decode c=64
+draft step (GLM-5.2 shapes): T=64 tokens, hidden 6144, k=8 BF16 partials with
+1% outlier channels x20, residual, RMSNorm, packed FP8 activation, then the
+FP8 LM head over vocab 151552 in 8 shards with the fused greedy argmax.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is draft tokens/s of the whole step
+with inputs resident in HBM; `e2e` repeats the measurement with the step's
+stage-1 inputs copied from pinned host memory and the tokens read back every
+step.  Each step reads the 932 MB FP8 LM-head weight (> L2) and a different
+one of 40 rotating stage-1 input sets (283 MB in all), so no step is served
+from L2.  With N > 1 (torchrun) every rank runs the same workload on its own
+GPU (independent replicas, weak scaling; the only collectives are the timing
+barrier and the max over ranks).
+
+--impl reference times the CPU oracle instead (rank 0 only): each step is a
+bounded sample (stage 1 on all 64 rows, the LM head for all 64 tokens over 32
+vocab rows), scaled to the whole workload.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "decode_c64"
+METRIC = "norm+FP8-quant GB/s; LM-head+argmax draft tokens/s; % of GB300 roofline"
+ROTATING_SETS = 40
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------ bytes & peaks --
+
+def stage1_bytes(T, H, k):
+    """Algorithmic HBM bytes of one stage-1 launch: k partials + residual +
+    norm weight read; BF16 hidden, e4m3 codes and fp32 group scales written."""
+    return k * T * H * 2 + T * H * 2 + H * 2 + T * H * 2 + T * H + T * (H // 128) * 4
+
+
+def stage2_bytes(T, H, V):
+    """Algorithmic HBM bytes of one LM-head launch: FP8 weight + block scales,
+    activation codes + scales read; int32 tokens written."""
+    G = H // 128
+    return V * H + ((V + 127) // 128) * G * 4 + T * H + T * G * 4 + T * 4
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "norm_fp8_quant_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu capture, if it was taken on
+    the kernel source as it stands (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)[kernel]
+        srcs = d["sources"]
+        if d["source_hash"] != kernel_source_hash(srcs):
+            return None
+        return d["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks --
+
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons every 100 ms."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 5:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[3], int(parts[4], 16)))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside and rows:   # timed region shorter than the sampling period
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        mhz = sorted(r[1] for r in inside)
+        mask = 0
+        for r in inside:
+            mask |= r[4]
+        reasons = [n for b, n in REASON_BITS.items() if mask & b and b != 0x1]
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": inside[0][2], "reasons": reasons,
+                "samples": len(inside)}
+
+
+# -------------------------------------------------------------- our impl --
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import norm_fp8_quant_gb300 as nfq
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = synth.workload(WORKLOAD)
+    T, H, k, V, S = w.T, w.H, w.k, w.V, w.S
+
+    # inputs: stage-1 tensors (rotating device copies) and the LM head
+    inp = synth.stage1_inputs(w)
+    to_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    host_parts = [to_bf16(p).pin_memory() for p in inp["partials"]]
+    host_res = to_bf16(inp["residual"]).pin_memory()
+    norm_w = to_bf16(inp["norm_w"]).to(dev)
+    sets = []
+    for _ in range(ROTATING_SETS):
+        sets.append(([p.to(dev) for p in host_parts], host_res.to(dev)))
+    qw, sw = synth.lm_head_weights(w)
+    qw_d = torch.from_numpy(qw).to(dev)
+    sw_d = torch.from_numpy(sw).to(dev)
+    del qw
+    hidden = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
+    tokens = torch.empty(T, dtype=torch.int32, device=dev)
+    ws = nfq.lm_head_workspace(T, S, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        parts, res = sets[i % ROTATING_SETS]
+        nfq.mtp_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
+        nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    if nfq.device_error() != nfq.NFQ_OK:
+        raise RuntimeError("a kernel reported an expired wait during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    t_wall0 = time.time()
+    for i in range(K):
+        parts, res = sets[i % ROTATING_SETS]
+        ev[i][0].record(stream)
+        nfq.mtp_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
+        ev[i][1].record(stream)
+        nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
+        ev[i][2].record(stream)
+    barrier()
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1) if sampler else None
+    if nfq.device_error() != nfq.NFQ_OK:
+        raise RuntimeError("a kernel reported an expired wait during the timed steps")
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    s1_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    s2_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    gpu_launches = 2 * K
+
+    # end to end through the public API from pinned host memory
+    h_tokens = torch.empty(T, dtype=torch.int32).pin_memory()
+    dev_parts = [torch.empty_like(p, device=dev) for p in host_parts]
+    dev_res = torch.empty_like(host_res, device=dev)
+    h2d = sum(p.numel() * 2 for p in host_parts) + host_res.numel() * 2
+    d2h = T * 4
+
+    def e2e_step():
+        for hp, dp in zip(host_parts, dev_parts):
+            dp.copy_(hp, non_blocking=True)
+        dev_res.copy_(host_res, non_blocking=True)
+        nfq.mtp_reduce_norm_quant(dev_parts, dev_res, norm_w, w.eps, hidden, codes, scales)
+        nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
+        h_tokens.copy_(tokens, non_blocking=True)
+        stream.synchronize()
+        return h_tokens
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    barrier()
+    c0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - c0) * 1e3
+    barrier()
+
+    times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = times.tolist()
+
+    result = None
+    if rank == 0:
+        peak, peak_kind = load_peaks()
+        b1 = stage1_bytes(T, H, k)
+        b2 = stage2_bytes(T, H, V)
+        gbs1 = b1 / (s1_ms * 1e-3) / 1e9
+        gbs2 = b2 / (s2_ms * 1e-3) / 1e9
+        value = world * T * K / (total_ms * 1e-3)
+        result = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": "draft tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(total_ms / K, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e4m3 MMA, fp32 accumulate; bf16 in, fp32 norm",
+            "data": "synthetic",
+            "config": {"workload": "decode c=64 draft step (GLM-5.2 shapes): T=64, hidden=6144, "
+                                   "k=8 BF16 partials N(0,0.5) with 1% outlier channels x20, "
+                                   "vocab=151552 in 8 shards, 128x128-block FP8 LM head",
+                       "l2": "inputs larger than L2: 932 MB FP8 weight read every step, "
+                             f"{ROTATING_SETS} rotating stage-1 input sets (283 MB)",
+                       "parallelism": f"replicas x{world}"},
+            "norm_quant": {"us": round(s1_ms * 1e3, 3), "GB/s": round(gbs1, 1),
+                           "frac": round(gbs1 / peak, 4), "bytes": b1},
+            "lm_head": {"us": round(s2_ms * 1e3, 3), "GB/s": round(gbs2, 1),
+                        "frac": round(gbs2 / peak, 4), "bytes": b2,
+                        "draft_tokens_per_s": round(T / (s2_ms * 1e-3), 1)},
+            "roofline": {"bound": "hbm", "achieved": round(gbs2, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(gbs2 / peak, 4),
+                         "traffic": ncu_traffic("lm_head"),
+                         "kernel": "lm_head_argmax_kernel", "peak_source": peak_kind},
+            "e2e": {"value": round(world * T * K / (e2e_ms * 1e-3), 1), "unit": "draft tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": gpu_launches,
+            "clocks": clocks,
+        }
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def oracle_sample(w, inp, qw, sw, rows, tokens):
+    """Oracle time of stage 1 on all rows plus the LM head for `tokens` over
+    `rows` vocab rows; returns (seconds, per-token seconds for the full vocab)."""
+    import oracle
+    t0 = time.perf_counter()
+    o = oracle.reduce_norm_quant(inp["partials"], inp["residual"], inp["norm_w"], w.eps)
+    t1 = time.perf_counter()
+    oracle.lm_head_logits(o["codes"], o["scales"], qw[:rows], sw[: (rows + 127) // 128],
+                          tokens=tokens)
+    t2 = time.perf_counter()
+    full = (t1 - t0) + (t2 - t1) * (w.V / rows)     # whole step, all T tokens
+    return t2 - t0, full
+
+
+def cpu_baseline(w):
+    import numpy as np
+    import synth
+    inp = synth.stage1_inputs(w)
+    rows = 2 * (w.V // w.S)
+    ww = synth.workload(WORKLOAD, V=rows, S=2)
+    qw, sw = synth.lm_head_weights(ww)
+    secs, full = oracle_sample(w, inp, qw, sw, rows, list(range(w.T)))
+    return {"value": round(w.T / full, 4), "unit": "draft tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"stage 1 on all {w.T} rows + LM head for all {w.T} tokens over "
+                      f"{rows} of {w.V} vocab rows ({secs:.1f} s), scaled to the full vocab"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import synth
+    w = synth.workload(WORKLOAD)
+    inp = synth.stage1_inputs(w)
+    rows = 32
+    ww = synth.workload(WORKLOAD, V=128, S=1)
+    qw, sw = synth.lm_head_weights(ww)
+    for _ in range(args.warmup):
+        oracle_sample(w, inp, qw, sw, rows, list(range(w.T)))
+    t0 = time.perf_counter()
+    fulls = []
+    for _ in range(args.steps):
+        fulls.append(oracle_sample(w, inp, qw, sw, rows, list(range(w.T)))[1])
+    elapsed = time.perf_counter() - t0
+    full = sum(fulls) / len(fulls)
+    value = w.T / full
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4),
+            "unit": "draft tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(full * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp32 (fp64 norm)", "data": "synthetic",
+            "config": {"workload": "decode c=64 draft step (GLM-5.2 shapes): T=64, "
+                                   "hidden=6144, k=8, vocab=151552 in 8 shards",
+                       "parallelism": "cpu oracle, rank 0"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "draft tokens/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"per step: stage 1 on all {w.T} rows + LM head for all "
+                                       f"{w.T} tokens over {rows} vocab rows, scaled to "
+                                       f"{w.V} rows; {elapsed:.1f} s timed"},
+            "e2e": {"value": round(value, 4), "unit": "draft tokens/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    from norm_fp8_quant_gb300 import build
+    if rank == 0:
+        build.build()
+    else:
+        while not os.path.exists(build.LIB):
+            time.sleep(0.5)
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            import synth
+            res["cpu_baseline"] = cpu_baseline(synth.workload(WORKLOAD))
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -137,19 +137,24 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 
   if (warp == 4 * EPI) {
     // -------------------------------------------------------------- producer --
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
-      uint32_t it = 0;
-      bool ok = true;
-      for (int vt = t_begin; vt < t_end && ok; ++vt) {
-        for (int kb = 0; kb < G; ++kb, ++it) {
-          const uint32_t s = it % (uint32_t)nstage;
-          const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-          if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2)) {
-            ok = false;
-            break;
-          }
+    // The whole warp walks the schedule; lane 0 waits and issues.
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int vt = t_begin; vt < t_end && ok; ++vt) {
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           const uint32_t fb = smem_u32(&sh->full[s]);
           mbar_arrive_expect_tx(fb, kWTileBytes + kATileBytes);
           tma_load_2d(smem_u32(w_tiles + (size_t)s * kWTileBytes), &tmap_w, kb * 128, vt * 128,
@@ -157,46 +162,58 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
           tma_load_2d(smem_u32(a_tiles + (size_t)s * kATileBytes), &tmap_a, kb * 128, 0, fb,
                       pol_a);
         }
+        __syncwarp();
       }
+    }
+    if (lane == 0) {
       const uint32_t issued = it;
       const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
       for (uint32_t j = first; j < issued; ++j)
         mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
     }
+    __syncwarp();
   } else if (warp == 4 * EPI + 1) {
     // ------------------------------------------------------------------- MMA --
-    if (lane == 0) {
-      uint32_t it = 0, kbi = 0;
-      bool ok = true;
-      for (int vt = t_begin; vt < t_end && ok; ++vt) {
-        for (int kb = 0; kb < G; ++kb, ++it, ++kbi) {
-          const uint32_t s = it % (uint32_t)nstage;
-          const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-          const uint32_t b = kbi % NBUF;
-          const uint32_t bph = (kbi / NBUF) & 1u;
-          if (!mbar_wait(smem_u32(&sh->tempty[b]), bph ^ 1u, abort_flag, p.err, kErrBitStage2) ||
-              !mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2)) {
-            ok = false;
-            break;
-          }
+    // The whole warp walks the schedule; lane 0 waits, issues the MMAs and
+    // commits them to the stage's empty barrier and the accumulator's full one.
+    uint32_t it = 0, kbi = 0;
+    bool ok = true;
+    for (int vt = t_begin; vt < t_end && ok; ++vt) {
+      for (int kb = 0; kb < G; ++kb, ++it, ++kbi) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        const uint32_t b = kbi % NBUF;
+        const uint32_t bph = (kbi / NBUF) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->tempty[b]), bph ^ 1u, abort_flag, p.err, kErrBitStage2) &&
+                mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           tc_fence_after();
           const uint32_t a_addr = smem_u32(w_tiles + (size_t)s * kWTileBytes);
           const uint32_t b_addr = smem_u32(a_tiles + (size_t)s * kATileBytes);
           const uint32_t d_tmem = tmem_base + b * N;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32),
-                   kIdesc, kk > 0 ? 1u : 0u);
+            mma_f8(d_tmem, sw128_kmajor_desc(a_addr + kk * 32),
+                   sw128_kmajor_desc(b_addr + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
           mma_commit(smem_u32(&sh->empty[s]));
           mma_commit(smem_u32(&sh->tfull[b]));
         }
-      }
-      // every MMA issued has finished before TMEM is released
-      if (kbi > 0) {
-        const uint32_t last = kbi - 1;
-        mbar_wait_drain(smem_u32(&sh->tfull[last % NBUF]), (last / NBUF) & 1u);
+        __syncwarp();
       }
     }
+    // every MMA issued has finished before TMEM is released
+    if (lane == 0 && kbi > 0) {
+      const uint32_t last = kbi - 1;
+      mbar_wait_drain(smem_u32(&sh->tfull[last % NBUF]), (last / NBUF) & 1u);
+    }
+    __syncwarp();
   } else {
     // -------------------------------------------------------------- epilogue --
     const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
@@ -217,7 +234,8 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
         if (kb + 1 < G) sw_next = __ldg(swrow + kb + 1);
         const uint32_t b = kbi % NBUF;
         const uint32_t bph = (kbi / NBUF) & 1u;
-        if (!mbar_wait(smem_u32(&sh->tfull[b]), bph, abort_flag, p.err, kErrBitStage2)) {
+        const bool got = mbar_wait(smem_u32(&sh->tfull[b]), bph, abort_flag, p.err, kErrBitStage2);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
@@ -279,6 +297,7 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
       }
     }
     __threadfence();
+    __syncwarp();
   }
 
   // ------------------------------------------------------------- teardown --

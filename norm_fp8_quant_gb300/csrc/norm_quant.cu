@@ -99,34 +99,46 @@ __global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      uint32_t it = 0;
-      bool ok = true;
-      for (int r = cid; r < p.T && ok; r += ncl) {
-        const size_t off = ((size_t)r * (size_t)p.H + (size_t)col0) * 2u;
-        for (int i = 0; i <= p.k; ++i, ++it) {
-          const uint32_t s = it % (uint32_t)p.nslot;
-          const uint32_t ph = (it / (uint32_t)p.nslot) & 1u;
-          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage1)) {
-            ok = false;
-            break;
-          }
+    // The whole warp walks the schedule (so it stays converged for the
+    // barriers at the end); lane 0 waits and issues, the others follow.
+    const uint64_t pol = policy_evict_first();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int r = cid; r < p.T && ok; r += ncl) {
+      const size_t off = ((size_t)r * (size_t)p.H + (size_t)col0) * 2u;
+      for (int i = 0; i <= p.k; ++i, ++it) {
+        const uint32_t s = it % (uint32_t)p.nslot;
+        const uint32_t ph = (it / (uint32_t)p.nslot) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage1);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           const uint8_t *src =
               static_cast<const uint8_t *>(i < p.k ? p.partials[i] : p.residual) + off;
           mbar_arrive_expect_tx(smem_u32(&full[s]), slot_bytes);
           bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes), src, slot_bytes,
                    smem_u32(&full[s]), pol);
         }
+        __syncwarp();
       }
-      // every copy issued lands before the CTA can leave
+    }
+    // every copy issued lands before the CTA can leave
+    if (lane == 0) {
       const uint32_t issued = it;
       const uint32_t first = issued > (uint32_t)p.nslot ? issued - (uint32_t)p.nslot : 0u;
       for (uint32_t j = first; j < issued; ++j)
         mbar_wait_drain(smem_u32(&full[j % (uint32_t)p.nslot]), (j / (uint32_t)p.nslot) & 1u);
     }
+    __syncwarp();
   } else {
     // ----------------------------------------------------------- consumers --
+    // Every lane of a consumer warp executes every shuffle and wait; lanes
+    // past n_active carry no data (whole 16-lane groups, as NA % 16 == 0).
     const int tc = (int)threadIdx.x - 32;
     const int cw = warp - 1;
     const int NA = p.n_active;
@@ -138,17 +150,25 @@ __global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel
           static_cast<const uint8_t *>(p.norm_w) + (size_t)col0 * 2u);
 #pragma unroll
       for (int v = 0; v < VPT; ++v) wpk[v] = __ldg(wsrc + v * NA + tc);
+    } else {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) wpk[v] = make_uint4(0u, 0u, 0u, 0u);
     }
 
     uint32_t it = 0;
     int row_iter = 0;
     for (int r = cid; r < p.T; r += ncl, ++row_iter) {
       float x[VPT][8];
+#pragma unroll
+      for (int v = 0; v < VPT; ++v)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[v][e] = 0.0f;
       bool ok = true;
       for (int i = 0; i <= p.k; ++i, ++it) {
         const uint32_t s = it % (uint32_t)p.nslot;
         const uint32_t ph = (it / (uint32_t)p.nslot) & 1u;
-        if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err, kErrBitStage1)) {
+        const bool got = mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err, kErrBitStage1);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
@@ -169,12 +189,10 @@ __global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel
 
       // sum of squares: thread -> warp -> CTA -> cluster, fixed orders
       float ss = 0.0f;
-      if (active) {
 #pragma unroll
-        for (int v = 0; v < VPT; ++v)
+      for (int v = 0; v < VPT; ++v)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) ss = fmaf(x[v][e], x[v][e], ss);
-      }
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[v][e], x[v][e], ss);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       const int par = row_iter & 1;
@@ -183,7 +201,10 @@ __global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel
         sums->red[par][cw] = ss;
         mbar_arrive(smem_u32(&red_bar[par]));   // release: the store above is visible
       }
-      if (!mbar_wait(smem_u32(&red_bar[par]), pph, abort_flag, p.err, kErrBitStage1)) break;
+      __syncwarp();
+      const bool got_red = mbar_wait(smem_u32(&red_bar[par]), pph, abort_flag, p.err,
+                                     kErrBitStage1);
+      if (!__all_sync(0xffffffffu, got_red)) break;
       float tot = 0.0f;
       for (int q = 0; q < n_cons_warps; ++q) tot += sums->red[par][q];
       if (C > 1) {
@@ -194,49 +215,50 @@ __global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel
             mbar_arrive_remote(smem_u32(&ss_bar[par]), (uint32_t)q);
           }
         }
-        if (!mbar_wait<true>(smem_u32(&ss_bar[par]), pph, abort_flag, p.err, kErrBitStage1))
-          break;
+        __syncwarp();
+        const bool got_cl =
+            mbar_wait<true>(smem_u32(&ss_bar[par]), pph, abort_flag, p.err, kErrBitStage1);
+        if (!__all_sync(0xffffffffu, got_cl)) break;
         tot = 0.0f;
         for (int q = 0; q < C; ++q) tot += sums->cl[par][q];
       }
       const float ms = __fdiv_rn(tot, (float)p.H);
       const float rr = __frsqrt_rn(__fadd_rn(ms, p.eps));
 
-      if (active) {
-        const size_t rowbase = (size_t)r * (size_t)p.H + (size_t)col0;
-        uint4 *hid = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.hidden) + rowbase * 2u);
-        uint2 *cod = reinterpret_cast<uint2 *>(p.codes + rowbase);
+      const size_t rowbase = (size_t)r * (size_t)p.H + (size_t)col0;
+      uint4 *hid = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.hidden) + rowbase * 2u);
+      uint2 *cod = reinterpret_cast<uint2 *>(p.codes + rowbase);
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-          float wv[8];
-          unpack_bf16x8(wpk[v], wv);
-          float y[8];
-          uint32_t hb[4];
-          float amax = 0.0f;
+      for (int v = 0; v < VPT; ++v) {
+        float wv[8];
+        unpack_bf16x8(wpk[v], wv);
+        float y[8];
+        uint32_t hb[4];
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const __nv_bfloat16 b0 = __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]));
+          const __nv_bfloat16 b1 =
+              __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
+          const uint32_t u0 = __bfloat16_as_ushort(b0), u1 = __bfloat16_as_ushort(b1);
+          hb[e / 2] = u0 | (u1 << 16);
+          y[e] = __uint_as_float(u0 << 16);
+          y[e + 1] = __uint_as_float(u1 << 16);
+          amax = fmaxf(amax, fmaxf(fabsf(y[e]), fabsf(y[e + 1])));
+        }
+        // 16 consecutive lanes hold one 128-channel group (all lanes shuffle)
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float scale = __fdiv_rn(amax, 448.0f);
+        uint32_t q[2] = {0u, 0u};
+        if (scale != 0.0f) {
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            const __nv_bfloat16 b0 = __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]));
-            const __nv_bfloat16 b1 =
-                __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
-            const uint32_t u0 = __bfloat16_as_ushort(b0), u1 = __bfloat16_as_ushort(b1);
-            hb[e / 2] = u0 | (u1 << 16);
-            y[e] = __uint_as_float(u0 << 16);
-            y[e + 1] = __uint_as_float(u1 << 16);
-            amax = fmaxf(amax, fmaxf(fabsf(y[e]), fabsf(y[e + 1])));
+            const uint32_t pr = e4m3x2(__fdiv_rn(y[e], scale), __fdiv_rn(y[e + 1], scale));
+            q[e / 4] |= pr << ((e % 4) * 8);
           }
-          // 16 lanes hold one 128-channel group
-#pragma unroll
-          for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          const float scale = __fdiv_rn(amax, 448.0f);
-          uint32_t q[2] = {0u, 0u};
-          if (scale != 0.0f) {
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const uint32_t pr =
-                  e4m3x2(__fdiv_rn(y[e], scale), __fdiv_rn(y[e + 1], scale));
-              q[e / 4] |= pr << ((e % 4) * 8);
-            }
-          }
+        }
+        if (active) {
           const int j = v * NA + tc;
           hid[j] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
           cod[j] = make_uint2(q[0], q[1]);
@@ -245,6 +267,7 @@ __global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel
         }
       }
     }
+    __syncwarp();
   }
 
   __syncthreads();
