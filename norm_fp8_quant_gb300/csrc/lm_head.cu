@@ -218,52 +218,105 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
     // -------------------------------------------------------------- epilogue --
     const int quad = warp & 3;          // TMEM lanes 32*quad .. 32*quad+31
     const int grp = warp >> 2;          // column group: columns grp*NCOL ..
-    constexpr int CH = NCOL < 32 ? NCOL : 32;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(grp * NCOL);
     uint32_t kbi = 0;
     bool ok = true;
+
+    // wait for accumulator kbi and start reading this warp's NCOL columns of it
+    auto issue = [&](uint32_t (&r)[NCOL], uint32_t kb_i) -> bool {
+      const uint32_t b = kb_i % NBUF;
+      const bool got = mbar_wait(smem_u32(&sh->tfull[b]), (kb_i / NBUF) & 1u, abort_flag, p.err,
+                                 kErrBitStage2);
+      if (!__all_sync(0xffffffffu, got)) return false;
+      tc_fence_after();
+      if constexpr (NCOL == 16) {
+        tmem_ld16(lane_base + b * N, r);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NCOL; c += 32)
+          tmem_ld32(lane_base + b * N + c, *reinterpret_cast<uint32_t(*)[32]>(&r[c]));
+      }
+      return true;
+    };
+    // finish the reads and hand the accumulator back to the MMA warp
+    auto release = [&](uint32_t (&r)[NCOL], uint32_t kb_i) {
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < NCOL; ++j) asm volatile("" : "+r"(r[j]));   // uses stay after the wait
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[kb_i % NBUF]));
+    };
+
     for (int vt = t_begin; vt < t_end && ok; ++vt) {
       const float *swrow = p.w_scales + (size_t)vt * G;
-      float sw_next = __ldg(swrow);
-
       float acc[NCOL];
 #pragma unroll
       for (int j = 0; j < NCOL; ++j) acc[j] = 0.0f;
-
-      for (int kb = 0; kb < G; ++kb, ++kbi) {
-        const float swv = sw_next;
-        if (kb + 1 < G) sw_next = __ldg(swrow + kb + 1);
-        const uint32_t b = kbi % NBUF;
-        const uint32_t bph = (kbi / NBUF) & 1u;
-        const bool got = mbar_wait(smem_u32(&sh->tfull[b]), bph, abort_flag, p.err, kErrBitStage2);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      // acc += P * (sw * sa) for K block kb
+      auto promote = [&](const uint32_t (&r)[NCOL], int kb, float swv) {
         const float *sak = sa_s + (size_t)kb * N + grp * NCOL;
-        const uint32_t taddr =
-            tmem_base + ((uint32_t)(quad * 32) << 16) + b * N + (uint32_t)(grp * NCOL);
 #pragma unroll
-        for (int c = 0; c < NCOL; c += CH) {
-          uint32_t r[CH];
-          if constexpr (CH == 32) {
-            tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(r));
-          } else {
-            tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r));
-          }
-          tmem_wait_ld();
-          if (c + CH >= NCOL) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
-          }
+        for (int j = 0; j < NCOL; j += 4) {
+          const float4 sa4 = *reinterpret_cast<const float4 *>(sak + j);
+          acc[j + 0] = fmaf(__uint_as_float(r[j + 0]), swv * sa4.x, acc[j + 0]);
+          acc[j + 1] = fmaf(__uint_as_float(r[j + 1]), swv * sa4.y, acc[j + 1]);
+          acc[j + 2] = fmaf(__uint_as_float(r[j + 2]), swv * sa4.z, acc[j + 2]);
+          acc[j + 3] = fmaf(__uint_as_float(r[j + 3]), swv * sa4.w, acc[j + 3]);
+        }
+      };
+
+      if constexpr (NCOL <= 32) {
+        // two register sets: block kb+1 is read from TMEM while kb is promoted
+        uint32_t ra[NCOL], rb[NCOL];
+        if (!issue(ra, kbi)) { ok = false; break; }
+        release(ra, kbi);
+        float sw_cur = __ldg(swrow);
+        for (int kb = 0; kb < G; kb += 2) {
+          const uint32_t k1 = kbi + (uint32_t)kb + 1u, k2 = k1 + 1u;
+          const bool more1 = kb + 1 < G;
+          float sw_nxt = more1 ? __ldg(swrow + kb + 1) : 0.0f;
+          if (more1 && !issue(rb, k1)) { ok = false; break; }
+          promote(ra, kb, sw_cur);
+          if (!more1) break;
+          release(rb, k1);
+          const bool more2 = kb + 2 < G;
+          sw_cur = more2 ? __ldg(swrow + kb + 2) : 0.0f;
+          if (more2 && !issue(ra, k2)) { ok = false; break; }
+          promote(rb, kb + 1, sw_nxt);
+          if (more2) release(ra, k2);
+        }
+        kbi += (uint32_t)G;
+      } else {
+        // wide column groups: 32 columns at a time to bound register use
+        for (int kb = 0; kb < G; ++kb, ++kbi) {
+          const float swv = __ldg(swrow + kb);
+          const uint32_t b = kbi % NBUF;
+          const bool got = mbar_wait(smem_u32(&sh->tfull[b]), (kbi / NBUF) & 1u, abort_flag,
+                                     p.err, kErrBitStage2);
+          if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+          tc_fence_after();
+          const float *sak = sa_s + (size_t)kb * N + grp * NCOL;
 #pragma unroll
-          for (int j = 0; j < CH; j += 4) {
-            const float4 sa4 = *reinterpret_cast<const float4 *>(sak + c + j);
-            acc[c + j + 0] = fmaf(__uint_as_float(r[j + 0]), swv * sa4.x, acc[c + j + 0]);
-            acc[c + j + 1] = fmaf(__uint_as_float(r[j + 1]), swv * sa4.y, acc[c + j + 1]);
-            acc[c + j + 2] = fmaf(__uint_as_float(r[j + 2]), swv * sa4.z, acc[c + j + 2]);
-            acc[c + j + 3] = fmaf(__uint_as_float(r[j + 3]), swv * sa4.w, acc[c + j + 3]);
+          for (int c = 0; c < NCOL; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + b * N + c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j]));
+            if (c + 32 >= NCOL) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 sa4 = *reinterpret_cast<const float4 *>(sak + c + j);
+              acc[c + j + 0] = fmaf(__uint_as_float(r[j + 0]), swv * sa4.x, acc[c + j + 0]);
+              acc[c + j + 1] = fmaf(__uint_as_float(r[j + 1]), swv * sa4.y, acc[c + j + 1]);
+              acc[c + j + 2] = fmaf(__uint_as_float(r[j + 2]), swv * sa4.z, acc[c + j + 2]);
+              acc[c + j + 3] = fmaf(__uint_as_float(r[j + 3]), swv * sa4.w, acc[c + j + 3]);
+            }
           }
         }
       }
@@ -396,9 +449,9 @@ size_t stage2_workspace_bytes(int S) {
 cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const void *w,
                           int num_sms, cudaStream_t stream) {
   if (p.T <= 16) return launch_cfg<16, 1>(p, act_codes, w, num_sms, stream);
-  if (p.T <= 32) return launch_cfg<32, 1>(p, act_codes, w, num_sms, stream);
-  if (p.T <= 64) return launch_cfg<64, 1>(p, act_codes, w, num_sms, stream);
-  if (p.T <= 128) return launch_cfg<64, 2>(p, act_codes, w, num_sms, stream);
+  if (p.T <= 32) return launch_cfg<16, 2>(p, act_codes, w, num_sms, stream);
+  if (p.T <= 64) return launch_cfg<32, 2>(p, act_codes, w, num_sms, stream);
+  if (p.T <= 128) return launch_cfg<32, 4>(p, act_codes, w, num_sms, stream);
   return launch_cfg<128, 2>(p, act_codes, w, num_sms, stream);
 }
 
