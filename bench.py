@@ -196,9 +196,13 @@ def run_ours(args, rank, world, local):
     for _ in range(ROTATING_SETS):
         sets.append(([p.to(dev) for p in host_parts], host_res.to(dev)))
     qw, sw = synth.lm_head_weights(w)
-    qw_d = torch.from_numpy(qw).to(dev)
+    qw_rowmajor = torch.from_numpy(qw).to(dev)
     sw_d = torch.from_numpy(sw).to(dev)
     del qw
+    # the weight is static: pack it once into the streaming layout (not timed)
+    qw_d = nfq.pack_lm_head_weights(qw_rowmajor)
+    torch.cuda.synchronize()
+    del qw_rowmajor
     hidden = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
     scales = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
@@ -304,6 +308,8 @@ def run_ours(args, rank, world, local):
             "config": {"workload": "decode c=64 draft step (GLM-5.2 shapes): T=64, hidden=6144, "
                                    "k=8 BF16 partials N(0,0.5) with 1% outlier channels x20, "
                                    "vocab=151552 in 8 shards, 128x128-block FP8 LM head",
+                       "weight_layout": "packed once at load: tile-contiguous, pre-swizzled "
+                                        "16 KB blocks of 128 rows x 128 columns",
                        "l2": "inputs larger than L2: 932 MB FP8 weight read every step, "
                              f"{ROTATING_SETS} rotating stage-1 input sets (283 MB)",
                        "parallelism": f"replicas x{world}"},

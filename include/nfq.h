@@ -145,12 +145,54 @@ int nfq_lm_head_fp8_argmax(const nfq_quant_act *a, const uint8_t *w, const float
                            size_t ws_bytes, void *stream);
 
 /*
+ * Packed LM-head weight: the same e4m3 bytes re-laid for streaming.  The
+ * row-major [V][H] weight is cut into blocks of 128 vocab rows x 128 columns
+ * (the 128x128 scale blocks); block (vt, kb) is stored contiguously at byte
+ * offset (vt * H/128 + kb) * 16384, row r of the block at r * 128, and within
+ * a row the 16-byte chunk c at chunk position c XOR (r mod 8) (the 128-byte
+ * shared-memory swizzle the tensor cores read).  Rows past V are zero.  Each
+ * K step of the LM head then fetches one contiguous 16 KB block.
+ *
+ * nfq_lm_head_packed_bytes: size of the packed weight, ceil(V/128) * H * 128
+ *   bytes (0 for invalid sizes).
+ * nfq_lm_head_pack_weights: one kernel on `stream` that writes w_packed from w
+ *   (device pointers, 16-byte aligned, no overlap).  Done once per weight;
+ *   errors as for the calls above (NFQ_ERR_WORKSPACE if packed_bytes is short).
+ * nfq_lm_head_fp8_argmax_packed: nfq_lm_head_fp8_argmax with the weight given
+ *   in the packed layout; identical results.
+ */
+size_t nfq_lm_head_packed_bytes(int V, int H);
+
+int nfq_lm_head_pack_weights(const uint8_t *w, int V, int H, uint8_t *w_packed,
+                             size_t packed_bytes, void *stream);
+
+int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packed,
+                                  const float *w_scales, int V, int S, int32_t *tokens_out,
+                                  float *max_logit_out, int32_t *shard_idx_out,
+                                  float *shard_val_out, void *workspace, size_t ws_bytes,
+                                  void *stream);
+
+/*
  * Reads the current device's error word that kernels set when a bounded wait
  * expires (bit 0: stage 1, bit 1: stage 2).  SYNCHRONISES the current device.
  * Returns NFQ_OK when clear, NFQ_ERR_TIMEOUT when set (and clears it when
  * `clear` != 0), NFQ_ERR_CUDA if the device cannot be read.
  */
 int nfq_device_error(int clear);
+
+/*
+ * Tuning hooks (process-wide, not thread-safe; for benchmarks and tests).
+ * nfq_stage1_plan: the stage-1 launch plan for (T, H, k) on a GPU with
+ *   num_sms SMs: out6 = {cluster CTAs per row, 16-byte vectors per thread,
+ *   active consumer threads, block threads, ring slots, shared bytes}.
+ * nfq_stage1_tune: force the cluster size, vectors per thread and ring slots
+ *   of later stage-1 launches (0 = automatic; invalid choices fall back).
+ * nfq_lm_head_small_batch: 1 (default) runs batches of at most 64 tokens on the
+ *   token-major kernel; 0 forces the weight-major kernel for every batch size.
+ */
+int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out6);
+void nfq_stage1_tune(int cluster, int vpt, int slots);
+void nfq_lm_head_small_batch(int enabled);
 
 #ifdef __cplusplus
 }

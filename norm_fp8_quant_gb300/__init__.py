@@ -70,12 +70,20 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_fp8_argmax.argtypes = [ctypes.POINTER(QuantAct), _P, _P, ctypes.c_int,
                                            ctypes.c_int, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
     lib.nfq_lm_head_fp8_argmax.restype = ctypes.c_int
+    lib.nfq_lm_head_packed_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.nfq_lm_head_packed_bytes.restype = ctypes.c_size_t
+    lib.nfq_lm_head_pack_weights.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, ctypes.c_size_t, _P]
+    lib.nfq_lm_head_pack_weights.restype = ctypes.c_int
+    lib.nfq_lm_head_fp8_argmax_packed.argtypes = lib.nfq_lm_head_fp8_argmax.argtypes
+    lib.nfq_lm_head_fp8_argmax_packed.restype = ctypes.c_int
     lib.nfq_device_error.argtypes = [ctypes.c_int]
     lib.nfq_device_error.restype = ctypes.c_int
     lib.nfq_stage1_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_stage1_plan.restype = ctypes.c_int
     lib.nfq_stage1_tune.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.nfq_stage1_tune.restype = None
+    lib.nfq_lm_head_small_batch.argtypes = [ctypes.c_int]
+    lib.nfq_lm_head_small_batch.restype = None
     _lib = lib
     return lib
 
@@ -153,17 +161,58 @@ def lm_head_workspace(T: int, S: int, device, stream=None):
     return ws
 
 
+def pack_lm_head_weights(w, stream=None):
+    """Pack a row-major [V][H] e4m3 LM-head weight into the streaming layout
+    (tile-contiguous, pre-swizzled 16 KB blocks); returns a PackedWeight."""
+    import torch
+    _need_cuda(w)
+    V, H = w.shape
+    n = int(load().nfq_lm_head_packed_bytes(V, H))
+    if n == 0:
+        raise ValueError("invalid LM-head weight shape")
+    out = torch.empty(n, dtype=torch.uint8, device=w.device)
+    with torch.cuda.device(w.device):
+        _check(load().nfq_lm_head_pack_weights(_ptr(w), V, H, _ptr(out), n, _stream_ptr(stream)),
+               "nfq_lm_head_pack_weights")
+    return PackedWeight(out, V, H)
+
+
+class PackedWeight:
+    """LM-head weight in the packed streaming layout (see nfq_lm_head_pack_weights)."""
+
+    def __init__(self, data, V: int, H: int):
+        self.data, self.V, self.H = data, V, H
+        self.device = data.device
+        self.dtype = data.dtype
+
+    @property
+    def shape(self):
+        return (self.V, self.H)
+
+    @property
+    def is_cuda(self):
+        return self.data.is_cuda
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return self.data.data_ptr()
+
+
 def lm_head_fp8_argmax(codes, scales, w, w_scales, S: int, workspace=None,
                        tokens_out=None, want_max: bool = False, want_shards: bool = False,
                        stream=None):
     """Greedy draft token per row of the packed FP8 activation against the
     block-scaled FP8 LM head, via a vocab-sharded argmax (ties -> lowest id).
+    `w` is the row-major e4m3 [V][H] weight or a PackedWeight.
 
     Returns tokens, or (tokens, max_logit, shard_idx, shard_val) with the
     optional ones None unless requested."""
     import torch
     T, H = codes.shape
     V = w.shape[0]
+    packed = isinstance(w, PackedWeight)
     _need_cuda(codes, scales, w, w_scales)
     if codes.dtype != torch.uint8 or w.dtype != torch.uint8:
         raise ValueError("codes and w must be uint8 e4m3 patterns")
@@ -177,10 +226,10 @@ def lm_head_fp8_argmax(codes, scales, w, w_scales, S: int, workspace=None,
     sval = torch.empty((S, T), dtype=torch.float32, device=dev) if want_shards else None
     q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
     opt = lambda t: ctypes.c_void_p(None) if t is None else _ptr(t)
+    fn = load().nfq_lm_head_fp8_argmax_packed if packed else load().nfq_lm_head_fp8_argmax
     with torch.cuda.device(dev):
-        st = load().nfq_lm_head_fp8_argmax(ctypes.byref(q), _ptr(w), _ptr(w_scales), V, S,
-                                           _ptr(tokens), opt(mx), opt(sidx), opt(sval),
-                                           _ptr(ws), ws.numel(), _stream_ptr(stream))
+        st = fn(ctypes.byref(q), _ptr(w), _ptr(w_scales), V, S, _ptr(tokens), opt(mx), opt(sidx),
+                opt(sval), _ptr(ws), ws.numel(), _stream_ptr(stream))
     _check(st, "nfq_lm_head_fp8_argmax")
     if want_max or want_shards:
         return tokens, mx, sidx, sval
@@ -202,3 +251,9 @@ def stage1_plan(T: int, H: int, k: int, num_sms: int = 152):
 def stage1_tune(cluster: int = 0, vpt: int = 0, slots: int = 0):
     """Override the stage-1 launch plan (0 = automatic); for tuning sweeps."""
     load().nfq_stage1_tune(cluster, vpt, slots)
+
+
+def lm_head_small_batch(enabled: bool = True):
+    """Choose the LM-head kernel family for batches of at most 64 tokens: the
+    token-major small-batch kernel (default) or the weight-major kernel."""
+    load().nfq_lm_head_small_batch(1 if enabled else 0)

@@ -129,10 +129,14 @@ int nfq_lm_head_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
   return map_cuda(cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
 }
 
-int nfq_lm_head_fp8_argmax(const nfq_quant_act *a, const uint8_t *w, const float *w_scales,
-                           int V, int S, int32_t *tokens_out, float *max_logit_out,
-                           int32_t *shard_idx_out, float *shard_val_out, void *workspace,
-                           size_t ws_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+int lm_head_common(const nfq_quant_act *a, const uint8_t *w, bool packed, const float *w_scales,
+                   int V, int S, int32_t *tokens_out, float *max_logit_out,
+                   int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                   size_t ws_bytes, void *stream) {
   if (!a || !w || !w_scales || !tokens_out) return NFQ_ERR_NULL;
   if (!a->codes || !a->scales) return NFQ_ERR_NULL;
   const int T = a->tokens, H = a->hidden;
@@ -154,6 +158,7 @@ int nfq_lm_head_fp8_argmax(const nfq_quant_act *a, const uint8_t *w, const float
   Stage2Params p;
   std::memset(&p, 0, sizeof(p));
   p.w_scales = w_scales;
+  p.w_packed = packed ? w : nullptr;
   p.shard_idx_out = shard_idx_out;
   p.shard_val_out = shard_val_out;
   p.keys = static_cast<unsigned long long *>(workspace);
@@ -183,6 +188,44 @@ int nfq_lm_head_fp8_argmax(const nfq_quant_act *a, const uint8_t *w, const float
   return NFQ_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int nfq_lm_head_fp8_argmax(const nfq_quant_act *a, const uint8_t *w, const float *w_scales,
+                           int V, int S, int32_t *tokens_out, float *max_logit_out,
+                           int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                           size_t ws_bytes, void *stream) {
+  return lm_head_common(a, w, false, w_scales, V, S, tokens_out, max_logit_out, shard_idx_out,
+                        shard_val_out, workspace, ws_bytes, stream);
+}
+
+size_t nfq_lm_head_packed_bytes(int V, int H) {
+  if (V < 1 || H < 128 || H % 128 != 0) return 0;
+  return packed_weight_bytes(V, H);
+}
+
+int nfq_lm_head_pack_weights(const uint8_t *w, int V, int H, uint8_t *w_packed,
+                             size_t packed_bytes, void *stream) {
+  if (!w || !w_packed) return NFQ_ERR_NULL;
+  if (V < 1 || H < 128 || H > 16384 || H % 128 != 0) return NFQ_ERR_SHAPE;
+  if (packed_bytes < packed_weight_bytes(V, H)) return NFQ_ERR_WORKSPACE;
+  if (!aligned16(w) || !aligned16(w_packed)) return NFQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_pack_weights(w, V, H, w_packed, static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packed,
+                                  const float *w_scales, int V, int S, int32_t *tokens_out,
+                                  float *max_logit_out, int32_t *shard_idx_out,
+                                  float *shard_val_out, void *workspace, size_t ws_bytes,
+                                  void *stream) {
+  return lm_head_common(a, w_packed, true, w_scales, V, S, tokens_out, max_logit_out,
+                        shard_idx_out, shard_val_out, workspace, ws_bytes, stream);
+}
+
 int nfq_device_error(int clear) {
   unsigned v = 0;
   if (cudaDeviceSynchronize() != cudaSuccess) return NFQ_ERR_CUDA;
@@ -203,5 +246,9 @@ int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out6) {
 }
 
 void nfq_stage1_tune(int cluster, int vpt, int slots) { stage1_set_tuning(cluster, vpt, slots); }
+
+// Selects the LM-head kernel family for T <= 64: 1 (default) the token-major
+// small-batch kernel, 0 the weight-major kernel used for larger batches.
+void nfq_lm_head_small_batch(int enabled) { stage2_set_small(enabled); }
 
 }  // extern "C"

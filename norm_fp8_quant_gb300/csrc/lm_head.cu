@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "nfq_internal.h"
 #include "ptx.cuh"
@@ -43,12 +44,16 @@ constexpr int kErrBitStage2 = 2;
 constexpr int kMaxStages = 16;
 constexpr int kKeyStride = 256;   // keys per shard in the workspace
 constexpr uint32_t kWTileBytes = 128 * 128;
+#ifndef NFQ_TMEM_BUFS
+#define NFQ_TMEM_BUFS 16
+#endif
+constexpr int kMaxTmemBufs = NFQ_TMEM_BUFS;   // accumulators in flight (TMEM holds 512 columns)
 
 struct Stage2Smem {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t tfull[4];
-  uint64_t tempty[4];
+  uint64_t tfull[16];
+  uint64_t tempty[16];
   uint32_t tmem_base;
   int abort;
   int last;
@@ -71,13 +76,13 @@ __device__ __forceinline__ int32_t key_index(unsigned long long key) {
   return (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
 
-template <int NCOL, int EPI>
+template <int NCOL, int EPI, bool kPacked>
 __global__ void __launch_bounds__(128 * EPI + 64, 1)
     lm_head_argmax_kernel(const __grid_constant__ CUtensorMap tmap_w,
                           const __grid_constant__ CUtensorMap tmap_a, const Stage2Params p,
                           int nstage) {
   constexpr int N = NCOL * EPI;                  // MMA N (token columns)
-  constexpr int NBUF = (512 / N) < 4 ? (512 / N) : 4;
+  constexpr int NBUF = (512 / N) < kMaxTmemBufs ? (512 / N) : kMaxTmemBufs;
   constexpr int TM_COLS_RAW = NBUF * N;
   constexpr uint32_t TM_COLS = TM_COLS_RAW <= 32 ? 32 : TM_COLS_RAW <= 64 ? 64
                                : TM_COLS_RAW <= 128 ? 128 : TM_COLS_RAW <= 256 ? 256 : 512;
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
   }
   if (warp == 4 * EPI) {
     if (lane == 0) {
-      prefetch_tmap(&tmap_w);
+      if constexpr (!kPacked) prefetch_tmap(&tmap_w);
       prefetch_tmap(&tmap_a);
     }
   }
@@ -157,8 +162,14 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
         if (lane == 0) {
           const uint32_t fb = smem_u32(&sh->full[s]);
           mbar_arrive_expect_tx(fb, kWTileBytes + kATileBytes);
-          tma_load_2d(smem_u32(w_tiles + (size_t)s * kWTileBytes), &tmap_w, kb * 128, vt * 128,
-                      fb, pol_w);
+          if constexpr (kPacked) {
+            // one contiguous, already swizzled 16 KB block per (tile, K block)
+            bulk_g2s(smem_u32(w_tiles + (size_t)s * kWTileBytes),
+                     p.w_packed + ((size_t)vt * G + kb) * kWTileBytes, kWTileBytes, fb, pol_w);
+          } else {
+            tma_load_2d(smem_u32(w_tiles + (size_t)s * kWTileBytes), &tmap_w, kb * 128, vt * 128,
+                        fb, pol_w);
+          }
           tma_load_2d(smem_u32(a_tiles + (size_t)s * kATileBytes), &tmap_a, kb * 128, 0, fb,
                       pol_a);
         }
@@ -248,46 +259,110 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
       if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[kb_i % NBUF]));
     };
 
-    for (int vt = t_begin; vt < t_end && ok; ++vt) {
-      const float *swrow = p.w_scales + (size_t)vt * G;
-      float acc[NCOL];
+    // acc[j] += P[j] * (sw * sa[kb][grp*NCOL + j]) for one K block
+    auto promote = [&](float (&acc)[NCOL], const uint32_t (&r)[NCOL], int kb, float swv) {
+      const float *sak = sa_s + (size_t)kb * N + grp * NCOL;
 #pragma unroll
-      for (int j = 0; j < NCOL; ++j) acc[j] = 0.0f;
-      // acc += P * (sw * sa) for K block kb
-      auto promote = [&](const uint32_t (&r)[NCOL], int kb, float swv) {
-        const float *sak = sa_s + (size_t)kb * N + grp * NCOL;
+      for (int j = 0; j < NCOL; j += 4) {
+        const float4 sa4 = *reinterpret_cast<const float4 *>(sak + j);
+        acc[j + 0] = fmaf(__uint_as_float(r[j + 0]), swv * sa4.x, acc[j + 0]);
+        acc[j + 1] = fmaf(__uint_as_float(r[j + 1]), swv * sa4.y, acc[j + 1]);
+        acc[j + 2] = fmaf(__uint_as_float(r[j + 2]), swv * sa4.z, acc[j + 2]);
+        acc[j + 3] = fmaf(__uint_as_float(r[j + 3]), swv * sa4.w, acc[j + 3]);
+      }
+    };
+    // per-warp argmax over its 32 rows for every token column, merged per shard
+    auto argmax_tile = [&](const float (&acc)[NCOL], int vt) {
+      const int row0 = vt * 128 + quad * 32;
+      const int v = row0 + lane;
+      const bool valid = v < p.V;
+      const int my_shard = valid ? v / p.shard_width : -1;
+      const int last_row = min(row0 + 31, p.V - 1);
+      if (row0 < p.V) {
+        const int s_lo = row0 / p.shard_width;
+        const int s_hi = last_row / p.shard_width;
+        for (int s = s_lo; s <= s_hi; ++s) {
+          const bool mine = (my_shard == s);
 #pragma unroll
-        for (int j = 0; j < NCOL; j += 4) {
-          const float4 sa4 = *reinterpret_cast<const float4 *>(sak + j);
-          acc[j + 0] = fmaf(__uint_as_float(r[j + 0]), swv * sa4.x, acc[j + 0]);
-          acc[j + 1] = fmaf(__uint_as_float(r[j + 1]), swv * sa4.y, acc[j + 1]);
-          acc[j + 2] = fmaf(__uint_as_float(r[j + 2]), swv * sa4.z, acc[j + 2]);
-          acc[j + 3] = fmaf(__uint_as_float(r[j + 3]), swv * sa4.w, acc[j + 3]);
+          for (int j = 0; j < NCOL; ++j) {
+            const float val = mine ? acc[j] : -INFINITY;
+            float mx = val;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const unsigned ball = __ballot_sync(0xffffffffu, mine && val == mx);
+            const int n = grp * NCOL + j;
+            if (lane == (j & 31) && n < p.T && ball != 0u) {
+              const uint32_t idx = (uint32_t)(row0 + __ffs((int)ball) - 1);
+              atomicMax(&p.keys[(size_t)s * kKeyStride + n], pack_key(mx, idx));
+            }
+          }
+        }
+      }
+    };
+
+    // double-buffered TMEM reads when two register sets fit next to the accumulators
+    constexpr bool kPipe = NCOL <= 32 && (3 * NCOL + 40) * (128 * EPI + 64) <= 65536;
+    static_assert(kPipe || NCOL % 32 == 0, "unpipelined epilogue reads 32 columns at a time");
+    if constexpr (kPipe) {
+      // One flat pipeline over every (tile, K block) of this CTA: the TMEM read
+      // of step q+1 is in flight while step q is promoted (and, at a tile's
+      // last K block, while the tile's argmax runs).  The weight-scale row of
+      // a tile sits in lane registers (lane l holds sw[32 i + l]) and is
+      // broadcast with shuffles.
+      const int n_steps = (t_end - t_begin) * G;
+      auto load_sw = [&](int vt, float (&r)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int kk = 32 * i + lane;
+          r[i] = (vt < t_end && kk < G) ? __ldg(p.w_scales + (size_t)vt * G + kk) : 0.0f;
         }
       };
-
-      if constexpr (NCOL <= 32) {
-        // two register sets: block kb+1 is read from TMEM while kb is promoted
-        uint32_t ra[NCOL], rb[NCOL];
-        if (!issue(ra, kbi)) { ok = false; break; }
-        release(ra, kbi);
-        float sw_cur = __ldg(swrow);
-        for (int kb = 0; kb < G; kb += 2) {
-          const uint32_t k1 = kbi + (uint32_t)kb + 1u, k2 = k1 + 1u;
-          const bool more1 = kb + 1 < G;
-          float sw_nxt = more1 ? __ldg(swrow + kb + 1) : 0.0f;
-          if (more1 && !issue(rb, k1)) { ok = false; break; }
-          promote(ra, kb, sw_cur);
-          if (!more1) break;
-          release(rb, k1);
-          const bool more2 = kb + 2 < G;
-          sw_cur = more2 ? __ldg(swrow + kb + 2) : 0.0f;
-          if (more2 && !issue(ra, k2)) { ok = false; break; }
-          promote(rb, kb + 1, sw_nxt);
-          if (more2) release(ra, k2);
+      auto sw_of = [&](const float (&r)[4], int kb) {
+        const float src = kb < 32 ? r[0] : kb < 64 ? r[1] : kb < 96 ? r[2] : r[3];
+        return __shfl_sync(0xffffffffu, src, kb & 31);
+      };
+      float acc[NCOL];
+      float swc[4], swn[4];
+      uint32_t ra[NCOL], rb[NCOL];
+      int vt = t_begin, kb = 0;
+      load_sw(vt, swc);
+      load_sw(vt + 1, swn);
+      if (n_steps > 0) {
+        if (!issue(ra, 0)) ok = false;
+        if (ok) release(ra, 0);
+      }
+      // one step: promote `cur` (step q), with step q+1 already issued into `nxt`
+      auto step = [&](uint32_t (&cur)[NCOL], uint32_t (&nxt)[NCOL], int q) -> bool {
+        const bool more = q + 1 < n_steps;
+        if (more && !issue(nxt, (uint32_t)(q + 1))) return false;
+        if (kb == 0) {
+#pragma unroll
+          for (int j = 0; j < NCOL; ++j) acc[j] = 0.0f;
         }
-        kbi += (uint32_t)G;
-      } else {
+        promote(acc, cur, kb, sw_of(swc, kb));
+        if (kb == G - 1) {
+          argmax_tile(acc, vt);
+          ++vt;
+          kb = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) swc[i] = swn[i];
+          load_sw(vt + 1, swn);
+        } else {
+          ++kb;
+        }
+        if (more) release(nxt, (uint32_t)(q + 1));
+        return true;
+      };
+      for (int q = 0; q < n_steps && ok; q += 2) {
+        if (!step(ra, rb, q)) { ok = false; break; }
+        if (q + 1 < n_steps && !step(rb, ra, q + 1)) { ok = false; break; }
+      }
+    } else {
+      for (int vt = t_begin; vt < t_end && ok; ++vt) {
+        const float *swrow = p.w_scales + (size_t)vt * G;
+        float acc[NCOL];
+#pragma unroll
+        for (int j = 0; j < NCOL; ++j) acc[j] = 0.0f;
         // wide column groups: 32 columns at a time to bound register use
         for (int kb = 0; kb < G; ++kb, ++kbi) {
           const float swv = __ldg(swrow + kb);
@@ -319,34 +394,8 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
             }
           }
         }
-      }
-      if (!ok) break;
-
-      // per-warp argmax over its 32 rows, per shard present in the warp
-      const int row0 = vt * 128 + quad * 32;
-      const int v = row0 + lane;
-      const bool valid = v < p.V;
-      const int my_shard = valid ? v / p.shard_width : -1;
-      const int last_row = min(row0 + 31, p.V - 1);
-      if (row0 < p.V) {
-        const int s_lo = row0 / p.shard_width;
-        const int s_hi = last_row / p.shard_width;
-        for (int s = s_lo; s <= s_hi; ++s) {
-          const bool mine = (my_shard == s);
-#pragma unroll
-          for (int j = 0; j < NCOL; ++j) {
-            const float val = mine ? acc[j] : -INFINITY;
-            float mx = val;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const unsigned ball = __ballot_sync(0xffffffffu, mine && val == mx);
-            const int n = grp * NCOL + j;
-            if (lane == (j & 31) && n < p.T && ball != 0u) {
-              const uint32_t idx = (uint32_t)(row0 + __ffs((int)ball) - 1);
-              atomicMax(&p.keys[(size_t)s * kKeyStride + n], pack_key(mx, idx));
-            }
-          }
-        }
+        if (!ok) break;
+        argmax_tile(acc, vt);
       }
     }
     __threadfence();
@@ -380,6 +429,319 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
     }
     if (threadIdx.x == 0) *p.counter = 0u;
   }
+}
+
+// ------------------------------------------------------- small token batch --
+//
+// T <= 64 form.  One tcgen05.mma K=32 step costs the same for any M in {64,
+// 128} and N up to 256, so the weight is made the N operand: a tile is 256
+// vocab rows (two 128-row scale blocks), the tokens are the M = 64 operand.
+// Each MMA then consumes 8 KB of weight instead of 4 KB.  The M = 64
+// accumulator puts token r in TMEM lane 32*(r/16) + r%16; a 16x64b load gives
+// every thread one token and 32 of a warp's 64 columns, so the promotion is one
+// multiply per K block (activation scale x weight scale) and 32 FMAs.
+//
+// Warps: 0..15 epilogue (lane quadrant w%4 = tokens 16*(w%4)..+15, column
+// group w/4 = tile columns 64*(w/4)..+63), 16 producer, 17 TMEM + MMA.
+// A CTA streams a contiguous range of 128-row blocks, two per tile (the last
+// tile of a range may hold one).  Two 256-column accumulators in TMEM.
+
+constexpr int kSmallMaxT = 64;
+constexpr int kSmallEpiWarps = 16;
+constexpr uint32_t kSmallATileBytes = 64 * 128;
+constexpr uint32_t kSmallStageBytes = 2 * kWTileBytes + kSmallATileBytes;   // 40 KB
+
+struct SmallSmem {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  int abort;
+  int last;
+};
+
+// After every CTA has merged its keys: the last CTA to finish turns the keys
+// into outputs and returns the workspace to zero.  All threads call this.
+__device__ __forceinline__ void finish_launch(const Stage2Params &p, int *last_flag) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.counter, 1u);
+    *last_flag = (prev == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*last_flag) {
+    __threadfence();
+    for (int n = (int)threadIdx.x; n < p.T; n += (int)blockDim.x) {
+      unsigned long long best = 0ull;
+      for (int s = 0; s < p.S; ++s) {
+        const unsigned long long k = atomicExch(&p.keys[(size_t)s * kKeyStride + n], 0ull);
+        if (p.shard_idx_out) p.shard_idx_out[(size_t)s * p.T_total + p.tok0 + n] = key_index(k);
+        if (p.shard_val_out) p.shard_val_out[(size_t)s * p.T_total + p.tok0 + n] = key_value(k);
+        if (k > best) best = k;
+      }
+      p.tokens_out[n] = key_index(best);
+      if (p.max_logit_out) p.max_logit_out[n] = key_value(best);
+    }
+    if (threadIdx.x == 0) *p.counter = 0u;
+  }
+}
+
+template <bool kPacked>
+__global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
+    lm_head_small_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                         const __grid_constant__ CUtensorMap tmap_a, const Stage2Params p,
+                         int nstage) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  const int G = p.G;
+  float *sa_s = reinterpret_cast<float *>(smem + (size_t)nstage * kSmallStageBytes);  // [G][64]
+  SmallSmem *sh = reinterpret_cast<SmallSmem *>(sa_s + (size_t)G * kSmallMaxT);
+  volatile int *abort_flag = &sh->abort;
+
+  const int warp = (int)(threadIdx.x / 32);
+  const int lane = (int)(threadIdx.x % 32);
+  constexpr int kProducer = kSmallEpiWarps, kMma = kSmallEpiWarps + 1;
+
+  // contiguous range of 128-row blocks, processed two per tile
+  const int b_begin = (int)(((long)blockIdx.x * p.n_vtiles) / gridDim.x);
+  const int b_end = (int)(((long)(blockIdx.x + 1) * p.n_vtiles) / gridDim.x);
+  const int n_tiles = (b_end - b_begin + 1) / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh->tfull[b]), 1);
+      mbar_init(smem_u32(&sh->tempty[b]), kSmallEpiWarps);
+    }
+    sh->abort = 0;
+    sh->last = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kProducer && lane == 0) {
+    if constexpr (!kPacked) prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_a);
+  }
+  if (warp == kMma) {
+    tmem_alloc(smem_u32(&sh->tmem_base), 512);
+    tmem_relinquish();
+  }
+  for (int i = (int)threadIdx.x; i < G * kSmallMaxT; i += (int)blockDim.x) {
+    const int kb = i / kSmallMaxT, n = i % kSmallMaxT;
+    sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+
+  if (warp == kProducer) {
+    // -------------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      const int blk0 = b_begin + 2 * ti;
+      const int nb = (blk0 + 1 < b_end) ? 2 : 1;
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *st = smem + (size_t)s * kSmallStageBytes;
+          const uint32_t fb = smem_u32(&sh->full[s]);
+          mbar_arrive_expect_tx(fb, (uint32_t)nb * kWTileBytes + kSmallATileBytes);
+          for (int h = 0; h < nb; ++h) {
+            if constexpr (kPacked) {
+              bulk_g2s(smem_u32(st + h * kWTileBytes),
+                       p.w_packed + ((size_t)(blk0 + h) * G + kb) * kWTileBytes, kWTileBytes, fb,
+                       pol_w);
+            } else {
+              tma_load_2d(smem_u32(st + h * kWTileBytes), &tmap_w, kb * 128, (blk0 + h) * 128, fb,
+                          pol_w);
+            }
+          }
+          tma_load_2d(smem_u32(st + 2 * kWTileBytes), &tmap_a, kb * 128, 0, fb, pol_a);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      const uint32_t issued = it;
+      const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
+      for (uint32_t j = first; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kMma) {
+    // ------------------------------------------------------------------- MMA --
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      const int blk0 = b_begin + 2 * ti;
+      const int nb = (blk0 + 1 < b_end) ? 2 : 1;
+      const uint32_t idesc = idesc_e4m3_f32(64, (uint32_t)(nb * 128));
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        const uint32_t b = it & 1u;
+        const uint32_t bph = (it >> 1) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->tempty[b]), bph ^ 1u, abort_flag, p.err, kErrBitStage2) &&
+                mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint8_t *st = smem + (size_t)s * kSmallStageBytes;
+          const uint32_t w_addr = smem_u32(st);
+          const uint32_t a_addr = smem_u32(st + 2 * kWTileBytes);
+          const uint32_t d_tmem = tmem_base + b * 256u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(w_addr + kk * 32),
+                   idesc, kk > 0 ? 1u : 0u);
+          mma_commit(smem_u32(&sh->empty[s]));
+          mma_commit(smem_u32(&sh->tfull[b]));
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && it > 0) {
+      const uint32_t last = it - 1;
+      mbar_wait_drain(smem_u32(&sh->tfull[last & 1u]), (last >> 1) & 1u);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue --
+    const int q = warp & 3;                        // tokens 16q .. 16q+15
+    const int g = warp >> 2;                       // tile columns 64g .. 64g+63
+    const int tok = 16 * q + (lane >> 2) + 8 * (lane & 1);
+    const int colpar = (lane >> 1) & 1;
+    const bool quad_active = 16 * q < p.T;
+    const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      const int blk0 = b_begin + 2 * ti;
+      const int nb = (blk0 + 1 < b_end) ? 2 : 1;
+      const bool active = quad_active && (g < 2 * nb);
+      const int blk = blk0 + (g >> 1);             // the 128-row scale block of this group
+      // this tile's weight-scale row, spread over the lanes (lane l: sw[32i + l])
+      float swr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kk = 32 * i + lane;
+        swr[i] = (active && kk < G) ? __ldg(p.w_scales + (size_t)blk * G + kk) : 0.0f;
+      }
+      float acc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const uint32_t b = it & 1u;
+        const bool got = mbar_wait(smem_u32(&sh->tfull[b]), (it >> 1) & 1u, abort_flag, p.err,
+                                   kErrBitStage2);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float src = kb < 32 ? swr[0] : kb < 64 ? swr[1] : kb < 96 ? swr[2] : swr[3];
+        const float swv = __shfl_sync(0xffffffffu, src, kb & 31);
+        uint32_t r[32];
+        if (active) {
+          tmem_ld_16x64b_x32(taddr0 + b * 256u, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+        if (active) {
+          const float sc = sa_s[kb * kSmallMaxT + tok] * swv;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(r[j]), sc, acc[j]);
+        }
+      }
+      if (!ok) break;
+      if (!active) continue;
+
+      // argmax over this thread's 32 columns (ascending rows), then merge
+      const int row0 = blk0 * 128 + 64 * g;          // first row of the group
+      const int last_row = min(row0 + 63, p.V - 1);
+      const bool tok_ok = tok < p.T;
+      if (row0 / p.shard_width == last_row / p.shard_width) {
+        // the whole group is one shard: thread max, then the partner lane
+        float best = -INFINITY;
+        int bi = -1;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int v = row0 + 2 * j + colpar;
+          if (v < p.V && (bi < 0 || acc[j] > best)) {
+            best = acc[j];
+            bi = v;
+          }
+        }
+        const float ob = __shfl_xor_sync(0xffffffffu, best, 2);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, 2);
+        if (oi >= 0 && (bi < 0 || ob > best || (ob == best && oi < bi))) {
+          best = ob;
+          bi = oi;
+        }
+        if ((lane & 2) == 0 && tok_ok && bi >= 0)
+          atomicMax(&p.keys[(size_t)(row0 / p.shard_width) * kKeyStride + tok],
+                    pack_key(best, (uint32_t)bi));
+      } else {
+        // shard boundaries inside the group: flush at every shard change
+        float best = -INFINITY;
+        int bi = -1, cur = -1;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int v = row0 + 2 * j + colpar;
+          if (v >= p.V) break;
+          const int sv = v / p.shard_width;
+          if (sv != cur) {
+            if (bi >= 0 && tok_ok)
+              atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+            cur = sv;
+            bi = -1;
+          }
+          if (bi < 0 || acc[j] > best) {
+            best = acc[j];
+            bi = v;
+          }
+        }
+        if (bi >= 0 && tok_ok)
+          atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+      }
+    }
+    __threadfence();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMma) tmem_dealloc(tmem_base, 512);
+  finish_launch(p, &sh->last);
 }
 
 // ------------------------------------------------------------------- host --
@@ -416,12 +778,14 @@ bool encode_u8_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t col
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NCOL, int EPI>
+template <int NCOL, int EPI, bool kPacked>
 cudaError_t launch_cfg(const Stage2Params &p, const void *act_codes, const void *w, int num_sms,
                        cudaStream_t stream) {
   constexpr int N = NCOL * EPI;
   CUtensorMap tw, ta;
-  if (!encode_u8_map(&tw, w, (uint64_t)p.V, (uint64_t)p.H, 128)) return cudaErrorInvalidValue;
+  std::memset(&tw, 0, sizeof(tw));
+  if (!kPacked && !encode_u8_map(&tw, w, (uint64_t)p.V, (uint64_t)p.H, 128))
+    return cudaErrorInvalidValue;
   if (!encode_u8_map(&ta, act_codes, (uint64_t)p.T, (uint64_t)p.H, (uint32_t)N))
     return cudaErrorInvalidValue;
   const size_t fixed = 1024 /*align pad*/ + (size_t)p.G * N * 4 + sizeof(Stage2Smem) + 64;
@@ -431,7 +795,7 @@ cudaError_t launch_cfg(const Stage2Params &p, const void *act_codes, const void 
   if (nstage > 12) nstage = 12;
   if (nstage < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)nstage * per_stage;
-  auto kern = lm_head_argmax_kernel<NCOL, EPI>;
+  auto kern = lm_head_argmax_kernel<NCOL, EPI, kPacked>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -440,19 +804,90 @@ cudaError_t launch_cfg(const Stage2Params &p, const void *act_codes, const void 
   return cudaGetLastError();
 }
 
+bool g_small_enabled = true;
+
+template <bool kPacked>
+cudaError_t launch_by_tokens(const Stage2Params &p, const void *act_codes, const void *w,
+                             int num_sms, cudaStream_t stream) {
+  if (p.T <= 16) return launch_cfg<16, 1, kPacked>(p, act_codes, w, num_sms, stream);
+  if (p.T <= 32) return launch_cfg<16, 2, kPacked>(p, act_codes, w, num_sms, stream);
+  if (p.T <= 64) return launch_cfg<16, 4, kPacked>(p, act_codes, w, num_sms, stream);
+  if (p.T <= 128) return launch_cfg<32, 4, kPacked>(p, act_codes, w, num_sms, stream);
+  return launch_cfg<128, 2, kPacked>(p, act_codes, w, num_sms, stream);
+}
+
+// Re-lays the row-major [V][H] e4m3 weight into [ceil(V/128)][H/128] blocks of
+// 128 rows x 128 bytes, each row's 16-byte chunks permuted by the 128-byte
+// swizzle (chunk c of row r stored at chunk c ^ (r mod 8)); rows past V are 0.
+__global__ void __launch_bounds__(256) pack_weights_kernel(const uint8_t *__restrict__ w, int V,
+                                                           int H, uint8_t *__restrict__ out) {
+  const int G = H / 128;
+  const size_t block = blockIdx.x;           // vt * G + kb
+  const int vt = (int)(block / (size_t)G), kb = (int)(block % (size_t)G);
+  uint4 *dst = reinterpret_cast<uint4 *>(out + block * kWTileBytes);
+  for (int i = (int)threadIdx.x; i < 1024; i += (int)blockDim.x) {
+    const int r = i >> 3, c = i & 7;
+    const int row = vt * 128 + r;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < V)
+      v = *reinterpret_cast<const uint4 *>(w + (size_t)row * H + (size_t)kb * 128 + c * 16);
+    dst[r * 8 + (c ^ (r & 7))] = v;
+  }
+}
+
 }  // namespace
 
 size_t stage2_workspace_bytes(int S) {
   return (size_t)S * kKeyStride * sizeof(unsigned long long) + 16u;
 }
 
+template <bool kPacked>
+cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const void *w,
+                         int num_sms, cudaStream_t stream) {
+  CUtensorMap tw, ta;
+  std::memset(&tw, 0, sizeof(tw));
+  if (!kPacked && !encode_u8_map(&tw, w, (uint64_t)p.V, (uint64_t)p.H, 128))
+    return cudaErrorInvalidValue;
+  if (!encode_u8_map(&ta, act_codes, (uint64_t)p.T, (uint64_t)p.H, (uint32_t)kSmallMaxT))
+    return cudaErrorInvalidValue;
+  const size_t fixed =
+      1024 /*align pad*/ + (size_t)p.G * kSmallMaxT * 4 + sizeof(SmallSmem) + 64;
+  const size_t budget = 227u * 1024u;
+  int nstage = (int)((budget - fixed) / kSmallStageBytes);
+  if (nstage > 8) nstage = 8;
+  if (nstage < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + (size_t)nstage * kSmallStageBytes;
+  auto kern = lm_head_small_kernel<kPacked>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = num_sms < p.n_vtiles ? num_sms : p.n_vtiles;
+  kern<<<grid, kSmallEpiWarps * 32 + 64, smem, stream>>>(tw, ta, p, nstage);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const void *w,
                           int num_sms, cudaStream_t stream) {
-  if (p.T <= 16) return launch_cfg<16, 1>(p, act_codes, w, num_sms, stream);
-  if (p.T <= 32) return launch_cfg<16, 2>(p, act_codes, w, num_sms, stream);
-  if (p.T <= 64) return launch_cfg<32, 2>(p, act_codes, w, num_sms, stream);
-  if (p.T <= 128) return launch_cfg<32, 4>(p, act_codes, w, num_sms, stream);
-  return launch_cfg<128, 2>(p, act_codes, w, num_sms, stream);
+  if (p.T <= kSmallMaxT && g_small_enabled) {
+    if (p.w_packed) return launch_small<true>(p, act_codes, w, num_sms, stream);
+    return launch_small<false>(p, act_codes, w, num_sms, stream);
+  }
+  if (p.w_packed) return launch_by_tokens<true>(p, act_codes, w, num_sms, stream);
+  return launch_by_tokens<false>(p, act_codes, w, num_sms, stream);
+}
+
+void stage2_set_small(int enabled) { g_small_enabled = enabled != 0; }
+
+size_t packed_weight_bytes(int V, int H) {
+  return (size_t)((V + 127) / 128) * (size_t)(H / 128) * kWTileBytes;
+}
+
+cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out,
+                                cudaStream_t stream) {
+  const size_t blocks = (size_t)((V + 127) / 128) * (size_t)(H / 128);
+  if (blocks == 0 || blocks > 0x7FFFFFFFu) return cudaErrorInvalidValue;
+  pack_weights_kernel<<<(unsigned)blocks, 256, 0, stream>>>(w, V, H, out);
+  return cudaGetLastError();
 }
 
 }  // namespace nfq

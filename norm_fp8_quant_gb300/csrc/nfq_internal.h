@@ -36,6 +36,7 @@ struct Stage2Params {
   const uint8_t *act_codes;   // e4m3 [T][H]   (this launch's token chunk)
   const float *act_scales;    // fp32 [T][G]
   const float *w_scales;      // fp32 [ceil(V/128)][G]
+  const uint8_t *w_packed;    // tile-contiguous weight blocks, or null for row-major [V][H]
   int32_t *tokens_out;        // [T]
   float *max_logit_out;       // [T] or null
   int32_t *shard_idx_out;     // [S][T_total] or null, column offset tok0
@@ -55,5 +56,8 @@ cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes_base, con
                           int num_sms, cudaStream_t stream);
 
 size_t stage2_workspace_bytes(int S);
+void stage2_set_small(int enabled);   // 0: always use the wide-batch kernel (tests, tuning)
+size_t packed_weight_bytes(int V, int H);
+cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out, cudaStream_t stream);
 
 }  // namespace nfq

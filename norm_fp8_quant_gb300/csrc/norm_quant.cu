@@ -37,7 +37,9 @@ namespace nfq {
 namespace {
 
 constexpr int kErrBitStage1 = 1;
-constexpr int kMaxStage1Threads = 288;   // producer warp + up to 256 consumers
+// register budget: up to 2 vectors per thread with 512 consumers (17 warps leave
+// 96 registers a thread), more with 256
+__host__ __device__ constexpr int stage1_max_threads(int vpt) { return vpt <= 2 ? 544 : 288; }
 
 struct RowSums {
   float red[2][32];     // per consumer warp, double-buffered by row parity
@@ -60,7 +62,8 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 }
 
 template <int VPT>
-__global__ void __launch_bounds__(kMaxStage1Threads, 1) reduce_norm_quant_kernel(const Stage1Params p) {
+__global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
+    reduce_norm_quant_kernel(const Stage1Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int E = p.E;
   const uint32_t slot_bytes = (uint32_t)E * 2u;
@@ -291,14 +294,26 @@ size_t stage1_smem_bytes(int nslot, int E) {
   return (size_t)nslot * (size_t)E * 2u + (size_t)nslot * 16u + 32u + sizeof(RowSums) + 16u;
 }
 
-// Vectors per consumer thread for a slice of Gc groups: whole warps with 192..256
-// active threads first, then at least 128, then whole warps, then anything.
-int pick_vpt(int Gc) {
+// Vectors per consumer thread for a slice of Gc groups.  With many rows per CTA
+// (streaming), whole warps of 192..256 threads and the most vectors per thread;
+// with at most one row per CTA (latency-bound), the most threads.
+int pick_vpt(int Gc, bool few_rows) {
+  if (few_rows) {
+    for (int pass = 0; pass < 2; ++pass)
+      for (int v = 1; v <= 8; ++v) {
+        if (Gc % v) continue;
+        const int na = 16 * Gc / v;
+        if (na + 32 > stage1_max_threads(v)) continue;
+        if (pass == 0 && na % 32 != 0) continue;
+        return v;
+      }
+    return 0;
+  }
   for (int pass = 0; pass < 4; ++pass)
     for (int v = 8; v >= 1; --v) {
       if (Gc % v) continue;
       const int na = 16 * Gc / v;
-      if (na > kMaxStage1Threads - 32) continue;
+      if (na + 32 > 288) continue;
       const bool whole = na % 32 == 0;
       if (pass == 0 && !(whole && na >= 192)) continue;
       if (pass == 1 && !(whole && na >= 128)) continue;
@@ -311,21 +326,24 @@ int pick_vpt(int Gc) {
 Stage1Choice choose_stage1(int T, int H, int k, int num_sms) {
   const int G = H / 128;
   Stage1Choice ch{};
-  // cluster split: enough CTAs to cover most SMs when rows are few, and small
-  // enough slices that a CTA of at most 256 consumer threads holds one
+  // one CTA per row slice; a row is split over a cluster only when no single
+  // CTA can hold it (very wide H) or when tuning asks for it
   int C = 0, vpt = 0;
   const int opts[4] = {1, 2, 4, 8};
   for (int c : opts) {
     if (G % c) continue;
     if (g_tune_C > 0 && c != g_tune_C) continue;
-    const int v = (g_tune_vpt > 0 && (G / c) % g_tune_vpt == 0 &&
-                   16 * (G / c) / g_tune_vpt <= kMaxStage1Threads - 32)
-                      ? g_tune_vpt
-                      : pick_vpt(G / c);
+    const bool few = (long)T * c <= (long)num_sms;
+    int v = 0;
+    if (g_tune_vpt > 0 && (G / c) % g_tune_vpt == 0 &&
+        16 * (G / c) / g_tune_vpt + 32 <= stage1_max_threads(g_tune_vpt))
+      v = g_tune_vpt;
+    else
+      v = pick_vpt(G / c, few);
     if (!v) continue;
     C = c;
     vpt = v;
-    if (g_tune_C > 0 || (long)T * c >= (long)num_sms * 3 / 4) break;
+    break;
   }
   if (!C) return ch;   // VPT == 0 signals an unsupported width
   ch.C = C;

@@ -26,50 +26,66 @@ def stage1_ref(w):
     return oracle.reduce_norm_quant(inp["partials"], inp["residual"], inp["norm_w"])
 
 
-def run_gpu(nfq, qa, sa, qw, sw, S, ws=None):
-    out = nfq.lm_head_fp8_argmax(to_dev(qa), to_dev(sa), to_dev(qw), to_dev(sw), S,
+@pytest.fixture(params=["rowmajor", "packed"])
+def layout(request):
+    return request.param
+
+
+@pytest.fixture(params=["small", "wide"])
+def family(request, nfq):
+    """Kernel family for T <= 64: token-major small-batch or weight-major wide."""
+    nfq.lm_head_small_batch(request.param == "small")
+    yield request.param
+    nfq.lm_head_small_batch(True)
+
+
+def run_gpu(nfq, qa, sa, qw, sw, S, ws=None, layout="rowmajor"):
+    w = to_dev(qw)
+    if layout == "packed":
+        w = nfq.pack_lm_head_weights(w)
+    out = nfq.lm_head_fp8_argmax(to_dev(qa), to_dev(sa), w, to_dev(sw), S,
                                  workspace=ws, want_max=True, want_shards=True)
     torch.cuda.synchronize()
     assert nfq.device_error() == 0
     return [None if x is None else x.cpu().numpy() for x in out]
 
 
-def test_stage2_tiny_all_tokens(nfq):
+def test_stage2_tiny_all_tokens(nfq, layout):
     w = synth.workload("tiny")
     ref = stage1_ref(w)
     qw, sw = synth.lm_head_weights(w)
-    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S, layout=layout)
     check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, list(range(w.T)),
                  mx, sidx, sval)
 
 
-def test_stage2_decode_c1_full_vocab(nfq):
+def test_stage2_decode_c1_full_vocab(nfq, layout):
     """T = 1, V = 129280 in 8 shards of 16160 rows: shard boundaries fall inside
     128-row scale blocks and tiles."""
     w = synth.workload("decode_c1")
     ref = stage1_ref(w)
     qw, sw = synth.lm_head_weights(w)
-    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S, layout=layout)
     check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, [0], mx, sidx, sval)
 
 
-def test_stage2_decode_c64_sampled_tokens(nfq):
+def test_stage2_decode_c64_sampled_tokens(nfq, layout, family):
     w = synth.workload("decode_c64")
     ref = stage1_ref(w)
     qw, sw = synth.lm_head_weights(w)
-    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S, layout=layout)
     assert tok.shape == (64,) and np.all((0 <= tok) & (tok < w.V))
     check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, [0, 31, 63], mx, sidx, sval)
 
 
-def test_stage2_tie_stress(nfq):
+def test_stage2_tie_stress(nfq, layout):
     """T = 256, V = 151552, S = 8; 30% of tokens have an exact duplicate maximum
     on either side of a shard boundary: the lower global index must win."""
     w = synth.workload("tie_stress")
     ref = stage1_ref(w)
     qw, sw = synth.lm_head_weights(w)
     expected = synth.plant_ties(w, qw, sw, ref["codes"])
-    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S, layout=layout)
     width = w.V // w.S
     for t, row in expected.items():
         assert tok[t] == row, f"token {t}: {tok[t]} != {row}"
@@ -87,17 +103,17 @@ def test_stage2_tie_stress(nfq):
                                      (64, 1024, 3000, 3), (100, 512, 1536, 6),
                                      (129, 256, 1024, 8), (256, 256, 640, 5),
                                      (300, 256, 512, 2)])
-def test_stage2_edge_shapes(nfq, T, H, V, S):
+def test_stage2_edge_shapes(nfq, T, H, V, S, layout, family):
     """Ragged vocab tails, shard widths below a tile or a warp, every token
     count class (padding inside the MMA N, two warpgroups, 256-token chunks)."""
     w = synth.workload("tiny", T=T, H=H, k=2, V=V, S=S, seed=T + H + V + S)
     ref = stage1_ref(w)
     qw, sw = synth.lm_head_weights(w)
-    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, S)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, S, layout=layout)
     check_stage2(tok, ref["codes"], ref["scales"], qw, sw, S, list(range(T)), mx, sidx, sval)
 
 
-def test_stage2_planted_ties_and_zero_logits(nfq):
+def test_stage2_planted_ties_and_zero_logits(nfq, layout, family):
     """Exact duplicates inside one warp, across warps of a tile, across tiles and
     at the last row; an all-zero activation row makes every logit +-0 and must
     give token 0."""
@@ -114,7 +130,7 @@ def test_stage2_planted_ties_and_zero_logits(nfq):
         row = np.where((qa[t] & 0x7F) == 0, 0, np.where(qa[t] & 0x80, 0xFE, 0x7E)).astype(np.uint8)
         qw[a] = row
         qw[b] = row
-    tok, mx, sidx, sval = run_gpu(nfq, qa, sa, qw, sw, S)
+    tok, mx, sidx, sval = run_gpu(nfq, qa, sa, qw, sw, S, layout=layout)
     for t, (a, b) in pairs.items():
         assert tok[t] == a
     assert tok[5] == 0 and mx[5] == 0.0 and not np.signbit(mx[5])
@@ -136,3 +152,22 @@ def test_stage2_workspace_stays_zero_across_calls(nfq):
             first = out
         for a, b in zip(first, out):
             assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("V,H", [(128, 128), (300, 256), (4096, 1024), (1000, 384)])
+def test_pack_weights_layout(nfq, V, H):
+    """The packed layout: block (vt, kb) at (vt * H/128 + kb) * 16 KB, row r at
+    r * 128, 16-byte chunk c of the row at chunk c ^ (r % 8), zero rows past V."""
+    rng = np.random.default_rng(V + H)
+    w = rng.integers(0, 256, (V, H), dtype=np.uint8)
+    packed = nfq.pack_lm_head_weights(to_dev(w)).data.cpu().numpy()
+    nvt, G = (V + 127) // 128, H // 128
+    assert packed.size == nvt * G * 16384
+    wp = np.zeros((nvt * 128, H), np.uint8)
+    wp[:V] = w
+    blocks = wp.reshape(nvt, 128, G, 8, 16).transpose(0, 2, 1, 3, 4)      # vt, kb, r, c, 16
+    r = np.arange(128)[:, None]
+    c = np.arange(8)[None, :]
+    expect = np.empty_like(blocks)
+    expect[:, :, r, c ^ (r % 8)] = blocks[:, :, r, c]
+    assert np.array_equal(packed, expect.reshape(-1))
