@@ -181,6 +181,31 @@ int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packe
 int nfq_device_error(int clear);
 
 /*
+ * nfq_lm_head_fp8_argmax_noalloc — the same LM head and argmax, for callers
+ * that cannot allocate device memory: code that runs where cudaMalloc is not
+ * allowed or not wanted (inside a host engine that hands out only fixed
+ * buffers, or a decode loop that must not hit the allocator, which may
+ * synchronise the device).  The source pages have no counterpart to this call.
+ *
+ * Instead of a caller workspace it uses a scratch array of 131,088 bytes that
+ * the library keeps in device memory for the life of the process on every GPU
+ * that loads it; calls needing more (more than 64 shards) return
+ * NFQ_ERR_WORKSPACE.  It allocates nothing and frees nothing.  Arguments,
+ * outputs and errors are those of nfq_lm_head_fp8_argmax minus the workspace.
+ * - The first call on a device looks up the array's device address for that
+ *   device (the current one); make that first call before any stream capture.
+ * - Each call clears the part of the array it uses with an asynchronous memset
+ *   on `stream`, then launches the LM head on `stream`.
+ * - All calls on a device share the one array: calls that overlap on the GPU
+ *   (different streams, no ordering between them) race and give wrong results.
+ *   Calls ordered on one stream are safe.
+ */
+int nfq_lm_head_fp8_argmax_noalloc(const nfq_quant_act *a, const uint8_t *w,
+                                   const float *w_scales, int V, int S, int32_t *tokens_out,
+                                   float *max_logit_out, int32_t *shard_idx_out,
+                                   float *shard_val_out, void *stream);
+
+/*
  * Tuning hooks (process-wide, not thread-safe; for benchmarks and tests).
  * nfq_stage1_plan: the stage-1 launch plan for (T, H, k) on a GPU with
  *   num_sms SMs: out6 = {cluster CTAs per row, 16-byte vectors per thread,
