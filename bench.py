@@ -108,6 +108,23 @@ def ncu_traffic(kernel):
         return None
 
 
+# ------------------------------------------------------------- aggregation --
+
+def max_over_ranks(values, world, device):
+    """Element-wise max of per-rank floats (timings) across the process group."""
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def tokens_per_s(world, T, K, ms):
+    """Whole-job draft tokens per second: every rank processed T tokens per step."""
+    return world * T * K / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ clocks --
 
 REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -278,11 +295,7 @@ def run_ours(args, rank, world, local):
     e2e_ms = (time.perf_counter() - c0) * 1e3
     barrier()
 
-    times = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = times.tolist()
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], world, dev)
 
     result = None
     if rank == 0:
@@ -291,7 +304,7 @@ def run_ours(args, rank, world, local):
         b2 = stage2_bytes(T, H, V)
         gbs1 = b1 / (s1_ms * 1e-3) / 1e9
         gbs2 = b2 / (s2_ms * 1e-3) / 1e9
-        value = world * T * K / (total_ms * 1e-3)
+        value = tokens_per_s(world, T, K, total_ms)
         result = {
             "metric": METRIC,
             "value": round(value, 1),
@@ -314,15 +327,17 @@ def run_ours(args, rank, world, local):
                              f"{ROTATING_SETS} rotating stage-1 input sets (283 MB)",
                        "parallelism": f"replicas x{world}"},
             "norm_quant": {"us": round(s1_ms * 1e3, 3), "GB/s": round(gbs1, 1),
-                           "frac": round(gbs1 / peak, 4), "bytes": b1},
+                           "frac": round(gbs1 / peak, 4), "bytes": b1,
+                           "traffic": ncu_traffic("norm_quant")},
             "lm_head": {"us": round(s2_ms * 1e3, 3), "GB/s": round(gbs2, 1),
                         "frac": round(gbs2 / peak, 4), "bytes": b2,
                         "draft_tokens_per_s": round(T / (s2_ms * 1e-3), 1)},
             "roofline": {"bound": "hbm", "achieved": round(gbs2, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(gbs2 / peak, 4),
                          "traffic": ncu_traffic("lm_head"),
-                         "kernel": "lm_head_argmax_kernel", "peak_source": peak_kind},
-            "e2e": {"value": round(world * T * K / (e2e_ms * 1e-3), 1), "unit": "draft tokens/s",
+                         "kernel": "lm_head_small_kernel" if T <= 64 else "lm_head_argmax_kernel",
+                         "peak_source": peak_kind},
+            "e2e": {"value": round(tokens_per_s(world, T, K, e2e_ms), 1), "unit": "draft tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": gpu_launches,
             "clocks": clocks,
