@@ -12,7 +12,8 @@ with inputs resident in HBM; `e2e` repeats the measurement with the step's
 stage-1 inputs copied from pinned host memory and the tokens read back every
 step.  Each step reads the 932 MB FP8 LM-head weight (> L2) and a different
 one of 40 rotating stage-1 input sets (283 MB in all), so no step is served
-from L2.  With N > 1 (torchrun) every rank runs the same workload on its own
+from L2.  --workload picks another of the five workloads (prefill runs the
+norm + quant stage alone).  With N > 1 (torchrun) every rank runs the same workload on its own
 GPU (independent replicas, weak scaling; the only collectives are the timing
 barrier and the max over ranks).
 
@@ -39,7 +40,7 @@ if ROOT not in sys.path:
 
 WORKLOAD = "decode_c64"
 METRIC = "norm+FP8-quant GB/s; LM-head+argmax draft tokens/s; % of GB300 roofline"
-ROTATING_SETS = 40
+ROTATION_BYTES = 280_000_000   # stage-1 input sets rotated per step: > 2 x L2
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -50,6 +51,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["decode_c64", "decode_c1", "prefill", "tie_stress", "tiny"])
     return ap.parse_args()
 
 
@@ -188,6 +191,18 @@ class ClockSampler:
 
 # -------------------------------------------------------------- our impl --
 
+WORKLOAD_TEXT = {
+    "decode_c64": "decode c=64 draft step (GLM-5.2 shapes): T=64, hidden=6144, k=8 BF16 partials "
+                  "N(0,0.5) with 1% outlier channels x20, vocab=151552 in 8 shards, "
+                  "128x128-block FP8 LM head",
+    "decode_c1": "decode c=1 draft step (DeepSeek-V3.2 shapes): T=1, hidden=7168, k=8, "
+                 "vocab=129280 in 8 shards",
+    "prefill": "prefill bandwidth: T=8192, hidden=7168, k=8, norm + quant only",
+    "tie_stress": "tie stress: T=256, hidden=6144, k=4, vocab=151552 in 8 shards",
+    "tiny": "tiny: T=4, hidden=1024, k=2, vocab=4096 in 2 shards",
+}
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -200,36 +215,39 @@ def run_ours(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = synth.workload(WORKLOAD)
+    w = synth.workload(args.workload)
     T, H, k, V, S = w.T, w.H, w.k, w.V, w.S
+    has_lm = V > 0
 
-    # inputs: stage-1 tensors (rotating device copies) and the LM head
+    # inputs: stage-1 tensors in rotating device copies (more than twice L2 in
+    # all), and the LM head weight packed once into the streaming layout
     inp = synth.stage1_inputs(w)
     to_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
     host_parts = [to_bf16(p).pin_memory() for p in inp["partials"]]
     host_res = to_bf16(inp["residual"]).pin_memory()
     norm_w = to_bf16(inp["norm_w"]).to(dev)
-    sets = []
-    for _ in range(ROTATING_SETS):
-        sets.append(([p.to(dev) for p in host_parts], host_res.to(dev)))
-    qw, sw = synth.lm_head_weights(w)
-    qw_rowmajor = torch.from_numpy(qw).to(dev)
-    sw_d = torch.from_numpy(sw).to(dev)
-    del qw
-    # the weight is static: pack it once into the streaming layout (not timed)
-    qw_d = nfq.pack_lm_head_weights(qw_rowmajor)
-    torch.cuda.synchronize()
-    del qw_rowmajor
+    set_bytes = (k + 1) * T * H * 2
+    nsets = int(min(64, max(2, -(-ROTATION_BYTES // set_bytes))))
+    sets = [([p.to(dev) for p in host_parts], host_res.to(dev)) for _ in range(nsets)]
+    if has_lm:
+        qw, sw = synth.lm_head_weights(w)
+        qw_rowmajor = torch.from_numpy(qw).to(dev)
+        sw_d = torch.from_numpy(sw).to(dev)
+        del qw
+        qw_d = nfq.pack_lm_head_weights(qw_rowmajor)
+        torch.cuda.synchronize()
+        del qw_rowmajor
+        ws = nfq.lm_head_workspace(T, S, dev)
     hidden = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
     scales = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
     tokens = torch.empty(T, dtype=torch.int32, device=dev)
-    ws = nfq.lm_head_workspace(T, S, dev)
     stream = torch.cuda.current_stream()
 
-    def step(i):
-        parts, res = sets[i % ROTATING_SETS]
+    def stage1(parts, res):
         nfq.mtp_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
+
+    def stage2():
         nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
 
     def barrier():
@@ -240,7 +258,9 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
 
     for i in range(args.warmup):
-        step(i)
+        stage1(*sets[i % nsets])
+        if has_lm:
+            stage2()
     barrier()
     if nfq.device_error() != nfq.NFQ_OK:
         raise RuntimeError("a kernel reported an expired wait during warm-up")
@@ -253,11 +273,11 @@ def run_ours(args, rank, world, local):
     barrier()
     t_wall0 = time.time()
     for i in range(K):
-        parts, res = sets[i % ROTATING_SETS]
         ev[i][0].record(stream)
-        nfq.mtp_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
+        stage1(*sets[i % nsets])
         ev[i][1].record(stream)
-        nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
+        if has_lm:
+            stage2()
         ev[i][2].record(stream)
     barrier()
     t_wall1 = time.time()
@@ -267,30 +287,34 @@ def run_ours(args, rank, world, local):
     total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
     s1_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     s2_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
-    gpu_launches = 2 * K
+    gpu_launches = (2 if has_lm else 1) * K
 
-    # end to end through the public API from pinned host memory
-    h_tokens = torch.empty(T, dtype=torch.int32).pin_memory()
+    # end to end through the public API: the step's stage-1 inputs come from
+    # pinned host memory and its result (tokens, or the group scales when there
+    # is no LM head) is read back every step
+    result_dev = tokens if has_lm else scales
+    h_result = torch.empty_like(result_dev, device="cpu").pin_memory()
     dev_parts = [torch.empty_like(p, device=dev) for p in host_parts]
     dev_res = torch.empty_like(host_res, device=dev)
     h2d = sum(p.numel() * 2 for p in host_parts) + host_res.numel() * 2
-    d2h = T * 4
+    d2h = result_dev.numel() * result_dev.element_size()
 
     def e2e_step():
         for hp, dp in zip(host_parts, dev_parts):
             dp.copy_(hp, non_blocking=True)
         dev_res.copy_(host_res, non_blocking=True)
-        nfq.mtp_reduce_norm_quant(dev_parts, dev_res, norm_w, w.eps, hidden, codes, scales)
-        nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
-        h_tokens.copy_(tokens, non_blocking=True)
+        stage1(dev_parts, dev_res)
+        if has_lm:
+            stage2()
+        h_result.copy_(result_dev, non_blocking=True)
         stream.synchronize()
-        return h_tokens
 
-    for _ in range(max(3, args.warmup)):
+    e2e_steps = K if set_bytes < (1 << 28) else max(3, min(K, 20))
+    for _ in range(max(3, min(args.warmup, 20))):
         e2e_step()
     barrier()
     c0 = time.perf_counter()
-    for _ in range(K):
+    for _ in range(e2e_steps):
         e2e_step()
     e2e_ms = (time.perf_counter() - c0) * 1e3
     barrier()
@@ -301,14 +325,12 @@ def run_ours(args, rank, world, local):
     if rank == 0:
         peak, peak_kind = load_peaks()
         b1 = stage1_bytes(T, H, k)
-        b2 = stage2_bytes(T, H, V)
         gbs1 = b1 / (s1_ms * 1e-3) / 1e9
-        gbs2 = b2 / (s2_ms * 1e-3) / 1e9
         value = tokens_per_s(world, T, K, total_ms)
         result = {
             "metric": METRIC,
             "value": round(value, 1),
-            "unit": "draft tokens/s",
+            "unit": "draft tokens/s" if has_lm else "tokens/s",
             "n_gpus": world,
             "steps": K,
             "warmup": args.warmup,
@@ -318,30 +340,37 @@ def run_ours(args, rank, world, local):
             "vs_baseline": None,
             "dtype": "e4m3 MMA, fp32 accumulate; bf16 in, fp32 norm",
             "data": "synthetic",
-            "config": {"workload": "decode c=64 draft step (GLM-5.2 shapes): T=64, hidden=6144, "
-                                   "k=8 BF16 partials N(0,0.5) with 1% outlier channels x20, "
-                                   "vocab=151552 in 8 shards, 128x128-block FP8 LM head",
-                       "weight_layout": "packed once at load: tile-contiguous, pre-swizzled "
-                                        "16 KB blocks of 128 rows x 128 columns",
-                       "l2": "inputs larger than L2: 932 MB FP8 weight read every step, "
-                             f"{ROTATING_SETS} rotating stage-1 input sets (283 MB)",
+            "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
+                       "l2": f"inputs larger than L2: {nsets} rotating stage-1 input sets "
+                             f"({nsets * set_bytes / 1e6:.0f} MB)"
+                             + (", 932 MB FP8 weight read every step" if has_lm else ""),
                        "parallelism": f"replicas x{world}"},
             "norm_quant": {"us": round(s1_ms * 1e3, 3), "GB/s": round(gbs1, 1),
                            "frac": round(gbs1 / peak, 4), "bytes": b1,
-                           "traffic": ncu_traffic("norm_quant")},
-            "lm_head": {"us": round(s2_ms * 1e3, 3), "GB/s": round(gbs2, 1),
-                        "frac": round(gbs2 / peak, 4), "bytes": b2,
-                        "draft_tokens_per_s": round(T / (s2_ms * 1e-3), 1)},
-            "roofline": {"bound": "hbm", "achieved": round(gbs2, 1), "peak": peak,
-                         "unit": "GB/s", "frac": round(gbs2 / peak, 4),
-                         "traffic": ncu_traffic("lm_head"),
-                         "kernel": "lm_head_small_kernel" if T <= 64 else "lm_head_argmax_kernel",
-                         "peak_source": peak_kind},
-            "e2e": {"value": round(tokens_per_s(world, T, K, e2e_ms), 1), "unit": "draft tokens/s",
+                           "traffic": ncu_traffic("norm_quant") if args.workload == WORKLOAD else None},
+            "e2e": {"value": round(tokens_per_s(world, T, e2e_steps, e2e_ms), 1),
+                    "unit": "draft tokens/s" if has_lm else "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": gpu_launches,
             "clocks": clocks,
         }
+        if has_lm:
+            b2 = stage2_bytes(T, H, V)
+            gbs2 = b2 / (s2_ms * 1e-3) / 1e9
+            result["config"]["weight_layout"] = ("packed once at load: tile-contiguous, "
+                                                 "pre-swizzled 16 KB blocks of 128 rows x 128 columns")
+            result["lm_head"] = {"us": round(s2_ms * 1e3, 3), "GB/s": round(gbs2, 1),
+                                 "frac": round(gbs2 / peak, 4), "bytes": b2,
+                                 "draft_tokens_per_s": round(T / (s2_ms * 1e-3), 1)}
+            result["roofline"] = {"bound": "hbm", "achieved": round(gbs2, 1), "peak": peak,
+                                  "unit": "GB/s", "frac": round(gbs2 / peak, 4),
+                                  "traffic": ncu_traffic("lm_head") if args.workload == WORKLOAD else None,
+                                  "kernel": "lm_head_small_kernel" if T <= 64 else "lm_head_argmax_kernel",
+                                  "peak_source": peak_kind}
+        else:
+            result["roofline"] = {"bound": "hbm", "achieved": round(gbs1, 1), "peak": peak,
+                                  "unit": "GB/s", "frac": round(gbs1 / peak, 4), "traffic": None,
+                                  "kernel": "reduce_norm_quant_kernel", "peak_source": peak_kind}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -351,12 +380,14 @@ def run_ours(args, rank, world, local):
 # ------------------------------------------------------------ CPU oracle --
 
 def oracle_sample(w, inp, qw, sw, rows, tokens):
-    """Oracle time of stage 1 on all rows plus the LM head for `tokens` over
-    `rows` vocab rows; returns (seconds, per-token seconds for the full vocab)."""
+    """Oracle time of stage 1 on the sampled rows plus the LM head for `tokens`
+    over `rows` vocab rows; returns (seconds, seconds for the whole step)."""
     import oracle
     t0 = time.perf_counter()
     o = oracle.reduce_norm_quant(inp["partials"], inp["residual"], inp["norm_w"], w.eps)
     t1 = time.perf_counter()
+    if qw is None:
+        return t1 - t0, (t1 - t0) * w.T / inp["partials"].shape[1]
     oracle.lm_head_logits(o["codes"], o["scales"], qw[:rows], sw[: (rows + 127) // 128],
                           tokens=tokens)
     t2 = time.perf_counter()
@@ -364,12 +395,18 @@ def oracle_sample(w, inp, qw, sw, rows, tokens):
     return t2 - t0, full
 
 
-def cpu_baseline(w):
-    import numpy as np
+def cpu_baseline(name):
     import synth
+    w = synth.workload(name)
+    if w.V == 0:
+        rows = list(range(min(w.T, 64)))
+        inp = synth.stage1_inputs(w, rows=rows)
+        secs, full = oracle_sample(w, inp, None, None, 0, None)
+        return {"value": round(w.T / full, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "sample": f"stage 1 on {len(rows)} of {w.T} rows ({secs:.1f} s), scaled to all rows"}
     inp = synth.stage1_inputs(w)
-    rows = 2 * (w.V // w.S)
-    ww = synth.workload(WORKLOAD, V=rows, S=2)
+    rows = max(128, 2 * (w.V // w.S)) if w.V >= 4096 else w.V
+    ww = synth.workload(name, V=rows, S=1)
     qw, sw = synth.lm_head_weights(ww)
     secs, full = oracle_sample(w, inp, qw, sw, rows, list(range(w.T)))
     return {"value": round(w.T / full, 4), "unit": "draft tokens/s", "cores": 1,
@@ -382,34 +419,37 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     import synth
-    w = synth.workload(WORKLOAD)
-    inp = synth.stage1_inputs(w)
-    rows = 32
-    ww = synth.workload(WORKLOAD, V=128, S=1)
-    qw, sw = synth.lm_head_weights(ww)
+    w = synth.workload(args.workload)
+    has_lm = w.V > 0
+    if has_lm:
+        inp = synth.stage1_inputs(w)
+        rows = 32
+        qw, sw = synth.lm_head_weights(synth.workload(args.workload, V=128, S=1))
+        sample = (f"per step: stage 1 on all {w.T} rows + LM head for all {w.T} tokens over "
+                  f"{rows} vocab rows, scaled to {w.V} rows")
+    else:
+        inp = synth.stage1_inputs(w, rows=[0])
+        rows, qw, sw = 0, None, None
+        sample = f"per step: stage 1 on 1 of {w.T} rows, scaled to all rows"
+    toks = list(range(w.T)) if has_lm else None
     for _ in range(args.warmup):
-        oracle_sample(w, inp, qw, sw, rows, list(range(w.T)))
+        oracle_sample(w, inp, qw, sw, rows, toks)
     t0 = time.perf_counter()
-    fulls = []
-    for _ in range(args.steps):
-        fulls.append(oracle_sample(w, inp, qw, sw, rows, list(range(w.T)))[1])
+    fulls = [oracle_sample(w, inp, qw, sw, rows, toks)[1] for _ in range(args.steps)]
     elapsed = time.perf_counter() - t0
     full = sum(fulls) / len(fulls)
     value = w.T / full
+    unit = "draft tokens/s" if has_lm else "tokens/s"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4),
-            "unit": "draft tokens/s", "n_gpus": world, "steps": args.steps,
+            "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(full * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp32 (fp64 norm)", "data": "synthetic",
-            "config": {"workload": "decode c=64 draft step (GLM-5.2 shapes): T=64, "
-                                   "hidden=6144, k=8, vocab=151552 in 8 shards",
+            "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
                        "parallelism": "cpu oracle, rank 0"},
-            "cpu_baseline": {"value": round(value, 4), "unit": "draft tokens/s", "cores": 1,
-                             "kind": "oracle",
-                             "sample": f"per step: stage 1 on all {w.T} rows + LM head for all "
-                                       f"{w.T} tokens over {rows} vocab rows, scaled to "
-                                       f"{w.V} rows; {elapsed:.1f} s timed"},
-            "e2e": {"value": round(value, 4), "unit": "draft tokens/s",
+            "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": 1,
+                             "kind": "oracle", "sample": f"{sample}; {elapsed:.1f} s timed"},
+            "e2e": {"value": round(value, 4), "unit": unit,
                     "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -431,7 +471,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             import synth
-            res["cpu_baseline"] = cpu_baseline(synth.workload(WORKLOAD))
+            res["cpu_baseline"] = cpu_baseline(args.workload)
         print(json.dumps(res), flush=True)
 
 

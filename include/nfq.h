@@ -208,15 +208,17 @@ int nfq_lm_head_fp8_argmax_noalloc(const nfq_quant_act *a, const uint8_t *w,
 /*
  * Tuning hooks (process-wide, not thread-safe; for benchmarks and tests).
  * nfq_stage1_plan: the stage-1 launch plan for (T, H, k) on a GPU with
- *   num_sms SMs: out6 = {cluster CTAs per row, 16-byte vectors per thread,
- *   active consumer threads, block threads, ring slots, shared bytes}.
- * nfq_stage1_tune: force the cluster size, vectors per thread and ring slots
- *   of later stage-1 launches (0 = automatic; invalid choices fall back).
+ *   num_sms SMs: out7 = {cluster CTAs per row, 16-byte vectors per thread,
+ *   active consumer threads, block threads, ring slots, shared bytes,
+ *   inputs per ring slot}.
+ * nfq_stage1_tune: force the cluster size, vectors per thread, ring slots and
+ *   inputs per slot of later stage-1 launches (0 = automatic; invalid choices
+ *   fall back).
  * nfq_lm_head_small_batch: 1 (default) runs batches of at most 64 tokens on the
  *   token-major kernel; 0 forces the weight-major kernel for every batch size.
  */
-int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out6);
-void nfq_stage1_tune(int cluster, int vpt, int slots);
+int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7);
+void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot);
 void nfq_lm_head_small_batch(int enabled);
 
 #ifdef __cplusplus

@@ -80,7 +80,7 @@ def load(path: str = LIB_PATH):
     lib.nfq_device_error.restype = ctypes.c_int
     lib.nfq_stage1_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_stage1_plan.restype = ctypes.c_int
-    lib.nfq_stage1_tune.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.nfq_stage1_tune.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.nfq_stage1_tune.restype = None
     lib.nfq_lm_head_small_batch.argtypes = [ctypes.c_int]
     lib.nfq_lm_head_small_batch.restype = None
@@ -243,14 +243,15 @@ def device_error(clear: bool = True) -> int:
 
 
 def stage1_plan(T: int, H: int, k: int, num_sms: int = 152):
-    out = (ctypes.c_int * 6)()
+    out = (ctypes.c_int * 7)()
     _check(load().nfq_stage1_plan(T, H, k, num_sms, out), "nfq_stage1_plan")
-    return dict(zip(["cluster", "vpt", "active_threads", "threads", "slots", "smem"], list(out)))
+    return dict(zip(["cluster", "vpt", "active_threads", "threads", "slots", "smem",
+                     "per_slot"], list(out)))
 
 
-def stage1_tune(cluster: int = 0, vpt: int = 0, slots: int = 0):
+def stage1_tune(cluster: int = 0, vpt: int = 0, slots: int = 0, per_slot: int = 0):
     """Override the stage-1 launch plan (0 = automatic); for tuning sweeps."""
-    load().nfq_stage1_tune(cluster, vpt, slots)
+    load().nfq_stage1_tune(cluster, vpt, slots, per_slot)
 
 
 def lm_head_small_batch(enabled: bool = True):

@@ -239,13 +239,15 @@ int nfq_device_error(int clear) {
 }
 
 // Launch-plan query and override for the stage-1 kernel (tuning sweeps; 0 = automatic).
-int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out6) {
-  if (!out6) return NFQ_ERR_NULL;
+int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7) {
+  if (!out7) return NFQ_ERR_NULL;
   if (H < 128 || H % 128 || T < 1 || k < 1 || num_sms < 1) return NFQ_ERR_SHAPE;
-  return stage1_plan(T, H, k, num_sms, out6);
+  return stage1_plan(T, H, k, num_sms, out7);
 }
 
-void nfq_stage1_tune(int cluster, int vpt, int slots) { stage1_set_tuning(cluster, vpt, slots); }
+void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot) {
+  stage1_set_tuning(cluster, vpt, slots, per_slot);
+}
 
 // Selects the LM-head kernel family for T <= 64: 1 (default) the token-major
 // small-batch kernel, 0 the weight-major kernel used for larger batches.

@@ -23,13 +23,14 @@ struct Stage1Params {
   int k, T, H;
   int C;          // CTAs per cluster (channel split of a row)
   int E;          // channels per CTA = H / C
-  int nslot;      // shared-memory ring slots of E BF16 values
+  int nslot;      // shared-memory ring slots
+  int per_slot;   // inputs (E BF16 values each) per ring slot
   int n_active;   // consumer threads holding data
 };
 
 cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream);
-void stage1_set_tuning(int cluster, int vpt, int slots);
-int stage1_plan(int T, int H, int k, int num_sms, int *out6);
+void stage1_set_tuning(int cluster, int vpt, int slots, int per_slot);
+int stage1_plan(int T, int H, int k, int num_sms, int *out7);
 
 // Stage 2 launch parameters.
 struct Stage2Params {

@@ -37,9 +37,11 @@ namespace nfq {
 namespace {
 
 constexpr int kErrBitStage1 = 1;
-// register budget: up to 2 vectors per thread with 512 consumers (17 warps leave
-// 96 registers a thread), more with 256
-__host__ __device__ constexpr int stage1_max_threads(int vpt) { return vpt <= 2 ? 544 : 288; }
+// register budget: one vector per thread with up to 992 consumers, two with up
+// to 512 (17 warps leave 96 registers a thread), more with up to 256
+__host__ __device__ constexpr int stage1_max_threads(int vpt) {
+  return vpt == 1 ? 1024 : vpt == 2 ? 544 : 288;
+}
 
 struct RowSums {
   float red[2][32];     // per consumer warp, double-buffered by row parity
@@ -55,6 +57,20 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8]) {
   }
 }
 
+// x[e] += bf16 value e of the 16-byte vector, as correctly rounded fp32 adds
+// (two lanes per add.rn.f32x2).
+__device__ __forceinline__ void add_bf16x8(float (&x)[8], const uint4 &v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint64_t acc, add, sum;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(x[2 * i]), "f"(x[2 * i + 1]));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(add) : "r"(w[i] << 16), "r"(w[i] & 0xFFFF0000u));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(acc), "l"(add));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x[2 * i]), "=f"(x[2 * i + 1]) : "l"(sum));
+  }
+}
+
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
@@ -66,7 +82,9 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
     reduce_norm_quant_kernel(const Stage1Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int E = p.E;
-  const uint32_t slot_bytes = (uint32_t)E * 2u;
+  const uint32_t in_bytes = (uint32_t)E * 2u;                  // one input's slice of a row
+  const int m = p.per_slot;                                      // inputs per ring slot
+  const uint32_t slot_bytes = in_bytes * (uint32_t)m;
   uint8_t *ring = smem;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)p.nslot * slot_bytes);
   uint64_t *empty = full + p.nslot;
@@ -109,7 +127,8 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
     bool ok = true;
     for (int r = cid; r < p.T && ok; r += ncl) {
       const size_t off = ((size_t)r * (size_t)p.H + (size_t)col0) * 2u;
-      for (int i = 0; i <= p.k; ++i, ++it) {
+      for (int i0 = 0; i0 <= p.k; i0 += m, ++it) {
+        const int cnt = (p.k + 1 - i0) < m ? (p.k + 1 - i0) : m;
         const uint32_t s = it % (uint32_t)p.nslot;
         const uint32_t ph = (it / (uint32_t)p.nslot) & 1u;
         int got = 1;
@@ -121,11 +140,14 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
           break;
         }
         if (lane == 0) {
-          const uint8_t *src =
-              static_cast<const uint8_t *>(i < p.k ? p.partials[i] : p.residual) + off;
-          mbar_arrive_expect_tx(smem_u32(&full[s]), slot_bytes);
-          bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes), src, slot_bytes,
-                   smem_u32(&full[s]), pol);
+          mbar_arrive_expect_tx(smem_u32(&full[s]), in_bytes * (uint32_t)cnt);
+          for (int c = 0; c < cnt; ++c) {
+            const int i = i0 + c;
+            const uint8_t *src =
+                static_cast<const uint8_t *>(i < p.k ? p.partials[i] : p.residual) + off;
+            bulk_g2s(smem_u32(ring + (size_t)s * slot_bytes + (size_t)c * in_bytes), src,
+                     in_bytes, smem_u32(&full[s]), pol);
+          }
         }
         __syncwarp();
       }
@@ -167,7 +189,8 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[v][e] = 0.0f;
       bool ok = true;
-      for (int i = 0; i <= p.k; ++i, ++it) {
+      for (int i0 = 0; i0 <= p.k; i0 += m, ++it) {
+        const int cnt = (p.k + 1 - i0) < m ? (p.k + 1 - i0) : m;
         const uint32_t s = it % (uint32_t)p.nslot;
         const uint32_t ph = (it / (uint32_t)p.nslot) & 1u;
         const bool got = mbar_wait(smem_u32(&full[s]), ph, abort_flag, p.err, kErrBitStage1);
@@ -176,13 +199,18 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
           break;
         }
         if (active) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(ring + (size_t)s * slot_bytes);
+          for (int c = 0; c < cnt; ++c) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(ring + (size_t)s * slot_bytes +
+                                                               (size_t)c * in_bytes);
 #pragma unroll
-          for (int v = 0; v < VPT; ++v) {
-            float f[8];
-            unpack_bf16x8(src[v * NA + tc], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[v][e] = (i == 0) ? f[e] : __fadd_rn(x[v][e], f[e]);
+            for (int v = 0; v < VPT; ++v) {
+              const uint4 d = src[v * NA + tc];
+              if (i0 + c == 0) {
+                unpack_bf16x8(d, x[v]);
+              } else {
+                add_bf16x8(x[v], d);   // x += input, element-wise, fp32, in input order
+              }
+            }
           }
         }
         __syncwarp();
@@ -240,13 +268,13 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
         float amax = 0.0f;
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-          const __nv_bfloat16 b0 = __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]));
-          const __nv_bfloat16 b1 =
-              __float2bfloat16_rn(__fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
-          const uint32_t u0 = __bfloat16_as_ushort(b0), u1 = __bfloat16_as_ushort(b1);
-          hb[e / 2] = u0 | (u1 << 16);
-          y[e] = __uint_as_float(u0 << 16);
-          y[e + 1] = __uint_as_float(u1 << 16);
+          const __nv_bfloat162 h2 =
+              __floats2bfloat162_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]),
+                                    __fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
+          const uint32_t hu = *reinterpret_cast<const uint32_t *>(&h2);   // .x low, .y high
+          hb[e / 2] = hu;
+          y[e] = __uint_as_float(hu << 16);
+          y[e + 1] = __uint_as_float(hu & 0xFFFF0000u);
           amax = fmaxf(amax, fmaxf(fabsf(y[e]), fabsf(y[e + 1])));
         }
         // 16 consecutive lanes hold one 128-channel group (all lanes shuffle)
@@ -284,40 +312,29 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
 namespace {
 
 struct Stage1Choice {
-  int C, VPT, NA, threads, nslot;
+  int C, VPT, NA, threads, nslot, per_slot;
   size_t smem;
 };
 
-int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0;
+int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0, g_tune_per_slot = 0;
 
-size_t stage1_smem_bytes(int nslot, int E) {
-  return (size_t)nslot * (size_t)E * 2u + (size_t)nslot * 16u + 32u + sizeof(RowSums) + 16u;
+size_t stage1_smem_bytes(int nslot, int per_slot, int E) {
+  return (size_t)nslot * (size_t)per_slot * (size_t)E * 2u + (size_t)nslot * 16u + 32u +
+         sizeof(RowSums) + 16u;
 }
 
-// Vectors per consumer thread for a slice of Gc groups.  With many rows per CTA
-// (streaming), whole warps of 192..256 threads and the most vectors per thread;
-// with at most one row per CTA (latency-bound), the most threads.
-int pick_vpt(int Gc, bool few_rows) {
-  if (few_rows) {
-    for (int pass = 0; pass < 2; ++pass)
-      for (int v = 1; v <= 8; ++v) {
-        if (Gc % v) continue;
-        const int na = 16 * Gc / v;
-        if (na + 32 > stage1_max_threads(v)) continue;
-        if (pass == 0 && na % 32 != 0) continue;
-        return v;
-      }
-    return 0;
-  }
-  for (int pass = 0; pass < 4; ++pass)
-    for (int v = 8; v >= 1; --v) {
+// Vectors per consumer thread for a slice of Gc groups: two where possible (on
+// GB300 two vectors a thread beat one and four for both one row per CTA and
+// streaming many rows per CTA), whole warps first, within the register budget
+// of each variant.
+int pick_vpt(int Gc) {
+  const int order[8] = {2, 1, 3, 4, 5, 6, 7, 8};   // two vectors per thread measured best
+  for (int pass = 0; pass < 2; ++pass)
+    for (int v : order) {
       if (Gc % v) continue;
       const int na = 16 * Gc / v;
-      if (na + 32 > 288) continue;
-      const bool whole = na % 32 == 0;
-      if (pass == 0 && !(whole && na >= 192)) continue;
-      if (pass == 1 && !(whole && na >= 128)) continue;
-      if (pass == 2 && !whole) continue;
+      if (na + 32 > stage1_max_threads(v)) continue;
+      if (pass == 0 && na % 32 != 0) continue;
       return v;
     }
   return 0;
@@ -333,13 +350,12 @@ Stage1Choice choose_stage1(int T, int H, int k, int num_sms) {
   for (int c : opts) {
     if (G % c) continue;
     if (g_tune_C > 0 && c != g_tune_C) continue;
-    const bool few = (long)T * c <= (long)num_sms;
     int v = 0;
     if (g_tune_vpt > 0 && (G / c) % g_tune_vpt == 0 &&
         16 * (G / c) / g_tune_vpt + 32 <= stage1_max_threads(g_tune_vpt))
       v = g_tune_vpt;
     else
-      v = pick_vpt(G / c, few);
+      v = pick_vpt(G / c);
     if (!v) continue;
     C = c;
     vpt = v;
@@ -351,18 +367,28 @@ Stage1Choice choose_stage1(int T, int H, int k, int num_sms) {
   ch.NA = 16 * (G / C) / vpt;
   ch.threads = 32 + ((ch.NA + 31) / 32) * 32;
   const int E = H / C;
+  const size_t in_bytes = (size_t)E * 2u;
+  // inputs per slot: about 42 KB per barrier round trip (three inputs of a
+  // 6144- or 7168-wide row measured best), at most a whole row
+  int m = (int)((42u * 1024u) / in_bytes);
+  if (m < 1) m = 1;
+  if (m > k + 1) m = k + 1;
+  if (g_tune_per_slot > 0) m = g_tune_per_slot < k + 1 ? g_tune_per_slot : k + 1;
   const size_t budget = 200u * 1024u;
-  int nslot = (int)(budget / ((size_t)E * 2u));
-  // chunks one CTA streams when the grid covers every SM
+  while (m > 1 && 2u * in_bytes * (size_t)m > budget) --m;   // room for two slots
+  const int slots_per_row = (k + 1 + m - 1) / m;
+  int nslot = (int)(budget / (in_bytes * (size_t)m));
+  // slots one CTA fills when the grid covers every SM
   const long clusters = (long)num_sms / C;
   const long rows_each = (T + clusters - 1) / clusters;
-  const long total_chunks = rows_each * (k + 1);
-  if (nslot > total_chunks) nslot = (int)total_chunks;
+  const long total_slots = rows_each * slots_per_row;
+  if (nslot > total_slots) nslot = (int)total_slots;
   if (nslot > 64) nslot = 64;
   if (nslot < 2) nslot = 2;
   if (g_tune_slots > 0) nslot = g_tune_slots;
   ch.nslot = nslot;
-  ch.smem = stage1_smem_bytes(nslot, E);
+  ch.per_slot = m;
+  ch.smem = stage1_smem_bytes(nslot, m, E);
   return ch;
 }
 
@@ -390,20 +416,22 @@ cudaError_t launch_vpt(const Stage1Params &p, const Stage1Choice &ch, int grid,
 
 }  // namespace
 
-void stage1_set_tuning(int cluster, int vpt, int slots) {
+void stage1_set_tuning(int cluster, int vpt, int slots, int per_slot) {
   g_tune_C = cluster;
   g_tune_vpt = vpt;
   g_tune_slots = slots;
+  g_tune_per_slot = per_slot;
 }
 
-int stage1_plan(int T, int H, int k, int num_sms, int *out6) {
+int stage1_plan(int T, int H, int k, int num_sms, int *out7) {
   Stage1Choice ch = choose_stage1(T, H, k, num_sms);
-  out6[0] = ch.C;
-  out6[1] = ch.VPT;
-  out6[2] = ch.NA;
-  out6[3] = ch.threads;
-  out6[4] = ch.nslot;
-  out6[5] = (int)ch.smem;
+  out7[0] = ch.C;
+  out7[1] = ch.VPT;
+  out7[2] = ch.NA;
+  out7[3] = ch.threads;
+  out7[4] = ch.nslot;
+  out7[5] = (int)ch.smem;
+  out7[6] = ch.per_slot;
   return 0;
 }
 
@@ -413,6 +441,7 @@ cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream) {
   p.C = ch.C;
   p.E = p.H / ch.C;
   p.nslot = ch.nslot;
+  p.per_slot = ch.per_slot;
   p.n_active = ch.NA;
   // persistent grid: at most one CTA per SM, whole clusters, no more rows than exist
   long clusters = num_sms / ch.C;

@@ -105,4 +105,4 @@ def test_stage1_plans_cover_the_workload_shapes(lib):
         p = nfq.stage1_plan(T, H, k, 152)
         assert p["vpt"] >= 1 and (H // 128) % (p["cluster"] * p["vpt"]) == 0
         assert p["active_threads"] * p["vpt"] * 8 * p["cluster"] == H
-        assert p["threads"] <= 544 and p["smem"] <= 227 * 1024
+        assert p["threads"] <= 1024 and p["smem"] <= 227 * 1024
