@@ -399,7 +399,7 @@ def cpu_baseline(name):
     import synth
     w = synth.workload(name)
     if w.V == 0:
-        rows = list(range(min(w.T, 64)))
+        rows = list(range(min(w.T, 2048)))
         inp = synth.stage1_inputs(w, rows=rows)
         secs, full = oracle_sample(w, inp, None, None, 0, None)
         return {"value": round(w.T / full, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
