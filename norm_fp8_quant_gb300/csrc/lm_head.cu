@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
     tmem_alloc(smem_u32(&sh->tmem_base), TM_COLS);
     tmem_relinquish();
   }
+  // everything below reads memory the previous kernel on the stream may write
+  grid_dependency_wait();
+  grid_launch_dependents();
   // activation scales of this token chunk, transposed to [kb][n]; zero beyond T
   for (int i = (int)threadIdx.x; i < G * N; i += (int)blockDim.x) {
     const int kb = i / N, n = i % N;
@@ -531,6 +534,9 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     tmem_alloc(smem_u32(&sh->tmem_base), 512);
     tmem_relinquish();
   }
+  // everything below reads memory the previous kernel on the stream may write
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int i = (int)threadIdx.x; i < G * kSmallMaxT; i += (int)blockDim.x) {
     const int kb = i / kSmallMaxT, n = i % kSmallMaxT;
     sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
@@ -764,6 +770,26 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// Launch with programmatic stream serialization: the kernel's set-up may
+// overlap the previous kernel on the stream; it waits (griddepcontrol) before
+// touching memory.
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, int grid, int block, size_t smem, cudaStream_t stream,
+                       const CUtensorMap &tw, const CUtensorMap &ta, const Stage2Params &p,
+                       int nstage) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tw, ta, p, nstage);
+}
+
 // 2-D uint8 map over [rows][cols] (cols contiguous), box 128 x box_rows, 128B swizzle.
 bool encode_u8_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
                    uint32_t box_rows) {
@@ -800,8 +826,7 @@ cudaError_t launch_cfg(const Stage2Params &p, const void *act_codes, const void 
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int grid = num_sms < p.n_vtiles ? num_sms : p.n_vtiles;
-  kern<<<grid, 128 * EPI + 64, smem, stream>>>(tw, ta, p, nstage);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, 128 * EPI + 64, smem, stream, tw, ta, p, nstage);
 }
 
 bool g_small_enabled = true;
@@ -862,8 +887,7 @@ cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const voi
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = num_sms < p.n_vtiles ? num_sms : p.n_vtiles;
-  kern<<<grid, kSmallEpiWarps * 32 + 64, smem, stream>>>(tw, ta, p, nstage);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, kSmallEpiWarps * 32 + 64, smem, stream, tw, ta, p, nstage);
 }
 
 cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const void *w,

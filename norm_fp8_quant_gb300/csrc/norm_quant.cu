@@ -114,6 +114,11 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
   }
   __syncthreads();
   if (C > 1) cluster_sync_all();   // peers' barriers exist before any remote arrive
+  // The set-up above overlaps the previous kernel's tail; every global read
+  // and write below waits for it (its outputs may be this kernel's inputs, and
+  // it may still read the buffers this kernel writes).
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   const int warp = (int)(threadIdx.x / 32);
   const int lane = (int)(threadIdx.x % 32);
@@ -404,13 +409,15 @@ cudaError_t launch_vpt(const Stage1Params &p, const Stage1Choice &ch, int grid,
   cfg.blockDim = dim3((unsigned)ch.threads);
   cfg.dynamicSmemBytes = ch.smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)ch.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

@@ -142,6 +142,20 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// ------------------------------------------------ programmatic dependent launch --
+
+// Wait until the grids this one depends on (the previous kernel on the stream,
+// when launched with programmatic stream serialization) have completed and
+// their memory is visible.  A no-op for an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel on the stream to start launching its CTAs.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // --------------------------------------------------------------- cluster --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
