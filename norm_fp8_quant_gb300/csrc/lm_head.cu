@@ -268,10 +268,7 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 #pragma unroll
       for (int j = 0; j < NCOL; j += 4) {
         const float4 sa4 = *reinterpret_cast<const float4 *>(sak + j);
-        acc[j + 0] = fmaf(__uint_as_float(r[j + 0]), swv * sa4.x, acc[j + 0]);
-        acc[j + 1] = fmaf(__uint_as_float(r[j + 1]), swv * sa4.y, acc[j + 1]);
-        acc[j + 2] = fmaf(__uint_as_float(r[j + 2]), swv * sa4.z, acc[j + 2]);
-        acc[j + 3] = fmaf(__uint_as_float(r[j + 3]), swv * sa4.w, acc[j + 3]);
+        promote4(&acc[j], &r[j], swv, sa4);
       }
     };
     // per-warp argmax over its 32 rows for every token column, merged per shard
@@ -390,10 +387,7 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
               const float4 sa4 = *reinterpret_cast<const float4 *>(sak + c + j);
-              acc[c + j + 0] = fmaf(__uint_as_float(r[j + 0]), swv * sa4.x, acc[c + j + 0]);
-              acc[c + j + 1] = fmaf(__uint_as_float(r[j + 1]), swv * sa4.y, acc[c + j + 1]);
-              acc[c + j + 2] = fmaf(__uint_as_float(r[j + 2]), swv * sa4.z, acc[c + j + 2]);
-              acc[c + j + 3] = fmaf(__uint_as_float(r[j + 3]), swv * sa4.w, acc[c + j + 3]);
+              promote4(&acc[c + j], &r[j], swv, sa4);
             }
           }
         }
@@ -684,7 +678,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         if (active) {
           const float sc = sa_s[kb * kSmallMaxT + tok] * swv;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[j] = fmaf(__uint_as_float(r[j]), sc, acc[j]);
+          for (int j = 0; j < 32; j += 2)
+            fma2(acc[j], acc[j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]), sc, sc);
         }
       }
       if (!ok) break;

@@ -142,6 +142,45 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// ------------------------------------------------------------ packed fp32 --
+
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+
+__device__ __forceinline__ void f2unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// acc[i] = fma(p[i], s[i], acc[i]) for i = 0, 1: two correctly rounded fp32
+// FMAs in one instruction.
+__device__ __forceinline__ void fma2(float &acc0, float &acc1, float p0, float p1, float s0,
+                                     float s1) {
+  uint64_t a = f2pack(acc0, acc1), d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2pack(p0, p1)), "l"(f2pack(s0, s1)), "l"(a));
+  f2unpack(d, acc0, acc1);
+}
+
+// (a0 * b0, a1 * b1), each correctly rounded.
+__device__ __forceinline__ void mul2(float &d0, float &d1, float a0, float a1, float b0,
+                                     float b1) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2pack(a0, a1)), "l"(f2pack(b0, b1)));
+  f2unpack(d, d0, d1);
+}
+
+// acc[j] += P[j] * (sw * sa[j]) for four consecutive columns (fp32, the scale
+// product rounded first, as two packed multiplies and two packed FMAs).
+__device__ __forceinline__ void promote4(float *acc, const uint32_t *r, float sw, float4 sa) {
+  float s0, s1, s2, s3;
+  mul2(s0, s1, sw, sw, sa.x, sa.y);
+  mul2(s2, s3, sw, sw, sa.z, sa.w);
+  fma2(acc[0], acc[1], __uint_as_float(r[0]), __uint_as_float(r[1]), s0, s1);
+  fma2(acc[2], acc[3], __uint_as_float(r[2]), __uint_as_float(r[3]), s2, s3);
+}
+
 // ------------------------------------------------ programmatic dependent launch --
 
 // Wait until the grids this one depends on (the previous kernel on the stream,
