@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mtp", type=int, default=1,
+                    help="draft positions per step (the hidden of each feeds the next)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["decode_c64", "decode_c1", "prefill", "tie_stress", "tiny"])
     return ap.parse_args()
@@ -285,15 +287,32 @@ def run_ours(args, rank, world, local):
 
     # (1) K steps one after another on one stream, events only at the two ends
     # (an event between two kernels would stop the second one's launch from
-    # overlapping the first one's tail): the reported rate
+    # overlapping the first one's tail): the reported rate.  With --mtp P a
+    # step is P chained draft positions: position p's hidden is the residual
+    # of position p+1 (nfq_mtp_draft_chain), each position with its own partials.
+    P = max(1, args.mtp) if has_lm else 1
+    if P > 1:
+        chain_hidden = [torch.empty_like(hidden) for _ in range(2)]
+        chain_tokens = torch.empty((P, T), dtype=torch.int32, device=dev)
+
+        def chain(i):
+            parts = [sets[(i * P + p) % nsets][0] for p in range(P)]
+            nfq.mtp_draft_chain(parts, sets[(i * P) % nsets][1], norm_w, qw_d, sw_d, S, w.eps,
+                                hidden_bufs=chain_hidden, codes=codes, scales=scales,
+                                tokens_out=chain_tokens, workspace=ws)
+        for i in range(max(1, args.warmup // P)):
+            chain(i)
     barrier()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
     for i in range(K):
-        stage1(*sets[i % nsets])
-        if has_lm:
-            stage2()
+        if P > 1:
+            chain(i)
+        else:
+            stage1(*sets[i % nsets])
+            if has_lm:
+                stage2()
     e_end.record(stream)
     barrier()
     total_ms = e_start.elapsed_time(e_end)
@@ -319,7 +338,7 @@ def run_ours(args, rank, world, local):
     instrumented_ms = ev[0][0].elapsed_time(ev[K - 1][2])
     s1_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
     s2_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
-    gpu_launches = (2 if has_lm else 1) * K
+    gpu_launches = (2 if has_lm else 1) * K * P
 
     # end to end through the public API: every step copies its stage-1 inputs
     # (one pinned host batch holding the k partials and the residual) to the
@@ -390,7 +409,7 @@ def run_ours(args, rank, world, local):
         peak, peak_kind = load_peaks()
         b1 = stage1_bytes(T, H, k)
         gbs1 = b1 / (s1_ms * 1e-3) / 1e9
-        value = tokens_per_s(world, T, K, total_ms)
+        value = tokens_per_s(world, T * P, K, total_ms)
         result = {
             "metric": METRIC,
             "value": round(value, 1),
@@ -399,6 +418,7 @@ def run_ours(args, rank, world, local):
             "steps": K,
             "warmup": args.warmup,
             "ms_per_step": round(total_ms / K, 5),
+            "draft_positions_per_step": P,
             "instrumented_ms_per_step": round(instrumented_ms / K, 5),
             "higher_is_better": True,
             "scaling": "weak",

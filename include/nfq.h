@@ -28,7 +28,8 @@
  *    NFQ_ERR_CUDA.  No C++ exception crosses this boundary.
  *  - Tensor values are not inspected: NaN or infinite inputs give unspecified
  *    (but memory-safe) results.
- *  - Row-major layouts throughout; every device pointer must be 16-byte aligned.
+ *  - Row-major layouts throughout.  Every device pointer must be 16-byte aligned,
+ *    except the LM head's int32 / fp32 per-token outputs (4-byte aligned).
  */
 #ifndef NFQ_H_
 #define NFQ_H_
@@ -179,6 +180,33 @@ int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packe
  * `clear` != 0), NFQ_ERR_CUDA if the device cannot be read.
  */
 int nfq_device_error(int clear);
+
+/*
+ * nfq_mtp_draft_chain — `positions` chained MTP draft steps on one stream.
+ * [R] Purpose: the post-final-norm BF16 hidden state is recycled into the next
+ * MTP position; [F] Benchmarks: the draft runs five positions per accepted
+ * token (MTP=5).  Position p runs nfq_mtp_reduce_norm_quant on its k partials
+ * with residual = residual0 (p = 0) or the hidden of position p-1, writing
+ * hidden_out[p], then the LM head on the packed activation, writing
+ * tokens_out[p][0..T).  (The transformer block that turns a draft token into
+ * the next position's partials is not part of this library: the caller
+ * supplies every position's partials.)
+ *   positions   1..64
+ *   partials    HOST array [positions][k] of device pointers, BF16 [T][H] each
+ *   hidden_out  HOST array [positions] of device pointers, BF16 [T][H]; buffers of
+ *               consecutive positions must differ (two alternating buffers do)
+ *               and none may be residual0
+ *   q           the packed activation buffer, reused by every position
+ *   w, w_is_packed  LM-head weight, row-major (0) or packed (1)
+ *   tokens_out  int32 [positions][T]
+ *   workspace   as for nfq_lm_head_fp8_argmax (one suffices for the chain)
+ * Errors are those of the two calls; the first failing position stops the chain.
+ */
+int nfq_mtp_draft_chain(int positions, const void *const *partials, int k,
+                        const void *residual0, const void *norm_w, float eps, int T, int H,
+                        void *const *hidden_out, const nfq_quant_act *q, const uint8_t *w,
+                        int w_is_packed, const float *w_scales, int V, int S,
+                        int32_t *tokens_out, void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * nfq_lm_head_fp8_argmax_noalloc — the same LM head and argmax, for callers

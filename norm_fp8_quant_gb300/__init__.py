@@ -76,6 +76,11 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_pack_weights.restype = ctypes.c_int
     lib.nfq_lm_head_fp8_argmax_packed.argtypes = lib.nfq_lm_head_fp8_argmax.argtypes
     lib.nfq_lm_head_fp8_argmax_packed.restype = ctypes.c_int
+    lib.nfq_mtp_draft_chain.argtypes = [ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_float,
+                                        ctypes.c_int, ctypes.c_int, _P, ctypes.POINTER(QuantAct),
+                                        _P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P, _P,
+                                        ctypes.c_size_t, _P]
+    lib.nfq_mtp_draft_chain.restype = ctypes.c_int
     lib.nfq_device_error.argtypes = [ctypes.c_int]
     lib.nfq_device_error.restype = ctypes.c_int
     lib.nfq_stage1_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
@@ -234,6 +239,42 @@ def lm_head_fp8_argmax(codes, scales, w, w_scales, S: int, workspace=None,
     if want_max or want_shards:
         return tokens, mx, sidx, sval
     return tokens
+
+
+def mtp_draft_chain(partials, residual0, norm_w, w, w_scales, S: int, eps: float = 1e-6,
+                    hidden_bufs=None, codes=None, scales=None, tokens_out=None,
+                    workspace=None, stream=None):
+    """Chained MTP draft positions: partials is a list (one per position) of
+    lists of k BF16 [T][H] tensors; the hidden of each position is the residual
+    of the next.  Returns (tokens int32 [P][T], hidden of every position)."""
+    import torch
+    P = len(partials)
+    k = len(partials[0])
+    T, H = residual0.shape
+    for ps in partials:
+        if len(ps) != k:
+            raise ValueError("every position needs k partials")
+        _need_cuda(*ps)
+    _need_cuda(residual0, norm_w, w_scales)
+    dev = residual0.device
+    if hidden_bufs is None:
+        hidden_bufs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(min(P, 2))]
+    hidden_of = [hidden_bufs[p % len(hidden_bufs)] for p in range(P)]
+    codes = codes if codes is not None else torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = scales if scales is not None else torch.empty((T, H // GROUP), dtype=torch.float32, device=dev)
+    tokens = tokens_out if tokens_out is not None else torch.empty((P, T), dtype=torch.int32, device=dev)
+    ws = workspace if workspace is not None else lm_head_workspace(T, S, dev, stream)
+    parr = (ctypes.c_void_p * (P * k))(*[t.data_ptr() for ps in partials for t in ps])
+    harr = (ctypes.c_void_p * P)(*[h.data_ptr() for h in hidden_of])
+    q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
+    packed = isinstance(w, PackedWeight)
+    with torch.cuda.device(dev):
+        st = load().nfq_mtp_draft_chain(P, parr, k, _ptr(residual0), _ptr(norm_w), float(eps), T, H,
+                                        harr, ctypes.byref(q), _ptr(w), 1 if packed else 0,
+                                        _ptr(w_scales), w.shape[0], S, _ptr(tokens), _ptr(ws),
+                                        ws.numel(), _stream_ptr(stream))
+    _check(st, "nfq_mtp_draft_chain")
+    return tokens, hidden_of
 
 
 def device_error(clear: bool = True) -> int:

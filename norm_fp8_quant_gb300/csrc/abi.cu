@@ -52,6 +52,7 @@ int device_info(DeviceInfo **out) {
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? NFQ_OK : NFQ_ERR_CUDA; }
 
@@ -144,11 +145,12 @@ int lm_head_common(const nfq_quant_act *a, const uint8_t *w, bool packed, const 
   if (V < 1 || S < 1 || S > 64 || V % S != 0) return NFQ_ERR_SHAPE;
   if (!workspace) return NFQ_ERR_WORKSPACE;
   if (ws_bytes < stage2_workspace_bytes(S)) return NFQ_ERR_WORKSPACE;
+  // the per-token outputs are written with 4-byte stores
   if (!aligned16(a->codes) || !aligned16(a->scales) || !aligned16(w) || !aligned16(w_scales) ||
-      !aligned16(tokens_out) || !aligned16(workspace) ||
-      (max_logit_out && !aligned16(max_logit_out)) ||
-      (shard_idx_out && !aligned16(shard_idx_out)) ||
-      (shard_val_out && !aligned16(shard_val_out)))
+      !aligned4(tokens_out) || !aligned16(workspace) ||
+      (max_logit_out && !aligned4(max_logit_out)) ||
+      (shard_idx_out && !aligned4(shard_idx_out)) ||
+      (shard_val_out && !aligned4(shard_val_out)))
     return NFQ_ERR_ALIGN;
   if (T == 0) return NFQ_OK;
   DeviceInfo *d = nullptr;
@@ -224,6 +226,35 @@ int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packe
                                   void *stream) {
   return lm_head_common(a, w_packed, true, w_scales, V, S, tokens_out, max_logit_out,
                         shard_idx_out, shard_val_out, workspace, ws_bytes, stream);
+}
+
+int nfq_mtp_draft_chain(int positions, const void *const *partials, int k,
+                        const void *residual0, const void *norm_w, float eps, int T, int H,
+                        void *const *hidden_out, const nfq_quant_act *q, const uint8_t *w,
+                        int w_is_packed, const float *w_scales, int V, int S,
+                        int32_t *tokens_out, void *workspace, size_t ws_bytes, void *stream) {
+  if (positions < 1 || positions > 64) return NFQ_ERR_SHAPE;
+  if (!partials || !hidden_out || !q || !tokens_out) return NFQ_ERR_NULL;
+  if (k < 1 || k > kMaxPartials) return NFQ_ERR_SHAPE;
+  for (int p = 0; p < positions; ++p) {
+    if (!hidden_out[p]) return NFQ_ERR_NULL;
+    // the residual of position p is the hidden of position p-1: distinct buffers
+    if (p > 0 && hidden_out[p] == hidden_out[p - 1]) return NFQ_ERR_SHAPE;
+    if (hidden_out[p] == residual0) return NFQ_ERR_SHAPE;
+  }
+  for (int p = 0; p < positions; ++p) {
+    const void *residual = p == 0 ? residual0 : hidden_out[p - 1];
+    int st = nfq_mtp_reduce_norm_quant(partials + (size_t)p * k, k, residual, norm_w, eps, T, H,
+                                       hidden_out[p], q, stream);
+    if (st != NFQ_OK) return st;
+    int32_t *tok = tokens_out + (size_t)p * (size_t)T;
+    st = w_is_packed ? nfq_lm_head_fp8_argmax_packed(q, w, w_scales, V, S, tok, nullptr, nullptr,
+                                                     nullptr, workspace, ws_bytes, stream)
+                     : nfq_lm_head_fp8_argmax(q, w, w_scales, V, S, tok, nullptr, nullptr,
+                                              nullptr, workspace, ws_bytes, stream);
+    if (st != NFQ_OK) return st;
+  }
+  return NFQ_OK;
 }
 
 int nfq_device_error(int clear) {

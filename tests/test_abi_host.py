@@ -94,7 +94,9 @@ def test_stage2_argument_validation(lib):
     assert _stage2(lib, ws=0) == nfq.NFQ_ERR_WORKSPACE
     assert _stage2(lib, ws_bytes=8) == nfq.NFQ_ERR_WORKSPACE
     assert _stage2(lib, w=MIS) == nfq.NFQ_ERR_ALIGN
-    assert _stage2(lib, mx=MIS) == nfq.NFQ_ERR_ALIGN
+    assert _stage2(lib, mx=FAKE + 2) == nfq.NFQ_ERR_ALIGN
+    assert _stage2(lib, tokens=FAKE + 2) == nfq.NFQ_ERR_ALIGN
+    assert _stage2(lib, mx=FAKE + 4, tokens=FAKE + 12, T=0) == nfq.NFQ_OK
     assert _stage2(lib, T=0) == nfq.NFQ_OK
     assert lib.nfq_lm_head_workspace_init(None, 16, None) == nfq.NFQ_ERR_NULL
 
@@ -106,3 +108,22 @@ def test_stage1_plans_cover_the_workload_shapes(lib):
         assert p["vpt"] >= 1 and (H // 128) % (p["cluster"] * p["vpt"]) == 0
         assert p["active_threads"] * p["vpt"] * 8 * p["cluster"] == H
         assert p["threads"] <= 1024 and p["smem"] <= 227 * 1024
+
+
+def test_chain_argument_validation(lib):
+    import ctypes as C
+    q = nfq.QuantAct(FAKE, FAKE, 4, 1024, 128)
+    parts = (C.c_void_p * 4)(FAKE, FAKE, FAKE, FAKE)
+    same = (C.c_void_p * 2)(FAKE + 4096, FAKE + 4096)
+    diff = (C.c_void_p * 2)(FAKE + 4096, FAKE + 8192)
+    ws = lib.nfq_lm_head_workspace_bytes(4, 2)
+    call = lambda P, h, res=FAKE, k=2: lib.nfq_mtp_draft_chain(
+        P, parts, k, res, FAKE, 1e-6, 4, 1024, h, C.byref(q), FAKE, 0, FAKE, 4096, 2, FAKE, FAKE,
+        ws, None)
+    assert call(0, diff) == nfq.NFQ_ERR_SHAPE
+    assert call(65, diff) == nfq.NFQ_ERR_SHAPE
+    assert call(2, same) == nfq.NFQ_ERR_SHAPE            # consecutive positions share a buffer
+    assert call(2, diff, res=FAKE + 4096) == nfq.NFQ_ERR_SHAPE   # hidden aliases the residual
+    assert call(2, diff, k=0) == nfq.NFQ_ERR_SHAPE
+    assert lib.nfq_mtp_draft_chain(2, None, 2, FAKE, FAKE, 1e-6, 4, 1024, diff, C.byref(q), FAKE,
+                                   0, FAKE, 4096, 2, FAKE, FAKE, ws, None) == nfq.NFQ_ERR_NULL

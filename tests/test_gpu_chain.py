@@ -1,0 +1,86 @@
+"""Chained MTP draft positions (the BF16 hidden of one position is the residual
+of the next) through nfq_mtp_draft_chain, against the CPU oracle: every link
+with the GPU's own previous hidden, and the whole chain end to end."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests._parity import bf16_host, check_stage1, check_stage2, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nfq():
+    import norm_fp8_quant_gb300 as m
+    from norm_fp8_quant_gb300 import build
+    build.build()
+    m.load()
+    return m
+
+
+def _hidden_within_one_ulp(gpu, ref):
+    o = lambda b: np.where(b.astype(np.int32) & 0x8000, -(b.astype(np.int32) & 0x7FFF),
+                           b.astype(np.int32) & 0x7FFF)
+    assert np.abs(o(gpu) - o(ref)).max(initial=0) <= 1
+
+
+@pytest.mark.parametrize("name,P,packed", [("tiny", 3, False), ("tiny", 5, True),
+                                           ("decode_c64", 5, True)])
+def test_chain_matches_oracle(nfq, name, P, packed):
+    w = synth.workload(name)
+    base = synth.stage1_inputs(w)
+    pos = [synth.stage1_inputs(synth.workload(name, seed=p + 1))["partials"] for p in range(P)]
+    qw, sw = synth.lm_head_weights(w)
+    wd = to_dev(qw)
+    if packed:
+        wd = nfq.pack_lm_head_weights(wd)
+    hidden = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    codes = torch.empty((w.T, w.H), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((w.T, w.H // 128), dtype=torch.float32, device="cuda")
+    toks, _ = nfq.mtp_draft_chain([[to_dev_bf16(x) for x in part] for part in pos],
+                                  to_dev_bf16(base["residual"]), to_dev_bf16(base["norm_w"]),
+                                  wd, to_dev(sw), w.S, w.eps, hidden_bufs=hidden,
+                                  codes=codes, scales=scales)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    toks = toks.cpu().numpy()
+    gh = [bf16_host(h) for h in hidden]
+    sample = list(range(w.T)) if w.T <= 8 else [0, 21, 63]
+    # every link: the oracle's stage 1 on the GPU's previous hidden
+    for p in range(P):
+        res = base["residual"] if p == 0 else gh[p - 1]
+        ref = oracle.reduce_norm_quant(pos[p], res, base["norm_w"], w.eps)
+        _hidden_within_one_ulp(gh[p], ref["hidden"])
+        if p == P - 1:       # the packed activation buffer holds the last position
+            check_stage1(gh[p], codes.cpu().numpy(), scales.cpu().numpy(), ref)
+        check_stage2(toks[p], ref["codes"], ref["scales"], qw, sw, w.S, sample)
+    # the whole chain in the oracle alone
+    res = base["residual"]
+    for p in range(P):
+        ref = oracle.reduce_norm_quant(pos[p], res, base["norm_w"], w.eps)
+        _hidden_within_one_ulp(gh[p], ref["hidden"]) if p == 0 else None
+        if w.T <= 8:
+            L = oracle.lm_head_logits(ref["codes"], ref["scales"], qw, sw)
+            r = oracle.argmax(L, w.S)
+            clear = (r["gap"] >= 1e-3) | (r["gap"] == 0)
+            assert np.array_equal(toks[p][clear], r["tokens"][clear])
+        res = ref["hidden"]
+
+
+def test_chain_with_two_alternating_hidden_buffers(nfq):
+    w = synth.workload("tiny", T=3, H=256, V=512, S=2)
+    base = synth.stage1_inputs(w)
+    pos = [synth.stage1_inputs(synth.workload("tiny", T=3, H=256, seed=p + 7))["partials"]
+           for p in range(4)]
+    qw, sw = synth.lm_head_weights(w)
+    parts = [[to_dev_bf16(x) for x in part] for part in pos]
+    res0, nw, wd, swd = to_dev_bf16(base["residual"]), to_dev_bf16(base["norm_w"]), to_dev(qw), to_dev(sw)
+    t2, h2 = nfq.mtp_draft_chain(parts, res0, nw, wd, swd, w.S)      # two buffers
+    hidden = [torch.empty_like(res0) for _ in range(4)]
+    t4, h4 = nfq.mtp_draft_chain(parts, res0, nw, wd, swd, w.S, hidden_bufs=hidden)
+    torch.cuda.synchronize()
+    assert torch.equal(t2, t4)
+    assert torch.equal(h2[3].view(torch.int16), h4[3].view(torch.int16))
