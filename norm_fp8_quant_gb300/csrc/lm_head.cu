@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 
     // double-buffered TMEM reads when two register sets fit next to the accumulators
     constexpr bool kPipe = NCOL <= 32 && (3 * NCOL + 40) * (128 * EPI + 64) <= 65536;
-    static_assert(kPipe || NCOL % 32 == 0, "unpipelined epilogue reads 32 columns at a time");
+    static_assert(kPipe || NCOL % 16 == 0, "unpipelined epilogue reads 16 or 32 columns at a time");
     if constexpr (kPipe) {
       // One flat pipeline over every (tile, K block) of this CTA: the TMEM read
       // of step q+1 is in flight while step q is promoted (and, at a tile's
@@ -372,20 +372,26 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
           if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
           tc_fence_after();
           const float *sak = sa_s + (size_t)kb * N + grp * NCOL;
+          // 16 columns at a time when the accumulators leave little room
+          constexpr int CHK = (16 * NCOL * EPI >= 4096) ? 16 : 32;
 #pragma unroll
-          for (int c = 0; c < NCOL; c += 32) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + b * N + c, r);
+          for (int c = 0; c < NCOL; c += CHK) {
+            uint32_t r[CHK];
+            if constexpr (CHK == 16) {
+              tmem_ld16(lane_base + b * N + c, r);
+            } else {
+              tmem_ld32(lane_base + b * N + c, r);
+            }
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j]));
-            if (c + 32 >= NCOL) {
+            for (int j = 0; j < CHK; ++j) asm volatile("" : "+r"(r[j]));
+            if (c + CHK >= NCOL) {
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
             }
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
+            for (int j = 0; j < CHK; j += 4) {
               const float4 sa4 = *reinterpret_cast<const float4 *>(sak + c + j);
               promote4(&acc[c + j], &r[j], swv, sa4);
             }
@@ -443,10 +449,10 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 // A CTA streams a contiguous range of 128-row blocks, two per tile (the last
 // tile of a range may hold one).  Two 256-column accumulators in TMEM.
 
-constexpr int kSmallMaxT = 64;
+constexpr int kSmallMaxT = 128;                 // tokens per launch of the token-major form
 constexpr int kSmallEpiWarps = 16;
-constexpr uint32_t kSmallATileBytes = 64 * 128;
-constexpr uint32_t kSmallStageBytes = 2 * kWTileBytes + kSmallATileBytes;   // 40 KB
+template <int MT>
+__host__ __device__ constexpr uint32_t small_stage_bytes() { return 2 * kWTileBytes + MT * 128; }
 
 struct SmallSmem {
   uint64_t full[kMaxStages];
@@ -484,7 +490,7 @@ __device__ __forceinline__ void finish_launch(const Stage2Params &p, int *last_f
   }
 }
 
-template <bool kPacked>
+template <int MT, bool kPacked>
 __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     lm_head_small_kernel(const __grid_constant__ CUtensorMap tmap_w,
                          const __grid_constant__ CUtensorMap tmap_a, const Stage2Params p,
@@ -494,8 +500,10 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
   const int G = p.G;
-  float *sa_s = reinterpret_cast<float *>(smem + (size_t)nstage * kSmallStageBytes);  // [G][64]
-  SmallSmem *sh = reinterpret_cast<SmallSmem *>(sa_s + (size_t)G * kSmallMaxT);
+  constexpr uint32_t kStage = small_stage_bytes<MT>();
+  constexpr uint32_t kATile = MT * 128;
+  float *sa_s = reinterpret_cast<float *>(smem + (size_t)nstage * kStage);  // [G][MT]
+  SmallSmem *sh = reinterpret_cast<SmallSmem *>(sa_s + (size_t)G * MT);
   volatile int *abort_flag = &sh->abort;
 
   const int warp = (int)(threadIdx.x / 32);
@@ -531,8 +539,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   // everything below reads memory the previous kernel on the stream may write
   grid_dependency_wait();
   grid_launch_dependents();
-  for (int i = (int)threadIdx.x; i < G * kSmallMaxT; i += (int)blockDim.x) {
-    const int kb = i / kSmallMaxT, n = i % kSmallMaxT;
+  for (int i = (int)threadIdx.x; i < G * MT; i += (int)blockDim.x) {
+    const int kb = i / MT, n = i % MT;
     sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
   }
   tc_fence_before();
@@ -561,9 +569,9 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
           break;
         }
         if (lane == 0) {
-          uint8_t *st = smem + (size_t)s * kSmallStageBytes;
+          uint8_t *st = smem + (size_t)s * kStage;
           const uint32_t fb = smem_u32(&sh->full[s]);
-          mbar_arrive_expect_tx(fb, (uint32_t)nb * kWTileBytes + kSmallATileBytes);
+          mbar_arrive_expect_tx(fb, (uint32_t)nb * kWTileBytes + kATile);
           for (int h = 0; h < nb; ++h) {
             if constexpr (kPacked) {
               bulk_g2s(smem_u32(st + h * kWTileBytes),
@@ -593,7 +601,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
       const int blk0 = b_begin + 2 * ti;
       const int nb = (blk0 + 1 < b_end) ? 2 : 1;
-      const uint32_t idesc = idesc_e4m3_f32(64, (uint32_t)(nb * 128));
+      const uint32_t idesc = idesc_e4m3_f32(MT, (uint32_t)(nb * 128));
       for (int kb = 0; kb < G; ++kb, ++it) {
         const uint32_t s = it % (uint32_t)nstage;
         const uint32_t ph = (it / (uint32_t)nstage) & 1u;
@@ -610,7 +618,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         }
         if (lane == 0) {
           tc_fence_after();
-          const uint8_t *st = smem + (size_t)s * kSmallStageBytes;
+          const uint8_t *st = smem + (size_t)s * kStage;
           const uint32_t w_addr = smem_u32(st);
           const uint32_t a_addr = smem_u32(st + 2 * kWTileBytes);
           const uint32_t d_tmem = tmem_base + b * 256u;
@@ -631,12 +639,19 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     __syncwarp();
   } else {
     // -------------------------------------------------------------- epilogue --
-    const int q = warp & 3;                        // tokens 16q .. 16q+15
+    // MT = 64: the accumulator puts token r in TMEM lane 32*(r/16) + r%16; a
+    //   16x64b load gives thread t token 16q + t/4 + 8*(t&1) and columns
+    //   64g + 2j + ((t>>1)&1), j < 32 (two lanes share a token).
+    // MT = 128: token r is TMEM lane r; 32x32b loads give thread t token
+    //   32q + t and columns 64g + j, j < 64, read 16 at a time.
+    constexpr int CPT = MT == 64 ? 32 : 64;        // columns per thread
+    const int q = warp & 3;                        // TMEM lane quadrant
     const int g = warp >> 2;                       // tile columns 64g .. 64g+63
-    const int tok = 16 * q + (lane >> 2) + 8 * (lane & 1);
+    const int tok = MT == 64 ? 16 * q + (lane >> 2) + 8 * (lane & 1) : 32 * q + lane;
     const int colpar = (lane >> 1) & 1;
-    const bool quad_active = 16 * q < p.T;
+    const bool quad_active = (MT == 64 ? 16 : 32) * q < p.T;
     const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
+    auto col_of = [&](int j) { return MT == 64 ? 2 * j + colpar : j; };
     uint32_t it = 0;
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
@@ -651,9 +666,9 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         const int kk = 32 * i + lane;
         swr[i] = (active && kk < G) ? __ldg(p.w_scales + (size_t)blk * G + kk) : 0.0f;
       }
-      float acc[32];
+      float acc[CPT];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < G; ++kb, ++it) {
         const uint32_t b = it & 1u;
         const bool got = mbar_wait(smem_u32(&sh->tfull[b]), (it >> 1) & 1u, abort_flag, p.err,
@@ -665,49 +680,75 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         tc_fence_after();
         const float src = kb < 32 ? swr[0] : kb < 64 ? swr[1] : kb < 96 ? swr[2] : swr[3];
         const float swv = __shfl_sync(0xffffffffu, src, kb & 31);
-        uint32_t r[32];
-        if (active) {
-          tmem_ld_16x64b_x32(taddr0 + b * 256u, r);
-          tmem_wait_ld();
+        const float sc = active ? sa_s[kb * MT + tok] * swv : 0.0f;
+        if constexpr (MT == 64) {
+          uint32_t r[32];
+          if (active) {
+            tmem_ld_16x64b_x32(taddr0 + b * 256u, r);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j]));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
-        if (active) {
-          const float sc = sa_s[kb * kSmallMaxT + tok] * swv;
+            for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r[j]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+          if (active) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            fma2(acc[j], acc[j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]), sc, sc);
+            for (int j = 0; j < 32; j += 2)
+              fma2(acc[j], acc[j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]), sc, sc);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) {
+            uint32_t r[16];
+            if (active) {
+              tmem_ld16(taddr0 + b * 256u + (uint32_t)c, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(r[j]));
+            }
+            if (c == 48) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&sh->tempty[b]));
+            }
+            if (active) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 2)
+                fma2(acc[c + j], acc[c + j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                     sc, sc);
+            }
+          }
         }
       }
       if (!ok) break;
       if (!active) continue;
 
-      // argmax over this thread's 32 columns (ascending rows), then merge
+      // argmax over this thread's columns (ascending rows), then merge
       const int row0 = blk0 * 128 + 64 * g;          // first row of the group
       const int last_row = min(row0 + 63, p.V - 1);
       const bool tok_ok = tok < p.T;
       if (row0 / p.shard_width == last_row / p.shard_width) {
-        // the whole group is one shard: thread max, then the partner lane
+        // the whole group is one shard: thread max, then (MT = 64) the partner lane
         float best = -INFINITY;
         int bi = -1;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int v = row0 + 2 * j + colpar;
+        for (int j = 0; j < CPT; ++j) {
+          const int v = row0 + col_of(j);
           if (v < p.V && (bi < 0 || acc[j] > best)) {
             best = acc[j];
             bi = v;
           }
         }
-        const float ob = __shfl_xor_sync(0xffffffffu, best, 2);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, 2);
-        if (oi >= 0 && (bi < 0 || ob > best || (ob == best && oi < bi))) {
-          best = ob;
-          bi = oi;
+        if constexpr (MT == 64) {
+          const float ob = __shfl_xor_sync(0xffffffffu, best, 2);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, 2);
+          if (oi >= 0 && (bi < 0 || ob > best || (ob == best && oi < bi))) {
+            best = ob;
+            bi = oi;
+          }
         }
-        if ((lane & 2) == 0 && tok_ok && bi >= 0)
+        if ((MT == 128 || (lane & 2) == 0) && tok_ok && bi >= 0)
           atomicMax(&p.keys[(size_t)(row0 / p.shard_width) * kKeyStride + tok],
                     pack_key(best, (uint32_t)bi));
       } else {
@@ -715,8 +756,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         float best = -INFINITY;
         int bi = -1, cur = -1;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int v = row0 + 2 * j + colpar;
+        for (int j = 0; j < CPT; ++j) {
+          const int v = row0 + col_of(j);
           if (v >= p.V) break;
           const int sv = v / p.shard_width;
           if (sv != cur) {
@@ -833,7 +874,7 @@ cudaError_t launch_by_tokens(const Stage2Params &p, const void *act_codes, const
   if (p.T <= 32) return launch_cfg<16, 2, kPacked>(p, act_codes, w, num_sms, stream);
   if (p.T <= 64) return launch_cfg<16, 4, kPacked>(p, act_codes, w, num_sms, stream);
   if (p.T <= 128) return launch_cfg<32, 4, kPacked>(p, act_codes, w, num_sms, stream);
-  return launch_cfg<128, 2, kPacked>(p, act_codes, w, num_sms, stream);
+  return launch_cfg<64, 4, kPacked>(p, act_codes, w, num_sms, stream);
 }
 
 // Re-lays the row-major [V][H] e4m3 weight into [ceil(V/128)][H/128] blocks of
@@ -861,23 +902,23 @@ size_t stage2_workspace_bytes(int S) {
   return (size_t)S * kKeyStride * sizeof(unsigned long long) + 16u;
 }
 
-template <bool kPacked>
+template <int MT, bool kPacked>
 cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const void *w,
                          int num_sms, cudaStream_t stream) {
   CUtensorMap tw, ta;
   std::memset(&tw, 0, sizeof(tw));
   if (!kPacked && !encode_u8_map(&tw, w, (uint64_t)p.V, (uint64_t)p.H, 128))
     return cudaErrorInvalidValue;
-  if (!encode_u8_map(&ta, act_codes, (uint64_t)p.T, (uint64_t)p.H, (uint32_t)kSmallMaxT))
+  if (!encode_u8_map(&ta, act_codes, (uint64_t)p.T, (uint64_t)p.H, (uint32_t)MT))
     return cudaErrorInvalidValue;
-  const size_t fixed =
-      1024 /*align pad*/ + (size_t)p.G * kSmallMaxT * 4 + sizeof(SmallSmem) + 64;
+  constexpr uint32_t kStage = small_stage_bytes<MT>();
+  const size_t fixed = 1024 /*align pad*/ + (size_t)p.G * MT * 4 + sizeof(SmallSmem) + 64;
   const size_t budget = 227u * 1024u;
-  int nstage = (int)((budget - fixed) / kSmallStageBytes);
+  int nstage = (int)((budget - fixed) / kStage);
   if (nstage > 8) nstage = 8;
   if (nstage < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = fixed + (size_t)nstage * kSmallStageBytes;
-  auto kern = lm_head_small_kernel<kPacked>;
+  const size_t smem = fixed + (size_t)nstage * kStage;
+  auto kern = lm_head_small_kernel<MT, kPacked>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -888,8 +929,11 @@ cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const voi
 cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const void *w,
                           int num_sms, cudaStream_t stream) {
   if (p.T <= kSmallMaxT && g_small_enabled) {
-    if (p.w_packed) return launch_small<true>(p, act_codes, w, num_sms, stream);
-    return launch_small<false>(p, act_codes, w, num_sms, stream);
+    if (p.T <= 64)
+      return p.w_packed ? launch_small<64, true>(p, act_codes, w, num_sms, stream)
+                        : launch_small<64, false>(p, act_codes, w, num_sms, stream);
+    return p.w_packed ? launch_small<128, true>(p, act_codes, w, num_sms, stream)
+                      : launch_small<128, false>(p, act_codes, w, num_sms, stream);
   }
   if (p.w_packed) return launch_by_tokens<true>(p, act_codes, w, num_sms, stream);
   return launch_by_tokens<false>(p, act_codes, w, num_sms, stream);
