@@ -110,3 +110,26 @@ def test_stage1_is_deterministic_and_reuses_outputs(nfq):
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.uint8) if x.dtype == torch.bfloat16 else x,
                            y.view(torch.uint8) if y.dtype == torch.bfloat16 else y)
+
+
+@pytest.mark.parametrize("cuts", [(0, 1, 40), (0, 17, 23, 40), (0, 39, 40)])
+def test_stage1_row_ranges_compose(nfq, cuts):
+    """A sequence-parallel rank owns a contiguous range of token rows: calling
+    the stage on each range (pointer offsets into the same buffers) gives the
+    same bytes as one call over all rows, because every row is independent."""
+    w = synth.workload("decode_c64", T=cuts[-1], seed=5)
+    inp = synth.stage1_inputs(w)
+    parts = [to_dev_bf16(p) for p in inp["partials"]]
+    res, nw = to_dev_bf16(inp["residual"]), to_dev_bf16(inp["norm_w"])
+    whole = nfq.mtp_reduce_norm_quant(parts, res, nw)
+    hid = torch.empty_like(whole[0])
+    cod = torch.empty_like(whole[1])
+    sca = torch.empty_like(whole[2])
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        nfq.mtp_reduce_norm_quant([p[a:b] for p in parts], res[a:b], nw,
+                                  hidden_out=hid[a:b], codes_out=cod[a:b], scales_out=sca[a:b])
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    assert torch.equal(hid.view(torch.int16), whole[0].view(torch.int16))
+    assert torch.equal(cod, whole[1]) and torch.equal(sca, whole[2])
+    check_stage1(bf16_host(hid), cod.cpu().numpy(), sca.cpu().numpy(), run_oracle(inp))
