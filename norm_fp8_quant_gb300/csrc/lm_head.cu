@@ -446,8 +446,8 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 //
 // Warps: 0..15 epilogue (lane quadrant w%4 = tokens 16*(w%4)..+15, column
 // group w/4 = tile columns 64*(w/4)..+63), 16 producer, 17 TMEM + MMA.
-// A CTA streams a contiguous range of 128-row blocks, two per tile (the last
-// tile of a range may hold one).  Two 256-column accumulators in TMEM.
+// A CTA streams a contiguous range of 128-row blocks, two per tile (the first
+// tile of an odd range holds one).  Two 256-column accumulators in TMEM.
 
 constexpr int kSmallMaxT = 128;                 // tokens per launch of the token-major form
 constexpr int kSmallEpiWarps = 16;
@@ -487,6 +487,21 @@ __device__ __forceinline__ void finish_launch(const Stage2Params &p, int *last_f
       if (p.max_logit_out) p.max_logit_out[n] = key_value(best);
     }
     if (threadIdx.x == 0) *p.counter = 0u;
+  }
+}
+
+// Tile ti of a CTA's block range [b_begin, b_end): pairs of 128-row blocks.
+// An odd range starts with its single block, so that the one tile whose MMAs
+// carry half the weight bytes runs while every CTA is still sharing HBM, not
+// at the end where it would set the finishing time.
+__device__ __forceinline__ void small_tile(int b_begin, int b_end, int ti, int &blk0, int &nb) {
+  const bool odd = ((b_end - b_begin) & 1) != 0;
+  if (odd && ti == 0) {
+    blk0 = b_begin;
+    nb = 1;
+  } else {
+    blk0 = b_begin + 2 * ti - (odd ? 1 : 0);
+    nb = 2;
   }
 }
 
@@ -555,8 +570,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      const int blk0 = b_begin + 2 * ti;
-      const int nb = (blk0 + 1 < b_end) ? 2 : 1;
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
       for (int kb = 0; kb < G; ++kb, ++it) {
         const uint32_t s = it % (uint32_t)nstage;
         const uint32_t ph = (it / (uint32_t)nstage) & 1u;
@@ -599,8 +614,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      const int blk0 = b_begin + 2 * ti;
-      const int nb = (blk0 + 1 < b_end) ? 2 : 1;
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
       const uint32_t idesc = idesc_e4m3_f32(MT, (uint32_t)(nb * 128));
       for (int kb = 0; kb < G; ++kb, ++it) {
         const uint32_t s = it % (uint32_t)nstage;
@@ -655,8 +670,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      const int blk0 = b_begin + 2 * ti;
-      const int nb = (blk0 + 1 < b_end) ? 2 : 1;
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
       const bool active = quad_active && (g < 2 * nb);
       const int blk = blk0 + (g >> 1);             // the 128-row scale block of this group
       // this tile's weight-scale row, spread over the lanes (lane l: sw[32i + l])
