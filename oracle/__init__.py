@@ -68,6 +68,16 @@ def _load():
         lib.or_argmax.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   _P, _P, _P, _P, _P]
         lib.or_argmax.restype = None
+        lib.or_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+        lib.or_e2m1_to_f32.restype = ctypes.c_float
+        lib.or_f32_to_e2m1.argtypes = [ctypes.c_float]
+        lib.or_f32_to_e2m1.restype = ctypes.c_uint8
+        lib.or_nvfp4_quant.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P]
+        lib.or_nvfp4_quant.restype = None
+        lib.or_lm_head_logits_nvfp4.argtypes = [_P, _P, _P, ctypes.c_int, _P, ctypes.c_int,
+                                                _P, _P, ctypes.c_float, ctypes.c_int,
+                                                ctypes.c_int, _P]
+        lib.or_lm_head_logits_nvfp4.restype = None
         _lib = lib
     return _lib
 
@@ -175,4 +185,63 @@ def shard_gaps(logits, S: int) -> np.ndarray:
     for s in range(S):
         r = argmax(L[:, s * w:(s + 1) * w], 1)
         out[:, s] = r["gap"]
+    return out
+
+
+# ---------------------------------------------------------- NVFP4 variant --
+
+NVFP4_BLOCK = 16
+
+
+def e2m1_to_f32(codes) -> np.ndarray:
+    """Decode 4-bit e2m1 codes (one per array element, 0..15)."""
+    lib = _load()
+    c = _c(codes, np.uint8).ravel()
+    return np.array([lib.or_e2m1_to_f32(int(v)) for v in c], dtype=np.float32).reshape(np.shape(codes))
+
+
+def f32_to_e2m1(x) -> np.ndarray:
+    lib = _load()
+    x = _c(x, np.float32).ravel()
+    return np.array([lib.or_f32_to_e2m1(float(v)) for v in x], dtype=np.uint8)
+
+
+def nvfp4_quant(hidden):
+    """NVFP4 codes [R][H/2] (packed), block scales [R][H/16], row scales [R] of
+    BF16 rows [R][H]."""
+    h = _c(hidden, np.uint16)
+    R, H = h.shape
+    assert H % NVFP4_BLOCK == 0
+    codes = np.empty((R, H // 2), np.uint8)
+    bs = np.empty((R, H // NVFP4_BLOCK), np.uint8)
+    gs = np.empty(R, np.float32)
+    _load().or_nvfp4_quant(h.ctypes.data, R, H, codes.ctypes.data, bs.ctypes.data, gs.ctypes.data)
+    return {"codes": codes, "block_scales": bs, "global_scales": gs}
+
+
+def reduce_norm_quant_nvfp4(partials, residual, norm_w, eps: float = EPS):
+    """Stage 1 with the NVFP4 activation: the BF16 hidden of reduce_norm_quant,
+    quantised by nvfp4_quant."""
+    o = reduce_norm_quant(partials, residual, norm_w, eps)
+    q = nvfp4_quant(o["hidden"])
+    return {"hidden": o["hidden"], **q}
+
+
+def lm_head_logits_nvfp4(qa, sa, ga, qw, sw, gw: float, tokens=None, v0: int = 0,
+                         v1: int | None = None):
+    """fp32 logits [len(tokens)][v1-v0] of the NVFP4 LM head."""
+    qa = _c(qa, np.uint8)
+    T, H2 = qa.shape
+    H = 2 * H2
+    sa = _c(sa, np.uint8)
+    ga = _c(ga, np.float32)
+    qw = _c(qw, np.uint8)
+    sw = _c(sw, np.uint8)
+    V = qw.shape[0]
+    v1 = V if v1 is None else v1
+    tok = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
+    out = np.empty((tok.size, v1 - v0), np.float32)
+    _load().or_lm_head_logits_nvfp4(qa.ctypes.data, sa.ctypes.data, ga.ctypes.data, H,
+                                    tok.ctypes.data, tok.size, qw.ctypes.data, sw.ctypes.data,
+                                    float(gw), v0, v1, out.ctypes.data)
     return out

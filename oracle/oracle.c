@@ -239,3 +239,132 @@ void or_argmax(const float *logits, int n, int V, int S, int32_t *tok, float *va
     }
   }
 }
+
+/* ======================================================= NVFP4 variant == */
+/*
+ * The benchmark pages serve an NVFP4 checkpoint ("[Spec Decode][Perf] Fuse the
+ * MTP trailing all-reduce; local-argmax draft tokens", Benchmarks) but define no
+ * FP4 arithmetic.  The readings here follow the published NVFP4 format: values
+ * are OCP FP4 e2m1 codes, each block of 16 consecutive elements along the hidden
+ * dimension carries one unsigned e4m3 scale, and a row (token or tensor) carries
+ * one fp32 scale chosen so that the largest block scale is 448:
+ *   g      = amax_row / (448 * 6)                                      (fp32)
+ *   sb     = e4m3_rne_sat(amax_block / (6 * g))                        (fp32, two roundings)
+ *   eff    = dec(sb) * g                                               (fp32)
+ *   code   = eff == 0 ? 0 : e2m1_rne_sat(x / eff)                      (fp32 divide)
+ * Codes are packed two to a byte, element 2i in the low nibble of byte i.
+ */
+
+/* OCP FP4 e2m1: 1 sign, 2 exponent (bias 1), 1 mantissa bit; magnitudes
+ * 0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6; no infinities or NaN. */
+float or_e2m1_to_f32(uint8_t c) {
+  int s = (c >> 3) & 1, ex = (c >> 1) & 3, m = c & 1;
+  double v = (ex == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, ex - 1);
+  return (float)(s ? -v : v);
+}
+
+/* f32 -> e2m1, round to nearest even, saturating to +-6.  The spacing is 0.5
+ * below 2, 1 in [2, 4) and 2 in [4, 8); an even multiple of the spacing has a
+ * zero mantissa bit.  A negative value that rounds to zero keeps its sign (8). */
+uint8_t or_f32_to_e2m1(float f) {
+  uint8_t sign = signbit(f) ? 8 : 0;
+  double a = fabs((double)f);
+  if (isnan(f)) return sign | 7;
+  if (a >= 6.0) return sign | 7;
+  double q = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+  double r = rint(a / q) * q;
+  if (r > 6.0) r = 6.0;
+  if (r == 0.0) return sign;
+  if (r == 0.5) return sign | 1;
+  int e;
+  frexp(r, &e);                       /* r in [2^(e-1), 2^e) */
+  int ex = e;                         /* biased exponent: r = (1 + m/2) * 2^(ex-1) */
+  int m = (int)((r / ldexp(1.0, e - 1) - 1.0) * 2.0);
+  return sign | (uint8_t)((ex << 1) | m);
+}
+
+/*
+ * NVFP4 quantisation of BF16 rows [R][H] (H a multiple of 16): codes [R][H/2]
+ * (packed), block scales [R][H/16] (unsigned e4m3 codes), row scales [R].
+ */
+void or_nvfp4_quant(const uint16_t *hidden, int R, int H, uint8_t *codes, uint8_t *bscales,
+                    float *gscales) {
+  const int B = H / 16;
+  for (int r = 0; r < R; ++r) {
+    const uint16_t *y = hidden + (size_t)r * (size_t)H;
+    float amax = 0.0f;
+    for (int h = 0; h < H; ++h) {
+      float v = fabsf(or_bf16_to_f32(y[h]));
+      if (v > amax) amax = v;
+    }
+    const float g = amax / 2688.0f;
+    gscales[r] = g;
+    for (int b = 0; b < B; ++b) {
+      float ab = 0.0f;
+      for (int j = 0; j < 16; ++j) {
+        float v = fabsf(or_bf16_to_f32(y[b * 16 + j]));
+        if (v > ab) ab = v;
+      }
+      uint8_t sb = 0;
+      if (g != 0.0f) {
+        const float d = 6.0f * g;
+        sb = or_f32_to_e4m3(ab / d);
+      }
+      bscales[(size_t)r * B + b] = sb;
+      const float eff = or_e4m3_to_f32(sb) * g;
+      for (int j = 0; j < 16; j += 2) {
+        uint8_t lo = 0, hi = 0;
+        if (eff != 0.0f) {
+          lo = or_f32_to_e2m1(or_bf16_to_f32(y[b * 16 + j]) / eff);
+          hi = or_f32_to_e2m1(or_bf16_to_f32(y[b * 16 + j + 1]) / eff);
+        }
+        codes[(size_t)r * (H / 2) + (size_t)(b * 16 + j) / 2] = (uint8_t)(lo | (hi << 4));
+      }
+    }
+  }
+}
+
+/*
+ * NVFP4 LM head logits for the tokens tok[0..n_tok) and rows v0 <= v < v1:
+ *   c_b = (dec(sa[t][b]) * dec(sw[v][b])) * sum_{j<16} e2m1(qa[t][16b+j]) * e2m1(qw[v][16b+j])
+ *   L   = (sum_b c_b, b ascending, fp32) * (ga[t] * gw)
+ * Each c_b is exact in fp32 (products of 4-bit significands); only the sum over
+ * blocks and the two final multiplications round.
+ * qa [T][H/2], sa [T][H/16], ga [T]; qw [V][H/2], sw [V][H/16]; gw a scalar.
+ */
+void or_lm_head_logits_nvfp4(const uint8_t *qa, const uint8_t *sa, const float *ga, int H,
+                             const int32_t *tok, int n_tok, const uint8_t *qw,
+                             const uint8_t *sw, float gw, int v0, int v1, float *logits) {
+  const int B = H / 16;
+  float *ad = (float *)malloc(sizeof(float) * (size_t)n_tok * (size_t)H);
+  float *wd = (float *)malloc(sizeof(float) * (size_t)H);
+  if (!ad || !wd) { free(ad); free(wd); return; }
+  for (int i = 0; i < n_tok; ++i) {
+    const size_t t = (size_t)tok[i];
+    for (int k = 0; k < H; ++k) {
+      uint8_t byte = qa[t * (size_t)(H / 2) + (size_t)k / 2];
+      ad[(size_t)i * H + k] = or_e2m1_to_f32((k & 1) ? (byte >> 4) : (byte & 15));
+    }
+  }
+  const size_t W = (size_t)(v1 - v0);
+  for (int v = v0; v < v1; ++v) {
+    for (int k = 0; k < H; ++k) {
+      uint8_t byte = qw[(size_t)v * (size_t)(H / 2) + (size_t)k / 2];
+      wd[k] = or_e2m1_to_f32((k & 1) ? (byte >> 4) : (byte & 15));
+    }
+    for (int i = 0; i < n_tok; ++i) {
+      const size_t t = (size_t)tok[i];
+      const float *a = ad + (size_t)i * H;
+      float acc = 0.0f;
+      for (int b = 0; b < B; ++b) {
+        float bs = 0.0f;
+        for (int j = 0; j < 16; ++j) bs = bs + a[b * 16 + j] * wd[b * 16 + j];
+        const float s = or_e4m3_to_f32(sa[t * (size_t)B + b]) * or_e4m3_to_f32(sw[(size_t)v * B + b]);
+        acc = acc + s * bs;
+      }
+      logits[(size_t)i * W + (size_t)(v - v0)] = acc * (ga[t] * gw);
+    }
+  }
+  free(ad);
+  free(wd);
+}

@@ -384,3 +384,166 @@ def test_tie_stress_construction_is_reproduced_by_the_oracle():
         assert r["gap"][t] == 0.0                       # an exact duplicate maximum
         twin = [v for v in range(w.V) if v != row and L[t, v] == L[t, row]]
         assert len(twin) == 1 and twin[0] // width == row // width + 1
+
+
+# ------------------------------------------------------------------ NVFP4 --
+# OCP Microscaling Formats v1.0, FP4 E2M1: the eight magnitudes of the format.
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_matches_the_format_table():
+    got = oracle.e2m1_to_f32(np.arange(16))
+    for c in range(16):
+        want = -E2M1_TABLE[c & 7] if c & 8 else E2M1_TABLE[c & 7]
+        assert got[c] == want and (math.copysign(1, got[c]) < 0) == bool(c & 8)
+
+
+def _e2m1_brute(x):
+    """nearest of the eight magnitudes, ties to the even code (mantissa bit 0),
+    saturating at 6; the sign is kept."""
+    a = min(abs(float(x)), 6.0)
+    d = [abs(a - v) for v in E2M1_TABLE]
+    best = min(d)
+    cands = [i for i in range(8) if d[i] == best]
+    c = cands[0] if len(cands) == 1 else [i for i in cands if i % 2 == 0][0]
+    return c | (8 if math.copysign(1, x) < 0 else 0)
+
+
+def test_e2m1_encode_is_nearest_even_by_brute_force():
+    xs = list(rng.uniform(-8, 8, 4000).astype(np.float32))
+    mids = [(E2M1_TABLE[i] + E2M1_TABLE[i + 1]) / 2 for i in range(7)]
+    xs += mids + [-m for m in mids] + [6.0, 6.5, 7.0, 1e9, -1e9, 0.0, -0.0, 1e-30, -1e-30]
+    got = oracle.f32_to_e2m1(np.array(xs, np.float32))
+    for x, g in zip(xs, got):
+        assert g == _e2m1_brute(np.float32(x)), (x, g)
+    # every code survives a round trip
+    assert np.array_equal(oracle.f32_to_e2m1(oracle.e2m1_to_f32(np.arange(16))), np.arange(16))
+
+
+def _read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, *vals = line.split()
+            out[key] = vals
+    return out
+
+
+def _unpack(codes):
+    c = np.asarray(codes, np.uint8)
+    return np.stack([c & 15, c >> 4], axis=-1).reshape(c.shape[0], -1)
+
+
+def test_nvfp4_quant_hand_derived_two_blocks():
+    g = _read_golden("nvfp4_two_blocks.txt")
+    vals = np.array([float(v) for v in g["values"]], np.float32)
+    q = oracle.nvfp4_quant(bf16_bits_of(vals)[None, :])
+    assert q["global_scales"][0] == np.float32(g["row_scale"][0])
+    assert q["block_scales"][0].tolist() == [int(v, 16) for v in g["block_scales"]]
+    assert _unpack(q["codes"])[0].tolist() == [int(v) for v in g["codes"]]
+
+
+def _random_rows(R, H, seed):
+    r = np.random.default_rng(seed)
+    x = r.normal(0, 1, (R, H)).astype(np.float32) * np.exp2(r.integers(-6, 6, (R, 1))).astype(np.float32)
+    x[:, r.integers(0, H, 3)] *= 30.0     # a few outlier channels
+    return torch_bf16_bits(x)
+
+
+def test_nvfp4_quant_invariants():
+    R, H = 24, 512
+    hid = _random_rows(R, H, 7)
+    hid[3] = 0                      # an all-zero row
+    hid[5, 32:48] = 0               # an all-zero block
+    q = oracle.nvfp4_quant(hid)
+    y = oracle.bf16_to_f32(hid).reshape(R, H)
+    codes = _unpack(q["codes"])
+    vals = np.where(codes & 8, -1.0, 1.0) * np.array(E2M1_TABLE)[codes & 7]
+    sb = torch_e4m3_decode(q["block_scales"]).astype(np.float64)
+    gs = q["global_scales"].astype(np.float64)
+    for r in range(R):
+        amax = np.abs(y[r]).max()
+        if amax == 0:
+            assert gs[r] == 0 and not q["block_scales"][r].any() and not codes[r].any()
+            continue
+        # the row scale is amax / (448 * 6) and the row's largest block scale is 448
+        assert gs[r] == np.float32(np.float32(amax) / np.float32(2688.0))
+        assert q["block_scales"][r].max() == 0x7E
+        for b in range(H // 16):
+            blk = y[r, 16 * b:16 * b + 16].astype(np.float64)
+            eff = np.float32(np.float32(sb[r, b]) * np.float32(gs[r]))
+            cb = codes[r, 16 * b:16 * b + 16]
+            if eff == 0:
+                assert not cb.any()
+                continue
+            # each code is the nearest e2m1 value of y / eff (brute force)
+            for j in range(16):
+                assert cb[j] == _e2m1_brute(np.float32(np.float32(blk[j]) / eff))
+            # a block whose scale is a normal e4m3 value maps its maximum to +-6
+            if sb[r, b] >= 2.0 ** -6:
+                jm = int(np.argmax(np.abs(blk)))
+                assert abs(vals[r, 16 * b + jm]) == 6.0
+            # reconstruction within half an e2m1 step of the scaled value
+            step = np.where(np.abs(blk) / eff < 2, 0.5, np.where(np.abs(blk) / eff < 4, 1.0, 2.0))
+            err = np.abs(blk - vals[r, 16 * b:16 * b + 16] * eff)
+            assert np.all(err <= 0.5 * step * eff * (1 + 1e-6) + 1e-30)
+
+
+def test_nvfp4_quant_is_invariant_to_power_of_two_row_scaling():
+    hid = _random_rows(6, 256, 11)
+    y = oracle.bf16_to_f32(hid).reshape(6, 256)
+    q1 = oracle.nvfp4_quant(hid)
+    q2 = oracle.nvfp4_quant(bf16_bits_of(y * np.float32(8.0)))
+    assert np.array_equal(q1["codes"], q2["codes"])
+    assert np.array_equal(q1["block_scales"], q2["block_scales"])
+    assert np.array_equal(q2["global_scales"], q1["global_scales"] * np.float32(8.0))
+
+
+def _nvfp4_dequant(codes, bs, gs):
+    c = _unpack(codes)
+    v = np.where(c & 8, -1.0, 1.0) * np.array(E2M1_TABLE)[c & 7]
+    s = torch_e4m3_decode(bs).astype(np.float64)
+    return v * np.repeat(s, 16, axis=1) * np.asarray(gs, np.float64)[:, None]
+
+
+def test_nvfp4_lm_head_one_hot_activation_gives_a_weight_column():
+    H, V = 256, 40
+    w = oracle.nvfp4_quant(_random_rows(V, H, 3))
+    gw = np.float32(0.75)
+    for k in (0, 1, 17, 255):
+        codes = np.zeros((1, H // 2), np.uint8)
+        codes[0, k // 2] = 0x2 << (4 * (k % 2))            # e2m1 1.0 at element k
+        sa = np.zeros((1, H // 16), np.uint8)
+        sa[0, k // 16] = 0x38                               # block scale 1.0
+        L = oracle.lm_head_logits_nvfp4(codes, sa, np.ones(1, np.float32), w["codes"],
+                                        w["block_scales"], gw)
+        wd = _nvfp4_dequant(w["codes"], w["block_scales"], np.ones(V))
+        want = (wd[:, k].astype(np.float32) * gw).astype(np.float32)
+        assert np.array_equal(L[0], want)
+
+
+def test_nvfp4_lm_head_matches_fp64_within_the_summation_bound():
+    H, V, T = 512, 96, 5
+    a = oracle.nvfp4_quant(_random_rows(T, H, 21))
+    w = oracle.nvfp4_quant(_random_rows(V, H, 22))
+    gw = np.float32(0.01)
+    L = oracle.lm_head_logits_nvfp4(a["codes"], a["block_scales"], a["global_scales"],
+                                    w["codes"], w["block_scales"], gw)
+    ad = _nvfp4_dequant(a["codes"], a["block_scales"], np.ones(T))
+    wd = _nvfp4_dequant(w["codes"], w["block_scales"], np.ones(V))
+    exact = ad @ wd.T
+    absd = np.abs(ad) @ np.abs(wd).T
+    n = H // 16 + 2
+    gam = n * 2.0 ** -24 / (1 - n * 2.0 ** -24)
+    scale = a["global_scales"].astype(np.float64)[:, None] * float(gw)
+    assert np.all(np.abs(L - exact * scale) <= gam * absd * scale + 1e-30)
+    # the activation row scale and the weight scale enter as plain factors
+    L2 = oracle.lm_head_logits_nvfp4(a["codes"], a["block_scales"], a["global_scales"] * 2,
+                                     w["codes"], w["block_scales"], gw)
+    assert np.array_equal(L2, L * 2)
+    # transposing the roles of tokens and rows gives the transposed logits
+    Lt = oracle.lm_head_logits_nvfp4(w["codes"], w["block_scales"], np.ones(V, np.float32),
+                                     a["codes"], a["block_scales"], np.float32(1.0))
+    assert np.allclose(Lt.T * scale, L, rtol=1e-5, atol=0)
