@@ -8,6 +8,8 @@
  *   nfq_lm_head_fp8_argmax      packed FP8 activation x block-scaled FP8 LM
  *                               head -> greedy draft token per row, via a
  *                               vocab-sharded argmax; logits are never stored
+ * and their NVFP4 variants (…_nvfp4), which carry the activation and the
+ * weight in the NVFP4 format and use the tensor cores' block scaling.
  *
  * Sources (page title, section):
  *   [R] "[Quant][MTP] Reuse packed FP8 logits inputs" (vLLM pull request 51947),
@@ -234,6 +236,80 @@ int nfq_lm_head_fp8_argmax_noalloc(const nfq_quant_act *a, const uint8_t *w,
                                    float *shard_val_out, void *stream);
 
 /*
+ * NVFP4 variant of both stages.  [F] Benchmarks serve an NVFP4 checkpoint
+ * (GLM-5.2-NVFP4); the pages define no FP4 arithmetic, so the published NVFP4
+ * format is used: OCP FP4 e2m1 values, one unsigned e4m3 scale per 16
+ * consecutive hidden elements, and one fp32 scale per row (per token for the
+ * activation, per tensor for the weight) so that a row's largest block scale is
+ * 448.  Element (t, h) represents
+ *   e2m1(codes[t][h/2] nibble h%2) * e4m3(block_scales[t][h/16]) * row_scales[t]
+ * with element 2i in the low nibble of byte i.
+ *   codes        uint8 [tokens][hidden/2]
+ *   block_scales uint8 [tokens][hidden/16]   (unsigned e4m3 codes, < 0x80)
+ *   row_scales   fp32  [tokens]
+ *   block        must be 16
+ */
+typedef struct {
+  uint8_t *codes;
+  uint8_t *block_scales;
+  float *row_scales;
+  int32_t tokens;
+  int32_t hidden;
+  int32_t block;
+} nfq_fp4_act;
+
+/*
+ * nfq_mtp_reduce_norm_quant_nvfp4 — stage 1 with the NVFP4 activation instead
+ * of the packed FP8 one; the reduction, residual, RMSNorm and BF16 hidden are
+ * those of nfq_mtp_reduce_norm_quant (same arguments and rules).  Per token:
+ *   g    = max_h |hidden| / (448 * 6)                            fp32
+ *   per block b of 16: sb = e4m3_rne_satfinite(max_b |hidden| / (6 * g)), 0 when g == 0
+ *   eff  = e4m3(sb) * g;  code = e2m1_rne_satfinite(hidden / eff), 0 when eff == 0
+ *   q_out  codes [T][H/2], block_scales [T][H/16], row_scales [T];
+ *          q_out->tokens == T, q_out->hidden == H, q_out->block == 16
+ *   H      H % 256 == 0 and 256 <= H <= 16384 (one CTA holds a row)
+ */
+int nfq_mtp_reduce_norm_quant_nvfp4(const void *const *partials, int k, const void *residual,
+                                    const void *norm_w, float eps, int T, int H,
+                                    void *hidden_out, const nfq_fp4_act *q_out, void *stream);
+
+/*
+ * NVFP4 LM-head weight in the streaming layout, built once from the row-major
+ * codes [V][H/2] and block scales [V][H/16].  Rows are cut into blocks of 128
+ * and the hidden dimension into steps of 256 elements (128 code bytes, 16 block
+ * scales).  The packed buffer holds ceil(V/128) * (H/256) code blocks of 16 KB
+ * (block (vt, s) at (vt * H/256 + s) * 16384; row r at r * 128, 16-byte chunk c
+ * at chunk position c XOR (r mod 8)) followed by as many 2 KB scale blocks
+ * (block (vt, s) at the same index * 2048 after the codes): word (kk, i, c) at
+ * ((kk * 32 + i) * 4 + c) * 4 holds the scales of the four 16-element blocks
+ * 4kk .. 4kk+3 of step s for row 32c + i, one byte each, lowest block first.
+ * Rows past V are zero.
+ * nfq_lm_head_nvfp4_packed_bytes: ceil(V/128) * (H/256) * 18432 (0 if invalid;
+ *   H % 256 == 0).
+ * nfq_lm_head_nvfp4_pack_weights: one kernel on `stream`; device pointers,
+ *   16-byte aligned, no overlap; NFQ_ERR_WORKSPACE if packed_bytes is short.
+ */
+size_t nfq_lm_head_nvfp4_packed_bytes(int V, int H);
+
+int nfq_lm_head_nvfp4_pack_weights(const uint8_t *codes, const uint8_t *block_scales, int V,
+                                   int H, void *w_packed, size_t packed_bytes, void *stream);
+
+/*
+ * nfq_lm_head_nvfp4_argmax — the LM head and argmax of nfq_lm_head_fp8_argmax
+ * on the NVFP4 activation and the packed NVFP4 weight (tensor scale w_scale):
+ *   L[t][v] = (sum_b e4m3(a.block_scales[t][b]) * e4m3(w_block_scales[v][b])
+ *                  * sum_{j<16} e2m1(a[t][16b+j]) * e2m1(w[v][16b+j]))
+ *             * (a.row_scales[t] * w_scale)
+ * The block-scaled products are summed by the tensor cores in fp32.  Outputs,
+ * shards, ties, workspace and errors as for nfq_lm_head_fp8_argmax; V >= 1,
+ * H % 256 == 0; rows are processed 128 tokens at a time.
+ */
+int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w_scale, int V,
+                             int S, int32_t *tokens_out, float *max_logit_out,
+                             int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                             size_t ws_bytes, void *stream);
+
+/*
  * Tuning hooks (process-wide, not thread-safe; for benchmarks and tests).
  * nfq_stage1_plan: the stage-1 launch plan for (T, H, k) on a GPU with
  *   num_sms SMs: out7 = {cluster CTAs per row, 16-byte vectors per thread,
@@ -242,7 +318,7 @@ int nfq_lm_head_fp8_argmax_noalloc(const nfq_quant_act *a, const uint8_t *w,
  * nfq_stage1_tune: force the cluster size, vectors per thread, ring slots and
  *   inputs per slot of later stage-1 launches (0 = automatic; invalid choices
  *   fall back).
- * nfq_lm_head_small_batch: 1 (default) runs batches of at most 64 tokens on the
+ * nfq_lm_head_small_batch: 1 (default) runs batches of at most 128 tokens on the
  *   token-major kernel; 0 forces the weight-major kernel for every batch size.
  */
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7);

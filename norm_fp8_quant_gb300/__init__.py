@@ -9,6 +9,8 @@ the device is not a compute-capability 10.3 GPU, calls raise.
       -> (hidden bf16 [T][H], codes uint8 [T][H], scales fp32 [T][H/128])
   lm_head_fp8_argmax(codes, scales, w, w_scales, S, workspace=None)
       -> draft tokens int32 [T] (optionally max logit and per-shard results)
+  mtp_reduce_norm_quant_nvfp4 / pack_lm_head_weights_nvfp4 / lm_head_nvfp4_argmax
+      the same two stages with the NVFP4 activation and weight
 """
 from __future__ import annotations
 
@@ -42,6 +44,15 @@ class QuantAct(ctypes.Structure):
                 ("tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("group", ctypes.c_int32)]
 
+
+class Fp4Act(ctypes.Structure):
+    """nfq_fp4_act: NVFP4 activation descriptor (host struct)."""
+    _fields_ = [("codes", ctypes.c_void_p), ("block_scales", ctypes.c_void_p),
+                ("row_scales", ctypes.c_void_p), ("tokens", ctypes.c_int32),
+                ("hidden", ctypes.c_int32), ("block", ctypes.c_int32)]
+
+
+FP4_BLOCK = 16
 
 _lib = None
 _P = ctypes.c_void_p
@@ -89,6 +100,19 @@ def load(path: str = LIB_PATH):
     lib.nfq_stage1_tune.restype = None
     lib.nfq_lm_head_small_batch.argtypes = [ctypes.c_int]
     lib.nfq_lm_head_small_batch.restype = None
+    lib.nfq_mtp_reduce_norm_quant_nvfp4.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
+                                                    ctypes.c_int, ctypes.c_int, _P,
+                                                    ctypes.POINTER(Fp4Act), _P]
+    lib.nfq_mtp_reduce_norm_quant_nvfp4.restype = ctypes.c_int
+    lib.nfq_lm_head_nvfp4_packed_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.nfq_lm_head_nvfp4_packed_bytes.restype = ctypes.c_size_t
+    lib.nfq_lm_head_nvfp4_pack_weights.argtypes = [_P, _P, ctypes.c_int, ctypes.c_int, _P,
+                                                   ctypes.c_size_t, _P]
+    lib.nfq_lm_head_nvfp4_pack_weights.restype = ctypes.c_int
+    lib.nfq_lm_head_nvfp4_argmax.argtypes = [ctypes.POINTER(Fp4Act), _P, ctypes.c_float,
+                                             ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _P,
+                                             ctypes.c_size_t, _P]
+    lib.nfq_lm_head_nvfp4_argmax.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -296,6 +320,104 @@ def stage1_tune(cluster: int = 0, vpt: int = 0, slots: int = 0, per_slot: int = 
 
 
 def lm_head_small_batch(enabled: bool = True):
-    """Choose the LM-head kernel family for batches of at most 64 tokens: the
+    """Choose the LM-head kernel family for batches of at most 128 tokens: the
     token-major small-batch kernel (default) or the weight-major kernel."""
     load().nfq_lm_head_small_batch(1 if enabled else 0)
+
+
+# ------------------------------------------------------------ NVFP4 form --
+
+def mtp_reduce_norm_quant_nvfp4(partials, residual, norm_w, eps: float = 1e-6,
+                                hidden_out=None, codes_out=None, block_scales_out=None,
+                                row_scales_out=None, stream=None):
+    """Stage 1 with the NVFP4 activation: returns (hidden bf16 [T][H], codes
+    uint8 [T][H/2] (e2m1 pairs), block scales uint8 [T][H/16] (e4m3), row
+    scales fp32 [T])."""
+    import torch
+    k = len(partials)
+    T, H = residual.shape
+    _need_cuda(residual, norm_w, *partials)
+    for p in partials:
+        if p.dtype != torch.bfloat16 or p.shape != (T, H):
+            raise ValueError("partials must be bf16 [T][H]")
+    if residual.dtype != torch.bfloat16 or norm_w.dtype != torch.bfloat16:
+        raise ValueError("residual and norm_w must be bf16")
+    dev = residual.device
+    hidden = hidden_out if hidden_out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    codes = codes_out if codes_out is not None else torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+    bs = (block_scales_out if block_scales_out is not None
+          else torch.empty((T, H // FP4_BLOCK), dtype=torch.uint8, device=dev))
+    gs = row_scales_out if row_scales_out is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    arr = (ctypes.c_void_p * max(k, 1))(*[p.data_ptr() for p in partials])
+    q = Fp4Act(codes.data_ptr(), bs.data_ptr(), gs.data_ptr(), T, H, FP4_BLOCK)
+    with torch.cuda.device(dev):
+        st = load().nfq_mtp_reduce_norm_quant_nvfp4(arr, k, _ptr(residual), _ptr(norm_w),
+                                                    float(eps), T, H, _ptr(hidden),
+                                                    ctypes.byref(q), _stream_ptr(stream))
+    _check(st, "nfq_mtp_reduce_norm_quant_nvfp4")
+    return hidden, codes, bs, gs
+
+
+class PackedFp4Weight:
+    """NVFP4 LM-head weight in the packed streaming layout, with its tensor scale."""
+
+    def __init__(self, data, V: int, H: int, scale: float):
+        self.data, self.V, self.H, self.scale = data, V, H, float(scale)
+        self.device = data.device
+
+    @property
+    def shape(self):
+        return (self.V, self.H)
+
+
+def pack_lm_head_weights_nvfp4(codes, block_scales, scale: float, stream=None):
+    """Pack row-major NVFP4 weight codes [V][H/2] and block scales [V][H/16]
+    (with the tensor scale) into the streaming layout."""
+    import torch
+    _need_cuda(codes, block_scales)
+    V, H2 = codes.shape
+    H = 2 * H2
+    if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or \
+            tuple(block_scales.shape) != (V, H // FP4_BLOCK):
+        raise ValueError("codes uint8 [V][H/2] and block scales uint8 [V][H/16] expected")
+    n = int(load().nfq_lm_head_nvfp4_packed_bytes(V, H))
+    if n == 0:
+        raise ValueError("invalid NVFP4 LM-head weight shape")
+    out = torch.empty(n, dtype=torch.uint8, device=codes.device)
+    with torch.cuda.device(codes.device):
+        _check(load().nfq_lm_head_nvfp4_pack_weights(_ptr(codes), _ptr(block_scales), V, H,
+                                                     _ptr(out), n, _stream_ptr(stream)),
+               "nfq_lm_head_nvfp4_pack_weights")
+    return PackedFp4Weight(out, V, H, scale)
+
+
+def lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4Weight, S: int,
+                         workspace=None, tokens_out=None, want_max: bool = False,
+                         want_shards: bool = False, stream=None):
+    """Greedy draft token per row of the NVFP4 activation against the packed
+    NVFP4 LM head (vocab-sharded argmax, ties -> lowest id)."""
+    import torch
+    T, H2 = codes.shape
+    H = 2 * H2
+    _need_cuda(codes, block_scales, row_scales)
+    if not isinstance(w, PackedFp4Weight):
+        raise ValueError("w must be a PackedFp4Weight")
+    if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or \
+            row_scales.dtype != torch.float32:
+        raise ValueError("codes/block scales uint8 and row scales float32 expected")
+    dev = codes.device
+    ws = workspace if workspace is not None else lm_head_workspace(T, S, dev, stream)
+    tokens = tokens_out if tokens_out is not None else torch.empty(T, dtype=torch.int32, device=dev)
+    mx = torch.empty(T, dtype=torch.float32, device=dev) if want_max else None
+    sidx = torch.empty((S, T), dtype=torch.int32, device=dev) if want_shards else None
+    sval = torch.empty((S, T), dtype=torch.float32, device=dev) if want_shards else None
+    q = Fp4Act(codes.data_ptr(), block_scales.data_ptr(), row_scales.data_ptr(), T, H, FP4_BLOCK)
+    opt = lambda t: ctypes.c_void_p(None) if t is None else _ptr(t)
+    with torch.cuda.device(dev):
+        st = load().nfq_lm_head_nvfp4_argmax(ctypes.byref(q), _ptr(w.data), float(w.scale), w.V,
+                                             S, _ptr(tokens), opt(mx), opt(sidx), opt(sval),
+                                             _ptr(ws), ws.numel(), _stream_ptr(stream))
+    _check(st, "nfq_lm_head_nvfp4_argmax")
+    if want_max or want_shards:
+        return tokens, mx, sidx, sval
+    return tokens

@@ -118,6 +118,48 @@ int nfq_mtp_reduce_norm_quant(const void *const *partials, int k, const void *re
   return map_cuda(e);
 }
 
+int nfq_mtp_reduce_norm_quant_nvfp4(const void *const *partials, int k, const void *residual,
+                                    const void *norm_w, float eps, int T, int H,
+                                    void *hidden_out, const nfq_fp4_act *q_out, void *stream) {
+  if (!partials || !residual || !norm_w || !hidden_out || !q_out) return NFQ_ERR_NULL;
+  if (k < 1 || k > kMaxPartials) return NFQ_ERR_SHAPE;
+  for (int i = 0; i < k; ++i)
+    if (!partials[i]) return NFQ_ERR_NULL;
+  if (!q_out->codes || !q_out->block_scales || !q_out->row_scales) return NFQ_ERR_NULL;
+  if (T < 0 || H < 256 || H > 16384 || H % 256 != 0) return NFQ_ERR_SHAPE;
+  if (!(eps >= 0.0f) || eps > 1.0f) return NFQ_ERR_SHAPE;
+  if (q_out->block != 16 || q_out->tokens != T || q_out->hidden != H) return NFQ_ERR_SHAPE;
+  for (int i = 0; i < k; ++i)
+    if (!aligned16(partials[i])) return NFQ_ERR_ALIGN;
+  if (!aligned16(residual) || !aligned16(norm_w) || !aligned16(hidden_out) ||
+      !aligned16(q_out->codes) || !aligned16(q_out->block_scales) ||
+      !aligned16(q_out->row_scales))
+    return NFQ_ERR_ALIGN;
+  if (!stage1_fp4_supported(H)) return NFQ_ERR_SHAPE;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  Stage1Params p;
+  std::memset(&p, 0, sizeof(p));
+  for (int i = 0; i < k; ++i) p.partials[i] = partials[i];
+  p.residual = residual;
+  p.norm_w = norm_w;
+  p.hidden = hidden_out;
+  p.codes = q_out->codes;
+  p.bscales = q_out->block_scales;
+  p.gscales = q_out->row_scales;
+  p.fp4 = 1;
+  p.err = d->err;
+  p.eps = eps;
+  p.k = k;
+  p.T = T;
+  p.H = H;
+  const cudaError_t e = launch_stage1(p, d->num_sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
+  return map_cuda(e);
+}
+
 size_t nfq_lm_head_workspace_bytes(int T, int S) {
   (void)T;
   if (S < 1 || S > 64) return 0;
@@ -226,6 +268,79 @@ int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packe
                                   void *stream) {
   return lm_head_common(a, w_packed, true, w_scales, V, S, tokens_out, max_logit_out,
                         shard_idx_out, shard_val_out, workspace, ws_bytes, stream);
+}
+
+size_t nfq_lm_head_nvfp4_packed_bytes(int V, int H) {
+  if (V < 1 || H < 256 || H > 16384 || H % 256 != 0) return 0;
+  return fp4_packed_weight_bytes(V, H);
+}
+
+int nfq_lm_head_nvfp4_pack_weights(const uint8_t *codes, const uint8_t *block_scales, int V,
+                                   int H, void *w_packed, size_t packed_bytes, void *stream) {
+  if (!codes || !block_scales || !w_packed) return NFQ_ERR_NULL;
+  if (V < 1 || H < 256 || H > 16384 || H % 256 != 0) return NFQ_ERR_SHAPE;
+  if (packed_bytes < fp4_packed_weight_bytes(V, H)) return NFQ_ERR_WORKSPACE;
+  if (!aligned16(codes) || !aligned16(block_scales) || !aligned16(w_packed)) return NFQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_pack_fp4_weights(codes, block_scales, V, H,
+                                          static_cast<uint8_t *>(w_packed),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w_scale, int V,
+                             int S, int32_t *tokens_out, float *max_logit_out,
+                             int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                             size_t ws_bytes, void *stream) {
+  if (!a || !w_packed || !tokens_out) return NFQ_ERR_NULL;
+  if (!a->codes || !a->block_scales || !a->row_scales) return NFQ_ERR_NULL;
+  const int T = a->tokens, H = a->hidden;
+  if (a->block != 16 || H < 256 || H > 16384 || H % 256 != 0 || T < 0) return NFQ_ERR_SHAPE;
+  if (V < 1 || S < 1 || S > 64 || V % S != 0) return NFQ_ERR_SHAPE;
+  if (!workspace) return NFQ_ERR_WORKSPACE;
+  if (ws_bytes < stage2_workspace_bytes(S)) return NFQ_ERR_WORKSPACE;
+  if (!aligned16(a->codes) || !aligned16(a->block_scales) || !aligned16(a->row_scales) ||
+      !aligned16(w_packed) || !aligned4(tokens_out) || !aligned16(workspace) ||
+      (max_logit_out && !aligned4(max_logit_out)) ||
+      (shard_idx_out && !aligned4(shard_idx_out)) ||
+      (shard_val_out && !aligned4(shard_val_out)))
+    return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  Stage2Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.w_packed = static_cast<const uint8_t *>(w_packed);
+  p.w_scale = w_scale;
+  p.shard_idx_out = shard_idx_out;
+  p.shard_val_out = shard_val_out;
+  p.keys = static_cast<unsigned long long *>(workspace);
+  p.counter = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(workspace) +
+                                           stage2_workspace_bytes(S) - 16u);
+  p.err = d->err;
+  p.T_total = T;
+  p.H = H;
+  p.G = H / 256;
+  p.V = V;
+  p.S = S;
+  p.shard_width = V / S;
+  p.n_vtiles = (V + 127) / 128;
+  for (int t0 = 0; t0 < T; t0 += kFp4MaxT) {
+    const int Tc = (T - t0) < kFp4MaxT ? (T - t0) : kFp4MaxT;
+    p.tok0 = t0;
+    p.T = Tc;
+    p.act_codes = a->codes + (size_t)t0 * (size_t)(H / 2);
+    p.act_bscales = a->block_scales + (size_t)t0 * (size_t)(H / 16);
+    p.act_gscales = a->row_scales + t0;
+    p.tokens_out = tokens_out + t0;
+    p.max_logit_out = max_logit_out ? max_logit_out + t0 : nullptr;
+    const cudaError_t e = launch_stage2_fp4(p, d->num_sms, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
+    if (e != cudaSuccess) return NFQ_ERR_CUDA;
+  }
+  return NFQ_OK;
 }
 
 int nfq_mtp_draft_chain(int positions, const void *const *partials, int k,

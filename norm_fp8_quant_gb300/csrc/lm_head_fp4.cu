@@ -1,0 +1,407 @@
+// Stage 2, NVFP4 form: the shared LM head on the NVFP4 activation and the
+// packed NVFP4 weight, with the same fused vocab-sharded argmax as the FP8 form.
+//
+// "[Spec Decode][Perf] Fuse the MTP trailing all-reduce; local-argmax draft
+// tokens", Benchmarks: the served checkpoint is NVFP4.  The FP4 format (e2m1
+// values, an unsigned e4m3 scale per 16 elements, an fp32 scale per row) is
+// the published NVFP4 one; the pages fix none of it.
+//
+// Unlike the FP8 form, whose fp32 128x128 block scales need a promotion out of
+// TMEM after every K block, the NVFP4 block scales are what the tensor cores'
+// block scaling consumes: tcgen05.mma kind::mxf4nvf4 with scale_vec::4X reads
+// one e4m3 scale per 16 K elements of every row of both operands from TMEM and
+// accumulates the scaled products over the whole hidden dimension.  The
+// epilogue only applies the two fp32 row scales and takes the argmax.
+//
+// Token-major, as the FP8 small-batch form: a tile is 256 vocab rows (two
+// 128-row blocks, the MMA's N), the tokens (up to 128, zero-padded) are M.
+// One K step is 128 code bytes = 256 elements = four MMAs of K = 64.
+//
+// Warps (704 threads):
+//   0 .. 15   epilogue: warp w reads TMEM lane quadrant w%4 (tokens
+//             32(w%4) .. +31), tile columns 64(w/4) .. +63
+//   16 .. 19  scale writers: per K step, copy the stage's activation and
+//             weight scales from shared memory into this step's TMEM scale
+//             slot, each warp into its own lane quadrant (every quadrant holds
+//             the same copy)
+//   20        producer: 1-D bulk copies of the packed weight codes and scales,
+//             2-D tensor copies of the activation codes and scales
+//   21        TMEM allocator and MMA issuer
+// TMEM (512 columns): the fp32 accumulator in columns 0..255, then one scale
+// slot of 48 columns per pipeline stage (16 for the activation: column
+// 4kk + c holds rows 32c + lane for MMA kk; 32 for the weight: column 8kk + c
+// holds rows 32c + lane).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "lm_head_common.cuh"
+#include "nfq_internal.h"
+#include "ptx.cuh"
+
+namespace nfq {
+
+namespace {
+
+constexpr int kF4EpiWarps = 16;
+constexpr int kF4SfWarps = 4;
+constexpr int kF4SfWarp0 = kF4EpiWarps;
+constexpr int kF4Producer = kF4EpiWarps + kF4SfWarps;
+constexpr int kF4Mma = kF4Producer + 1;
+constexpr int kF4Threads = (kF4Mma + 1) * 32;
+constexpr int kF4MaxStages = 4;
+constexpr uint32_t kF4ScaleBlock = 2048;                 // 128 rows x 16 scale bytes
+constexpr uint32_t kF4WBytes = 2 * kWTileBytes;          // 256 rows x 128 code bytes
+constexpr uint32_t kF4ABytes = kFp4MaxT * 128;           // 128 token rows x 128 code bytes
+constexpr uint32_t kF4SfbBytes = 2 * kF4ScaleBlock;      // 256 rows x 16 scale bytes
+constexpr uint32_t kF4SfaBytes = kFp4MaxT * 16;          // 128 token rows x 16 scale bytes
+constexpr uint32_t kF4Stage = kF4WBytes + kF4ABytes + kF4SfbBytes + kF4SfaBytes;
+constexpr uint32_t kF4SfBase = 256;                      // first scale column in TMEM
+constexpr uint32_t kF4SfCols = 48;                       // scale columns per stage
+static_assert(kF4Stage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+static_assert(kF4SfBase + kF4MaxStages * kF4SfCols <= 512, "scale slots fit in TMEM");
+
+struct Fp4Smem {
+  uint64_t full[kF4MaxStages];
+  uint64_t empty[kF4MaxStages];
+  uint64_t sfready[kF4MaxStages];
+  uint64_t tfull;
+  uint64_t tempty;
+  uint32_t tmem_base;
+  int abort;
+  int last;
+};
+
+__global__ void __launch_bounds__(kF4Threads, 1)
+    lm_head_fp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                       const __grid_constant__ CUtensorMap tmap_sa, const Stage2Params p,
+                       int nstage) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  float *gs_s = reinterpret_cast<float *>(smem + (size_t)nstage * kF4Stage);   // [128]
+  Fp4Smem *sh = reinterpret_cast<Fp4Smem *>(gs_s + kFp4MaxT);
+  volatile int *abort_flag = &sh->abort;
+
+  const int warp = (int)(threadIdx.x / 32);
+  const int lane = (int)(threadIdx.x % 32);
+  const int G = p.G;                                           // K steps of 256 elements
+  const size_t scale_region = (size_t)p.n_vtiles * (size_t)G * kWTileBytes;
+
+  const int b_begin = (int)(((long)blockIdx.x * p.n_vtiles) / gridDim.x);
+  const int b_end = (int)(((long)(blockIdx.x + 1) * p.n_vtiles) / gridDim.x);
+  const int n_tiles = (b_end - b_begin + 1) / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+      mbar_init(smem_u32(&sh->sfready[s]), kF4SfWarps);
+    }
+    mbar_init(smem_u32(&sh->tfull), 1);
+    mbar_init(smem_u32(&sh->tempty), kF4EpiWarps);
+    sh->abort = 0;
+    sh->last = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kF4Producer && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    prefetch_tmap(&tmap_sa);
+  }
+  if (warp == kF4Mma) {
+    tmem_alloc(smem_u32(&sh->tmem_base), 512);
+    tmem_relinquish();
+  }
+  // everything below reads memory the previous kernel on the stream may write
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int i = (int)threadIdx.x; i < kFp4MaxT; i += (int)blockDim.x)
+    gs_s[i] = (i < p.T) ? __fmul_rn(p.act_gscales[i], p.w_scale) : 0.0f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+
+  if (warp == kF4Producer) {
+    // -------------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
+      for (int ks = 0; ks < G; ++ks, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *st = smem + (size_t)s * kF4Stage;
+          const uint32_t fb = smem_u32(&sh->full[s]);
+          mbar_arrive_expect_tx(fb, (uint32_t)nb * (kWTileBytes + kF4ScaleBlock) + kF4ABytes +
+                                        kF4SfaBytes);
+          for (int h = 0; h < nb; ++h) {
+            const size_t blk = (size_t)(blk0 + h) * (size_t)G + (size_t)ks;
+            bulk_g2s(smem_u32(st + h * kWTileBytes), p.w_packed + blk * kWTileBytes, kWTileBytes,
+                     fb, pol_w);
+            bulk_g2s(smem_u32(st + kF4WBytes + kF4ABytes + h * kF4ScaleBlock),
+                     p.w_packed + scale_region + blk * kF4ScaleBlock, kF4ScaleBlock, fb, pol_w);
+          }
+          tma_load_2d(smem_u32(st + kF4WBytes), &tmap_a, ks * 128, 0, fb, pol_a);
+          tma_load_2d(smem_u32(st + kF4WBytes + kF4ABytes + kF4SfbBytes), &tmap_sa, ks * 16, 0, fb,
+                      pol_a);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      const uint32_t issued = it;
+      const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
+      for (uint32_t j = first; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kF4Mma) {
+    // ------------------------------------------------------------------- MMA --
+    uint32_t it = 0;
+    int committed = 0;                             // tiles whose last MMA was committed
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
+      const uint32_t idesc = idesc_nvfp4(128, (uint32_t)(nb * 128));
+      // the single accumulator is free once the epilogue has read tile ti-1
+      int got = 1;
+      if (lane == 0)
+        got = mbar_wait(smem_u32(&sh->tempty), (uint32_t)(ti & 1) ^ 1u, abort_flag, p.err,
+                        kErrBitStage2);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) break;
+      for (int ks = 0; ks < G; ++ks, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2) &&
+                mbar_wait(smem_u32(&sh->sfready[s]), ph, abort_flag, p.err, kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint8_t *st = smem + (size_t)s * kF4Stage;
+          const uint32_t w_addr = smem_u32(st);
+          const uint32_t a_addr = smem_u32(st + kF4WBytes);
+          const uint32_t sfa = tmem_base + kF4SfBase + s * kF4SfCols;
+          const uint32_t sfb = sfa + 16u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_fp4_block16(tmem_base, sw128_kmajor_desc(a_addr + kk * 32),
+                            sw128_kmajor_desc(w_addr + kk * 32), idesc, sfa + 4u * kk,
+                            sfb + 8u * kk, (ks > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&sh->empty[s]));
+          if (ks == G - 1) mma_commit(smem_u32(&sh->tfull));
+        }
+        __syncwarp();
+      }
+      if (ok) committed = ti + 1;
+    }
+    if (lane == 0 && committed > 0)
+      mbar_wait_drain(smem_u32(&sh->tfull), (uint32_t)((committed - 1) & 1));
+    __syncwarp();
+  } else if (warp >= kF4SfWarp0) {
+    // --------------------------------------------------------- scale writers --
+    const int q = warp & 3;                        // this warp's TMEM lane quadrant
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      for (int ks = 0; ks < G; ++ks, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        const bool got = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint8_t *sfb_s = smem + (size_t)s * kF4Stage + kF4WBytes + kF4ABytes;
+        const uint8_t *sfa_s = sfb_s + kF4SfbBytes;
+        uint32_t ra[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // token row 32c + lane: its 16 scale bytes = words for MMAs 0..3
+          const uint4 v = *reinterpret_cast<const uint4 *>(sfa_s + (32 * c + lane) * 16);
+          ra[0 + c] = v.x;
+          ra[4 + c] = v.y;
+          ra[8 + c] = v.z;
+          ra[12 + c] = v.w;
+        }
+        uint32_t rb[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // packed scale block: words (kk, lane, c = 0..3) = rows 32c + lane
+            const uint4 v = *reinterpret_cast<const uint4 *>(sfb_s + h * kF4ScaleBlock +
+                                                             (kk * 32 + lane) * 16);
+            rb[kk * 8 + h * 4 + 0] = v.x;
+            rb[kk * 8 + h * 4 + 1] = v.y;
+            rb[kk * 8 + h * 4 + 2] = v.z;
+            rb[kk * 8 + h * 4 + 3] = v.w;
+          }
+        const uint32_t col =
+            tmem_base + ((uint32_t)(32 * q) << 16) + kF4SfBase + s * kF4SfCols;
+        tmem_st16(col, ra);
+        tmem_st32(col + 16u, rb);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh->sfready[s]));
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue --
+    // Token 32q + lane is TMEM lane 32q + lane; column n of the accumulator is
+    // row n of the tile.  Each thread streams its 64 columns 16 at a time,
+    // keeping the running (max, lowest row) of the current shard.
+    const int q = warp & 3;
+    const int g = warp >> 2;
+    const int tok = 32 * q + lane;
+    const bool quad_active = 32 * q < p.T;
+    const bool tok_ok = tok < p.T;
+    const float sc = gs_s[tok];
+    const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
+    for (int ti = 0; ti < n_tiles; ++ti) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
+      const bool got = mbar_wait(smem_u32(&sh->tfull), (uint32_t)(ti & 1), abort_flag, p.err,
+                                 kErrBitStage2);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const bool active = quad_active && (g < 2 * nb);
+      const int row0 = blk0 * 128 + 64 * g;
+      int cur = active ? row0 / p.shard_width : 0;     // shard of the running maximum
+      int next_bound = (cur + 1) * p.shard_width;      // first row of the next shard
+      float best = -INFINITY;
+      int bi = -1;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t r[16];
+        if (active) {
+          tmem_ld16(taddr0 + (uint32_t)(16 * c4), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(r[j]));
+        }
+        if (c4 == 3) {
+          // every TMEM read of this tile is complete: the MMA may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
+        }
+        if (active) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int v = row0 + 16 * c4 + j;
+            if (v >= p.V) break;
+            if (v >= next_bound) {
+              if (bi >= 0 && tok_ok)
+                atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+              cur = v / p.shard_width;
+              next_bound = (cur + 1) * p.shard_width;
+              bi = -1;
+            }
+            const float logit = __fmul_rn(__uint_as_float(r[j]), sc);
+            if (bi < 0 || logit > best) {
+              best = logit;
+              bi = v;
+            }
+          }
+        }
+      }
+      if (active && bi >= 0 && tok_ok)
+        atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+    }
+    __threadfence();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kF4Mma) tmem_dealloc(tmem_base, 512);
+  finish_launch(p, &sh->last);
+}
+
+// Scale blocks of the packed NVFP4 weight: block (vt, s) holds, at word
+// (kk * 32 + i) * 4 + c, the four block scales 4kk .. 4kk+3 of K step s for
+// row vt * 128 + 32c + i (zero past V).
+__global__ void __launch_bounds__(256) pack_fp4_scales_kernel(const uint8_t *__restrict__ bs,
+                                                              int V, int H,
+                                                              uint8_t *__restrict__ out) {
+  const int G = H / 256, B16 = H / 16;
+  const size_t block = blockIdx.x;                // vt * G + s
+  const int vt = (int)(block / (size_t)G), s = (int)(block % (size_t)G);
+  uint32_t *dst = reinterpret_cast<uint32_t *>(out + block * kF4ScaleBlock);
+  for (int w = (int)threadIdx.x; w < (int)(kF4ScaleBlock / 4); w += (int)blockDim.x) {
+    const int kk = w >> 7, i = (w >> 2) & 31, c = w & 3;
+    const int row = vt * 128 + 32 * c + i;
+    uint32_t val = 0u;
+    if (row < V)
+      val = *reinterpret_cast<const uint32_t *>(bs + (size_t)row * B16 + (size_t)s * 16 + 4 * kk);
+    dst[w] = val;
+  }
+}
+
+}  // namespace
+
+size_t fp4_packed_weight_bytes(int V, int H) {
+  return (size_t)((V + 127) / 128) * (size_t)(H / 256) * (kWTileBytes + kF4ScaleBlock);
+}
+
+cudaError_t launch_pack_fp4_weights(const uint8_t *codes, const uint8_t *bscales, int V, int H,
+                                    uint8_t *out, cudaStream_t stream) {
+  const size_t blocks = (size_t)((V + 127) / 128) * (size_t)(H / 256);
+  if (blocks == 0 || blocks > 0x7FFFFFFFu) return cudaErrorInvalidValue;
+  // the code blocks have the FP8 layout of a [V][H/2] byte matrix
+  cudaError_t e = launch_pack_weights(codes, V, H / 2, out, stream);
+  if (e != cudaSuccess) return e;
+  pack_fp4_scales_kernel<<<(unsigned)blocks, 256, 0, stream>>>(bscales, V, H,
+                                                                out + blocks * kWTileBytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) {
+  if (p.T < 1 || p.T > kFp4MaxT) return cudaErrorInvalidConfiguration;
+  CUtensorMap ta, tsa;
+  if (!encode_u8_map(&ta, p.act_codes, (uint64_t)p.T, (uint64_t)(p.H / 2), (uint32_t)kFp4MaxT))
+    return cudaErrorInvalidValue;
+  if (!encode_u8_map_plain(&tsa, p.act_bscales, (uint64_t)p.T, (uint64_t)(p.H / 16), 16u,
+                           (uint32_t)kFp4MaxT))
+    return cudaErrorInvalidValue;
+  const size_t fixed = 1024 /*align pad*/ + kFp4MaxT * sizeof(float) + sizeof(Fp4Smem) + 64;
+  const size_t budget = 227u * 1024u;
+  int nstage = (int)((budget - fixed) / kF4Stage);
+  if (nstage > kF4MaxStages) nstage = kF4MaxStages;
+  if (nstage < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + (size_t)nstage * kF4Stage;
+  cudaError_t e = cudaFuncSetAttribute(lm_head_fp4_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = num_sms < p.n_vtiles ? num_sms : p.n_vtiles;
+  return launch_pdl(lm_head_fp4_kernel, grid, kF4Threads, smem, stream, ta, tsa, p, nstage);
+}
+
+}  // namespace nfq

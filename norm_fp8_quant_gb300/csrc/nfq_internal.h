@@ -16,8 +16,10 @@ struct Stage1Params {
   const void *residual;                // BF16 [T][H]
   const void *norm_w;                  // BF16 [H]
   void *hidden;                        // BF16 [T][H]
-  uint8_t *codes;                      // e4m3 [T][H]
-  float *scales;                       // fp32 [T][H/128]
+  uint8_t *codes;                      // e4m3 [T][H], or NVFP4 e2m1 pairs [T][H/2]
+  float *scales;                       // fp32 [T][H/128] (FP8 form)
+  uint8_t *bscales;                    // e4m3 [T][H/16] (NVFP4 form)
+  float *gscales;                      // fp32 [T] (NVFP4 form)
   unsigned *err;                       // device error word
   float eps;
   int k, T, H;
@@ -26,11 +28,13 @@ struct Stage1Params {
   int nslot;      // shared-memory ring slots
   int per_slot;   // inputs (E BF16 values each) per ring slot
   int n_active;   // consumer threads holding data
+  int fp4;        // 1: NVFP4 activation (codes, bscales, gscales), 0: FP8 (codes, scales)
 };
 
 cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream);
 void stage1_set_tuning(int cluster, int vpt, int slots, int per_slot);
 int stage1_plan(int T, int H, int k, int num_sms, int *out7);
+bool stage1_fp4_supported(int H);
 
 // Stage 2 launch parameters.
 struct Stage2Params {
@@ -51,6 +55,10 @@ struct Stage2Params {
   int H, G, V, S;
   int shard_width;            // V / S
   int n_vtiles;               // ceil(V / 128)
+  // NVFP4 form: act_codes are e2m1 pairs [T][H/2], G = H / 256 (K steps)
+  const uint8_t *act_bscales; // e4m3 [T][H/16]
+  const float *act_gscales;   // fp32 [T]
+  float w_scale;              // the weight's tensor scale
 };
 
 cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes_base, const void *w,
@@ -60,5 +68,12 @@ size_t stage2_workspace_bytes(int S);
 void stage2_set_small(int enabled);   // 0: always use the wide-batch kernel (tests, tuning)
 size_t packed_weight_bytes(int V, int H);
 cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out, cudaStream_t stream);
+
+// NVFP4 LM head (token-major, block-scaled tensor cores), T <= 128 per launch
+constexpr int kFp4MaxT = 128;
+cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream);
+size_t fp4_packed_weight_bytes(int V, int H);
+cudaError_t launch_pack_fp4_weights(const uint8_t *codes, const uint8_t *bscales, int V, int H,
+                                    uint8_t *out, cudaStream_t stream);
 
 }  // namespace nfq

@@ -25,6 +25,7 @@
 //    division); codes = cvt.rn.satfinite.e4m3x2(y / scale).  Hidden (16 B),
 //    codes (8 B) and scales go straight to global memory, coalesced.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -46,6 +47,7 @@ __host__ __device__ constexpr int stage1_max_threads(int vpt) {
 struct RowSums {
   float red[2][32];     // per consumer warp, double-buffered by row parity
   float cl[2][8];       // per cluster rank, double-buffered by row parity
+  float amx[2][32];     // per consumer warp: row maximum |hidden| (NVFP4 form)
 };
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8]) {
@@ -77,7 +79,26 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-template <int VPT>
+// Two fp32 values -> one byte of e2m1 codes (lo in bits 0-3), nearest even,
+// saturating at +-6.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Value of an e4m3 code (exact, via the f16 conversion).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "r"(code));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+template <int VPT, bool kFp4>
 __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
     reduce_norm_quant_kernel(const Stage1Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -90,7 +111,8 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
   uint64_t *empty = full + p.nslot;
   uint64_t *ss_bar = empty + p.nslot;               // [2], cluster exchange
   uint64_t *red_bar = ss_bar + 2;                   // [2], consumer warps of this CTA
-  RowSums *sums = reinterpret_cast<RowSums *>(red_bar + 2);
+  uint64_t *amx_bar = red_bar + 2;                  // [2], row maximum (NVFP4 form)
+  RowSums *sums = reinterpret_cast<RowSums *>(amx_bar + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sums + 1);
 
   const int C = p.C;
@@ -109,6 +131,8 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
     mbar_init(smem_u32(&ss_bar[1]), (uint32_t)C);
     mbar_init(smem_u32(&red_bar[0]), (uint32_t)n_cons_warps);
     mbar_init(smem_u32(&red_bar[1]), (uint32_t)n_cons_warps);
+    mbar_init(smem_u32(&amx_bar[0]), (uint32_t)n_cons_warps);
+    mbar_init(smem_u32(&amx_bar[1]), (uint32_t)n_cons_warps);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -263,6 +287,69 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
 
       const size_t rowbase = (size_t)r * (size_t)p.H + (size_t)col0;
       uint4 *hid = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.hidden) + rowbase * 2u);
+      if constexpr (kFp4) {
+        // NVFP4 form (one CTA holds the row): hidden, then the row maximum
+        // over the CTA, then per 16-element block (two adjacent lanes) the
+        // e4m3 block scale and the e2m1 codes.
+        float yv[VPT][8];
+        uint32_t hbv[VPT][4];
+        float am = 0.0f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          float wv[8];
+          unpack_bf16x8(wpk[v], wv);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const __nv_bfloat162 h2 =
+                __floats2bfloat162_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]),
+                                      __fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
+            const uint32_t hu = *reinterpret_cast<const uint32_t *>(&h2);
+            hbv[v][e / 2] = hu;
+            yv[v][e] = __uint_as_float(hu << 16);
+            yv[v][e + 1] = __uint_as_float(hu & 0xFFFF0000u);
+            am = fmaxf(am, fmaxf(fabsf(yv[v][e]), fabsf(yv[v][e + 1])));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) {
+          sums->amx[par][cw] = am;
+          mbar_arrive(smem_u32(&amx_bar[par]));
+        }
+        __syncwarp();
+        const bool got_am = mbar_wait(smem_u32(&amx_bar[par]), pph, abort_flag, p.err,
+                                      kErrBitStage1);
+        if (!__all_sync(0xffffffffu, got_am)) break;
+        float amax_row = 0.0f;
+        for (int q = 0; q < n_cons_warps; ++q) amax_row = fmaxf(amax_row, sums->amx[par][q]);
+        const float g = __fdiv_rn(amax_row, 2688.0f);     // 448 * 6
+        const float d = __fmul_rn(6.0f, g);
+        uint32_t *cod4 = reinterpret_cast<uint32_t *>(p.codes + rowbase / 2u);
+        uint8_t *bsc = p.bscales + (size_t)r * (size_t)(p.H / 16);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          float ab = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ab = fmaxf(ab, fabsf(yv[v][e]));
+          ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));   // the block's other half
+          const uint32_t sb = (g != 0.0f) ? (uint32_t)(e4m3x2(__fdiv_rn(ab, d), 0.0f) & 0xFFu) : 0u;
+          const float eff = __fmul_rn(e4m3_value(sb), g);
+          uint32_t packed = 0u;
+          if (eff != 0.0f) {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2)
+              packed |= e2m1x2(__fdiv_rn(yv[v][e], eff), __fdiv_rn(yv[v][e + 1], eff)) << (4 * e);
+          }
+          if (active) {
+            const int j = v * NA + tc;
+            hid[j] = make_uint4(hbv[v][0], hbv[v][1], hbv[v][2], hbv[v][3]);
+            cod4[j] = packed;
+            if ((tc & 1) == 0) bsc[j / 2] = (uint8_t)sb;
+          }
+        }
+        if (active && tc == 0) p.gscales[r] = g;
+        continue;
+      }
       uint2 *cod = reinterpret_cast<uint2 *>(p.codes + rowbase);
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
@@ -324,7 +411,7 @@ struct Stage1Choice {
 int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0, g_tune_per_slot = 0;
 
 size_t stage1_smem_bytes(int nslot, int per_slot, int E) {
-  return (size_t)nslot * (size_t)per_slot * (size_t)E * 2u + (size_t)nslot * 16u + 32u +
+  return (size_t)nslot * (size_t)per_slot * (size_t)E * 2u + (size_t)nslot * 16u + 48u +
          sizeof(RowSums) + 16u;
 }
 
@@ -345,7 +432,7 @@ int pick_vpt(int Gc) {
   return 0;
 }
 
-Stage1Choice choose_stage1(int T, int H, int k, int num_sms) {
+Stage1Choice choose_stage1(int T, int H, int k, int num_sms, bool fp4 = false) {
   const int G = H / 128;
   Stage1Choice ch{};
   // one CTA per row slice; a row is split over a cluster only when no single
@@ -354,7 +441,8 @@ Stage1Choice choose_stage1(int T, int H, int k, int num_sms) {
   const int opts[4] = {1, 2, 4, 8};
   for (int c : opts) {
     if (G % c) continue;
-    if (g_tune_C > 0 && c != g_tune_C) continue;
+    if (fp4 && c != 1) continue;           // the NVFP4 row maximum is taken inside one CTA
+    if (!fp4 && g_tune_C > 0 && c != g_tune_C) continue;
     int v = 0;
     if (g_tune_vpt > 0 && (G / c) % g_tune_vpt == 0 &&
         16 * (G / c) / g_tune_vpt + 32 <= stage1_max_threads(g_tune_vpt))
@@ -400,7 +488,7 @@ Stage1Choice choose_stage1(int T, int H, int k, int num_sms) {
 template <int VPT>
 cudaError_t launch_vpt(const Stage1Params &p, const Stage1Choice &ch, int grid,
                        cudaStream_t stream) {
-  auto kern = reduce_norm_quant_kernel<VPT>;
+  auto kern = p.fp4 ? reduce_norm_quant_kernel<VPT, true> : reduce_norm_quant_kernel<VPT, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)ch.smem);
   if (e != cudaSuccess) return e;
@@ -442,8 +530,12 @@ int stage1_plan(int T, int H, int k, int num_sms, int *out7) {
   return 0;
 }
 
+bool stage1_fp4_supported(int H) {
+  return H % 256 == 0 && H >= 256 && H <= 16384 && choose_stage1(1, H, 1, 1, true).VPT != 0;
+}
+
 cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream) {
-  Stage1Choice ch = choose_stage1(p.T, p.H, p.k, num_sms);
+  Stage1Choice ch = choose_stage1(p.T, p.H, p.k, num_sms, p.fp4 != 0);
   if (ch.VPT == 0) return cudaErrorInvalidConfiguration;
   p.C = ch.C;
   p.E = p.H / ch.C;

@@ -238,6 +238,58 @@ def lm_head_weights(w: Workload, chunk_blocks: int = 64):
     return codes, scales
 
 
+def nvfp4_quantise_rows(x, g):
+    """NVFP4 form of fp32 rows x [R][H] (H a multiple of 16) with the fp32 row
+    scales g [R] (or one scalar for a whole tensor): per 16 consecutive values
+    the block scale is e4m3(amax / (6 g)) (torch's round-to-nearest-even cast,
+    clamped at 448), the effective scale dec(block scale) * g, and the codes
+    are the e2m1 values nearest to x / effective scale (ties to the even code,
+    saturating at 6; codes 0 where the effective scale is 0), packed two to a
+    byte with element 2i in the low nibble.  Returns (codes uint8 [R][H/2],
+    block scales uint8 [R][H/16])."""
+    import torch
+    xt = torch.as_tensor(np.ascontiguousarray(x, np.float32))
+    R, H = xt.shape
+    gt = torch.as_tensor(np.asarray(g, np.float32)).reshape(-1, 1)
+    gt = gt.expand(R, 1) if gt.shape[0] == 1 else gt
+    xb = xt.view(R, H // 16, 16)
+    amax = xb.abs().amax(dim=2)
+    d = gt * np.float32(6.0)
+    u = torch.where(d > 0, amax / torch.where(d > 0, d, torch.ones_like(d)), torch.zeros_like(amax))
+    sb = u.clamp(max=448.0).to(torch.float8_e4m3fn)
+    eff = sb.float() * gt
+    q = xb / torch.where(eff > 0, eff, torch.ones_like(eff))[:, :, None]
+    a = q.abs().clamp(max=6.0)
+    step = torch.where(a < 2, 0.5, torch.where(a < 4, 1.0, 2.0))
+    r = (torch.round(a / step) * step).clamp(max=6.0)      # torch.round: half to even
+    lut = torch.tensor([0, 1, 2, 3, 4, 0, 5, 0, 6, 0, 0, 0, 7], dtype=torch.uint8)
+    code = lut[(r * 2).long()] | (torch.signbit(q).to(torch.uint8) << 3)
+    code = torch.where((eff > 0)[:, :, None], code, torch.zeros_like(code)).view(R, H)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).contiguous()
+    return packed.numpy(), sb.view(torch.uint8).numpy()
+
+
+def lm_head_weights_nvfp4(w: Workload, chunk_rows: int = 8192):
+    """NVFP4 LM-head weight from the same fp32 N(0, weight_std) draws as
+    lm_head_weights: one fp32 scale for the whole tensor, amax / (448 * 6),
+    then nvfp4_quantise_rows.  Returns (codes uint8 [V][H/2], block scales
+    uint8 [V][H/16], tensor scale float)."""
+    V, H = w.V, w.H
+    amax = np.float32(0.0)
+    for r0 in range(0, V, chunk_rows):
+        r1 = min(V, r0 + chunk_rows)
+        f = normal_f32(w.seed, STREAM_LM_W, (r1 - r0) * H, 0.0, w.weight_std, r0 * H)
+        amax = max(amax, np.float32(np.abs(f).max()))
+    gw = np.float32(amax / np.float32(2688.0))
+    codes = np.empty((V, H // 2), np.uint8)
+    bs = np.empty((V, H // 16), np.uint8)
+    for r0 in range(0, V, chunk_rows):
+        r1 = min(V, r0 + chunk_rows)
+        f = normal_f32(w.seed, STREAM_LM_W, (r1 - r0) * H, 0.0, w.weight_std, r0 * H)
+        codes[r0:r1], bs[r0:r1] = nvfp4_quantise_rows(f.reshape(r1 - r0, H), gw)
+    return codes, bs, float(gw)
+
+
 # planted e4m3 codes: +448 and -448
 _PLUS_MAX, _MINUS_MAX = 0x7E, 0xFE
 

@@ -130,3 +130,83 @@ def check_stage2(tokens, qa, sa, qw, sw, S, sample, max_logit=None, shard_idx=No
                 if shard_val is not None:
                     assert abs(float(shard_val[s, t]) - float(r["shard_val"][i, s])) <= stol + 1e-30
     return near, len(sample)
+
+
+# ------------------------------------------------------------------ NVFP4 --
+
+def _nib(c):
+    """unpacked e2m1 codes [R][2*B] of packed bytes [R][B], -0 written as +0"""
+    c = np.asarray(c, np.uint8)
+    u = np.stack([c & 15, c >> 4], axis=-1).reshape(c.shape[0], -1)
+    return np.where((u & 7) == 0, 0, u)
+
+
+def check_stage1_fp4(hidden, codes, bscales, gscales, ref_hidden):
+    """hidden within 1 BF16 ulp of the oracle; the oracle's NVFP4 quantiser
+    applied to the GPU's own hidden reproduces the GPU's codes, block scales and
+    row scales bit for bit (zero codes compared without their sign).  Returns
+    the number of rows whose hidden differs from the oracle's."""
+    dh = np.abs(_ordered_bf16(hidden) - _ordered_bf16(ref_hidden))
+    assert dh.max(initial=0) <= 1, f"hidden differs by {dh.max()} bf16 ulps"
+    q = oracle.nvfp4_quant(hidden)
+    assert np.array_equal(np.asarray(gscales, np.float32).view(np.uint32),
+                          q["global_scales"].view(np.uint32)), "row scales"
+    assert np.array_equal(bscales, q["block_scales"]), "block scales"
+    assert np.array_equal(_nib(codes), _nib(q["codes"])), "e2m1 codes"
+    return int((dh.max(axis=1) > 0).sum())
+
+
+def _nvfp4_dequant(codes, bs):
+    u = np.asarray(codes, np.uint8)
+    u = np.stack([u & 15, u >> 4], axis=-1).reshape(u.shape[0], -1)
+    mag = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])[u & 7]
+    v = np.where(u & 8, -mag, mag)
+    s = oracle.e4m3_to_f32(np.asarray(bs, np.uint8).ravel()).reshape(bs.shape).astype(np.float64)
+    return v * np.repeat(s, 16, axis=1)
+
+
+def check_stage2_fp4(tokens, qa, sa, ga, qw, sw, gw, S, sample, max_logit=None,
+                     shard_idx=None, shard_val=None, expected=None):
+    """As check_stage2, for the NVFP4 LM head: the logit bound is
+    2 gamma_n sum_b |c_b| |ga gw| with n = H/16 + 2 (the block-scaled products
+    are exact; only their fp32 sum and the final scaling round)."""
+    H = qa.shape[1] * 2
+    n = H // 16 + 2
+    gamma = n * U / (1 - n * U)
+    L = oracle.lm_head_logits_nvfp4(qa, sa, ga, qw, sw, gw, tokens=sample)
+    r = oracle.argmax(L, S)
+    V = qw.shape[0]
+    width = V // S
+    near = 0
+    for i, t in enumerate(sample):
+        a = np.abs(_nvfp4_dequant(qa[t:t + 1], sa[t:t + 1]))[0]
+        scale = abs(float(np.float32(ga[t]) * np.float32(gw)))
+
+        def tol_of(v):
+            w = np.abs(_nvfp4_dequant(qw[v:v + 1], sw[v:v + 1]))[0]
+            return 2 * gamma * float(a @ w) * scale + 4 * U * abs(float(L[i, v])) + 1e-30
+        gap = r["gap"][i]
+        tol = tol_of(int(r["tokens"][i]))
+        if expected is not None and t in expected:
+            assert r["tokens"][i] == expected[t], "oracle misses a planted tie"
+        if gap >= 1e-3 or gap == 0.0:
+            assert tokens[t] == r["tokens"][i], f"token {t}: gpu {tokens[t]} oracle {r['tokens'][i]} gap {gap}"
+        else:
+            near += 1
+            assert L[i, tokens[t]] >= r["values"][i] - 2 * tol
+        if max_logit is not None:
+            assert abs(float(max_logit[t]) - float(r["values"][i])) <= tol
+        if shard_idx is not None:
+            sg = oracle.shard_gaps(L[i:i + 1], S)[0]
+            for s in range(S):
+                oi = int(r["shard_idx"][i, s])
+                gi = int(shard_idx[s, t])
+                assert s * width <= gi < (s + 1) * width
+                stol = tol_of(oi)
+                if sg[s] >= 1e-3 or sg[s] == 0.0:
+                    assert gi == oi, f"token {t} shard {s}: gpu {gi} oracle {oi}"
+                else:
+                    assert L[i, gi] >= r["shard_val"][i, s] - 2 * stol
+                if shard_val is not None:
+                    assert abs(float(shard_val[s, t]) - float(r["shard_val"][i, s])) <= stol
+    return near, len(sample)

@@ -127,3 +127,55 @@ def test_chain_argument_validation(lib):
     assert call(2, diff, k=0) == nfq.NFQ_ERR_SHAPE
     assert lib.nfq_mtp_draft_chain(2, None, 2, FAKE, FAKE, 1e-6, 4, 1024, diff, C.byref(q), FAKE,
                                    0, FAKE, 4096, 2, FAKE, FAKE, ws, None) == nfq.NFQ_ERR_NULL
+
+
+def _stage1_fp4(lib, partials=(FAKE, FAKE), k=2, T=4, H=1024, codes=FAKE, bs=FAKE, gs=FAKE,
+                tokens=None, block=16, hidden=FAKE):
+    arr = (ctypes.c_void_p * len(partials))(*partials)
+    q = nfq.Fp4Act(codes, bs, gs, T if tokens is None else tokens, H, block)
+    return lib.nfq_mtp_reduce_norm_quant_nvfp4(arr, k, FAKE, FAKE, 1e-6, T, H, hidden,
+                                               ctypes.byref(q), None)
+
+
+def test_stage1_nvfp4_argument_validation(lib):
+    assert _stage1_fp4(lib, codes=0) == nfq.NFQ_ERR_NULL
+    assert _stage1_fp4(lib, bs=0) == nfq.NFQ_ERR_NULL
+    assert _stage1_fp4(lib, gs=0) == nfq.NFQ_ERR_NULL
+    assert _stage1_fp4(lib, H=1152) == nfq.NFQ_ERR_SHAPE          # not a multiple of 256
+    assert _stage1_fp4(lib, H=32768) == nfq.NFQ_ERR_SHAPE         # a row must fit one CTA
+    assert _stage1_fp4(lib, block=32) == nfq.NFQ_ERR_SHAPE
+    assert _stage1_fp4(lib, tokens=5) == nfq.NFQ_ERR_SHAPE
+    assert _stage1_fp4(lib, bs=MIS) == nfq.NFQ_ERR_ALIGN
+    assert _stage1_fp4(lib, T=0, tokens=0) == nfq.NFQ_OK
+    assert _stage1_fp4(lib, T=0, tokens=0, H=16384) == nfq.NFQ_OK
+
+
+def _stage2_fp4(lib, T=4, H=1024, block=16, codes=FAKE, bs=FAKE, gs=FAKE, w=FAKE, V=4096, S=2,
+                tokens=FAKE, ws=FAKE, ws_bytes=None):
+    q = nfq.Fp4Act(codes, bs, gs, T, H, block)
+    if ws_bytes is None:
+        ws_bytes = lib.nfq_lm_head_workspace_bytes(T, S)
+    return lib.nfq_lm_head_nvfp4_argmax(ctypes.byref(q), w, 0.5, V, S, tokens, None, None, None,
+                                        ws, ws_bytes, None)
+
+
+def test_stage2_nvfp4_argument_validation(lib):
+    assert lib.nfq_lm_head_nvfp4_packed_bytes(4096, 1152) == 0
+    assert lib.nfq_lm_head_nvfp4_packed_bytes(129280, 7168) == 1010 * 28 * 18432
+    assert _stage2_fp4(lib, codes=0) == nfq.NFQ_ERR_NULL
+    assert _stage2_fp4(lib, gs=0) == nfq.NFQ_ERR_NULL
+    assert _stage2_fp4(lib, w=0) == nfq.NFQ_ERR_NULL
+    assert _stage2_fp4(lib, H=1152) == nfq.NFQ_ERR_SHAPE
+    assert _stage2_fp4(lib, block=32) == nfq.NFQ_ERR_SHAPE
+    assert _stage2_fp4(lib, V=4095) == nfq.NFQ_ERR_SHAPE
+    assert _stage2_fp4(lib, ws=0) == nfq.NFQ_ERR_WORKSPACE
+    assert _stage2_fp4(lib, ws_bytes=8) == nfq.NFQ_ERR_WORKSPACE
+    assert _stage2_fp4(lib, bs=MIS) == nfq.NFQ_ERR_ALIGN
+    assert _stage2_fp4(lib, tokens=FAKE + 2) == nfq.NFQ_ERR_ALIGN
+    assert _stage2_fp4(lib, T=0) == nfq.NFQ_OK
+    pk = lambda codes=FAKE, bs=FAKE, V=4096, H=1024, n=None: lib.nfq_lm_head_nvfp4_pack_weights(
+        codes, bs, V, H, FAKE, lib.nfq_lm_head_nvfp4_packed_bytes(V, H) if n is None else n, None)
+    assert pk(codes=0) == nfq.NFQ_ERR_NULL
+    assert pk(H=1000) == nfq.NFQ_ERR_SHAPE
+    assert pk(n=16) == nfq.NFQ_ERR_WORKSPACE
+    assert pk(bs=MIS) == nfq.NFQ_ERR_ALIGN

@@ -45,3 +45,32 @@ def test_lm_head_weight_block_quantisation():
     # each block holds its amax at +-448
     assert np.all(((blocks & 0x7F) == 0x7E).any(axis=(1, 3)))
     assert 0.02 * 3 / 448 < sw.mean() < 0.02 * 6 / 448
+
+
+def test_nvfp4_weight_quantiser_matches_the_oracle_on_bf16_rows():
+    """The input generator's vectorised NVFP4 quantiser agrees with the
+    oracle's row quantiser when both see the same BF16 rows and row scales."""
+    import oracle
+    rng = np.random.default_rng(5)
+    x = (rng.normal(0, 1, (32, 256)) * np.exp2(rng.integers(-8, 8, (32, 1)))).astype(np.float32)
+    x[4] = 0
+    x[7, 16:32] = 0
+    bits = synth.to_bf16_bits(x)
+    xb = (bits.astype(np.uint32) << 16).view(np.float32)
+    ref = oracle.nvfp4_quant(bits)
+    codes, bs = synth.nvfp4_quantise_rows(xb, ref["global_scales"])
+    assert np.array_equal(bs, ref["block_scales"])
+    # +-0 codes are the same value
+    zero = lambda c: np.where((c & 7) == 0, 0, c)
+    lo = lambda c: zero(c & 15)
+    hi = lambda c: zero(c >> 4)
+    assert np.array_equal(lo(codes), lo(ref["codes"])) and np.array_equal(hi(codes), hi(ref["codes"]))
+
+
+def test_nvfp4_weights_shape_and_scale():
+    w = synth.workload("tiny")
+    codes, bs, gw = synth.lm_head_weights_nvfp4(w)
+    assert codes.shape == (w.V, w.H // 2) and bs.shape == (w.V, w.H // 16)
+    f = synth.normal_f32(w.seed, synth.STREAM_LM_W, w.V * w.H, 0.0, w.weight_std)
+    assert gw == np.float32(np.float32(np.abs(f).max()) / np.float32(2688.0))
+    assert bs.max() == 0x7E            # the tensor's largest block reaches 448
