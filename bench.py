@@ -59,6 +59,8 @@ def parse():
                     help="draft positions per step (the hidden of each feeds the next)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["decode_c64", "decode_c1", "prefill", "tie_stress", "tiny"])
+    ap.add_argument("--variant", choices=["fp8", "nvfp4"], default="fp8",
+                    help="activation / LM-head format: packed FP8 (default) or NVFP4")
     return ap.parse_args()
 
 
@@ -82,6 +84,19 @@ def stage2_bytes(T, H, V):
     activation codes + scales read; int32 tokens written."""
     G = H // 128
     return V * H + ((V + 127) // 128) * G * 4 + T * H + T * G * 4 + T * 4
+
+
+def stage1_bytes_nvfp4(T, H, k):
+    """Stage 1 with the NVFP4 activation: the same reads; BF16 hidden, e2m1
+    codes (H/2 bytes a row), e4m3 block scales (H/16) and fp32 row scales written."""
+    return k * T * H * 2 + T * H * 2 + H * 2 + T * H * 2 + T * H // 2 + T * H // 16 + T * 4
+
+
+def stage2_bytes_nvfp4(T, H, V):
+    """NVFP4 LM head: e2m1 weight codes and e4m3 block scales (9/16 byte per
+    weight), the activation's codes, block scales and row scales read; int32
+    tokens written."""
+    return V * H // 2 + V * H // 16 + T * H // 2 + T * H // 16 + T * 4 + T * 4
 
 
 def load_peaks():
@@ -235,7 +250,8 @@ def run_ours(args, rank, world, local):
     set_bytes = (k + 1) * T * H * 2
     nsets = int(min(64, max(2, -(-ROTATION_BYTES // set_bytes))))
     sets = [([p.to(dev) for p in host_parts], host_res.to(dev)) for _ in range(nsets)]
-    if has_lm:
+    fp4 = args.variant == "nvfp4"
+    if has_lm and not fp4:
         qw, sw = synth.lm_head_weights(w)
         qw_rowmajor = torch.from_numpy(qw).to(dev)
         sw_d = torch.from_numpy(sw).to(dev)
@@ -243,18 +259,35 @@ def run_ours(args, rank, world, local):
         qw_d = nfq.pack_lm_head_weights(qw_rowmajor)
         torch.cuda.synchronize()
         del qw_rowmajor
+    if has_lm and fp4:
+        qw, sw, gw = synth.lm_head_weights_nvfp4(w)
+        qw_d = nfq.pack_lm_head_weights_nvfp4(torch.from_numpy(qw).to(dev),
+                                              torch.from_numpy(sw).to(dev), gw)
+        torch.cuda.synchronize()
+        del qw, sw
+    if has_lm:
         ws = nfq.lm_head_workspace(T, S, dev)
     hidden = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    codes = torch.empty((T, H // 2 if fp4 else H), dtype=torch.uint8, device=dev)
     scales = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
+    bscales = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
+    gscales = torch.empty(T, dtype=torch.float32, device=dev)
     tokens = torch.empty(T, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
     def stage1(parts, res):
-        nfq.mtp_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
+        if fp4:
+            nfq.mtp_reduce_norm_quant_nvfp4(parts, res, norm_w, w.eps, hidden, codes, bscales,
+                                            gscales)
+        else:
+            nfq.mtp_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
 
     def stage2():
-        nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
+        if fp4:
+            nfq.lm_head_nvfp4_argmax(codes, bscales, gscales, qw_d, S, workspace=ws,
+                                     tokens_out=tokens)
+        else:
+            nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
 
     def barrier():
         torch.cuda.synchronize()
@@ -290,7 +323,7 @@ def run_ours(args, rank, world, local):
     # overlapping the first one's tail): the reported rate.  With --mtp P a
     # step is P chained draft positions: position p's hidden is the residual
     # of position p+1 (nfq_mtp_draft_chain), each position with its own partials.
-    P = max(1, args.mtp) if has_lm else 1
+    P = max(1, args.mtp) if has_lm and not fp4 else 1
     if P > 1:
         chain_hidden = [torch.empty_like(hidden) for _ in range(2)]
         chain_tokens = torch.empty((P, T), dtype=torch.int32, device=dev)
@@ -381,7 +414,7 @@ def run_ours(args, rank, world, local):
     NB = 3                                     # input buffers / result slots in rotation
     bufs = [torch.empty((k + 1, T, H), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
     copied = [torch.cuda.Event() for _ in range(NB)]
-    result_dev = tokens if has_lm else scales
+    result_dev = tokens if has_lm else (gscales if fp4 else scales)
     result_host = [torch.empty(result_dev.shape, dtype=result_dev.dtype).pin_memory()
                    for _ in range(NB)]
     done = [torch.cuda.Event() for _ in range(NB)]
@@ -434,7 +467,7 @@ def run_ours(args, rank, world, local):
     result = None
     if rank == 0:
         peak, peak_kind = load_peaks()
-        b1 = stage1_bytes(T, H, k)
+        b1 = stage1_bytes_nvfp4(T, H, k) if fp4 else stage1_bytes(T, H, k)
         gbs1 = b1 / (s1_ms * 1e-3) / 1e9
         value = tokens_per_s(world, T * P, K, total_ms)
         result = {
@@ -450,16 +483,22 @@ def run_ours(args, rank, world, local):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "e4m3 MMA, fp32 accumulate; bf16 in, fp32 norm",
+            "dtype": ("e2m1 MMA with e4m3 block-16 scales (NVFP4), fp32 accumulate; bf16 in, "
+                      "fp32 norm" if fp4 else "e4m3 MMA, fp32 accumulate; bf16 in, fp32 norm"),
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
+            "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload)
+                                   + ("; NVFP4 activation and LM head" if fp4 else ""),
+                       "variant": args.variant,
                        "l2": f"inputs larger than L2: {nsets} rotating stage-1 input sets "
                              f"({nsets * set_bytes / 1e6:.0f} MB)"
-                             + (", 932 MB FP8 weight read every step" if has_lm else ""),
+                             + (f", {(stage2_bytes_nvfp4(T, H, V) if fp4 else stage2_bytes(T, H, V)) / 1e6:.0f}"
+                                f" MB {'NVFP4' if fp4 else 'FP8'} weight read every step"
+                                if has_lm else ""),
                        "parallelism": f"replicas x{world}"},
             "norm_quant": {"us": round(s1_ms * 1e3, 3), "GB/s": round(gbs1, 1),
                            "frac": round(gbs1 / peak, 4), "bytes": b1,
-                           "traffic": ncu_traffic("norm_quant") if args.workload == WORKLOAD else None},
+                           "traffic": (ncu_traffic("norm_quant_nvfp4" if fp4 else "norm_quant")
+                                       if args.workload == WORKLOAD else None)},
             "e2e": {"value": round(tokens_per_s(world, T, e2e_steps, e2e_ms), 1),
                     "unit": "draft tokens/s" if has_lm else "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -469,20 +508,25 @@ def run_ours(args, rank, world, local):
         if graph_ms is not None:
             result["graph"] = {"ms_per_step": round(graph_ms, 5),
                                "value": round(tokens_per_s(world, T, 1, graph_ms), 1),
-                               "launch_overhead_us_per_step": round((total_ms / K - graph_ms) * 1e3, 2),
+                               # positive: what host launches cost over a graph replay
+                               "stream_minus_graph_us_per_step": round((total_ms / K - graph_ms) * 1e3, 2),
                                "gpu_launches": gpu_launches_graph}
         if has_lm:
-            b2 = stage2_bytes(T, H, V)
+            b2 = stage2_bytes_nvfp4(T, H, V) if fp4 else stage2_bytes(T, H, V)
             gbs2 = b2 / (s2_ms * 1e-3) / 1e9
             result["config"]["weight_layout"] = ("packed once at load: tile-contiguous, "
-                                                 "pre-swizzled 16 KB blocks of 128 rows x 128 columns")
+                                                 "pre-swizzled 16 KB blocks of 128 rows x 128 bytes"
+                                                 + (" + 2 KB block-scale blocks" if fp4 else ""))
             result["lm_head"] = {"us": round(s2_ms * 1e3, 3), "GB/s": round(gbs2, 1),
                                  "frac": round(gbs2 / peak, 4), "bytes": b2,
                                  "draft_tokens_per_s": round(T / (s2_ms * 1e-3), 1)}
             result["roofline"] = {"bound": "hbm", "achieved": round(gbs2, 1), "peak": peak,
                                   "unit": "GB/s", "frac": round(gbs2 / peak, 4),
-                                  "traffic": ncu_traffic("lm_head") if args.workload == WORKLOAD else None,
-                                  "kernel": "lm_head_small_kernel" if T <= 64 else "lm_head_argmax_kernel",
+                                  "traffic": (ncu_traffic("lm_head_nvfp4" if fp4 else "lm_head")
+                                              if args.workload == WORKLOAD else None),
+                                  "kernel": ("lm_head_fp4_kernel" if fp4 else
+                                             "lm_head_small_kernel" if T <= 128 else
+                                             "lm_head_argmax_kernel"),
                                   "peak_source": peak_kind}
         else:
             result["roofline"] = {"bound": "hbm", "achieved": round(gbs1, 1), "peak": peak,
@@ -506,7 +550,7 @@ def _split(n, parts):
     return [(i * n // parts, (i + 1) * n // parts) for i in range(parts)]
 
 
-def oracle_sample(w, inp, qw, sw, rows, tokens, threads=1):
+def oracle_sample(w, inp, qw, sw, rows, tokens, threads=1, gw=None):
     """Oracle time of stage 1 on the sampled rows plus the LM head for `tokens`
     over `rows` vocab rows; returns (seconds, seconds for the whole step).
 
@@ -518,49 +562,70 @@ def oracle_sample(w, inp, qw, sw, rows, tokens, threads=1):
     import numpy as np
 
     import oracle
+    fp4 = gw is not None                           # the NVFP4 variant of both stages
+    stage1 = oracle.reduce_norm_quant_nvfp4 if fp4 else oracle.reduce_norm_quant
     R = inp["partials"].shape[1]
     with ThreadPoolExecutor(max_workers=threads) as pool:
         t0 = time.perf_counter()
         outs = list(pool.map(
-            lambda ab: oracle.reduce_norm_quant(inp["partials"][:, ab[0]:ab[1]],
-                                                inp["residual"][ab[0]:ab[1]], inp["norm_w"], w.eps),
+            lambda ab: stage1(inp["partials"][:, ab[0]:ab[1]], inp["residual"][ab[0]:ab[1]],
+                              inp["norm_w"], w.eps),
             _split(R, threads)))
         t1 = time.perf_counter()
         if qw is None:
             return t1 - t0, (t1 - t0) * w.T / R
-        codes = np.concatenate([o["codes"] for o in outs])
-        scales = np.concatenate([o["scales"] for o in outs])
+        cat = lambda key: np.concatenate([o[key] for o in outs])
         tok = np.asarray(tokens, np.int32)
         jobs = [(tok, a, b) for a, b in _split(rows, threads)]
-        list(pool.map(lambda j: oracle.lm_head_logits(codes, scales, qw[:rows],
-                                                      sw[: (rows + 127) // 128],
-                                                      tokens=j[0], v0=j[1], v1=j[2]), jobs))
+        if fp4:
+            codes, bs, gs = cat("codes"), cat("block_scales"), cat("global_scales")
+            head = lambda j: oracle.lm_head_logits_nvfp4(codes, bs, gs, qw[:rows], sw[:rows], gw,
+                                                         tokens=j[0], v0=j[1], v1=j[2])
+        else:
+            codes, scales = cat("codes"), cat("scales")
+            head = lambda j: oracle.lm_head_logits(codes, scales, qw[:rows],
+                                                   sw[: (rows + 127) // 128],
+                                                   tokens=j[0], v0=j[1], v1=j[2])
+        list(pool.map(head, jobs))
         t2 = time.perf_counter()
     full = (t1 - t0) + (t2 - t1) * (w.V / rows)     # whole step, all T tokens
     return t2 - t0, full
 
 
-def cpu_baseline(name):
+def sample_weights(name, rows, fp4):
+    """The first `rows` vocab rows of the workload's LM-head weight (the
+    generator draws rows in order), FP8 (codes, scales, None) or NVFP4
+    (codes, block scales, tensor scale of the sample)."""
+    import synth
+    ww = synth.workload(name, V=rows, S=1)
+    if fp4:
+        return synth.lm_head_weights_nvfp4(ww)
+    qw, sw = synth.lm_head_weights(ww)
+    return qw, sw, None
+
+
+def cpu_baseline(name, variant="fp8"):
     import synth
     w = synth.workload(name)
     n = oracle_threads()
+    fp4 = variant == "nvfp4"
+    g1 = 1.0 if fp4 else None
     if w.V == 0:
         rows = list(range(min(w.T, 2048)))
         inp = synth.stage1_inputs(w, rows=rows)
-        _, full1 = oracle_sample(w, inp, None, None, 0, None, threads=1)
-        secs, full = oracle_sample(w, inp, None, None, 0, None, threads=n)
+        _, full1 = oracle_sample(w, inp, None, None, 0, None, threads=1, gw=g1)
+        secs, full = oracle_sample(w, inp, None, None, 0, None, threads=n, gw=g1)
         return {"value": round(w.T / full, 2), "unit": "tokens/s", "cores": n, "kind": "oracle",
                 "single_thread_value": round(w.T / full1, 2),
                 "sample": f"stage 1 on {len(rows)} of {w.T} rows, rows split over {n} host "
                           f"threads ({secs:.1f} s), scaled to all rows"}
     inp = synth.stage1_inputs(w)
     rows = min(w.V, 8 * (w.V // w.S)) if w.V >= 4096 else w.V
-    ww = synth.workload(name, V=rows, S=1)
-    qw, sw = synth.lm_head_weights(ww)
+    qw, sw, gw = sample_weights(name, rows, fp4)
     toks = list(range(w.T))
-    secs, full = oracle_sample(w, inp, qw, sw, rows, toks, threads=n)
+    secs, full = oracle_sample(w, inp, qw, sw, rows, toks, threads=n, gw=gw)
     rows1 = max(128, rows // 32)
-    secs1, full1 = oracle_sample(w, inp, qw, sw, rows1, toks, threads=1)
+    secs1, full1 = oracle_sample(w, inp, qw, sw, rows1, toks, threads=1, gw=gw)
     return {"value": round(w.T / full, 4), "unit": "draft tokens/s", "cores": n,
             "kind": "oracle",
             "single_thread_value": round(w.T / full1, 4),
@@ -576,22 +641,24 @@ def run_reference(args, rank, world):
     import synth
     w = synth.workload(args.workload)
     has_lm = w.V > 0
+    fp4 = args.variant == "nvfp4"
     if has_lm:
         inp = synth.stage1_inputs(w)
         rows = 32
-        qw, sw = synth.lm_head_weights(synth.workload(args.workload, V=128, S=1))
+        qw, sw, gw = sample_weights(args.workload, 128, fp4)
         sample = (f"per step: stage 1 on all {w.T} rows + LM head for all {w.T} tokens over "
                   f"{rows} vocab rows, scaled to {w.V} rows")
     else:
         inp = synth.stage1_inputs(w, rows=[0])
-        rows, qw, sw = 0, None, None
+        rows, qw, sw, gw = 0, None, None, (1.0 if fp4 else None)
         sample = f"per step: stage 1 on 1 of {w.T} rows, scaled to all rows"
     toks = list(range(w.T)) if has_lm else None
     n = oracle_threads()
     for _ in range(args.warmup):
-        oracle_sample(w, inp, qw, sw, rows, toks, threads=n)
+        oracle_sample(w, inp, qw, sw, rows, toks, threads=n, gw=gw)
     t0 = time.perf_counter()
-    fulls = [oracle_sample(w, inp, qw, sw, rows, toks, threads=n)[1] for _ in range(args.steps)]
+    fulls = [oracle_sample(w, inp, qw, sw, rows, toks, threads=n, gw=gw)[1]
+             for _ in range(args.steps)]
     elapsed = time.perf_counter() - t0
     full = sum(fulls) / len(fulls)
     value = w.T / full
@@ -602,6 +669,7 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp32 (fp64 norm)", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
+                       "variant": args.variant,
                        "parallelism": "cpu oracle, rank 0"},
             "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": n,
                              "kind": "oracle",
@@ -629,7 +697,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             import synth
-            res["cpu_baseline"] = cpu_baseline(args.workload)
+            res["cpu_baseline"] = cpu_baseline(args.workload, args.variant)
         print(json.dumps(res), flush=True)
 
 

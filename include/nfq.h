@@ -320,10 +320,13 @@ int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w
  *   fall back).
  * nfq_lm_head_small_batch: 1 (default) runs batches of at most 128 tokens on the
  *   token-major kernel; 0 forces the weight-major kernel for every batch size.
+ * nfq_lm_head_nvfp4_tune: pipeline stages of later NVFP4 LM-head launches
+ *   (0 = as many as fit, at most 5; values below 2 or above what fits fall back).
  */
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7);
 void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot);
 void nfq_lm_head_small_batch(int enabled);
+void nfq_lm_head_nvfp4_tune(int stages);
 
 #ifdef __cplusplus
 }

@@ -113,6 +113,8 @@ def load(path: str = LIB_PATH):
                                              ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _P,
                                              ctypes.c_size_t, _P]
     lib.nfq_lm_head_nvfp4_argmax.restype = ctypes.c_int
+    lib.nfq_lm_head_nvfp4_tune.argtypes = [ctypes.c_int]
+    lib.nfq_lm_head_nvfp4_tune.restype = None
     _lib = lib
     return lib
 
@@ -421,3 +423,8 @@ def lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4Weight, S:
     if want_max or want_shards:
         return tokens, mx, sidx, sval
     return tokens
+
+
+def lm_head_nvfp4_tune(stages: int = 0):
+    """Pipeline stages of the NVFP4 LM head (0 = as many as fit); for sweeps."""
+    load().nfq_lm_head_nvfp4_tune(stages)

@@ -385,6 +385,8 @@ int nfq_device_error(int clear) {
 }
 
 // Launch-plan query and override for the stage-1 kernel (tuning sweeps; 0 = automatic).
+void nfq_lm_head_nvfp4_tune(int stages) { stage2_fp4_set_stages(stages); }
+
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7) {
   if (!out7) return NFQ_ERR_NULL;
   if (H < 128 || H % 128 || T < 1 || k < 1 || num_sms < 1) return NFQ_ERR_SHAPE;

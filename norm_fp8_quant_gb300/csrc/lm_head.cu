@@ -459,7 +459,6 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   uint8_t *smem = smem_raw + pad;
   const int G = p.G;
   constexpr uint32_t kStage = small_stage_bytes<MT>();
-  constexpr uint32_t kATile = MT * 128;
   float *sa_s = reinterpret_cast<float *>(smem + (size_t)nstage * kStage);  // [G][MT]
   SmallSmem *sh = reinterpret_cast<SmallSmem *>(sa_s + (size_t)G * MT);
   volatile int *abort_flag = &sh->abort;
@@ -529,7 +528,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         if (lane == 0) {
           uint8_t *st = smem + (size_t)s * kStage;
           const uint32_t fb = smem_u32(&sh->full[s]);
-          mbar_arrive_expect_tx(fb, (uint32_t)nb * kWTileBytes + kATile);
+          mbar_arrive_expect_tx(fb, (uint32_t)nb * kWTileBytes + (uint32_t)p.T * 128u);
           for (int h = 0; h < nb; ++h) {
             if constexpr (kPacked) {
               bulk_g2s(smem_u32(st + h * kWTileBytes),
@@ -818,7 +817,9 @@ cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const voi
   std::memset(&tw, 0, sizeof(tw));
   if (!kPacked && !encode_u8_map(&tw, w, (uint64_t)p.V, (uint64_t)p.H, 128))
     return cudaErrorInvalidValue;
-  if (!encode_u8_map(&ta, act_codes, (uint64_t)p.T, (uint64_t)p.H, (uint32_t)MT))
+  // a box of exactly T rows: rows T..MT-1 of the tile keep stale bytes, which
+  // only reach accumulator rows of tokens that do not exist (never read)
+  if (!encode_u8_map(&ta, act_codes, (uint64_t)p.T, (uint64_t)p.H, (uint32_t)p.T))
     return cudaErrorInvalidValue;
   constexpr uint32_t kStage = small_stage_bytes<MT>();
   const size_t fixed = 1024 /*align pad*/ + (size_t)p.G * MT * 4 + sizeof(SmallSmem) + 64;

@@ -14,12 +14,14 @@
 // epilogue only applies the two fp32 row scales and takes the argmax.
 //
 // Token-major, as the FP8 small-batch form: a tile is 256 vocab rows (two
-// 128-row blocks, the MMA's N), the tokens (up to 128, zero-padded) are M.
+// 128-row blocks, the MMA's N), the tokens (up to 128, zero-padded; MT = 64
+// rows loaded for batches of at most 64) are M.
 // One K step is 128 code bytes = 256 elements = four MMAs of K = 64.
 //
 // Warps (704 threads):
 //   0 .. 15   epilogue: warp w reads TMEM lane quadrant w%4 (tokens
-//             32(w%4) .. +31), tile columns 64(w/4) .. +63
+//             32(w%4) .. +31), tile columns 64(w/4) .. +63, all 64 at once,
+//             releases the accumulator, then reduces them
 //   16 .. 19  scale writers: per K step, copy the stage's activation and
 //             weight scales from shared memory into this step's TMEM scale
 //             slot, each warp into its own lane quadrant (every quadrant holds
@@ -51,17 +53,31 @@ constexpr int kF4SfWarp0 = kF4EpiWarps;
 constexpr int kF4Producer = kF4EpiWarps + kF4SfWarps;
 constexpr int kF4Mma = kF4Producer + 1;
 constexpr int kF4Threads = (kF4Mma + 1) * 32;
-constexpr int kF4MaxStages = 4;
+constexpr int kF4MaxStages = 5;
 constexpr uint32_t kF4ScaleBlock = 2048;                 // 128 rows x 16 scale bytes
 constexpr uint32_t kF4WBytes = 2 * kWTileBytes;          // 256 rows x 128 code bytes
-constexpr uint32_t kF4ABytes = kFp4MaxT * 128;           // 128 token rows x 128 code bytes
 constexpr uint32_t kF4SfbBytes = 2 * kF4ScaleBlock;      // 256 rows x 16 scale bytes
-constexpr uint32_t kF4SfaBytes = kFp4MaxT * 16;          // 128 token rows x 16 scale bytes
-constexpr uint32_t kF4Stage = kF4WBytes + kF4ABytes + kF4SfbBytes + kF4SfaBytes;
 constexpr uint32_t kF4SfBase = 256;                      // first scale column in TMEM
 constexpr uint32_t kF4SfCols = 48;                       // scale columns per stage
-static_assert(kF4Stage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 static_assert(kF4SfBase + kF4MaxStages * kF4SfCols <= 512, "scale slots fit in TMEM");
+
+// Stage layout for MT token rows: [A codes MT x 128 B][W 256 x 128 B][W scales
+// 4 KB][A scales MT x 16 B].  Only the T <= MT rows of the batch are copied in.
+// The MMA always reads 128 A rows; rows T..127 hold whatever the buffer held
+// before (with MT = 64, rows 64..127 are the first weight rows of the stage).
+// They only produce accumulator rows of tokens that do not exist — a row of D
+// depends on the same row of A and its scales alone — and are never read.
+template <int MT>
+struct Fp4Layout {
+  static constexpr uint32_t kA = 0;
+  static constexpr uint32_t kABytes = MT * 128;
+  static constexpr uint32_t kW = kABytes;
+  static constexpr uint32_t kSfb = kW + kF4WBytes;
+  static constexpr uint32_t kSfa = kSfb + kF4SfbBytes;
+  static constexpr uint32_t kSfaBytes = MT * 16;
+  static constexpr uint32_t kStage = kSfa + MT * 16 + (MT == 64 ? 1024 - 64 * 16 : 0);
+  static_assert(kStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+};
 
 struct Fp4Smem {
   uint64_t full[kF4MaxStages];
@@ -74,15 +90,17 @@ struct Fp4Smem {
   int last;
 };
 
+template <int MT>
 __global__ void __launch_bounds__(kF4Threads, 1)
     lm_head_fp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_sa, const Stage2Params p,
                        int nstage) {
+  using L = Fp4Layout<MT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
-  float *gs_s = reinterpret_cast<float *>(smem + (size_t)nstage * kF4Stage);   // [128]
+  float *gs_s = reinterpret_cast<float *>(smem + (size_t)nstage * L::kStage);   // [128]
   Fp4Smem *sh = reinterpret_cast<Fp4Smem *>(gs_s + kFp4MaxT);
   volatile int *abort_flag = &sh->abort;
 
@@ -146,20 +164,20 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           break;
         }
         if (lane == 0) {
-          uint8_t *st = smem + (size_t)s * kF4Stage;
+          uint8_t *st = smem + (size_t)s * L::kStage;
           const uint32_t fb = smem_u32(&sh->full[s]);
-          mbar_arrive_expect_tx(fb, (uint32_t)nb * (kWTileBytes + kF4ScaleBlock) + kF4ABytes +
-                                        kF4SfaBytes);
+          // the activation boxes hold exactly the T token rows (no out-of-range rows)
+          mbar_arrive_expect_tx(fb, (uint32_t)nb * (kWTileBytes + kF4ScaleBlock) +
+                                        (uint32_t)p.T * (128u + 16u));
           for (int h = 0; h < nb; ++h) {
             const size_t blk = (size_t)(blk0 + h) * (size_t)G + (size_t)ks;
-            bulk_g2s(smem_u32(st + h * kWTileBytes), p.w_packed + blk * kWTileBytes, kWTileBytes,
-                     fb, pol_w);
-            bulk_g2s(smem_u32(st + kF4WBytes + kF4ABytes + h * kF4ScaleBlock),
+            bulk_g2s(smem_u32(st + L::kW + h * kWTileBytes), p.w_packed + blk * kWTileBytes,
+                     kWTileBytes, fb, pol_w);
+            bulk_g2s(smem_u32(st + L::kSfb + h * kF4ScaleBlock),
                      p.w_packed + scale_region + blk * kF4ScaleBlock, kF4ScaleBlock, fb, pol_w);
           }
-          tma_load_2d(smem_u32(st + kF4WBytes), &tmap_a, ks * 128, 0, fb, pol_a);
-          tma_load_2d(smem_u32(st + kF4WBytes + kF4ABytes + kF4SfbBytes), &tmap_sa, ks * 16, 0, fb,
-                      pol_a);
+          tma_load_2d(smem_u32(st + L::kA), &tmap_a, ks * 128, 0, fb, pol_a);
+          tma_load_2d(smem_u32(st + L::kSfa), &tmap_sa, ks * 16, 0, fb, pol_a);
         }
         __syncwarp();
       }
@@ -201,9 +219,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         }
         if (lane == 0) {
           tc_fence_after();
-          const uint8_t *st = smem + (size_t)s * kF4Stage;
-          const uint32_t w_addr = smem_u32(st);
-          const uint32_t a_addr = smem_u32(st + kF4WBytes);
+          const uint8_t *st = smem + (size_t)s * L::kStage;
+          const uint32_t w_addr = smem_u32(st + L::kW);
+          const uint32_t a_addr = smem_u32(st + L::kA);
           const uint32_t sfa = tmem_base + kF4SfBase + s * kF4SfCols;
           const uint32_t sfb = sfa + 16u;
 #pragma unroll
@@ -235,13 +253,16 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           ok = false;
           break;
         }
-        const uint8_t *sfb_s = smem + (size_t)s * kF4Stage + kF4WBytes + kF4ABytes;
-        const uint8_t *sfa_s = sfb_s + kF4SfbBytes;
+        const uint8_t *sfb_s = smem + (size_t)s * L::kStage + L::kSfb;
+        const uint8_t *sfa_s = smem + (size_t)s * L::kStage + L::kSfa;
         uint32_t ra[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           // token row 32c + lane: its 16 scale bytes = words for MMAs 0..3
-          const uint4 v = *reinterpret_cast<const uint4 *>(sfa_s + (32 * c + lane) * 16);
+          // (rows past MT feed accumulator rows that are never read)
+          const uint4 v = (32 * c + lane < p.T)
+                              ? *reinterpret_cast<const uint4 *>(sfa_s + (32 * c + lane) * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
           ra[0 + c] = v.x;
           ra[4 + c] = v.y;
           ra[8 + c] = v.z;
@@ -279,7 +300,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     const int q = warp & 3;
     const int g = warp >> 2;
     const int tok = 32 * q + lane;
-    const bool quad_active = 32 * q < p.T;
+    const bool quad_active = 32 * q < p.T && 32 * q < MT;
     const bool tok_ok = tok < p.T;
     const float sc = gs_s[tok];
     const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
@@ -296,25 +317,25 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       int next_bound = (cur + 1) * p.shard_width;      // first row of the next shard
       float best = -INFINITY;
       int bi = -1;
+      uint32_t r0[32], r1[32];
+      if (active) {
+        tmem_ld32(taddr0, r0);
+        tmem_ld32(taddr0 + 32u, r1);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t r[16];
+        for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r0[j]), "+r"(r1[j]));
+      }
+      // every TMEM read of this tile is complete: the MMA may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
+#pragma unroll
+      for (int c4 = 0; c4 < 2; ++c4) {
+        const uint32_t(&r)[32] = c4 ? r1 : r0;
         if (active) {
-          tmem_ld16(taddr0 + (uint32_t)(16 * c4), r);
-          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(r[j]));
-        }
-        if (c4 == 3) {
-          // every TMEM read of this tile is complete: the MMA may overwrite it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sh->tempty));
-        }
-        if (active) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int v = row0 + 16 * c4 + j;
+          for (int j = 0; j < 32; ++j) {
+            const int v = row0 + 32 * c4 + j;
             if (v >= p.V) break;
             if (v >= next_bound) {
               if (bi >= 0 && tok_ok)
@@ -383,25 +404,43 @@ cudaError_t launch_pack_fp4_weights(const uint8_t *codes, const uint8_t *bscales
   return cudaGetLastError();
 }
 
-cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) {
-  if (p.T < 1 || p.T > kFp4MaxT) return cudaErrorInvalidConfiguration;
+namespace {
+
+int g_fp4_stages = 0;   // 0: as many as fit
+
+template <int MT>
+cudaError_t launch_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) {
+  using L = Fp4Layout<MT>;
   CUtensorMap ta, tsa;
-  if (!encode_u8_map(&ta, p.act_codes, (uint64_t)p.T, (uint64_t)(p.H / 2), (uint32_t)kFp4MaxT))
+  // boxes of exactly T rows: a box reaching past the tensor's last row is
+  // filled with zeros by the copy engine, which measured slow for tiny T
+  if (!encode_u8_map(&ta, p.act_codes, (uint64_t)p.T, (uint64_t)(p.H / 2), (uint32_t)p.T))
     return cudaErrorInvalidValue;
   if (!encode_u8_map_plain(&tsa, p.act_bscales, (uint64_t)p.T, (uint64_t)(p.H / 16), 16u,
-                           (uint32_t)kFp4MaxT))
+                           (uint32_t)p.T))
     return cudaErrorInvalidValue;
   const size_t fixed = 1024 /*align pad*/ + kFp4MaxT * sizeof(float) + sizeof(Fp4Smem) + 64;
   const size_t budget = 227u * 1024u;
-  int nstage = (int)((budget - fixed) / kF4Stage);
+  int nstage = (int)((budget - fixed) / L::kStage);
   if (nstage > kF4MaxStages) nstage = kF4MaxStages;
+  if (g_fp4_stages >= 2 && g_fp4_stages < nstage) nstage = g_fp4_stages;
   if (nstage < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = fixed + (size_t)nstage * kF4Stage;
-  cudaError_t e = cudaFuncSetAttribute(lm_head_fp4_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = fixed + (size_t)nstage * L::kStage;
+  auto kern = lm_head_fp4_kernel<MT>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = num_sms < p.n_vtiles ? num_sms : p.n_vtiles;
-  return launch_pdl(lm_head_fp4_kernel, grid, kF4Threads, smem, stream, ta, tsa, p, nstage);
+  return launch_pdl(kern, grid, kF4Threads, smem, stream, ta, tsa, p, nstage);
+}
+
+}  // namespace
+
+void stage2_fp4_set_stages(int n) { g_fp4_stages = n; }
+
+cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) {
+  if (p.T < 1 || p.T > kFp4MaxT) return cudaErrorInvalidConfiguration;
+  return p.T <= 64 ? launch_fp4<64>(p, num_sms, stream) : launch_fp4<128>(p, num_sms, stream);
 }
 
 }  // namespace nfq

@@ -72,6 +72,7 @@ cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out, cu
 // NVFP4 LM head (token-major, block-scaled tensor cores), T <= 128 per launch
 constexpr int kFp4MaxT = 128;
 cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream);
+void stage2_fp4_set_stages(int n);   // 0: as many pipeline stages as fit
 size_t fp4_packed_weight_bytes(int V, int H);
 cudaError_t launch_pack_fp4_weights(const uint8_t *codes, const uint8_t *bscales, int V, int H,
                                     uint8_t *out, cudaStream_t stream);
