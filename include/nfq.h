@@ -32,6 +32,14 @@
  *    (but memory-safe) results.
  *  - Row-major layouts throughout.  Every device pointer must be 16-byte aligned,
  *    except the LM head's int32 / fp32 per-token outputs (4-byte aligned).
+ *  - Kernels are launched with programmatic stream serialisation: a launch may
+ *    begin while the previous kernel on the stream is finishing, and waits for
+ *    it before it touches that kernel's outputs.  The LM-head calls read the
+ *    LM-head weight (FP8 codes, or NVFP4 codes and block scales) before that
+ *    wait: the weight is a constant, which the kernel immediately preceding an
+ *    LM-head call must not write.  The pack calls below end with an ordering
+ *    point that makes their output safe to use right away; a weight written by
+ *    another kernel needs an event or a synchronisation before the LM head.
  */
 #ifndef NFQ_H_
 #define NFQ_H_

@@ -51,6 +51,22 @@ int device_info(DeviceInfo **out) {
   return NFQ_OK;
 }
 
+// The LM heads request their first weight stages before they wait for the
+// kernel that precedes them on the stream.  A pack call therefore ends with an
+// ordering point (an event recorded and waited on the same stream), after which
+// a following kernel starts only once the packed weight is complete.
+int stream_ordering_point(cudaStream_t stream) {
+  static cudaEvent_t ev[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NFQ_ERR_CUDA;
+  if (!ev[dev] && cudaEventCreateWithFlags(&ev[dev], cudaEventDisableTiming) != cudaSuccess)
+    return NFQ_ERR_CUDA;
+  if (cudaEventRecord(ev[dev], stream) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, ev[dev], 0) != cudaSuccess)
+    return NFQ_ERR_CUDA;
+  return NFQ_OK;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -258,7 +274,8 @@ int nfq_lm_head_pack_weights(const uint8_t *w, int V, int H, uint8_t *w_packed,
   DeviceInfo *d = nullptr;
   const int st = device_info(&d);
   if (st != NFQ_OK) return st;
-  return map_cuda(launch_pack_weights(w, V, H, w_packed, static_cast<cudaStream_t>(stream)));
+  const int r = map_cuda(launch_pack_weights(w, V, H, w_packed, static_cast<cudaStream_t>(stream)));
+  return r != NFQ_OK ? r : stream_ordering_point(static_cast<cudaStream_t>(stream));
 }
 
 int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packed,
@@ -284,9 +301,10 @@ int nfq_lm_head_nvfp4_pack_weights(const uint8_t *codes, const uint8_t *block_sc
   DeviceInfo *d = nullptr;
   const int st = device_info(&d);
   if (st != NFQ_OK) return st;
-  return map_cuda(launch_pack_fp4_weights(codes, block_scales, V, H,
-                                          static_cast<uint8_t *>(w_packed),
-                                          static_cast<cudaStream_t>(stream)));
+  const int r = map_cuda(launch_pack_fp4_weights(codes, block_scales, V, H,
+                                                 static_cast<uint8_t *>(w_packed),
+                                                 static_cast<cudaStream_t>(stream)));
+  return r != NFQ_OK ? r : stream_ordering_point(static_cast<cudaStream_t>(stream));
 }
 
 int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w_scale, int V,

@@ -493,6 +493,33 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     tmem_alloc(smem_u32(&sh->tmem_base), 512);
     tmem_relinquish();
   }
+  __syncthreads();   // the barriers exist
+  // The weight is a constant of the model, never written by the kernel this
+  // one may overlap: the weight part of the first stages is requested before
+  // the wait for the previous kernel (whose output is the activation).
+  const int total_steps = n_tiles * G;
+  const int npre = total_steps < nstage ? total_steps : nstage;
+  if (warp == kProducer && lane == 0) {
+    const uint64_t pol_w = policy_evict_first();
+    for (int it = 0; it < npre; ++it) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, it / G, blk0, nb);
+      const int kb = it % G;
+      uint8_t *st = smem + (size_t)it * kStage;
+      const uint32_t fb = smem_u32(&sh->full[it]);
+      mbar_expect_tx(fb, (uint32_t)nb * kWTileBytes);
+      for (int h = 0; h < nb; ++h) {
+        if constexpr (kPacked) {
+          bulk_g2s(smem_u32(st + h * kWTileBytes),
+                   p.w_packed + ((size_t)(blk0 + h) * G + kb) * kWTileBytes, kWTileBytes, fb,
+                   pol_w);
+        } else {
+          tma_load_2d(smem_u32(st + h * kWTileBytes), &tmap_w, kb * 128, (blk0 + h) * 128, fb,
+                      pol_w);
+        }
+      }
+    }
+  }
   // everything below reads memory the previous kernel on the stream may write
   grid_dependency_wait();
   grid_launch_dependents();
@@ -517,8 +544,9 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
       for (int kb = 0; kb < G; ++kb, ++it) {
         const uint32_t s = it % (uint32_t)nstage;
         const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        const bool pre = (int)it < npre;           // weight part already requested
         int got = 1;
-        if (lane == 0)
+        if (lane == 0 && !pre)
           got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2);
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
@@ -528,8 +556,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         if (lane == 0) {
           uint8_t *st = smem + (size_t)s * kStage;
           const uint32_t fb = smem_u32(&sh->full[s]);
-          mbar_arrive_expect_tx(fb, (uint32_t)nb * kWTileBytes + (uint32_t)p.T * 128u);
-          for (int h = 0; h < nb; ++h) {
+          mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * kWTileBytes) + (uint32_t)p.T * 128u);
+          for (int h = 0; h < nb && !pre; ++h) {
             if constexpr (kPacked) {
               bulk_g2s(smem_u32(st + h * kWTileBytes),
                        p.w_packed + ((size_t)(blk0 + h) * G + kb) * kWTileBytes, kWTileBytes, fb,
@@ -545,7 +573,10 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
       }
     }
     if (lane == 0) {
-      const uint32_t issued = it;
+      // stages whose weight was requested but which the loop never reached:
+      // arrive, so their phase completes once those bytes have landed
+      for (uint32_t j = it; j < (uint32_t)npre; ++j) mbar_arrive(smem_u32(&sh->full[j]));
+      const uint32_t issued = it > (uint32_t)npre ? it : (uint32_t)npre;
       const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
       for (uint32_t j = first; j < issued; ++j)
         mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);

@@ -133,6 +133,31 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     tmem_alloc(smem_u32(&sh->tmem_base), 512);
     tmem_relinquish();
   }
+  __syncthreads();   // the barriers exist
+  // The weight is a constant of the model, never written by the kernel this
+  // one may overlap: the weight part of the first stages is requested before
+  // the wait for the previous kernel (whose output is the activation), so
+  // the pipeline is full when the activation becomes readable.
+  const int total_steps = n_tiles * G;
+  const int npre = total_steps < nstage ? total_steps : nstage;
+  if (warp == kF4Producer && lane == 0) {
+    const uint64_t pol_w = policy_evict_first();
+    for (int it = 0; it < npre; ++it) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, it / G, blk0, nb);
+      const int ks = it % G;
+      uint8_t *st = smem + (size_t)it * L::kStage;
+      const uint32_t fb = smem_u32(&sh->full[it]);
+      mbar_expect_tx(fb, (uint32_t)nb * (kWTileBytes + kF4ScaleBlock));
+      for (int h = 0; h < nb; ++h) {
+        const size_t blk = (size_t)(blk0 + h) * (size_t)G + (size_t)ks;
+        bulk_g2s(smem_u32(st + L::kW + h * kWTileBytes), p.w_packed + blk * kWTileBytes,
+                 kWTileBytes, fb, pol_w);
+        bulk_g2s(smem_u32(st + L::kSfb + h * kF4ScaleBlock),
+                 p.w_packed + scale_region + blk * kF4ScaleBlock, kF4ScaleBlock, fb, pol_w);
+      }
+    }
+  }
   // everything below reads memory the previous kernel on the stream may write
   grid_dependency_wait();
   grid_launch_dependents();
@@ -155,8 +180,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       for (int ks = 0; ks < G; ++ks, ++it) {
         const uint32_t s = it % (uint32_t)nstage;
         const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        const bool pre = (int)it < npre;           // weight part already requested
         int got = 1;
-        if (lane == 0)
+        if (lane == 0 && !pre)
           got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2);
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
@@ -167,9 +193,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
           uint8_t *st = smem + (size_t)s * L::kStage;
           const uint32_t fb = smem_u32(&sh->full[s]);
           // the activation boxes hold exactly the T token rows (no out-of-range rows)
-          mbar_arrive_expect_tx(fb, (uint32_t)nb * (kWTileBytes + kF4ScaleBlock) +
+          mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * (kWTileBytes + kF4ScaleBlock)) +
                                         (uint32_t)p.T * (128u + 16u));
-          for (int h = 0; h < nb; ++h) {
+          for (int h = 0; h < nb && !pre; ++h) {
             const size_t blk = (size_t)(blk0 + h) * (size_t)G + (size_t)ks;
             bulk_g2s(smem_u32(st + L::kW + h * kWTileBytes), p.w_packed + blk * kWTileBytes,
                      kWTileBytes, fb, pol_w);
@@ -183,7 +209,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
       }
     }
     if (lane == 0) {
-      const uint32_t issued = it;
+      // stages whose weight was requested but which the loop never reached:
+      // arrive, so their phase completes once those bytes have landed
+      for (uint32_t j = it; j < (uint32_t)npre; ++j) mbar_arrive(smem_u32(&sh->full[j]));
+      const uint32_t issued = it > (uint32_t)npre ? it : (uint32_t)npre;
       const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
       for (uint32_t j = first; j < issued; ++j)
         mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
