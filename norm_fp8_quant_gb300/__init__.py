@@ -134,6 +134,23 @@ def _stream_ptr(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _raw_stream(dev_index: int, stream=None) -> int:
+    """cudaStream_t (as an int) of `stream`, or of the current stream of the device."""
+    import torch
+    if stream is not None:
+        return stream.cuda_stream
+    return torch._C._cuda_getCurrentRawStream(dev_index)
+
+
+def _on_device(dev_index: int, fn, *args):
+    """Call fn with dev_index as the current CUDA device (switching only if needed)."""
+    import torch
+    if torch._C._cuda_getDevice() == dev_index:
+        return fn(*args)
+    with torch.cuda.device(dev_index):
+        return fn(*args)
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
@@ -167,10 +184,9 @@ def mtp_reduce_norm_quant(partials, residual, norm_w, eps: float = 1e-6,
     scales = scales_out if scales_out is not None else torch.empty((T, H // GROUP), dtype=torch.float32, device=dev)
     arr = (ctypes.c_void_p * max(k, 1))(*[p.data_ptr() for p in partials])
     q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
-    with torch.cuda.device(dev):
-        st = load().nfq_mtp_reduce_norm_quant(arr, k, _ptr(residual), _ptr(norm_w), float(eps),
-                                              T, H, _ptr(hidden), ctypes.byref(q),
-                                              _stream_ptr(stream))
+    st = _on_device(dev.index, load().nfq_mtp_reduce_norm_quant, arr, k, residual.data_ptr(),
+                    norm_w.data_ptr(), float(eps), T, H, hidden.data_ptr(), ctypes.byref(q),
+                    _raw_stream(dev.index, stream))
     _check(st, "nfq_mtp_reduce_norm_quant")
     return hidden, codes, scales
 
@@ -256,11 +272,11 @@ def lm_head_fp8_argmax(codes, scales, w, w_scales, S: int, workspace=None,
     sidx = torch.empty((S, T), dtype=torch.int32, device=dev) if want_shards else None
     sval = torch.empty((S, T), dtype=torch.float32, device=dev) if want_shards else None
     q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
-    opt = lambda t: ctypes.c_void_p(None) if t is None else _ptr(t)
+    opt = lambda t: None if t is None else t.data_ptr()
     fn = load().nfq_lm_head_fp8_argmax_packed if packed else load().nfq_lm_head_fp8_argmax
-    with torch.cuda.device(dev):
-        st = fn(ctypes.byref(q), _ptr(w), _ptr(w_scales), V, S, _ptr(tokens), opt(mx), opt(sidx),
-                opt(sval), _ptr(ws), ws.numel(), _stream_ptr(stream))
+    st = _on_device(dev.index, fn, ctypes.byref(q), w.data_ptr(), w_scales.data_ptr(), V, S,
+                    tokens.data_ptr(), opt(mx), opt(sidx), opt(sval), ws.data_ptr(), ws.numel(),
+                    _raw_stream(dev.index, stream))
     _check(st, "nfq_lm_head_fp8_argmax")
     if want_max or want_shards:
         return tokens, mx, sidx, sval
@@ -352,10 +368,9 @@ def mtp_reduce_norm_quant_nvfp4(partials, residual, norm_w, eps: float = 1e-6,
     gs = row_scales_out if row_scales_out is not None else torch.empty(T, dtype=torch.float32, device=dev)
     arr = (ctypes.c_void_p * max(k, 1))(*[p.data_ptr() for p in partials])
     q = Fp4Act(codes.data_ptr(), bs.data_ptr(), gs.data_ptr(), T, H, FP4_BLOCK)
-    with torch.cuda.device(dev):
-        st = load().nfq_mtp_reduce_norm_quant_nvfp4(arr, k, _ptr(residual), _ptr(norm_w),
-                                                    float(eps), T, H, _ptr(hidden),
-                                                    ctypes.byref(q), _stream_ptr(stream))
+    st = _on_device(dev.index, load().nfq_mtp_reduce_norm_quant_nvfp4, arr, k,
+                    residual.data_ptr(), norm_w.data_ptr(), float(eps), T, H, hidden.data_ptr(),
+                    ctypes.byref(q), _raw_stream(dev.index, stream))
     _check(st, "nfq_mtp_reduce_norm_quant_nvfp4")
     return hidden, codes, bs, gs
 
@@ -414,11 +429,10 @@ def lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4Weight, S:
     sidx = torch.empty((S, T), dtype=torch.int32, device=dev) if want_shards else None
     sval = torch.empty((S, T), dtype=torch.float32, device=dev) if want_shards else None
     q = Fp4Act(codes.data_ptr(), block_scales.data_ptr(), row_scales.data_ptr(), T, H, FP4_BLOCK)
-    opt = lambda t: ctypes.c_void_p(None) if t is None else _ptr(t)
-    with torch.cuda.device(dev):
-        st = load().nfq_lm_head_nvfp4_argmax(ctypes.byref(q), _ptr(w.data), float(w.scale), w.V,
-                                             S, _ptr(tokens), opt(mx), opt(sidx), opt(sval),
-                                             _ptr(ws), ws.numel(), _stream_ptr(stream))
+    opt = lambda t: None if t is None else t.data_ptr()
+    st = _on_device(dev.index, load().nfq_lm_head_nvfp4_argmax, ctypes.byref(q), w.data.data_ptr(),
+                    float(w.scale), w.V, S, tokens.data_ptr(), opt(mx), opt(sidx), opt(sval),
+                    ws.data_ptr(), ws.numel(), _raw_stream(dev.index, stream))
     _check(st, "nfq_lm_head_nvfp4_argmax")
     if want_max or want_shards:
         return tokens, mx, sidx, sval
