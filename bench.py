@@ -275,19 +275,26 @@ def run_ours(args, rank, world, local):
     tokens = torch.empty(T, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def stage1(parts, res):
+    # every call of the timed loops goes through the public API as a prepared
+    # call (arguments checked and marshalled once, per buffer set)
+    def prepare_stage1(parts, res):
         if fp4:
-            nfq.mtp_reduce_norm_quant_nvfp4(parts, res, norm_w, w.eps, hidden, codes, bscales,
-                                            gscales)
-        else:
-            nfq.mtp_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
+            return nfq.prepare_reduce_norm_quant_nvfp4(parts, res, norm_w, w.eps, hidden, codes,
+                                                       bscales, gscales)
+        return nfq.prepare_reduce_norm_quant(parts, res, norm_w, w.eps, hidden, codes, scales)
 
-    def stage2():
-        if fp4:
-            nfq.lm_head_nvfp4_argmax(codes, bscales, gscales, qw_d, S, workspace=ws,
-                                     tokens_out=tokens)
-        else:
-            nfq.lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, workspace=ws, tokens_out=tokens)
+    stage1_calls = {}
+
+    def stage1(parts, res):
+        key = id(res)
+        if key not in stage1_calls:
+            stage1_calls[key] = prepare_stage1(parts, res)
+        stage1_calls[key]()
+
+    if has_lm:
+        stage2 = (nfq.prepare_lm_head_nvfp4_argmax(codes, bscales, gscales, qw_d, S, ws, tokens)
+                  if fp4 else nfq.prepare_lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, ws,
+                                                             tokens))
 
     def barrier():
         torch.cuda.synchronize()
@@ -429,11 +436,12 @@ def run_ours(args, rank, world, local):
             bufs[b].copy_(h_in, non_blocking=True)
             copied[b].record()
 
+    buf_views = [([bufs[b][j] for j in range(k)], bufs[b][k]) for b in range(NB)]
+
     def e2e_compute(i):
         b = i % NB
         stream.wait_event(copied[b])
-        inp = bufs[b]
-        stage1([inp[j] for j in range(k)], inp[k])
+        stage1(*buf_views[b])
         if has_lm:
             stage2()
         result_host[b].copy_(result_dev, non_blocking=True)

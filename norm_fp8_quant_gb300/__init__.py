@@ -442,3 +442,103 @@ def lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4Weight, S:
 def lm_head_nvfp4_tune(stages: int = 0):
     """Pipeline stages of the NVFP4 LM head (0 = as many as fit); for sweeps."""
     load().nfq_lm_head_nvfp4_tune(stages)
+
+
+# --------------------------------------------------------- prepared calls --
+
+class PreparedCall:
+    """One library call with its arguments checked and marshalled once.
+
+    Calling it issues the C entry point on the given (or the current) stream of
+    the tensors' device; the tensors it was prepared with must stay alive and
+    unmoved (the object keeps references to them).  Each call costs a few
+    microseconds of host time instead of the full argument checks, which
+    matters in a decode loop that issues a step every ~100 us."""
+
+    def __init__(self, fn, args, dev_index: int, what: str, keep):
+        self._fn, self._args, self._dev, self._what, self._keep = fn, args, dev_index, what, keep
+
+    def __call__(self, stream=None):
+        st = _on_device(self._dev, self._fn, *self._args, _raw_stream(self._dev, stream))
+        if st != NFQ_OK:
+            raise NfqError(st, self._what)
+
+
+def _check_stage1_args(partials, residual, norm_w):
+    import torch
+    T, H = residual.shape
+    _need_cuda(residual, norm_w, *partials)
+    for p in partials:
+        if p.dtype != torch.bfloat16 or p.shape != (T, H):
+            raise ValueError("partials must be bf16 [T][H]")
+    if residual.dtype != torch.bfloat16 or norm_w.dtype != torch.bfloat16:
+        raise ValueError("residual and norm_w must be bf16")
+    return T, H
+
+
+def prepare_reduce_norm_quant(partials, residual, norm_w, eps, hidden_out, codes_out,
+                              scales_out) -> PreparedCall:
+    """mtp_reduce_norm_quant with fixed buffers, as a PreparedCall."""
+    T, H = _check_stage1_args(partials, residual, norm_w)
+    _need_cuda(hidden_out, codes_out, scales_out)
+    arr = (ctypes.c_void_p * len(partials))(*[p.data_ptr() for p in partials])
+    q = QuantAct(codes_out.data_ptr(), scales_out.data_ptr(), T, H, GROUP)
+    args = (arr, len(partials), residual.data_ptr(), norm_w.data_ptr(), float(eps), T, H,
+            hidden_out.data_ptr(), ctypes.byref(q))
+    return PreparedCall(load().nfq_mtp_reduce_norm_quant, args, residual.device.index,
+                        "nfq_mtp_reduce_norm_quant",
+                        (partials, residual, norm_w, hidden_out, codes_out, scales_out, arr, q))
+
+
+def prepare_reduce_norm_quant_nvfp4(partials, residual, norm_w, eps, hidden_out, codes_out,
+                                    block_scales_out, row_scales_out) -> PreparedCall:
+    """mtp_reduce_norm_quant_nvfp4 with fixed buffers, as a PreparedCall."""
+    T, H = _check_stage1_args(partials, residual, norm_w)
+    _need_cuda(hidden_out, codes_out, block_scales_out, row_scales_out)
+    arr = (ctypes.c_void_p * len(partials))(*[p.data_ptr() for p in partials])
+    q = Fp4Act(codes_out.data_ptr(), block_scales_out.data_ptr(), row_scales_out.data_ptr(), T, H,
+               FP4_BLOCK)
+    args = (arr, len(partials), residual.data_ptr(), norm_w.data_ptr(), float(eps), T, H,
+            hidden_out.data_ptr(), ctypes.byref(q))
+    return PreparedCall(load().nfq_mtp_reduce_norm_quant_nvfp4, args, residual.device.index,
+                        "nfq_mtp_reduce_norm_quant_nvfp4",
+                        (partials, residual, norm_w, hidden_out, codes_out, block_scales_out,
+                         row_scales_out, arr, q))
+
+
+def prepare_lm_head_fp8_argmax(codes, scales, w, w_scales, S: int, workspace,
+                               tokens_out) -> PreparedCall:
+    """lm_head_fp8_argmax (tokens only) with fixed buffers, as a PreparedCall."""
+    import torch
+    T, H = codes.shape
+    _need_cuda(codes, scales, w, w_scales, workspace, tokens_out)
+    if codes.dtype != torch.uint8 or w.dtype != torch.uint8 or scales.dtype != torch.float32 \
+            or w_scales.dtype != torch.float32:
+        raise ValueError("uint8 codes / weight and float32 scales expected")
+    packed = isinstance(w, PackedWeight)
+    q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
+    fn = load().nfq_lm_head_fp8_argmax_packed if packed else load().nfq_lm_head_fp8_argmax
+    args = (ctypes.byref(q), w.data_ptr(), w_scales.data_ptr(), w.shape[0], S,
+            tokens_out.data_ptr(), None, None, None, workspace.data_ptr(), workspace.numel())
+    return PreparedCall(fn, args, codes.device.index, "nfq_lm_head_fp8_argmax",
+                        (codes, scales, w, w_scales, workspace, tokens_out, q))
+
+
+def prepare_lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4Weight, S: int,
+                                 workspace, tokens_out) -> PreparedCall:
+    """lm_head_nvfp4_argmax (tokens only) with fixed buffers, as a PreparedCall."""
+    import torch
+    T, H2 = codes.shape
+    _need_cuda(codes, block_scales, row_scales, workspace, tokens_out)
+    if not isinstance(w, PackedFp4Weight):
+        raise ValueError("w must be a PackedFp4Weight")
+    if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or \
+            row_scales.dtype != torch.float32:
+        raise ValueError("codes/block scales uint8 and row scales float32 expected")
+    q = Fp4Act(codes.data_ptr(), block_scales.data_ptr(), row_scales.data_ptr(), T, 2 * H2,
+               FP4_BLOCK)
+    args = (ctypes.byref(q), w.data.data_ptr(), float(w.scale), w.V, S, tokens_out.data_ptr(),
+            None, None, None, workspace.data_ptr(), workspace.numel())
+    return PreparedCall(load().nfq_lm_head_nvfp4_argmax, args, codes.device.index,
+                        "nfq_lm_head_nvfp4_argmax",
+                        (codes, block_scales, row_scales, w, workspace, tokens_out, q))
