@@ -143,8 +143,8 @@ int nfq_mtp_reduce_norm_quant(const void *const *partials, int k, const void *re
  *              every call returns it to all-zero, so one zeroing suffices for
  *              any number of calls that run one after another on a stream.
  *              Concurrent calls need separate workspaces.
- * T = a->tokens may be any size >= 1; rows are processed 256 at a time (each
- * chunk streams the weights once).
+ * T = a->tokens may be any size >= 1; rows are processed 128 at a time (256
+ * with nfq_lm_head_small_batch(0)); each chunk streams the weights once.
  */
 size_t nfq_lm_head_workspace_bytes(int T, int S);
 
@@ -330,11 +330,14 @@ int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w
  *   token-major kernel; 0 forces the weight-major kernel for every batch size.
  * nfq_lm_head_nvfp4_tune: pipeline stages of later NVFP4 LM-head launches
  *   (0 = as many as fit, at most 5; values below 2 or above what fits fall back).
+ * nfq_stage1_grid: at most max_ctas CTAs for later stage-1 launches, each then
+ *   taking several rows in turn (0 = one CTA per SM at most).
  */
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7);
 void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot);
 void nfq_lm_head_small_batch(int enabled);
 void nfq_lm_head_nvfp4_tune(int stages);
+void nfq_stage1_grid(int max_ctas);
 
 #ifdef __cplusplus
 }

@@ -115,6 +115,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_nvfp4_argmax.restype = ctypes.c_int
     lib.nfq_lm_head_nvfp4_tune.argtypes = [ctypes.c_int]
     lib.nfq_lm_head_nvfp4_tune.restype = None
+    lib.nfq_stage1_grid.argtypes = [ctypes.c_int]
+    lib.nfq_stage1_grid.restype = None
     _lib = lib
     return lib
 
@@ -542,3 +544,8 @@ def prepare_lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4We
     return PreparedCall(load().nfq_lm_head_nvfp4_argmax, args, codes.device.index,
                         "nfq_lm_head_nvfp4_argmax",
                         (codes, block_scales, row_scales, w, workspace, tokens_out, q))
+
+
+def stage1_grid(max_ctas: int = 0):
+    """Cap the stage-1 grid (each CTA then takes several rows); 0 = automatic."""
+    load().nfq_stage1_grid(max_ctas)

@@ -232,8 +232,9 @@ int lm_head_common(const nfq_quant_act *a, const uint8_t *w, bool packed, const 
   p.S = S;
   p.shard_width = V / S;
   p.n_vtiles = (V + 127) / 128;
-  for (int t0 = 0; t0 < T; t0 += 256) {
-    const int Tc = (T - t0) < 256 ? (T - t0) : 256;
+  const int chunk = stage2_token_chunk();
+  for (int t0 = 0; t0 < T; t0 += chunk) {
+    const int Tc = (T - t0) < chunk ? (T - t0) : chunk;
     p.tok0 = t0;
     p.T = Tc;
     p.act_codes = a->codes + (size_t)t0 * H;
@@ -404,6 +405,8 @@ int nfq_device_error(int clear) {
 
 // Launch-plan query and override for the stage-1 kernel (tuning sweeps; 0 = automatic).
 void nfq_lm_head_nvfp4_tune(int stages) { stage2_fp4_set_stages(stages); }
+
+void nfq_stage1_grid(int max_ctas) { stage1_set_grid(max_ctas); }
 
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7) {
   if (!out7) return NFQ_ERR_NULL;

@@ -882,6 +882,11 @@ cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const vo
 
 void stage2_set_small(int enabled) { g_small_enabled = enabled != 0; }
 
+// Tokens per launch: batches above 128 tokens run as 128-token launches of the
+// token-major kernel (each streams the weight once; at 256 tokens two such
+// launches take 288 us against 335 us for one weight-major launch).
+int stage2_token_chunk() { return g_small_enabled ? kSmallMaxT : 256; }
+
 size_t packed_weight_bytes(int V, int H) {
   return (size_t)((V + 127) / 128) * (size_t)(H / 128) * kWTileBytes;
 }

@@ -33,6 +33,7 @@ struct Stage1Params {
 
 cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream);
 void stage1_set_tuning(int cluster, int vpt, int slots, int per_slot);
+void stage1_set_grid(int max_ctas);   // 0: one CTA (cluster) per SM at most
 int stage1_plan(int T, int H, int k, int num_sms, int *out7);
 bool stage1_fp4_supported(int H);
 
@@ -66,6 +67,7 @@ cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes_base, con
 
 size_t stage2_workspace_bytes(int S);
 void stage2_set_small(int enabled);   // 0: always use the wide-batch kernel (tests, tuning)
+int stage2_token_chunk();             // tokens per LM-head launch
 size_t packed_weight_bytes(int V, int H);
 cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out, cudaStream_t stream);
 

@@ -408,7 +408,7 @@ struct Stage1Choice {
   size_t smem;
 };
 
-int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0, g_tune_per_slot = 0;
+int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0, g_tune_per_slot = 0, g_tune_ctas = 0;
 
 size_t stage1_smem_bytes(int nslot, int per_slot, int E) {
   return (size_t)nslot * (size_t)per_slot * (size_t)E * 2u + (size_t)nslot * 16u + 48u +
@@ -511,6 +511,8 @@ cudaError_t launch_vpt(const Stage1Params &p, const Stage1Choice &ch, int grid,
 
 }  // namespace
 
+void stage1_set_grid(int max_ctas) { g_tune_ctas = max_ctas; }
+
 void stage1_set_tuning(int cluster, int vpt, int slots, int per_slot) {
   g_tune_C = cluster;
   g_tune_vpt = vpt;
@@ -544,6 +546,8 @@ cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream) {
   p.n_active = ch.NA;
   // persistent grid: at most one CTA per SM, whole clusters, no more rows than exist
   long clusters = num_sms / ch.C;
+  if (g_tune_ctas > 0 && g_tune_ctas / ch.C >= 1 && g_tune_ctas / ch.C < clusters)
+    clusters = g_tune_ctas / ch.C;
   if (clusters > p.T) clusters = p.T;
   if (clusters < 1) clusters = 1;
   const int grid = (int)(clusters * ch.C);
