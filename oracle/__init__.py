@@ -78,6 +78,17 @@ def _load():
                                                 _P, _P, ctypes.c_float, ctypes.c_int,
                                                 ctypes.c_int, _P]
         lib.or_lm_head_logits_nvfp4.restype = None
+        lib.or_unfused_reduce_bf16.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+        lib.or_unfused_reduce_bf16.restype = None
+        lib.or_unfused_add_rmsnorm.argtypes = [_P, _P, _P, ctypes.c_double, ctypes.c_int,
+                                               ctypes.c_int, _P]
+        lib.or_unfused_add_rmsnorm.restype = None
+        lib.or_quant_fp8_rows.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P]
+        lib.or_quant_fp8_rows.restype = None
+        lib.or_argmax_bf16.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P]
+        lib.or_argmax_bf16.restype = None
+        lib.or_f32_to_bf16_array.argtypes = [_P, ctypes.c_size_t, _P]
+        lib.or_f32_to_bf16_array.restype = None
         _lib = lib
     return _lib
 
@@ -94,9 +105,10 @@ def bf16_to_f32(bits) -> np.ndarray:
 
 
 def f32_to_bf16(x) -> np.ndarray:
-    lib = _load()
     x = _c(x, np.float32).ravel()
-    return np.array([lib.or_f32_to_bf16(float(v)) for v in x], dtype=np.uint16)
+    out = np.empty(x.size, np.uint16)
+    _load().or_f32_to_bf16_array(x.ctypes.data, x.size, out.ctypes.data)
+    return out
 
 
 def f64_to_bf16(x) -> np.ndarray:
@@ -245,3 +257,53 @@ def lm_head_logits_nvfp4(qa, sa, ga, qw, sw, gw: float, tokens=None, v0: int = 0
                                     tok.ctypes.data, tok.size, qw.ctypes.data, sw.ctypes.data,
                                     float(gw), v0, v1, out.ctypes.data)
     return out
+
+
+# ------------------------------------------------------ unfused reference arm --
+
+def unfused_reduce_bf16(partials):
+    """bf16(sum of the k BF16 partials in fp32), the separate all-reduce's output."""
+    p = _c(partials, np.uint16)
+    k, R, H = p.shape
+    out = np.empty((R, H), np.uint16)
+    _load().or_unfused_reduce_bf16(p.ctypes.data, k, R, H, out.ctypes.data)
+    return out
+
+
+def unfused_add_rmsnorm(x, residual, norm_w, eps: float = EPS):
+    x = _c(x, np.uint16)
+    R, H = x.shape
+    res = _c(residual, np.uint16)
+    w = _c(norm_w, np.uint16)
+    out = np.empty((R, H), np.uint16)
+    _load().or_unfused_add_rmsnorm(x.ctypes.data, res.ctypes.data, w.ctypes.data, eps, R, H,
+                                   out.ctypes.data)
+    return out
+
+
+def quant_fp8_rows(hidden):
+    h = _c(hidden, np.uint16)
+    R, H = h.shape
+    codes = np.empty((R, H), np.uint8)
+    scales = np.empty((R, H // GROUP), np.float32)
+    _load().or_quant_fp8_rows(h.ctypes.data, R, H, codes.ctypes.data, scales.ctypes.data)
+    return {"codes": codes, "scales": scales}
+
+
+def argmax_bf16(logits_bits):
+    L = _c(logits_bits, np.uint16)
+    n, V = L.shape
+    tok = np.empty(n, np.int32)
+    _load().or_argmax_bf16(L.ctypes.data, n, V, tok.ctypes.data)
+    return tok
+
+
+def unfused_step(partials, residual, norm_w, qw, sw, eps: float = EPS, tokens=None):
+    """The unfused path end to end: BF16 all-reduce, add + RMSNorm, group quant,
+    BF16 logits, full-vocab argmax.  Returns its intermediate results."""
+    s = unfused_reduce_bf16(partials)
+    hidden = unfused_add_rmsnorm(s, residual, norm_w, eps)
+    q = quant_fp8_rows(hidden)
+    L = lm_head_logits(q["codes"], q["scales"], qw, sw, tokens=tokens)
+    Lb = f32_to_bf16(L.ravel()).reshape(L.shape)
+    return {"sum": s, "hidden": hidden, **q, "logits": Lb, "tokens": argmax_bf16(Lb)}

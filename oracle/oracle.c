@@ -368,3 +368,81 @@ void or_lm_head_logits_nvfp4(const uint8_t *qa, const uint8_t *sa, const float *
   free(ad);
   free(wd);
 }
+
+/* ================================================= unfused reference arm == */
+/*
+ * The path without the fusions ("[Spec Decode][Perf] Fuse the MTP trailing
+ * all-reduce; local-argmax draft tokens", intro and Accuracy: the trailing
+ * all-reduce is a separate BF16 collective before the final RMSNorm, and the
+ * draft tokens come from the argmax of the gathered full-vocab logits):
+ *   s      = bf16_rne((p_0 + p_1) + ... + p_{k-1})               fp32 sum, one rounding
+ *   hidden = bf16_rne((s + residual) * rsqrt(mean(.^2) + eps) * w)   as stage 1 (fp64 norm)
+ *   codes/scales from hidden exactly as stage 1
+ *   logits = bf16_rne(fp32 LM-head logits) [T][V]; token = lowest index of the maximum
+ */
+void or_unfused_reduce_bf16(const uint16_t *partials, int k, int R, int H, uint16_t *out) {
+  const size_t plane = (size_t)R * (size_t)H;
+  for (size_t i = 0; i < plane; ++i) {
+    float s = or_bf16_to_f32(partials[i]);
+    for (int j = 1; j < k; ++j) s = s + or_bf16_to_f32(partials[(size_t)j * plane + i]);
+    out[i] = or_f32_to_bf16(s);
+  }
+}
+
+/* RMSNorm of (x + residual), both BF16 rows [R][H]: the hidden only. */
+void or_unfused_add_rmsnorm(const uint16_t *x, const uint16_t *residual, const uint16_t *norm_w,
+                            double eps, int R, int H, uint16_t *hidden) {
+  float *v = (float *)malloc(sizeof(float) * (size_t)H);
+  if (!v) return;
+  for (int r = 0; r < R; ++r) {
+    const size_t row = (size_t)r * (size_t)H;
+    double ss = 0.0;
+    for (int h = 0; h < H; ++h) {
+      v[h] = or_bf16_to_f32(x[row + h]) + or_bf16_to_f32(residual[row + h]);
+      ss += (double)v[h] * (double)v[h];
+    }
+    const double rr = 1.0 / sqrt(ss / (double)H + eps);
+    for (int h = 0; h < H; ++h)
+      hidden[row + h] = or_f64_to_bf16(((double)v[h] * rr) * (double)or_bf16_to_f32(norm_w[h]));
+  }
+  free(v);
+}
+
+/* Packed FP8 quantisation of BF16 rows [R][H], exactly stage 1's rule. */
+void or_quant_fp8_rows(const uint16_t *hidden, int R, int H, uint8_t *codes, float *scales) {
+  const int G = H / 128;
+  for (int r = 0; r < R; ++r) {
+    for (int g = 0; g < G; ++g) {
+      const size_t base = (size_t)r * (size_t)H + (size_t)g * 128;
+      float amax = 0.0f;
+      for (int j = 0; j < 128; ++j) {
+        float a = fabsf(or_bf16_to_f32(hidden[base + j]));
+        if (a > amax) amax = a;
+      }
+      const float scale = amax / 448.0f;
+      scales[(size_t)r * G + g] = scale;
+      for (int j = 0; j < 128; ++j)
+        codes[base + j] = (scale == 0.0f) ? 0 : or_f32_to_e4m3(or_bf16_to_f32(hidden[base + j]) / scale);
+    }
+  }
+}
+
+/* Greedy token per row of BF16 logits [n][V]: the lowest index of the maximum
+ * (-0 == +0).  The BF16 rounding makes exact ties common. */
+void or_argmax_bf16(const uint16_t *logits, int n, int V, int32_t *tok) {
+  for (int i = 0; i < n; ++i) {
+    const uint16_t *L = logits + (size_t)i * (size_t)V;
+    float best = or_bf16_to_f32(L[0]);
+    int bi = 0;
+    for (int v = 1; v < V; ++v) {
+      const float x = or_bf16_to_f32(L[v]);
+      if (x > best) { best = x; bi = v; }
+    }
+    tok[i] = bi;
+  }
+}
+
+/* Element-wise or_f32_to_bf16 over an array (one call for many values). */
+void or_f32_to_bf16_array(const float *x, size_t n, uint16_t *out) {
+  for (size_t i = 0; i < n; ++i) out[i] = or_f32_to_bf16(x[i]);
+}

@@ -547,3 +547,51 @@ def test_nvfp4_lm_head_matches_fp64_within_the_summation_bound():
     Lt = oracle.lm_head_logits_nvfp4(w["codes"], w["block_scales"], np.ones(V, np.float32),
                                      a["codes"], a["block_scales"], np.float32(1.0))
     assert np.allclose(Lt.T * scale, L, rtol=1e-5, atol=0)
+
+
+# --------------------------------------------------- unfused reference arm --
+
+def test_unfused_reduce_rounds_the_sum_once_to_bf16():
+    # 1 + 2^-8 + 2^-9: the fp32 sum is exact, its BF16 rounding goes up to
+    # 1 + 2^-7 (above the midpoint); the fused path would keep the fp32 value
+    p = np.array([[[1.0, 3.0]], [[2.0 ** -8, -1.0]], [[2.0 ** -9, 0.5]]], np.float32)
+    bits = np.stack([bf16_bits_of(p[i]) for i in range(3)])
+    s = oracle.unfused_reduce_bf16(bits)
+    assert oracle.bf16_to_f32(s).tolist() == [[1.0 + 2.0 ** -7, 2.5]]
+    # k = 1 is the identity; integer partials sum exactly
+    x = torch_bf16_bits(rng.normal(0, 3, (3, 64)).astype(np.float32))
+    assert np.array_equal(oracle.unfused_reduce_bf16(x[None]), x)
+    ints = rng.integers(-50, 50, (4, 2, 32)).astype(np.float32)
+    got = oracle.bf16_to_f32(oracle.unfused_reduce_bf16(np.stack([bf16_bits_of(v) for v in ints])))
+    assert np.array_equal(got, ints.sum(axis=0))
+
+
+def test_unfused_norm_and_quant_equal_the_fused_ones_on_the_same_sum():
+    """With k = 1 and a zero partial the unfused chain reduces to the fused
+    stage 1 (no rounding is added): a cross-check of the two oracle paths."""
+    R, H = 5, 384
+    x = torch_bf16_bits(rng.normal(0, 1, (R, H)).astype(np.float32))
+    res = torch_bf16_bits(rng.normal(0, 1, (R, H)).astype(np.float32))
+    w = torch_bf16_bits((1 + rng.normal(0, 0.1, H)).astype(np.float32))
+    fused = oracle.reduce_norm_quant(x[None], res, w)
+    hid = oracle.unfused_add_rmsnorm(x, res, w)
+    assert np.array_equal(hid, fused["hidden"])
+    q = oracle.quant_fp8_rows(hid)
+    assert np.array_equal(q["codes"], fused["codes"]) and np.array_equal(q["scales"], fused["scales"])
+    # the group quantiser equals torch's e4m3 cast of hidden / (amax / 448)
+    y = oracle.bf16_to_f32(hid).reshape(R, H // 128, 128)
+    sc = (np.abs(y).max(axis=2) / np.float32(448)).astype(np.float32)
+    want = torch_e4m3_codes((y / sc[:, :, None]).astype(np.float32)).reshape(R, H)
+    assert np.array_equal(q["codes"], want)
+
+
+def test_bf16_argmax_is_lowest_index_by_brute_force():
+    for trial in range(20):
+        r = np.random.default_rng(trial)
+        L = r.integers(-3, 4, (3, 37)).astype(np.float32)   # many exact ties
+        L[0, 5] = -0.0
+        bits = bf16_bits_of(L)
+        tok = oracle.argmax_bf16(bits)
+        for i in range(3):
+            m = L[i].max()
+            assert tok[i] == min(v for v in range(37) if L[i, v] == m)
