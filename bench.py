@@ -59,8 +59,9 @@ def parse():
                     help="draft positions per step (the hidden of each feeds the next)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["decode_c64", "decode_c1", "prefill", "tie_stress", "tiny"])
-    ap.add_argument("--variant", choices=["fp8", "nvfp4"], default="fp8",
-                    help="activation / LM-head format: packed FP8 (default) or NVFP4")
+    ap.add_argument("--variant", choices=["fp8", "nvfp4", "unfused"], default="fp8",
+                    help="packed FP8 path (default), its NVFP4 form, or the unfused "
+                         "reference arm (separate kernels, BF16 logits, full-vocab argmax)")
     return ap.parse_args()
 
 
@@ -97,6 +98,20 @@ def stage2_bytes_nvfp4(T, H, V):
     weight), the activation's codes, block scales and row scales read; int32
     tokens written."""
     return V * H // 2 + V * H // 16 + T * H // 2 + T * H // 16 + T * 4 + T * 4
+
+
+def stage1_bytes_unfused(T, H, k):
+    """The unfused stage 1: BF16 all-reduce (k partials in, sum out), add +
+    RMSNorm (sum and residual in, hidden out), group quantisation (hidden in,
+    codes and scales out)."""
+    return (k * T * H * 2 + T * H * 2) + (3 * T * H * 2 + H * 2) + \
+        (T * H * 2 + T * H + T * (H // 128) * 4)
+
+
+def stage2_bytes_unfused(T, H, V):
+    """The unfused LM head: the FP8 LM head's reads plus BF16 logits written and
+    read back by the full-vocab argmax."""
+    return stage2_bytes(T, H, V) + 2 * T * V * 2
 
 
 def load_peaks():
@@ -251,6 +266,7 @@ def run_ours(args, rank, world, local):
     nsets = int(min(64, max(2, -(-ROTATION_BYTES // set_bytes))))
     sets = [([p.to(dev) for p in host_parts], host_res.to(dev)) for _ in range(nsets)]
     fp4 = args.variant == "nvfp4"
+    unfused = args.variant == "unfused"
     if has_lm and not fp4:
         qw, sw = synth.lm_head_weights(w)
         qw_rowmajor = torch.from_numpy(qw).to(dev)
@@ -295,6 +311,19 @@ def run_ours(args, rank, world, local):
         stage2 = (nfq.prepare_lm_head_nvfp4_argmax(codes, bscales, gscales, qw_d, S, ws, tokens)
                   if fp4 else nfq.prepare_lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, ws,
                                                              tokens))
+    if unfused:
+        # the unfused reference arm: five separate kernels a step
+        s_sum = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        logits = torch.empty((T, V), dtype=torch.bfloat16, device=dev) if has_lm else None
+
+        def stage1(parts, res):
+            nfq.unfused_allreduce_bf16(parts, out=s_sum)
+            nfq.unfused_add_rmsnorm(s_sum, res, norm_w, w.eps, hidden_out=hidden)
+            nfq.unfused_quant_fp8(hidden, codes_out=codes, scales_out=scales)
+
+        def stage2():
+            nfq.unfused_lm_head_logits(codes, scales, qw_d, sw_d, logits_out=logits)
+            nfq.unfused_argmax_bf16(logits, tokens_out=tokens)
 
     def barrier():
         torch.cuda.synchronize()
@@ -330,7 +359,7 @@ def run_ours(args, rank, world, local):
     # overlapping the first one's tail): the reported rate.  With --mtp P a
     # step is P chained draft positions: position p's hidden is the residual
     # of position p+1 (nfq_mtp_draft_chain), each position with its own partials.
-    P = max(1, args.mtp) if has_lm and not fp4 else 1
+    P = max(1, args.mtp) if has_lm and not (fp4 or unfused) else 1
     if P > 1:
         chain_hidden = [torch.empty_like(hidden) for _ in range(2)]
         chain_tokens = torch.empty((P, T), dtype=torch.int32, device=dev)
@@ -400,11 +429,11 @@ def run_ours(args, rank, world, local):
         g1.record(stream)
         barrier()
         graph_ms = g0.elapsed_time(g1) / (reps * nsets)
-        gpu_launches_graph = (2 if has_lm else 1) * reps * nsets
+        gpu_launches_graph = ((5 if has_lm else 3) if unfused else (2 if has_lm else 1)) * reps * nsets
         del g
         if nfq.device_error() != nfq.NFQ_OK:
             raise RuntimeError("a kernel reported an expired wait in the graph replay")
-    gpu_launches = (2 if has_lm else 1) * K * P
+    gpu_launches = ((5 if has_lm else 3) if unfused else (2 if has_lm else 1)) * K * P
 
     # end to end through the public API: every step copies its stage-1 inputs
     # (one pinned host batch holding the k partials and the residual) to the
@@ -475,7 +504,8 @@ def run_ours(args, rank, world, local):
     result = None
     if rank == 0:
         peak, peak_kind = load_peaks()
-        b1 = stage1_bytes_nvfp4(T, H, k) if fp4 else stage1_bytes(T, H, k)
+        b1 = (stage1_bytes_nvfp4(T, H, k) if fp4 else
+              stage1_bytes_unfused(T, H, k) if unfused else stage1_bytes(T, H, k))
         gbs1 = b1 / (s1_ms * 1e-3) / 1e9
         value = tokens_per_s(world, T * P, K, total_ms)
         result = {
@@ -495,7 +525,9 @@ def run_ours(args, rank, world, local):
                       "fp32 norm" if fp4 else "e4m3 MMA, fp32 accumulate; bf16 in, fp32 norm"),
             "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload)
-                                   + ("; NVFP4 activation and LM head" if fp4 else ""),
+                                   + ("; NVFP4 activation and LM head" if fp4 else
+                                      "; unfused reference arm: BF16 all-reduce, add+RMSNorm, "
+                                      "quant, BF16 logits, full-vocab argmax" if unfused else ""),
                        "variant": args.variant,
                        "l2": f"inputs larger than L2: {nsets} rotating stage-1 input sets "
                              f"({nsets * set_bytes / 1e6:.0f} MB)"
@@ -506,7 +538,7 @@ def run_ours(args, rank, world, local):
             "norm_quant": {"us": round(s1_ms * 1e3, 3), "GB/s": round(gbs1, 1),
                            "frac": round(gbs1 / peak, 4), "bytes": b1,
                            "traffic": (ncu_traffic("norm_quant_nvfp4" if fp4 else "norm_quant")
-                                       if args.workload == WORKLOAD else None)},
+                                       if args.workload == WORKLOAD and not unfused else None)},
             "e2e": {"value": round(tokens_per_s(world, T, e2e_steps, e2e_ms), 1),
                     "unit": "draft tokens/s" if has_lm else "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -520,7 +552,8 @@ def run_ours(args, rank, world, local):
                                "stream_minus_graph_us_per_step": round((total_ms / K - graph_ms) * 1e3, 2),
                                "gpu_launches": gpu_launches_graph}
         if has_lm:
-            b2 = stage2_bytes_nvfp4(T, H, V) if fp4 else stage2_bytes(T, H, V)
+            b2 = (stage2_bytes_nvfp4(T, H, V) if fp4 else
+                  stage2_bytes_unfused(T, H, V) if unfused else stage2_bytes(T, H, V))
             gbs2 = b2 / (s2_ms * 1e-3) / 1e9
             result["config"]["weight_layout"] = ("packed once at load: tile-contiguous, "
                                                  "pre-swizzled 16 KB blocks of 128 rows x 128 bytes"
@@ -531,8 +564,11 @@ def run_ours(args, rank, world, local):
             result["roofline"] = {"bound": "hbm", "achieved": round(gbs2, 1), "peak": peak,
                                   "unit": "GB/s", "frac": round(gbs2 / peak, 4),
                                   "traffic": (ncu_traffic("lm_head_nvfp4" if fp4 else "lm_head")
-                                              if args.workload == WORKLOAD else None),
+                                              if args.workload == WORKLOAD and not unfused
+                                              else None),
                                   "kernel": ("lm_head_fp4_kernel" if fp4 else
+                                             "lm_head_small_kernel (BF16 logits) + "
+                                             "unfused_argmax_kernel" if unfused else
                                              "lm_head_small_kernel" if T <= 128 else
                                              "lm_head_argmax_kernel"),
                                   "peak_source": peak_kind}

@@ -318,6 +318,37 @@ int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w
                              size_t ws_bytes, void *stream);
 
 /*
+ * The unfused reference arm: the same step as separate kernels, the way it runs
+ * without the two fusions of [F] (intro, Accuracy): the trailing all-reduce as a
+ * separate BF16 collective (here the BF16-rounded sum of the partials), then
+ * add + RMSNorm, then the group quantisation, then an LM head that writes the
+ * full BF16 logits, then a full-vocab argmax ([F] Benchmarks: the gathered
+ * logits are 64 x 151k x 2 bytes per draft step at c=64).  For measuring what
+ * the fused path saves; arguments follow the fused calls.
+ *   nfq_unfused_allreduce_bf16  out = bf16(p_0 + ... + p_{k-1}), fp32 sum in order,
+ *                               out BF16 [T][H]; H % 8 == 0
+ *   nfq_unfused_add_rmsnorm     hidden = bf16((x + residual) * rsqrt(mean(.^2) + eps) * w)
+ *                               for BF16 x, residual [T][H]; 128 <= H <= 16384
+ *   nfq_unfused_quant_fp8       the packed FP8 quantisation of stage 1 applied to a
+ *                               BF16 hidden [T][H]
+ *   nfq_unfused_lm_head_logits  BF16 logits [T][V] (round to nearest even of the fp32
+ *                               logit) from the activation and the packed FP8 weight
+ *                               (nfq_lm_head_pack_weights) with its block scales
+ *   nfq_unfused_argmax_bf16     tokens_out[t] = lowest index of the maximum of the BF16
+ *                               logits row t (-0 == +0)
+ */
+int nfq_unfused_allreduce_bf16(const void *const *partials, int k, int T, int H, void *out,
+                               void *stream);
+int nfq_unfused_add_rmsnorm(const void *x, const void *residual, const void *norm_w, float eps,
+                            int T, int H, void *hidden_out, void *stream);
+int nfq_unfused_quant_fp8(const void *hidden, int T, int H, const nfq_quant_act *q_out,
+                          void *stream);
+int nfq_unfused_lm_head_logits(const nfq_quant_act *a, const uint8_t *w_packed,
+                               const float *w_scales, int V, void *logits_out, void *stream);
+int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_out,
+                            void *stream);
+
+/*
  * Tuning hooks (process-wide, not thread-safe; for benchmarks and tests).
  * nfq_stage1_plan: the stage-1 launch plan for (T, H, k) on a GPU with
  *   num_sms SMs: out7 = {cluster CTAs per row, 16-byte vectors per thread,

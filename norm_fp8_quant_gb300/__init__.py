@@ -117,6 +117,18 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_nvfp4_tune.restype = None
     lib.nfq_stage1_grid.argtypes = [ctypes.c_int]
     lib.nfq_stage1_grid.restype = None
+    lib.nfq_unfused_allreduce_bf16.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P]
+    lib.nfq_unfused_add_rmsnorm.argtypes = [_P, _P, _P, ctypes.c_float, ctypes.c_int,
+                                            ctypes.c_int, _P, _P]
+    lib.nfq_unfused_quant_fp8.argtypes = [_P, ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(QuantAct), _P]
+    lib.nfq_unfused_lm_head_logits.argtypes = [ctypes.POINTER(QuantAct), _P, _P, ctypes.c_int,
+                                               _P, _P]
+    lib.nfq_unfused_argmax_bf16.argtypes = [_P, ctypes.c_int, ctypes.c_int, _P, _P]
+    for fn in (lib.nfq_unfused_allreduce_bf16, lib.nfq_unfused_add_rmsnorm,
+               lib.nfq_unfused_quant_fp8, lib.nfq_unfused_lm_head_logits,
+               lib.nfq_unfused_argmax_bf16):
+        fn.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -549,3 +561,75 @@ def prepare_lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4We
 def stage1_grid(max_ctas: int = 0):
     """Cap the stage-1 grid (each CTA then takes several rows); 0 = automatic."""
     load().nfq_stage1_grid(max_ctas)
+
+
+# ---------------------------------------------------- unfused reference arm --
+
+def unfused_allreduce_bf16(partials, out=None, stream=None):
+    """bf16(sum of the k BF16 partials): the separate all-reduce of the unfused path."""
+    import torch
+    T, H = partials[0].shape
+    _need_cuda(*partials)
+    dev = partials[0].device
+    out = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    arr = (ctypes.c_void_p * len(partials))(*[p.data_ptr() for p in partials])
+    st = _on_device(dev.index, load().nfq_unfused_allreduce_bf16, arr, len(partials), T, H,
+                    out.data_ptr(), _raw_stream(dev.index, stream))
+    _check(st, "nfq_unfused_allreduce_bf16")
+    return out
+
+
+def unfused_add_rmsnorm(x, residual, norm_w, eps: float = 1e-6, hidden_out=None, stream=None):
+    import torch
+    T, H = x.shape
+    _need_cuda(x, residual, norm_w)
+    dev = x.device
+    hidden = hidden_out if hidden_out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    st = _on_device(dev.index, load().nfq_unfused_add_rmsnorm, x.data_ptr(), residual.data_ptr(),
+                    norm_w.data_ptr(), float(eps), T, H, hidden.data_ptr(),
+                    _raw_stream(dev.index, stream))
+    _check(st, "nfq_unfused_add_rmsnorm")
+    return hidden
+
+
+def unfused_quant_fp8(hidden, codes_out=None, scales_out=None, stream=None):
+    import torch
+    T, H = hidden.shape
+    _need_cuda(hidden)
+    dev = hidden.device
+    codes = codes_out if codes_out is not None else torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = scales_out if scales_out is not None else torch.empty((T, H // GROUP), dtype=torch.float32, device=dev)
+    q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
+    st = _on_device(dev.index, load().nfq_unfused_quant_fp8, hidden.data_ptr(), T, H,
+                    ctypes.byref(q), _raw_stream(dev.index, stream))
+    _check(st, "nfq_unfused_quant_fp8")
+    return codes, scales
+
+
+def unfused_lm_head_logits(codes, scales, w: PackedWeight, w_scales, logits_out=None,
+                           stream=None):
+    """BF16 logits [T][V] of the packed FP8 LM head."""
+    import torch
+    T, H = codes.shape
+    _need_cuda(codes, scales, w_scales)
+    if not isinstance(w, PackedWeight):
+        raise ValueError("w must be a PackedWeight")
+    dev = codes.device
+    out = logits_out if logits_out is not None else torch.empty((T, w.V), dtype=torch.bfloat16, device=dev)
+    q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
+    st = _on_device(dev.index, load().nfq_unfused_lm_head_logits, ctypes.byref(q), w.data_ptr(),
+                    w_scales.data_ptr(), w.V, out.data_ptr(), _raw_stream(dev.index, stream))
+    _check(st, "nfq_unfused_lm_head_logits")
+    return out
+
+
+def unfused_argmax_bf16(logits, tokens_out=None, stream=None):
+    import torch
+    T, V = logits.shape
+    _need_cuda(logits)
+    dev = logits.device
+    tok = tokens_out if tokens_out is not None else torch.empty(T, dtype=torch.int32, device=dev)
+    st = _on_device(dev.index, load().nfq_unfused_argmax_bf16, logits.data_ptr(), T, V,
+                    tok.data_ptr(), _raw_stream(dev.index, stream))
+    _check(st, "nfq_unfused_argmax_bf16")
+    return tok

@@ -288,6 +288,111 @@ int nfq_lm_head_fp8_argmax_packed(const nfq_quant_act *a, const uint8_t *w_packe
                         shard_idx_out, shard_val_out, workspace, ws_bytes, stream);
 }
 
+int nfq_unfused_allreduce_bf16(const void *const *partials, int k, int T, int H, void *out,
+                               void *stream) {
+  if (!partials || !out) return NFQ_ERR_NULL;
+  if (k < 1 || k > kMaxPartials || T < 0 || H < 8 || H % 8 != 0) return NFQ_ERR_SHAPE;
+  for (int i = 0; i < k; ++i) {
+    if (!partials[i]) return NFQ_ERR_NULL;
+    if (!aligned16(partials[i])) return NFQ_ERR_ALIGN;
+  }
+  if (!aligned16(out)) return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  UnfusedReduceParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int i = 0; i < k; ++i) p.partials[i] = partials[i];
+  p.k = k;
+  p.n_vec = (size_t)T * (size_t)H / 8u;
+  p.out = out;
+  return map_cuda(launch_unfused_reduce(p, d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_unfused_add_rmsnorm(const void *x, const void *residual, const void *norm_w, float eps,
+                            int T, int H, void *hidden_out, void *stream) {
+  if (!x || !residual || !norm_w || !hidden_out) return NFQ_ERR_NULL;
+  if (T < 0 || H < 128 || H > 16384 || H % 128 != 0) return NFQ_ERR_SHAPE;
+  if (!(eps >= 0.0f) || eps > 1.0f) return NFQ_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(norm_w) || !aligned16(hidden_out))
+    return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_unfused_add_rmsnorm(x, residual, norm_w, eps, T, H, hidden_out,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_unfused_quant_fp8(const void *hidden, int T, int H, const nfq_quant_act *q_out,
+                          void *stream) {
+  if (!hidden || !q_out || !q_out->codes || !q_out->scales) return NFQ_ERR_NULL;
+  if (T < 0 || H < 128 || H > 32768 || H % 128 != 0) return NFQ_ERR_SHAPE;
+  if (q_out->group != 128 || q_out->tokens != T || q_out->hidden != H) return NFQ_ERR_SHAPE;
+  if (!aligned16(hidden) || !aligned16(q_out->codes) || !aligned16(q_out->scales))
+    return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_unfused_quant(hidden, T, H, q_out->codes, q_out->scales,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_unfused_lm_head_logits(const nfq_quant_act *a, const uint8_t *w_packed,
+                               const float *w_scales, int V, void *logits_out, void *stream) {
+  if (!a || !w_packed || !w_scales || !logits_out || !a->codes || !a->scales)
+    return NFQ_ERR_NULL;
+  const int T = a->tokens, H = a->hidden;
+  if (a->group != 128 || H < 128 || H > 16384 || H % 128 != 0 || T < 0 || V < 1)
+    return NFQ_ERR_SHAPE;
+  if (!aligned16(a->codes) || !aligned16(a->scales) || !aligned16(w_packed) ||
+      !aligned16(w_scales) || !aligned16(logits_out))
+    return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  Stage2Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.w_scales = w_scales;
+  p.w_packed = w_packed;
+  p.err = d->err;
+  p.H = H;
+  p.G = H / 128;
+  p.V = V;
+  p.S = 1;
+  p.shard_width = V;
+  p.n_vtiles = (V + 127) / 128;
+  for (int t0 = 0; t0 < T; t0 += 128) {
+    const int Tc = (T - t0) < 128 ? (T - t0) : 128;
+    p.T = Tc;
+    p.T_total = T;
+    p.tok0 = t0;
+    p.act_codes = a->codes + (size_t)t0 * H;
+    p.act_scales = a->scales + (size_t)t0 * (H / 128);
+    p.logits_out = static_cast<uint16_t *>(logits_out) + (size_t)t0 * (size_t)V;
+    const cudaError_t e = launch_lm_head_logits(p, d->num_sms, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
+    if (e != cudaSuccess) return NFQ_ERR_CUDA;
+  }
+  return NFQ_OK;
+}
+
+int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_out,
+                            void *stream) {
+  if (!logits || !tokens_out) return NFQ_ERR_NULL;
+  if (T < 0 || V < 1) return NFQ_ERR_SHAPE;
+  if (!aligned16(logits) || !aligned4(tokens_out)) return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_unfused_argmax(logits, T, V, tokens_out,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 size_t nfq_lm_head_nvfp4_packed_bytes(int V, int H) {
   if (V < 1 || H < 256 || H > 16384 || H % 256 != 0) return 0;
   return fp4_packed_weight_bytes(V, H);

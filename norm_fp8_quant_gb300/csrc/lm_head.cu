@@ -28,6 +28,7 @@
 // and merges it into a packed 64-bit key with atomicMax; the last CTA to
 // finish turns the keys into tokens and resets the workspace.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -448,7 +449,7 @@ struct SmallSmem {
 
 
 
-template <int MT, bool kPacked>
+template <int MT, bool kPacked, bool kLogits = false>
 __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     lm_head_small_kernel(const __grid_constant__ CUtensorMap tmap_w,
                          const __grid_constant__ CUtensorMap tmap_a, const Stage2Params p,
@@ -712,6 +713,47 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
       if (!ok) break;
       if (!active) continue;
 
+      if constexpr (kLogits) {
+        // unfused reference arm: the promoted logits go to memory as BF16,
+        // two adjacent columns per 4-byte store when the row allows it
+        const int row0 = blk0 * 128 + 64 * g;
+        uint16_t *dst = p.logits_out + (size_t)(tok < p.T ? tok : 0) * (size_t)p.V;
+        const bool pairs = (p.V & 1) == 0;
+        if constexpr (MT == 64) {
+          // this lane holds columns 2j + colpar, its partner (lane ^ 2) the others
+#pragma unroll
+          for (int j = 0; j < CPT; ++j) {
+            const float other = __shfl_xor_sync(0xffffffffu, acc[j], 2);
+            const int v0 = row0 + 2 * j;
+            if (tok < p.T && (j & 1) == colpar) {
+              const float lo = colpar ? other : acc[j], hi = colpar ? acc[j] : other;
+              if (pairs && v0 + 1 < p.V) {
+                *reinterpret_cast<uint32_t *>(dst + v0) =
+                    (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+              } else {
+                if (v0 < p.V) dst[v0] = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+                if (v0 + 1 < p.V) dst[v0 + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+              }
+            }
+          }
+        } else if (tok < p.T) {
+#pragma unroll
+          for (int j = 0; j < CPT; j += 2) {
+            const int v0 = row0 + j;
+            if (pairs && v0 + 1 < p.V) {
+              *reinterpret_cast<uint32_t *>(dst + v0) =
+                  (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[j])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[j + 1])) << 16);
+            } else {
+              if (v0 < p.V) dst[v0] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j]));
+              if (v0 + 1 < p.V) dst[v0 + 1] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j + 1]));
+            }
+          }
+        }
+        continue;
+      }
+
       // argmax over this thread's columns (ascending rows), then merge
       const int row0 = blk0 * 128 + 64 * g;          // first row of the group
       const int last_row = min(row0 + 63, p.V - 1);
@@ -771,7 +813,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMma) tmem_dealloc(tmem_base, 512);
-  finish_launch(p, &sh->last);
+  if constexpr (!kLogits) finish_launch(p, &sh->last);
 }
 
 // ------------------------------------------------------------------- host --
@@ -841,7 +883,7 @@ size_t stage2_workspace_bytes(int S) {
   return (size_t)S * kKeyStride * sizeof(unsigned long long) + 16u;
 }
 
-template <int MT, bool kPacked>
+template <int MT, bool kPacked, bool kLogits = false>
 cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const void *w,
                          int num_sms, cudaStream_t stream) {
   CUtensorMap tw, ta;
@@ -859,7 +901,7 @@ cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const voi
   if (nstage > 8) nstage = 8;
   if (nstage < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)nstage * kStage;
-  auto kern = lm_head_small_kernel<MT, kPacked>;
+  auto kern = lm_head_small_kernel<MT, kPacked, kLogits>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -881,6 +923,13 @@ cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const vo
 }
 
 void stage2_set_small(int enabled) { g_small_enabled = enabled != 0; }
+
+cudaError_t launch_lm_head_logits(const Stage2Params &p, int num_sms, cudaStream_t stream) {
+  if (!p.w_packed || !p.logits_out || p.T < 1 || p.T > kSmallMaxT)
+    return cudaErrorInvalidConfiguration;
+  return p.T <= 64 ? launch_small<64, true, true>(p, p.act_codes, p.w_packed, num_sms, stream)
+                   : launch_small<128, true, true>(p, p.act_codes, p.w_packed, num_sms, stream);
+}
 
 // Tokens per launch: batches above 128 tokens run as 128-token launches of the
 // token-major kernel (each streams the weight once; at 256 tokens two such

@@ -56,6 +56,7 @@ struct Stage2Params {
   int H, G, V, S;
   int shard_width;            // V / S
   int n_vtiles;               // ceil(V / 128)
+  uint16_t *logits_out;       // unfused arm: BF16 logits [T][V] instead of the argmax
   // NVFP4 form: act_codes are e2m1 pairs [T][H/2], G = H / 256 (K steps)
   const uint8_t *act_bscales; // e4m3 [T][H/16]
   const float *act_gscales;   // fp32 [T]
@@ -70,6 +71,24 @@ void stage2_set_small(int enabled);   // 0: always use the wide-batch kernel (te
 int stage2_token_chunk();             // tokens per LM-head launch
 size_t packed_weight_bytes(int V, int H);
 cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out, cudaStream_t stream);
+
+// Unfused reference arm: the FP8 LM head writing BF16 logits (packed weight,
+// T <= 128 per launch), and the separate kernels of the unfused path.
+cudaError_t launch_lm_head_logits(const Stage2Params &p, int num_sms, cudaStream_t stream);
+struct UnfusedReduceParams {
+  const void *partials[kMaxPartials];
+  int k;
+  size_t n_vec;                        // 16-byte vectors per tensor
+  void *out;
+};
+cudaError_t launch_unfused_reduce(const UnfusedReduceParams &p, int num_sms, cudaStream_t stream);
+cudaError_t launch_unfused_add_rmsnorm(const void *x, const void *residual, const void *norm_w,
+                                       float eps, int T, int H, void *hidden,
+                                       cudaStream_t stream);
+cudaError_t launch_unfused_quant(const void *hidden, int T, int H, uint8_t *codes,
+                                 float *scales, cudaStream_t stream);
+cudaError_t launch_unfused_argmax(const void *logits, int T, int V, int32_t *tokens,
+                                  cudaStream_t stream);
 
 // NVFP4 LM head (token-major, block-scaled tensor cores), T <= 128 per launch
 constexpr int kFp4MaxT = 128;
