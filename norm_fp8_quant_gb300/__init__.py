@@ -633,3 +633,15 @@ def unfused_argmax_bf16(logits, tokens_out=None, stream=None):
                     tok.data_ptr(), _raw_stream(dev.index, stream))
     _check(st, "nfq_unfused_argmax_bf16")
     return tok
+
+
+# ------------------------------------------------ sequence-parallel rows --
+
+def sp_row_range(T: int, rank: int, world: int):
+    """The contiguous token rows [r0, r1) that rank `rank` of `world`
+    sequence-parallel ranks owns: after the reduce-scatter of the partials a
+    rank holds the summed rows of its range and runs stage 1 on them alone
+    (rows are independent).  Ranges differ in size by at most one row."""
+    if world < 1 or not 0 <= rank < world or T < 0:
+        raise ValueError("need 0 <= rank < world and T >= 0")
+    return rank * T // world, (rank + 1) * T // world
