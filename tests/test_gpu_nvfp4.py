@@ -145,7 +145,8 @@ def test_nvfp4_lm_head_decode_c64_sampled_tokens(nfq):
 @pytest.mark.parametrize("T,H,V,S", [(1, 256, 128, 1), (2, 512, 200, 2), (31, 1024, 1000, 5),
                                      (33, 256, 4100, 4), (64, 768, 2048, 64),
                                      (100, 512, 3000, 3), (128, 256, 1536, 6),
-                                     (129, 256, 1024, 8), (250, 512, 640, 5)])
+                                     (129, 256, 1024, 8), (250, 512, 640, 5),
+                                     (7, 16384, 1000, 4)])
 def test_nvfp4_lm_head_edge_shapes(nfq, T, H, V, S):
     """Ragged vocab tails, one-block tiles, shards narrower than a warp's
     columns, every lane quadrant and the 128-token chunks."""

@@ -102,7 +102,8 @@ def test_stage2_tie_stress(nfq, layout):
                                      (17, 384, 4100, 4), (33, 256, 2048, 64),
                                      (64, 1024, 3000, 3), (100, 512, 1536, 6),
                                      (129, 256, 1024, 8), (256, 256, 640, 5),
-                                     (300, 256, 512, 2)])
+                                     (300, 256, 512, 2), (5, 16384, 1000, 4),
+                                     (200, 16384, 384, 3)])
 def test_stage2_edge_shapes(nfq, T, H, V, S, layout, family):
     """Ragged vocab tails, shard widths below a tile or a warp, every token
     count class (padding inside the MMA N, two warpgroups, 256-token chunks)."""
