@@ -359,16 +359,22 @@ def run_ours(args, rank, world, local):
     # overlapping the first one's tail): the reported rate.  With --mtp P a
     # step is P chained draft positions: position p's hidden is the residual
     # of position p+1 (nfq_mtp_draft_chain), each position with its own partials.
-    P = max(1, args.mtp) if has_lm and not (fp4 or unfused) else 1
+    P = max(1, args.mtp) if has_lm and not unfused else 1
     if P > 1:
         chain_hidden = [torch.empty_like(hidden) for _ in range(2)]
         chain_tokens = torch.empty((P, T), dtype=torch.int32, device=dev)
 
         def chain(i):
             parts = [sets[(i * P + p) % nsets][0] for p in range(P)]
-            nfq.mtp_draft_chain(parts, sets[(i * P) % nsets][1], norm_w, qw_d, sw_d, S, w.eps,
-                                hidden_bufs=chain_hidden, codes=codes, scales=scales,
-                                tokens_out=chain_tokens, workspace=ws)
+            if fp4:
+                nfq.mtp_draft_chain_nvfp4(parts, sets[(i * P) % nsets][1], norm_w, qw_d, S, w.eps,
+                                          hidden_bufs=chain_hidden, codes=codes,
+                                          block_scales=bscales, row_scales=gscales,
+                                          tokens_out=chain_tokens, workspace=ws)
+            else:
+                nfq.mtp_draft_chain(parts, sets[(i * P) % nsets][1], norm_w, qw_d, sw_d, S,
+                                    w.eps, hidden_bufs=chain_hidden, codes=codes, scales=scales,
+                                    tokens_out=chain_tokens, workspace=ws)
         for i in range(max(1, args.warmup // P)):
             chain(i)
     barrier()

@@ -318,6 +318,19 @@ int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w
                              size_t ws_bytes, void *stream);
 
 /*
+ * nfq_mtp_draft_chain_nvfp4 — nfq_mtp_draft_chain with the NVFP4 forms of both
+ * stages: q is the NVFP4 activation buffer reused by every position, w_packed
+ * the packed NVFP4 weight with its tensor scale w_scale.  Rules and errors as
+ * for nfq_mtp_draft_chain and the two NVFP4 calls.
+ */
+int nfq_mtp_draft_chain_nvfp4(int positions, const void *const *partials, int k,
+                              const void *residual0, const void *norm_w, float eps, int T, int H,
+                              void *const *hidden_out, const nfq_fp4_act *q,
+                              const void *w_packed, float w_scale, int V, int S,
+                              int32_t *tokens_out, void *workspace, size_t ws_bytes,
+                              void *stream);
+
+/*
  * The unfused reference arm: the same step as separate kernels, the way it runs
  * without the two fusions of [F] (intro, Accuracy): the trailing all-reduce as a
  * separate BF16 collective (here the BF16-rounded sum of the partials), then

@@ -117,6 +117,12 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_nvfp4_tune.restype = None
     lib.nfq_stage1_grid.argtypes = [ctypes.c_int]
     lib.nfq_stage1_grid.restype = None
+    lib.nfq_mtp_draft_chain_nvfp4.argtypes = [ctypes.c_int, _P, ctypes.c_int, _P, _P,
+                                              ctypes.c_float, ctypes.c_int, ctypes.c_int, _P,
+                                              ctypes.POINTER(Fp4Act), _P, ctypes.c_float,
+                                              ctypes.c_int, ctypes.c_int, _P, _P,
+                                              ctypes.c_size_t, _P]
+    lib.nfq_mtp_draft_chain_nvfp4.restype = ctypes.c_int
     lib.nfq_unfused_allreduce_bf16.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P]
     lib.nfq_unfused_add_rmsnorm.argtypes = [_P, _P, _P, ctypes.c_float, ctypes.c_int,
                                             ctypes.c_int, _P, _P]
@@ -645,3 +651,40 @@ def sp_row_range(T: int, rank: int, world: int):
     if world < 1 or not 0 <= rank < world or T < 0:
         raise ValueError("need 0 <= rank < world and T >= 0")
     return rank * T // world, (rank + 1) * T // world
+
+
+def mtp_draft_chain_nvfp4(partials, residual0, norm_w, w: PackedFp4Weight, S: int,
+                          eps: float = 1e-6, hidden_bufs=None, codes=None, block_scales=None,
+                          row_scales=None, tokens_out=None, workspace=None, stream=None):
+    """mtp_draft_chain with the NVFP4 forms of both stages.  Returns (tokens
+    int32 [P][T], hidden of every position)."""
+    import torch
+    P = len(partials)
+    k = len(partials[0])
+    T, H = residual0.shape
+    for ps in partials:
+        if len(ps) != k:
+            raise ValueError("every position needs k partials")
+        _need_cuda(*ps)
+    _need_cuda(residual0, norm_w)
+    if not isinstance(w, PackedFp4Weight):
+        raise ValueError("w must be a PackedFp4Weight")
+    dev = residual0.device
+    if hidden_bufs is None:
+        hidden_bufs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(min(P, 2))]
+    hidden_of = [hidden_bufs[p % len(hidden_bufs)] for p in range(P)]
+    codes = codes if codes is not None else torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+    bs = (block_scales if block_scales is not None
+          else torch.empty((T, H // FP4_BLOCK), dtype=torch.uint8, device=dev))
+    gs = row_scales if row_scales is not None else torch.empty(T, dtype=torch.float32, device=dev)
+    tokens = tokens_out if tokens_out is not None else torch.empty((P, T), dtype=torch.int32, device=dev)
+    ws = workspace if workspace is not None else lm_head_workspace(T, S, dev, stream)
+    parr = (ctypes.c_void_p * (P * k))(*[t.data_ptr() for ps in partials for t in ps])
+    harr = (ctypes.c_void_p * P)(*[h.data_ptr() for h in hidden_of])
+    q = Fp4Act(codes.data_ptr(), bs.data_ptr(), gs.data_ptr(), T, H, FP4_BLOCK)
+    st = _on_device(dev.index, load().nfq_mtp_draft_chain_nvfp4, P, parr, k, residual0.data_ptr(),
+                    norm_w.data_ptr(), float(eps), T, H, harr, ctypes.byref(q), w.data.data_ptr(),
+                    float(w.scale), w.V, S, tokens.data_ptr(), ws.data_ptr(), ws.numel(),
+                    _raw_stream(dev.index, stream))
+    _check(st, "nfq_mtp_draft_chain_nvfp4")
+    return tokens, hidden_of

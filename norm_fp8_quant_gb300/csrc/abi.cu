@@ -496,6 +496,32 @@ int nfq_mtp_draft_chain(int positions, const void *const *partials, int k,
   return NFQ_OK;
 }
 
+int nfq_mtp_draft_chain_nvfp4(int positions, const void *const *partials, int k,
+                              const void *residual0, const void *norm_w, float eps, int T, int H,
+                              void *const *hidden_out, const nfq_fp4_act *q,
+                              const void *w_packed, float w_scale, int V, int S,
+                              int32_t *tokens_out, void *workspace, size_t ws_bytes,
+                              void *stream) {
+  if (positions < 1 || positions > 64) return NFQ_ERR_SHAPE;
+  if (!partials || !hidden_out || !q || !tokens_out) return NFQ_ERR_NULL;
+  if (k < 1 || k > kMaxPartials) return NFQ_ERR_SHAPE;
+  for (int p = 0; p < positions; ++p) {
+    if (!hidden_out[p]) return NFQ_ERR_NULL;
+    if (p > 0 && hidden_out[p] == hidden_out[p - 1]) return NFQ_ERR_SHAPE;
+    if (hidden_out[p] == residual0) return NFQ_ERR_SHAPE;
+  }
+  for (int p = 0; p < positions; ++p) {
+    const void *residual = p == 0 ? residual0 : hidden_out[p - 1];
+    int st = nfq_mtp_reduce_norm_quant_nvfp4(partials + (size_t)p * k, k, residual, norm_w, eps,
+                                             T, H, hidden_out[p], q, stream);
+    if (st != NFQ_OK) return st;
+    st = nfq_lm_head_nvfp4_argmax(q, w_packed, w_scale, V, S, tokens_out + (size_t)p * (size_t)T,
+                                  nullptr, nullptr, nullptr, workspace, ws_bytes, stream);
+    if (st != NFQ_OK) return st;
+  }
+  return NFQ_OK;
+}
+
 int nfq_device_error(int clear) {
   unsigned v = 0;
   if (cudaDeviceSynchronize() != cudaSuccess) return NFQ_ERR_CUDA;

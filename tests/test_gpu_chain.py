@@ -84,3 +84,32 @@ def test_chain_with_two_alternating_hidden_buffers(nfq):
     torch.cuda.synchronize()
     assert torch.equal(t2, t4)
     assert torch.equal(h2[3].view(torch.int16), h4[3].view(torch.int16))
+
+
+@pytest.mark.parametrize("name,P", [("tiny", 3), ("decode_c64", 5)])
+def test_nvfp4_chain_matches_oracle(nfq, name, P):
+    """The NVFP4 chain: every link against the oracle fed the GPU's previous
+    hidden (hidden within 1 ulp; the oracle's NVFP4 quantiser on the GPU's
+    hidden is the activation the LM head saw, whose tokens the oracle checks)."""
+    from tests._parity import check_stage2_fp4
+    w = synth.workload(name)
+    base = synth.stage1_inputs(w)
+    pos = [synth.stage1_inputs(synth.workload(name, seed=p + 1))["partials"] for p in range(P)]
+    qw, sw, gw = synth.lm_head_weights_nvfp4(w)
+    wp = nfq.pack_lm_head_weights_nvfp4(to_dev(qw), to_dev(sw), gw)
+    hidden = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    toks, _ = nfq.mtp_draft_chain_nvfp4([[to_dev_bf16(x) for x in part] for part in pos],
+                                        to_dev_bf16(base["residual"]), to_dev_bf16(base["norm_w"]),
+                                        wp, w.S, w.eps, hidden_bufs=hidden)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    toks = toks.cpu().numpy()
+    gh = [bf16_host(h) for h in hidden]
+    sample = list(range(w.T)) if w.T <= 8 else [0, 30, 63]
+    for p in range(P):
+        res = base["residual"] if p == 0 else gh[p - 1]
+        ref = oracle.reduce_norm_quant(pos[p], res, base["norm_w"], w.eps)
+        _hidden_within_one_ulp(gh[p], ref["hidden"])
+        act = oracle.nvfp4_quant(gh[p])
+        check_stage2_fp4(toks[p], act["codes"], act["block_scales"], act["global_scales"], qw, sw,
+                         gw, w.S, sample)
