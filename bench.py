@@ -459,6 +459,16 @@ def run_ours(args, rank, world, local):
     result_dev = tokens if has_lm else (gscales if fp4 else scales)
     result_host = [torch.empty(result_dev.shape, dtype=result_dev.dtype).pin_memory()
                    for _ in range(NB)]
+    # the LM head writes each step's tokens straight into that step's pinned
+    # host slot (the device addresses pinned memory directly), so no copy node
+    # sits between the kernels of consecutive steps
+    direct = has_lm and not unfused
+    if direct:
+        stage2_direct = [
+            (nfq.prepare_lm_head_nvfp4_argmax(codes, bscales, gscales, qw_d, S, ws, result_host[b])
+             if fp4 else nfq.prepare_lm_head_fp8_argmax(codes, scales, qw_d, sw_d, S, ws,
+                                                        result_host[b]))
+            for b in range(NB)]
     done = [torch.cuda.Event() for _ in range(NB)]
     h2d = h_in.numel() * h_in.element_size()
     d2h = result_dev.numel() * result_dev.element_size()
@@ -477,9 +487,12 @@ def run_ours(args, rank, world, local):
         b = i % NB
         stream.wait_event(copied[b])
         stage1(*buf_views[b])
-        if has_lm:
-            stage2()
-        result_host[b].copy_(result_dev, non_blocking=True)
+        if direct:
+            stage2_direct[b]()
+        else:
+            if has_lm:
+                stage2()
+            result_host[b].copy_(result_dev, non_blocking=True)
         done[b].record(stream)
 
     def e2e_read(i):

@@ -127,7 +127,10 @@ int nfq_mtp_reduce_norm_quant(const void *const *partials, int k, const void *re
  *   L[t][v] = sum_k decode(a.codes[t][k]) * a.scales[t][k/128]
  *                 * decode(w[v][k]) * w_scales[v/128][k/128]     (fp32 accumulate)
  * The V vocab rows form S equal shards [s*V/S, (s+1)*V/S).  Outputs:
- *   tokens_out    int32 [T]    argmax_v L[t][v], lowest index among equal maxima
+ *   tokens_out    int32 [T]    argmax_v L[t][v], lowest index among equal maxima; may
+ *                              also be pinned host memory that the device addresses
+ *                              directly (unified addressing): the tokens are then
+ *                              written straight to the host by the kernel's last CTA
  *   max_logit_out fp32 [T]     L at that index, or NULL
  *   shard_idx_out int32 [S][T] per-shard argmax (global index), or NULL
  *   shard_val_out fp32 [S][T]  per-shard maximum, or NULL

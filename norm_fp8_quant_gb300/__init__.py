@@ -183,6 +183,17 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def _need_tokens_out(t):
+    """Token outputs may be device memory or pinned host memory, which the
+    device addresses directly under unified addressing (the LM head then writes
+    the tokens straight to the host)."""
+    import torch
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError("tokens_out must be a contiguous int32 tensor")
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("tokens_out must be device memory or pinned host memory")
+
+
 # ----------------------------------------------------------------- stage 1 --
 
 def mtp_reduce_norm_quant(partials, residual, norm_w, eps: float = 1e-6,
@@ -531,7 +542,8 @@ def prepare_lm_head_fp8_argmax(codes, scales, w, w_scales, S: int, workspace,
     """lm_head_fp8_argmax (tokens only) with fixed buffers, as a PreparedCall."""
     import torch
     T, H = codes.shape
-    _need_cuda(codes, scales, w, w_scales, workspace, tokens_out)
+    _need_cuda(codes, scales, w, w_scales, workspace)
+    _need_tokens_out(tokens_out)
     if codes.dtype != torch.uint8 or w.dtype != torch.uint8 or scales.dtype != torch.float32 \
             or w_scales.dtype != torch.float32:
         raise ValueError("uint8 codes / weight and float32 scales expected")
@@ -549,7 +561,8 @@ def prepare_lm_head_nvfp4_argmax(codes, block_scales, row_scales, w: PackedFp4We
     """lm_head_nvfp4_argmax (tokens only) with fixed buffers, as a PreparedCall."""
     import torch
     T, H2 = codes.shape
-    _need_cuda(codes, block_scales, row_scales, workspace, tokens_out)
+    _need_cuda(codes, block_scales, row_scales, workspace)
+    _need_tokens_out(tokens_out)
     if not isinstance(w, PackedFp4Weight):
         raise ValueError("w must be a PackedFp4Weight")
     if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or \

@@ -70,3 +70,28 @@ def test_prepared_nvfp4_matches_plain_calls(nfq):
                  (t0, t1)):
         assert torch.equal(a, b)
     assert np.all(t1.cpu().numpy() < w.V)
+
+
+def test_tokens_written_straight_to_pinned_host_memory(nfq):
+    """tokens_out in pinned host memory (addressed by the device directly):
+    the same tokens as a device buffer, for both LM heads."""
+    w = synth.workload("tiny", T=33, H=1024, V=8192, S=4, seed=6)
+    parts, res, nw = _inputs(w)
+    h, c, s = nfq.mtp_reduce_norm_quant(parts, res, nw, w.eps)
+    qw, sw = synth.lm_head_weights(w)
+    wp, swd = nfq.pack_lm_head_weights(to_dev(qw)), to_dev(sw)
+    ws = nfq.lm_head_workspace(w.T, w.S, "cuda")
+    dev_tok = nfq.lm_head_fp8_argmax(c, s, wp, swd, w.S, workspace=ws)
+    host_tok = torch.full((w.T,), -1, dtype=torch.int32).pin_memory()
+    nfq.prepare_lm_head_fp8_argmax(c, s, wp, swd, w.S, ws, host_tok)()
+    torch.cuda.synchronize()
+    assert torch.equal(host_tok, dev_tok.cpu())
+    h4, c4, b4, g4 = nfq.mtp_reduce_norm_quant_nvfp4(parts, res, nw, w.eps)
+    q4, s4, gw = synth.lm_head_weights_nvfp4(w)
+    wp4 = nfq.pack_lm_head_weights_nvfp4(to_dev(q4), to_dev(s4), gw)
+    dev4 = nfq.lm_head_nvfp4_argmax(c4, b4, g4, wp4, w.S, workspace=ws)
+    host4 = torch.full((w.T,), -1, dtype=torch.int32).pin_memory()
+    nfq.prepare_lm_head_nvfp4_argmax(c4, b4, g4, wp4, w.S, ws, host4)()
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    assert torch.equal(host4, dev4.cpu())
