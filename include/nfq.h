@@ -321,6 +321,25 @@ int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w
                              size_t ws_bytes, void *stream);
 
 /*
+ * nfq_mtp_step_fp8 — one whole draft step: nfq_mtp_reduce_norm_quant followed by
+ * nfq_lm_head_fp8_argmax_packed, with the same arguments, rules, outputs (the
+ * hidden, the packed activation in q, the tokens and the optional maxima) and
+ * the same results bit for bit.  Where it applies (1 <= T <= 64, H % 512 == 0,
+ * H <= 8192, at least T CTAs in the LM head's grid) it is ONE launch: the
+ * LM-head kernel's epilogue warps compute stage 1 for one token row per CTA
+ * while its producer already streams the first weight stages, and the MMAs
+ * start once every row is published through a counter in the workspace (the
+ * counter returns to zero with the rest of the workspace).  Otherwise it is
+ * the two launches.  Requires the packed weight (nfq_lm_head_pack_weights).
+ */
+int nfq_mtp_step_fp8(const void *const *partials, int k, const void *residual,
+                     const void *norm_w, float eps, int T, int H, void *hidden_out,
+                     const nfq_quant_act *q, const uint8_t *w_packed, const float *w_scales,
+                     int V, int S, int32_t *tokens_out, float *max_logit_out,
+                     int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                     size_t ws_bytes, void *stream);
+
+/*
  * nfq_mtp_draft_chain_nvfp4 — nfq_mtp_draft_chain with the NVFP4 forms of both
  * stages: q is the NVFP4 activation buffer reused by every position, w_packed
  * the packed NVFP4 weight with its tensor scale w_scale.  Rules and errors as

@@ -123,6 +123,11 @@ def load(path: str = LIB_PATH):
                                               ctypes.c_int, ctypes.c_int, _P, _P,
                                               ctypes.c_size_t, _P]
     lib.nfq_mtp_draft_chain_nvfp4.restype = ctypes.c_int
+    lib.nfq_mtp_step_fp8.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float, ctypes.c_int,
+                                     ctypes.c_int, _P, ctypes.POINTER(QuantAct), _P, _P,
+                                     ctypes.c_int, ctypes.c_int, _P, _P, _P, _P, _P,
+                                     ctypes.c_size_t, _P]
+    lib.nfq_mtp_step_fp8.restype = ctypes.c_int
     lib.nfq_unfused_allreduce_bf16.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P]
     lib.nfq_unfused_add_rmsnorm.argtypes = [_P, _P, _P, ctypes.c_float, ctypes.c_int,
                                             ctypes.c_int, _P, _P]
@@ -701,3 +706,62 @@ def mtp_draft_chain_nvfp4(partials, residual0, norm_w, w: PackedFp4Weight, S: in
                     _raw_stream(dev.index, stream))
     _check(st, "nfq_mtp_draft_chain_nvfp4")
     return tokens, hidden_of
+
+
+# ------------------------------------------------------------- fused step --
+
+def _step_args(partials, residual, norm_w, eps, hidden, codes, scales, w, w_scales, S, ws,
+               tokens, mx, sidx, sval):
+    T, H = residual.shape
+    arr = (ctypes.c_void_p * len(partials))(*[p.data_ptr() for p in partials])
+    q = QuantAct(codes.data_ptr(), scales.data_ptr(), T, H, GROUP)
+    opt = lambda t: None if t is None else t.data_ptr()
+    args = (arr, len(partials), residual.data_ptr(), norm_w.data_ptr(), float(eps), T, H,
+            hidden.data_ptr(), ctypes.byref(q), w.data_ptr(), w_scales.data_ptr(), w.V, S,
+            tokens.data_ptr(), opt(mx), opt(sidx), opt(sval), ws.data_ptr(), ws.numel())
+    return args, (arr, q)
+
+
+def mtp_step_fp8(partials, residual, norm_w, w: PackedWeight, w_scales, S: int,
+                 eps: float = 1e-6, hidden_out=None, codes_out=None, scales_out=None,
+                 tokens_out=None, workspace=None, want_max: bool = False,
+                 want_shards: bool = False, stream=None):
+    """One whole draft step (stage 1 + the FP8 LM head, one launch where it
+    applies).  Returns (hidden, codes, scales, tokens) or, with want_max /
+    want_shards, (hidden, codes, scales, tokens, max_logit, shard_idx, shard_val)."""
+    import torch
+    T, H = _check_stage1_args(partials, residual, norm_w)
+    if not isinstance(w, PackedWeight):
+        raise ValueError("w must be a PackedWeight")
+    _need_cuda(w_scales)
+    dev = residual.device
+    hidden = hidden_out if hidden_out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    codes = codes_out if codes_out is not None else torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scales = scales_out if scales_out is not None else torch.empty((T, H // GROUP), dtype=torch.float32, device=dev)
+    tokens = tokens_out if tokens_out is not None else torch.empty(T, dtype=torch.int32, device=dev)
+    ws = workspace if workspace is not None else lm_head_workspace(T, S, dev, stream)
+    mx = torch.empty(T, dtype=torch.float32, device=dev) if want_max else None
+    sidx = torch.empty((S, T), dtype=torch.int32, device=dev) if want_shards else None
+    sval = torch.empty((S, T), dtype=torch.float32, device=dev) if want_shards else None
+    args, keep = _step_args(partials, residual, norm_w, eps, hidden, codes, scales, w, w_scales,
+                            S, ws, tokens, mx, sidx, sval)
+    st = _on_device(dev.index, load().nfq_mtp_step_fp8, *args, _raw_stream(dev.index, stream))
+    _check(st, "nfq_mtp_step_fp8")
+    if want_max or want_shards:
+        return hidden, codes, scales, tokens, mx, sidx, sval
+    return hidden, codes, scales, tokens
+
+
+def prepare_mtp_step_fp8(partials, residual, norm_w, eps, hidden_out, codes_out, scales_out,
+                         w: PackedWeight, w_scales, S: int, workspace, tokens_out) -> PreparedCall:
+    """mtp_step_fp8 (tokens only) with fixed buffers, as a PreparedCall."""
+    T, H = _check_stage1_args(partials, residual, norm_w)
+    _need_cuda(hidden_out, codes_out, scales_out, w_scales, workspace)
+    _need_tokens_out(tokens_out)
+    if not isinstance(w, PackedWeight):
+        raise ValueError("w must be a PackedWeight")
+    args, keep = _step_args(partials, residual, norm_w, eps, hidden_out, codes_out, scales_out,
+                            w, w_scales, S, workspace, tokens_out, None, None, None)
+    return PreparedCall(load().nfq_mtp_step_fp8, args, residual.device.index, "nfq_mtp_step_fp8",
+                        (partials, residual, norm_w, hidden_out, codes_out, scales_out, w,
+                         w_scales, workspace, tokens_out, keep))

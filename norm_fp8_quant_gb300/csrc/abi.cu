@@ -496,6 +496,83 @@ int nfq_mtp_draft_chain(int positions, const void *const *partials, int k,
   return NFQ_OK;
 }
 
+int nfq_mtp_step_fp8(const void *const *partials, int k, const void *residual,
+                     const void *norm_w, float eps, int T, int H, void *hidden_out,
+                     const nfq_quant_act *q, const uint8_t *w_packed, const float *w_scales,
+                     int V, int S, int32_t *tokens_out, float *max_logit_out,
+                     int32_t *shard_idx_out, float *shard_val_out, void *workspace,
+                     size_t ws_bytes, void *stream) {
+  if (!partials || !residual || !norm_w || !hidden_out || !q || !w_packed || !w_scales ||
+      !tokens_out || !q->codes || !q->scales)
+    return NFQ_ERR_NULL;
+  if (k < 1 || k > kMaxPartials) return NFQ_ERR_SHAPE;
+  for (int i = 0; i < k; ++i) {
+    if (!partials[i]) return NFQ_ERR_NULL;
+    if (!aligned16(partials[i])) return NFQ_ERR_ALIGN;
+  }
+  if (T < 0 || H < 128 || H > 16384 || H % 128 != 0) return NFQ_ERR_SHAPE;
+  if (!(eps >= 0.0f) || eps > 1.0f) return NFQ_ERR_SHAPE;
+  if (q->group != 128 || q->tokens != T || q->hidden != H) return NFQ_ERR_SHAPE;
+  if (V < 1 || S < 1 || S > 64 || V % S != 0) return NFQ_ERR_SHAPE;
+  if (!workspace || ws_bytes < stage2_workspace_bytes(S)) return NFQ_ERR_WORKSPACE;
+  if (!aligned16(residual) || !aligned16(norm_w) || !aligned16(hidden_out) ||
+      !aligned16(q->codes) || !aligned16(q->scales) || !aligned16(w_packed) ||
+      !aligned16(w_scales) || !aligned16(workspace) || !aligned4(tokens_out) ||
+      (max_logit_out && !aligned4(max_logit_out)) ||
+      (shard_idx_out && !aligned4(shard_idx_out)) ||
+      (shard_val_out && !aligned4(shard_val_out)))
+    return NFQ_ERR_ALIGN;
+  if (T == 0) return NFQ_OK;
+  DeviceInfo *d = nullptr;
+  int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  if (!fused_step_supported(T, H, k, V, d->num_sms)) {
+    // the same results as two launches
+    st = nfq_mtp_reduce_norm_quant(partials, k, residual, norm_w, eps, T, H, hidden_out, q,
+                                   stream);
+    if (st != NFQ_OK) return st;
+    return nfq_lm_head_fp8_argmax_packed(q, w_packed, w_scales, V, S, tokens_out,
+                                         max_logit_out, shard_idx_out, shard_val_out,
+                                         workspace, ws_bytes, stream);
+  }
+  Stage2Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.act_codes = q->codes;
+  p.act_scales = q->scales;
+  p.w_scales = w_scales;
+  p.w_packed = w_packed;
+  p.tokens_out = tokens_out;
+  p.max_logit_out = max_logit_out;
+  p.shard_idx_out = shard_idx_out;
+  p.shard_val_out = shard_val_out;
+  p.keys = static_cast<unsigned long long *>(workspace);
+  p.counter = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(workspace) +
+                                           stage2_workspace_bytes(S) - 16u);
+  p.err = d->err;
+  p.T = T;
+  p.T_total = T;
+  p.tok0 = 0;
+  p.H = H;
+  p.G = H / 128;
+  p.V = V;
+  p.S = S;
+  p.shard_width = V / S;
+  p.n_vtiles = (V + 127) / 128;
+  for (int i = 0; i < k; ++i) p.s1.partials[i] = partials[i];
+  p.s1.residual = residual;
+  p.s1.norm_w = norm_w;
+  p.s1.hidden = hidden_out;
+  p.s1.codes = q->codes;
+  p.s1.scales = q->scales;
+  p.s1.ready = p.counter + 1;
+  p.s1.eps = eps;
+  p.s1.k = k;
+  p.s1.na = H / 16;
+  const cudaError_t e = launch_fused_step(p, d->num_sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
+  return map_cuda(e);
+}
+
 int nfq_mtp_draft_chain_nvfp4(int positions, const void *const *partials, int k,
                               const void *residual0, const void *norm_w, float eps, int T, int H,
                               void *const *hidden_out, const nfq_fp4_act *q,

@@ -37,6 +37,7 @@
 #include "lm_head_common.cuh"
 #include "nfq_internal.h"
 #include "ptx.cuh"
+#include "stage1_math.cuh"
 
 namespace nfq {
 
@@ -449,7 +450,105 @@ struct SmallSmem {
 
 
 
-template <int MT, bool kPacked, bool kLogits = false>
+// The fused step's stage 1, run by the 16 epilogue warps (512 threads) of a
+// CTA.  CTA r < T computes token row r exactly as the stand-alone stage-1
+// kernel does (same per-thread vectors, same order of every fp32 operation),
+// reading its inputs straight from global memory, and publishes the row with
+// a release increment of s1.ready.  Every CTA then waits (bounded) until all T
+// rows are published.  Returns false when the wait gave up.
+__device__ bool fused_stage1(const Stage2Params &p, float *red, int *flag,
+                             volatile int *abort_flag) {
+  const FusedStage1 &s = p.s1;
+  const int tc = (int)threadIdx.x;
+  const int lane = tc & 31, warp = tc >> 5;
+  const int r = (int)blockIdx.x;
+  if (r < p.T) {                                          // CTA-uniform
+    const int NA = s.na;
+    const bool active = tc < NA;
+    const size_t rowv = (size_t)r * (size_t)(p.H / 8);     // first 16-byte vector of the row
+    float x[2][8];
+    // inputs p_0 .. p_{k-1}, then the residual, in batches of up to 9 loads a vector
+    for (int i0 = 0; i0 <= s.k; i0 += 9) {
+      uint4 in[9][2];
+#pragma unroll
+      for (int c = 0; c < 9; ++c) {
+        const int i = i0 + c;
+        if (active && i <= s.k) {
+          const uint4 *src = static_cast<const uint4 *>(i < s.k ? s.partials[i] : s.residual) + rowv;
+          in[c][0] = __ldg(src + tc);
+          in[c][1] = __ldg(src + NA + tc);
+        } else {
+          in[c][0] = in[c][1] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 9; ++c) {
+        const int i = i0 + c;
+        if (i > s.k) break;
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+          if (i == 0) unpack_bf16x8(in[c][v], x[v]);
+          else add_bf16x8(x[v], in[c][v]);
+        }
+      }
+    }
+    // sum of squares: thread, warp, then the warps holding data in order
+    float ss = 0.0f;
+#pragma unroll
+    for (int v = 0; v < 2; ++v)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[v][e], x[v][e], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    named_bar_sync(1, kSmallEpiWarps * 32);
+    float tot = 0.0f;
+    for (int q = 0; q < NA / 32; ++q) tot += red[q];
+    const float ms = __fdiv_rn(tot, (float)p.H);
+    const float rr = __frsqrt_rn(__fadd_rn(ms, s.eps));
+    const uint4 *wsrc = static_cast<const uint4 *>(s.norm_w);
+    uint4 *hid = static_cast<uint4 *>(s.hidden) + rowv;
+    uint2 *cod = reinterpret_cast<uint2 *>(s.codes) + rowv;
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+      const int j = v * NA + tc;
+      const uint4 wpk = active ? __ldg(wsrc + j) : make_uint4(0u, 0u, 0u, 0u);
+      uint4 hv;
+      uint2 cv;
+      float scale;
+      fp8_vector_epilogue(x[v], wpk, rr, hv, cv, scale);     // all lanes (group shuffles)
+      if (active) {
+        hid[j] = hv;
+        cod[j] = cv;
+        if ((tc & 15) == 0) s.scales[(size_t)r * (size_t)(p.H / 128) + (size_t)(j / 16)] = scale;
+      }
+    }
+    __threadfence();
+    named_bar_sync(1, kSmallEpiWarps * 32);
+    if (tc == 0) red_release_gpu_add(s.ready, 1u);
+  }
+  // every row of the batch is published before any CTA reads the activation
+  if (tc == 0) {
+    int ok = 1;
+    if (ld_acquire_gpu(s.ready) < (unsigned)p.T) {
+      const unsigned long long t0 = globaltimer();
+      while (ld_acquire_gpu(s.ready) < (unsigned)p.T) {
+        if (*abort_flag || globaltimer() - t0 > kWaitLimitNs) {
+          atomicOr(p.err, (unsigned)kErrBitStage2);
+          *abort_flag = 1;
+          ok = 0;
+          break;
+        }
+      }
+    }
+    fence_proxy_async_global();
+    *flag = ok;
+  }
+  named_bar_sync(1, kSmallEpiWarps * 32);
+  return *flag != 0;
+}
+
+template <int MT, bool kPacked, bool kLogits = false, bool kFused = false>
 __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     lm_head_small_kernel(const __grid_constant__ CUtensorMap tmap_w,
                          const __grid_constant__ CUtensorMap tmap_a, const Stage2Params p,
@@ -524,9 +623,21 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   // everything below reads memory the previous kernel on the stream may write
   grid_dependency_wait();
   grid_launch_dependents();
-  for (int i = (int)threadIdx.x; i < G * MT; i += (int)blockDim.x) {
-    const int kb = i / MT, n = i % MT;
-    sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
+  if constexpr (kFused) {
+    // stage 1 of the step, then the activation scales, by the epilogue warps
+    __shared__ float s1_red[kSmallEpiWarps];
+    __shared__ int s1_flag;
+    if (warp < kSmallEpiWarps && fused_stage1(p, s1_red, &s1_flag, abort_flag)) {
+      for (int i = (int)threadIdx.x; i < G * MT; i += kSmallEpiWarps * 32) {
+        const int kb = i / MT, n = i % MT;
+        sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
+      }
+    }
+  } else {
+    for (int i = (int)threadIdx.x; i < G * MT; i += (int)blockDim.x) {
+      const int kb = i / MT, n = i % MT;
+      sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -537,8 +648,10 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     // -------------------------------------------------------------- producer --
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
+    // the fused step's activation was written by other CTAs' generic stores
+    if constexpr (kFused) fence_proxy_async_global();
     uint32_t it = 0;
-    bool ok = true;
+    bool ok = !(kFused && *abort_flag);
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
       int blk0, nb;
       small_tile(b_begin, b_end, ti, blk0, nb);
@@ -883,7 +996,7 @@ size_t stage2_workspace_bytes(int S) {
   return (size_t)S * kKeyStride * sizeof(unsigned long long) + 16u;
 }
 
-template <int MT, bool kPacked, bool kLogits = false>
+template <int MT, bool kPacked, bool kLogits = false, bool kFused = false>
 cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const void *w,
                          int num_sms, cudaStream_t stream) {
   CUtensorMap tw, ta;
@@ -901,7 +1014,7 @@ cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const voi
   if (nstage > 8) nstage = 8;
   if (nstage < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)nstage * kStage;
-  auto kern = lm_head_small_kernel<MT, kPacked, kLogits>;
+  auto kern = lm_head_small_kernel<MT, kPacked, kLogits, kFused>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -923,6 +1036,22 @@ cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const vo
 }
 
 void stage2_set_small(int enabled) { g_small_enabled = enabled != 0; }
+
+// The fused step: batches of at most 64 tokens (one CTA per row among the
+// grid), rows whose H/16 data-holding threads are whole warps within the 512
+// epilogue threads, at most 16 inputs, packed weight.
+bool fused_step_supported(int T, int H, int k, int V, int num_sms) {
+  const int n_vtiles = (V + 127) / 128;
+  const int grid = num_sms < n_vtiles ? num_sms : n_vtiles;
+  return T >= 1 && T <= 64 && T <= grid && H % 512 == 0 && H / 16 <= kSmallEpiWarps * 32 &&
+         k >= 1 && k <= kMaxPartials;
+}
+
+cudaError_t launch_fused_step(const Stage2Params &p, int num_sms, cudaStream_t stream) {
+  if (!p.w_packed || !p.s1.ready || !fused_step_supported(p.T, p.H, p.s1.k, p.V, num_sms))
+    return cudaErrorInvalidConfiguration;
+  return launch_small<64, true, false, true>(p, p.act_codes, p.w_packed, num_sms, stream);
+}
 
 cudaError_t launch_lm_head_logits(const Stage2Params &p, int num_sms, cudaStream_t stream) {
   if (!p.w_packed || !p.logits_out || p.T < 1 || p.T > kSmallMaxT)

@@ -58,7 +58,10 @@ __device__ __forceinline__ void finish_launch(const Stage2Params &p, int *last_f
       p.tokens_out[n] = key_index(best);
       if (p.max_logit_out) p.max_logit_out[n] = key_value(best);
     }
-    if (threadIdx.x == 0) *p.counter = 0u;
+    if (threadIdx.x == 0) {
+      *p.counter = 0u;
+      if (p.s1.ready) *p.s1.ready = 0u;     // the fused step's row counter
+    }
   }
 }
 

@@ -74,7 +74,6 @@ struct Fp4Layout {
   static constexpr uint32_t kW = kABytes;
   static constexpr uint32_t kSfb = kW + kF4WBytes;
   static constexpr uint32_t kSfa = kSfb + kF4SfbBytes;
-  static constexpr uint32_t kSfaBytes = MT * 16;
   static constexpr uint32_t kStage = kSfa + MT * 16 + (MT == 64 ? 1024 - 64 * 16 : 0);
   static_assert(kStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 };

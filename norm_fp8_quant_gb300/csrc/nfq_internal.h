@@ -37,6 +37,21 @@ void stage1_set_grid(int max_ctas);   // 0: one CTA (cluster) per SM at most
 int stage1_plan(int T, int H, int k, int num_sms, int *out7);
 bool stage1_fp4_supported(int H);
 
+// Stage 1 folded into the LM-head launch (the fused step): the epilogue warps
+// of CTA r < T compute row r and publish it through `ready`.
+struct FusedStage1 {
+  const void *partials[kMaxPartials];  // k BF16 [T][H]
+  const void *residual;                // BF16 [T][H]
+  const void *norm_w;                  // BF16 [H]
+  void *hidden;                        // BF16 [T][H]
+  uint8_t *codes;                      // the activation the LM head reads (act_codes)
+  float *scales;                       // (act_scales)
+  unsigned *ready;                     // workspace word: rows published (reset by the last CTA)
+  float eps;
+  int k;
+  int na;                              // threads holding data: H / 16 (two vectors each)
+};
+
 // Stage 2 launch parameters.
 struct Stage2Params {
   const uint8_t *act_codes;   // e4m3 [T][H]   (this launch's token chunk)
@@ -57,6 +72,7 @@ struct Stage2Params {
   int shard_width;            // V / S
   int n_vtiles;               // ceil(V / 128)
   uint16_t *logits_out;       // unfused arm: BF16 logits [T][V] instead of the argmax
+  FusedStage1 s1;             // the fused step (s1.ready != null)
   // NVFP4 form: act_codes are e2m1 pairs [T][H/2], G = H / 256 (K steps)
   const uint8_t *act_bscales; // e4m3 [T][H/16]
   const float *act_gscales;   // fp32 [T]
@@ -75,6 +91,9 @@ cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out, cu
 // Unfused reference arm: the FP8 LM head writing BF16 logits (packed weight,
 // T <= 128 per launch), and the separate kernels of the unfused path.
 cudaError_t launch_lm_head_logits(const Stage2Params &p, int num_sms, cudaStream_t stream);
+// The fused FP8 step (stage 1 inside the token-major LM head), when it applies.
+bool fused_step_supported(int T, int H, int k, int V, int num_sms);
+cudaError_t launch_fused_step(const Stage2Params &p, int num_sms, cudaStream_t stream);
 struct UnfusedReduceParams {
   const void *partials[kMaxPartials];
   int k;

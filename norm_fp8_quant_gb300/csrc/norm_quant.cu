@@ -32,6 +32,7 @@
 
 #include "nfq_internal.h"
 #include "ptx.cuh"
+#include "stage1_math.cuh"
 
 namespace nfq {
 
@@ -49,54 +50,6 @@ struct RowSums {
   float cl[2][8];       // per cluster rank, double-buffered by row parity
   float amx[2][32];     // per consumer warp: row maximum |hidden| (NVFP4 form)
 };
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// x[e] += bf16 value e of the 16-byte vector, as correctly rounded fp32 adds
-// (two lanes per add.rn.f32x2).
-__device__ __forceinline__ void add_bf16x8(float (&x)[8], const uint4 &v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint64_t acc, add, sum;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(x[2 * i]), "f"(x[2 * i + 1]));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(add) : "r"(w[i] << 16), "r"(w[i] & 0xFFFF0000u));
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(acc), "l"(add));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(x[2 * i]), "=f"(x[2 * i + 1]) : "l"(sum));
-  }
-}
-
-__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Two fp32 values -> one byte of e2m1 codes (lo in bits 0-3), nearest even,
-// saturating at +-6.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r)
-      : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Value of an e4m3 code (exact, via the f16 conversion).
-__device__ __forceinline__ float e4m3_value(uint32_t code) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
-      : "=r"(h2)
-      : "r"(code));
-  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
-}
 
 template <int VPT, bool kFp4>
 __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
@@ -353,38 +306,14 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
       uint2 *cod = reinterpret_cast<uint2 *>(p.codes + rowbase);
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
-        float wv[8];
-        unpack_bf16x8(wpk[v], wv);
-        float y[8];
-        uint32_t hb[4];
-        float amax = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const __nv_bfloat162 h2 =
-              __floats2bfloat162_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]),
-                                    __fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
-          const uint32_t hu = *reinterpret_cast<const uint32_t *>(&h2);   // .x low, .y high
-          hb[e / 2] = hu;
-          y[e] = __uint_as_float(hu << 16);
-          y[e + 1] = __uint_as_float(hu & 0xFFFF0000u);
-          amax = fmaxf(amax, fmaxf(fabsf(y[e]), fabsf(y[e + 1])));
-        }
-        // 16 consecutive lanes hold one 128-channel group (all lanes shuffle)
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float scale = __fdiv_rn(amax, 448.0f);
-        uint32_t q[2] = {0u, 0u};
-        if (scale != 0.0f) {
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const uint32_t pr = e4m3x2(__fdiv_rn(y[e], scale), __fdiv_rn(y[e + 1], scale));
-            q[e / 4] |= pr << ((e % 4) * 8);
-          }
-        }
+        uint4 hv;
+        uint2 cv;
+        float scale;
+        fp8_vector_epilogue(x[v], wpk[v], rr, hv, cv, scale);   // all lanes (group shuffles)
         if (active) {
           const int j = v * NA + tc;
-          hid[j] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
-          cod[j] = make_uint2(q[0], q[1]);
+          hid[j] = hv;
+          cod[j] = cv;
           if ((tc & 15) == 0)
             p.scales[(size_t)r * (size_t)(p.H / 128) + (size_t)((col0 + j * 8) / 128)] = scale;
         }
