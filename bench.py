@@ -705,10 +705,11 @@ def run_reference(args, rank, world):
     w = synth.workload(args.workload)
     has_lm = w.V > 0
     fp4 = args.variant == "nvfp4"
+    n = oracle_threads()
     if has_lm:
         inp = synth.stage1_inputs(w)
-        rows = 32
-        qw, sw, gw = sample_weights(args.workload, 128, fp4)
+        rows = min(w.V, 32 * n)                   # 32 vocab rows a host thread per step
+        qw, sw, gw = sample_weights(args.workload, max(128, (rows + 127) // 128 * 128), fp4)
         sample = (f"per step: stage 1 on all {w.T} rows + LM head for all {w.T} tokens over "
                   f"{rows} vocab rows, scaled to {w.V} rows")
     else:
@@ -716,7 +717,6 @@ def run_reference(args, rank, world):
         rows, qw, sw, gw = 0, None, None, (1.0 if fp4 else None)
         sample = f"per step: stage 1 on 1 of {w.T} rows, scaled to all rows"
     toks = list(range(w.T)) if has_lm else None
-    n = oracle_threads()
     for _ in range(args.warmup):
         oracle_sample(w, inp, qw, sw, rows, toks, threads=n, gw=gw)
     t0 = time.perf_counter()
