@@ -1,4 +1,4 @@
-"""Sequence-parallel rows (SURVEY §8(f) f3) on the host: every token row is
+"""Sequence-parallel rows on the host: every token row is
 owned by exactly one rank, and stage 1 run by each rank on its own rows
 composes, across gloo ranks, to stage 1 on all rows (the oracle on CPU)."""
 import os
