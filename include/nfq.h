@@ -146,8 +146,8 @@ int nfq_mtp_reduce_norm_quant(const void *const *partials, int k, const void *re
  *              every call returns it to all-zero, so one zeroing suffices for
  *              any number of calls that run one after another on a stream.
  *              Concurrent calls need separate workspaces.
- * T = a->tokens may be any size >= 1; rows are processed 128 at a time (256
- * with nfq_lm_head_small_batch(0)); each chunk streams the weights once.
+ * T = a->tokens may be any size >= 1; rows are processed 256 at a time, and
+ * each such chunk streams the weights from HBM once.
  */
 size_t nfq_lm_head_workspace_bytes(int T, int S);
 
@@ -392,8 +392,9 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  * nfq_stage1_tune: force the cluster size, vectors per thread, ring slots and
  *   inputs per slot of later stage-1 launches (0 = automatic; invalid choices
  *   fall back).
- * nfq_lm_head_small_batch: 1 (default) runs batches of at most 128 tokens on the
- *   token-major kernel; 0 forces the weight-major kernel for every batch size.
+ * nfq_lm_head_small_batch: 1 (default) runs the FP8 LM head on the token-major
+ *   kernel (up to 256 tokens per launch, as two 128-token groups above 128);
+ *   0 forces the weight-major kernel for every batch size.
  * nfq_lm_head_nvfp4_tune: pipeline stages of later NVFP4 LM-head launches
  *   (0 = as many as fit, at most 5; values below 2 or above what fits fall back).
  * nfq_stage1_grid: at most max_ctas CTAs for later stage-1 launches, each then

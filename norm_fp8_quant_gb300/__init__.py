@@ -374,8 +374,8 @@ def stage1_tune(cluster: int = 0, vpt: int = 0, slots: int = 0, per_slot: int = 
 
 
 def lm_head_small_batch(enabled: bool = True):
-    """Choose the LM-head kernel family for batches of at most 128 tokens: the
-    token-major small-batch kernel (default) or the weight-major kernel."""
+    """Choose the FP8 LM-head kernel family: the token-major kernel (default;
+    up to 256 tokens per launch) or the weight-major kernel."""
     load().nfq_lm_head_small_batch(1 if enabled else 0)
 
 

@@ -432,8 +432,11 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 // group w/4 = tile columns 64*(w/4)..+63), 16 producer, 17 TMEM + MMA.
 // A CTA streams a contiguous range of 128-row blocks, two per tile (the first
 // tile of an odd range holds one).  Two 256-column accumulators in TMEM.
+// Batches of 129..256 tokens run in one launch as two token groups: CTAs 2i
+// and 2i+1 stream the same block range for tokens 0..127 and 128.., so every
+// weight block is fetched from HBM once and served to the second CTA by L2.
 
-constexpr int kSmallMaxT = 128;                 // tokens per launch of the token-major form
+constexpr int kSmallMaxT = 128;                 // tokens per token group of the token-major form
 constexpr int kSmallEpiWarps = 16;
 template <int MT>
 __host__ __device__ constexpr uint32_t small_stage_bytes() { return 2 * kWTileBytes + MT * 128; }
@@ -551,7 +554,8 @@ __device__ bool fused_stage1(const Stage2Params &p, float *red, int *flag,
 template <int MT, bool kPacked, bool kLogits = false, bool kFused = false>
 __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     lm_head_small_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                         const __grid_constant__ CUtensorMap tmap_a, const Stage2Params p,
+                         const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_a2, const Stage2Params p,
                          int nstage) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -567,9 +571,16 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   const int lane = (int)(threadIdx.x % 32);
   constexpr int kProducer = kSmallEpiWarps, kMma = kSmallEpiWarps + 1;
 
+  // token group: tokens t_base .. t_base + Tc - 1 of the launch
+  const int n_grp = p.n_groups;
+  const int grp = (int)blockIdx.x % n_grp;
+  const int cta = (int)blockIdx.x / n_grp, n_cta = (int)gridDim.x / n_grp;
+  const int t_base = grp * MT;
+  const int Tc = min(p.T - t_base, MT);
+  const CUtensorMap *tmap_act = grp ? &tmap_a2 : &tmap_a;
   // contiguous range of 128-row blocks, processed two per tile
-  const int b_begin = (int)(((long)blockIdx.x * p.n_vtiles) / gridDim.x);
-  const int b_end = (int)(((long)(blockIdx.x + 1) * p.n_vtiles) / gridDim.x);
+  const int b_begin = (int)(((long)cta * p.n_vtiles) / n_cta);
+  const int b_end = (int)(((long)(cta + 1) * p.n_vtiles) / n_cta);
   const int n_tiles = (b_end - b_begin + 1) / 2;
 
   if (threadIdx.x == 0) {
@@ -587,7 +598,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   }
   if (warp == kProducer && lane == 0) {
     if constexpr (!kPacked) prefetch_tmap(&tmap_w);
-    prefetch_tmap(&tmap_a);
+    prefetch_tmap(tmap_act);
   }
   if (warp == kMma) {
     tmem_alloc(smem_u32(&sh->tmem_base), 512);
@@ -600,7 +611,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   const int total_steps = n_tiles * G;
   const int npre = total_steps < nstage ? total_steps : nstage;
   if (warp == kProducer && lane == 0) {
-    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_w = n_grp > 1 ? policy_evict_normal() : policy_evict_first();
     for (int it = 0; it < npre; ++it) {
       int blk0, nb;
       small_tile(b_begin, b_end, it / G, blk0, nb);
@@ -630,13 +641,13 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     if (warp < kSmallEpiWarps && fused_stage1(p, s1_red, &s1_flag, abort_flag)) {
       for (int i = (int)threadIdx.x; i < G * MT; i += kSmallEpiWarps * 32) {
         const int kb = i / MT, n = i % MT;
-        sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
+        sa_s[i] = (n < Tc) ? p.act_scales[(size_t)(t_base + n) * G + kb] : 0.0f;
       }
     }
   } else {
     for (int i = (int)threadIdx.x; i < G * MT; i += (int)blockDim.x) {
       const int kb = i / MT, n = i % MT;
-      sa_s[i] = (n < p.T) ? p.act_scales[(size_t)n * G + kb] : 0.0f;
+      sa_s[i] = (n < Tc) ? p.act_scales[(size_t)(t_base + n) * G + kb] : 0.0f;
     }
   }
   tc_fence_before();
@@ -646,7 +657,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
 
   if (warp == kProducer) {
     // -------------------------------------------------------------- producer --
-    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_w = n_grp > 1 ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     // the fused step's activation was written by other CTAs' generic stores
     if constexpr (kFused) fence_proxy_async_global();
@@ -670,7 +681,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         if (lane == 0) {
           uint8_t *st = smem + (size_t)s * kStage;
           const uint32_t fb = smem_u32(&sh->full[s]);
-          mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * kWTileBytes) + (uint32_t)p.T * 128u);
+          mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * kWTileBytes) + (uint32_t)Tc * 128u);
           for (int h = 0; h < nb && !pre; ++h) {
             if constexpr (kPacked) {
               bulk_g2s(smem_u32(st + h * kWTileBytes),
@@ -681,7 +692,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
                           pol_w);
             }
           }
-          tma_load_2d(smem_u32(st + 2 * kWTileBytes), &tmap_a, kb * 128, 0, fb, pol_a);
+          tma_load_2d(smem_u32(st + 2 * kWTileBytes), tmap_act, kb * 128, 0, fb, pol_a);
         }
         __syncwarp();
       }
@@ -751,7 +762,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     const int g = warp >> 2;                       // tile columns 64g .. 64g+63
     const int tok = MT == 64 ? 16 * q + (lane >> 2) + 8 * (lane & 1) : 32 * q + lane;
     const int colpar = (lane >> 1) & 1;
-    const bool quad_active = (MT == 64 ? 16 : 32) * q < p.T;
+    const bool quad_active = (MT == 64 ? 16 : 32) * q < Tc;
     const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
     auto col_of = [&](int j) { return MT == 64 ? 2 * j + colpar : j; };
     uint32_t it = 0;
@@ -830,7 +841,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
         // unfused reference arm: the promoted logits go to memory as BF16,
         // two adjacent columns per 4-byte store when the row allows it
         const int row0 = blk0 * 128 + 64 * g;
-        uint16_t *dst = p.logits_out + (size_t)(tok < p.T ? tok : 0) * (size_t)p.V;
+        uint16_t *dst = p.logits_out + (size_t)(t_base + (tok < Tc ? tok : 0)) * (size_t)p.V;
         const bool pairs = (p.V & 1) == 0;
         if constexpr (MT == 64) {
           // this lane holds columns 2j + colpar, its partner (lane ^ 2) the others
@@ -838,7 +849,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
           for (int j = 0; j < CPT; ++j) {
             const float other = __shfl_xor_sync(0xffffffffu, acc[j], 2);
             const int v0 = row0 + 2 * j;
-            if (tok < p.T && (j & 1) == colpar) {
+            if (tok < Tc && (j & 1) == colpar) {
               const float lo = colpar ? other : acc[j], hi = colpar ? acc[j] : other;
               if (pairs && v0 + 1 < p.V) {
                 *reinterpret_cast<uint32_t *>(dst + v0) =
@@ -850,7 +861,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
               }
             }
           }
-        } else if (tok < p.T) {
+        } else if (tok < Tc) {
 #pragma unroll
           for (int j = 0; j < CPT; j += 2) {
             const int v0 = row0 + j;
@@ -870,7 +881,8 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
       // argmax over this thread's columns (ascending rows), then merge
       const int row0 = blk0 * 128 + 64 * g;          // first row of the group
       const int last_row = min(row0 + 63, p.V - 1);
-      const bool tok_ok = tok < p.T;
+      const bool tok_ok = tok < Tc;
+      const int key = t_base + tok;                  // the token's index in the launch
       if (row0 / p.shard_width == last_row / p.shard_width) {
         // the whole group is one shard: thread max, then (MT = 64) the partner lane
         float best = -INFINITY;
@@ -892,7 +904,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
           }
         }
         if ((MT == 128 || (lane & 2) == 0) && tok_ok && bi >= 0)
-          atomicMax(&p.keys[(size_t)(row0 / p.shard_width) * kKeyStride + tok],
+          atomicMax(&p.keys[(size_t)(row0 / p.shard_width) * kKeyStride + key],
                     pack_key(best, (uint32_t)bi));
       } else {
         // shard boundaries inside the group: flush at every shard change
@@ -905,7 +917,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
           const int sv = v / p.shard_width;
           if (sv != cur) {
             if (bi >= 0 && tok_ok)
-              atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+              atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
             cur = sv;
             bi = -1;
           }
@@ -915,7 +927,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
           }
         }
         if (bi >= 0 && tok_ok)
-          atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+          atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
       }
     }
     __threadfence();
@@ -997,16 +1009,28 @@ size_t stage2_workspace_bytes(int S) {
 }
 
 template <int MT, bool kPacked, bool kLogits = false, bool kFused = false>
-cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const void *w,
+cudaError_t launch_small(const Stage2Params &p_in, const void *act_codes, const void *w,
                          int num_sms, cudaStream_t stream) {
-  CUtensorMap tw, ta;
+  // two token groups (the second CTA of each pair reads the weight from L2)
+  // for 129..256 tokens in the plain argmax form
+  const int n_grp = (MT == 128 && !kLogits && !kFused && p_in.T > MT) ? 2 : 1;
+  if (p_in.T < 1 || p_in.T > n_grp * MT || num_sms < n_grp) return cudaErrorInvalidConfiguration;
+  Stage2Params p = p_in;
+  p.n_groups = n_grp;
+  CUtensorMap tw, ta[2];
   std::memset(&tw, 0, sizeof(tw));
   if (!kPacked && !encode_u8_map(&tw, w, (uint64_t)p.V, (uint64_t)p.H, 128))
     return cudaErrorInvalidValue;
-  // a box of exactly T rows: rows T..MT-1 of the tile keep stale bytes, which
-  // only reach accumulator rows of tokens that do not exist (never read)
-  if (!encode_u8_map(&ta, act_codes, (uint64_t)p.T, (uint64_t)p.H, (uint32_t)p.T))
-    return cudaErrorInvalidValue;
+  // per group a box of exactly its token count: rows Tc..MT-1 of the tile keep
+  // stale bytes, which only reach accumulator rows of tokens that do not exist
+  // (never read)
+  for (int g = 0; g < n_grp; ++g) {
+    const int Tg = (p.T - g * MT) < MT ? (p.T - g * MT) : MT;
+    if (!encode_u8_map(&ta[g], static_cast<const uint8_t *>(act_codes) + (size_t)g * MT * p.H,
+                       (uint64_t)Tg, (uint64_t)p.H, (uint32_t)Tg))
+      return cudaErrorInvalidValue;
+  }
+  if (n_grp == 1) ta[1] = ta[0];
   constexpr uint32_t kStage = small_stage_bytes<MT>();
   const size_t fixed = 1024 /*align pad*/ + (size_t)p.G * MT * 4 + sizeof(SmallSmem) + 64;
   const size_t budget = 227u * 1024u;
@@ -1018,13 +1042,14 @@ cudaError_t launch_small(const Stage2Params &p, const void *act_codes, const voi
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = num_sms < p.n_vtiles ? num_sms : p.n_vtiles;
-  return launch_pdl(kern, grid, kSmallEpiWarps * 32 + 64, smem, stream, tw, ta, p, nstage);
+  const int per_grp = (num_sms / n_grp) < p.n_vtiles ? (num_sms / n_grp) : p.n_vtiles;
+  return launch_pdl(kern, per_grp * n_grp, kSmallEpiWarps * 32 + 64, smem, stream, tw, ta[0],
+                    ta[1], p, nstage);
 }
 
 cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const void *w,
                           int num_sms, cudaStream_t stream) {
-  if (p.T <= kSmallMaxT && g_small_enabled) {
+  if (p.T <= 2 * kSmallMaxT && g_small_enabled) {
     if (p.T <= 64)
       return p.w_packed ? launch_small<64, true>(p, act_codes, w, num_sms, stream)
                         : launch_small<64, false>(p, act_codes, w, num_sms, stream);
@@ -1060,10 +1085,9 @@ cudaError_t launch_lm_head_logits(const Stage2Params &p, int num_sms, cudaStream
                    : launch_small<128, true, true>(p, p.act_codes, p.w_packed, num_sms, stream);
 }
 
-// Tokens per launch: batches above 128 tokens run as 128-token launches of the
-// token-major kernel (each streams the weight once; at 256 tokens two such
-// launches take 288 us against 335 us for one weight-major launch).
-int stage2_token_chunk() { return g_small_enabled ? kSmallMaxT : 256; }
+// Tokens per launch: up to 256 in either family (the token-major form runs
+// 129..256 tokens as two token groups over one weight stream).
+int stage2_token_chunk() { return 2 * kSmallMaxT; }
 
 size_t packed_weight_bytes(int V, int H) {
   return (size_t)((V + 127) / 128) * (size_t)(H / 128) * kWTileBytes;

@@ -65,12 +65,13 @@ struct Stage2Params {
   unsigned long long *keys;   // workspace [S][NPAD] packed (value, index) maxima
   unsigned *counter;          // workspace: CTAs finished
   unsigned *err;              // device error word
-  int T;                      // tokens in this chunk (<= 256)
+  int T;                      // tokens in this launch (<= 256)
   int T_total;                // row stride of the per-shard outputs
   int tok0;                   // first token of this chunk
   int H, G, V, S;
   int shard_width;            // V / S
   int n_vtiles;               // ceil(V / 128)
+  int n_groups;               // token-major form: token groups of 128 (1 or 2), set at launch
   uint16_t *logits_out;       // unfused arm: BF16 logits [T][V] instead of the argmax
   FusedStage1 s1;             // the fused step (s1.ready != null)
   // NVFP4 form: act_codes are e2m1 pairs [T][H/2], G = H / 256 (K steps)
