@@ -589,7 +589,9 @@ def run_ours(args, rank, world, local):
                                              "lm_head_small_kernel (BF16 logits) + "
                                              "unfused_argmax_kernel" if unfused else
                                              "lm_head_small_kernel" if T <= 128 else
-                                             "lm_head_argmax_kernel"),
+                                             "lm_head_small_kernel, two token groups"
+                                             if T <= 256 else
+                                             f"lm_head_small_kernel x {(T + 255) // 256}"),
                                   "peak_source": peak_kind}
         else:
             result["roofline"] = {"bound": "hbm", "achieved": round(gbs1, 1), "peak": peak,
