@@ -98,6 +98,21 @@ def test_stage2_tie_stress(nfq, layout):
                  expected=expected)
 
 
+@pytest.mark.parametrize("T", [136, 255])
+def test_stage2_two_token_groups_full_grid(nfq, layout, T):
+    """129..256 tokens run as two token groups over one weight stream: with a
+    full-size vocab every CTA pair is busy, and the second group holds a ragged
+    8 or 127 tokens.  Tokens on both sides of the group boundary and at the
+    ragged end are checked against the oracle."""
+    w = synth.workload("tiny", T=T, H=1024, k=2, V=151552, S=8, seed=T)
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S, layout=layout)
+    assert tok.shape == (T,) and np.all((0 <= tok) & (tok < w.V))
+    check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, [0, 127, 128, T - 1], mx, sidx,
+                 sval)
+
+
 @pytest.mark.parametrize("T,H,V,S", [(1, 128, 128, 1), (3, 256, 200, 2), (16, 512, 1000, 5),
                                      (17, 384, 4100, 4), (33, 256, 2048, 64),
                                      (64, 1024, 3000, 3), (100, 512, 1536, 6),
