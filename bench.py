@@ -584,7 +584,9 @@ def run_ours(args, rank, world, local):
                                   "unit": "GB/s", "frac": round(gbs2 / peak, 4),
                                   "traffic": (ncu_traffic("lm_head_nvfp4" if fp4 else "lm_head")
                                               if args.workload == WORKLOAD and not unfused
-                                              else None),
+                                              else ncu_traffic("lm_head_tie_stress")
+                                              if args.workload == "tie_stress" and not fp4
+                                              and not unfused else None),
                                   "kernel": ("lm_head_fp4_kernel" if fp4 else
                                              "lm_head_small_kernel (BF16 logits) + "
                                              "unfused_argmax_kernel" if unfused else
