@@ -1,0 +1,73 @@
+"""The hand-derived end-to-end case (tests/golden/e2e_two_tokens.txt) on the
+GPU through the C ABI: stage 1, then the LM head with its sharded argmax and
+the fused step.  Every value of the case is an exact dyadic number, so the
+GPU must reproduce the hand-derived hidden, codes, scales, tokens, maxima and
+per-shard results bit for bit, whatever its summation order."""
+import numpy as np
+import pytest
+import torch
+
+from tests._parity import bf16_host, to_dev, to_dev_bf16
+from tests.test_oracle_pins import e2e_golden_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nfq():
+    import norm_fp8_quant_gb300 as m
+    from norm_fp8_quant_gb300 import build
+    build.build()
+    m.load()
+    assert torch.cuda.is_available()
+    return m
+
+
+def _check_stage1(g, hidden, codes, scales):
+    for t in range(2):
+        h0, h1e, h1o = (int(v, 16) for v in g[f"hidden_t{t}"])
+        assert np.all(hidden[t, :128] == h0)
+        assert np.all(hidden[t, 128::2] == h1e) and np.all(hidden[t, 129::2] == h1o)
+        c0, c1e, c1o = (int(v, 16) for v in g[f"codes_t{t}"])
+        assert np.all(codes[t, :128] == c0)
+        assert np.all(codes[t, 128::2] == c1e) and np.all(codes[t, 129::2] == c1o)
+        assert scales[t].view(np.uint32).tolist() == [int(v, 16) for v in g["scales"]]
+
+
+def _check_stage2(g, tok, mx, sidx, sval):
+    assert tok.tolist() == [int(v) for v in g["tokens"]]
+    assert mx.tolist() == [float(g["logits_t0"][0]), float(g["logits_t1"][3])]
+    for t in range(2):
+        assert sidx[:, t].tolist() == [int(v) for v in g[f"shard_idx_t{t}"]]
+        assert sval[:, t].tolist() == [float(v) for v in g[f"shard_val_t{t}"]]
+
+
+@pytest.mark.parametrize("layout", ["rowmajor", "packed"])
+def test_e2e_golden_two_calls(nfq, layout):
+    g, p, r, w, qw, sw = e2e_golden_inputs()
+    h, c, s = nfq.mtp_reduce_norm_quant([to_dev_bf16(x) for x in p], to_dev_bf16(r),
+                                        to_dev_bf16(w))
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    _check_stage1(g, bf16_host(h), c.cpu().numpy(), s.cpu().numpy())
+    wd = to_dev(qw)
+    if layout == "packed":
+        wd = nfq.pack_lm_head_weights(wd)
+    out = nfq.lm_head_fp8_argmax(c, s, wd, to_dev(sw), 2, want_max=True, want_shards=True)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    _check_stage2(g, *[x.cpu().numpy() for x in out])
+
+
+def test_e2e_golden_step_call(nfq):
+    """The one-call step API gives the same hand-derived results (at H = 256 it
+    runs as its two launches; the one-launch form needs H % 512 == 0)."""
+    g, p, r, w, qw, sw = e2e_golden_inputs()
+    wp = nfq.pack_lm_head_weights(to_dev(qw))
+    out = nfq.mtp_step_fp8([to_dev_bf16(x) for x in p], to_dev_bf16(r), to_dev_bf16(w), wp,
+                           to_dev(sw), 2, want_max=True, want_shards=True)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    hidden, codes, scales, tok, mx, sidx, sval = out
+    _check_stage1(g, bf16_host(hidden), codes.cpu().numpy(), scales.cpu().numpy())
+    _check_stage2(g, *[x.cpu().numpy() for x in (tok, mx, sidx, sval)])

@@ -595,3 +595,59 @@ def test_bf16_argmax_is_lowest_index_by_brute_force():
         for i in range(3):
             m = L[i].max()
             assert tok[i] == min(v for v in range(37) if L[i, v] == m)
+
+
+# ------------------------------------------------------------- end to end --
+
+def e2e_golden_inputs():
+    """The inputs of tests/golden/e2e_two_tokens.txt, as the arrays both sides
+    take: partials [k][T][H], residual [T][H], norm weight [H] (BF16 bits), the
+    weight codes [V][H] and block scales [1][H/128]."""
+    g = _read_golden("e2e_two_tokens.txt")
+    H = int(g["H"][0])
+    T = 2
+    k = len(g["partials_t0"])
+    p = np.zeros((k, T, H), np.float32)
+    r = np.zeros((T, H), np.float32)
+    for t in range(T):
+        for j, v in enumerate(g[f"partials_t{t}"]):
+            p[j, t, :] = float(v)
+        r[t, :] = float(g[f"residual_t{t}"][0])
+    w = np.empty(H, np.float32)
+    w[:128] = float(g["w_group0"][0])
+    w[128::2] = float(g["w_group1_even"][0])
+    w[129::2] = float(g["w_group1_odd"][0])
+    qw = np.zeros((4, H), np.uint8)
+    qw[0, :] = 0x38
+    qw[1, :128], qw[1, 128:] = 0x38, 0xB8
+    qw[2, :64] = 0x40
+    qw[3, 255] = 0x38
+    sw = np.array([[float(v) for v in g["wsc"]]], np.float32)
+    return g, bf16_bits_of(p), bf16_bits_of(r), bf16_bits_of(w), qw, sw
+
+
+def test_end_to_end_hand_derived_two_tokens():
+    """Stage 1 into the LM head and the sharded argmax on a case worked by hand
+    (tests/golden/e2e_two_tokens.txt): pins how the packed activation, its
+    scales and the weight block scales compose, and the argmax outputs."""
+    g, p, r, w, qw, sw = e2e_golden_inputs()
+    H = p.shape[2]
+    o = oracle.reduce_norm_quant(p, r, w)
+    for t in range(2):
+        h0, h1e, h1o = (int(v, 16) for v in g[f"hidden_t{t}"])
+        assert np.all(o["hidden"][t, :128] == h0)
+        assert np.all(o["hidden"][t, 128::2] == h1e) and np.all(o["hidden"][t, 129::2] == h1o)
+        c0, c1e, c1o = (int(v, 16) for v in g[f"codes_t{t}"])
+        assert np.all(o["codes"][t, :128] == c0)
+        assert np.all(o["codes"][t, 128::2] == c1e) and np.all(o["codes"][t, 129::2] == c1o)
+        assert o["scales"][t].view(np.uint32).tolist() == [int(v, 16) for v in g["scales"]]
+    L = oracle.lm_head_logits(o["codes"], o["scales"], qw, sw)
+    assert L.shape == (2, 4)
+    for t in range(2):
+        assert L[t].tolist() == [float(v) for v in g[f"logits_t{t}"]]
+    a = oracle.argmax(L, 2)
+    assert a["tokens"].tolist() == [int(v) for v in g["tokens"]]
+    for t in range(2):
+        assert a["shard_idx"][t].tolist() == [int(v) for v in g[f"shard_idx_t{t}"]]
+        assert a["shard_val"][t].tolist() == [float(v) for v in g[f"shard_val_t{t}"]]
+    assert H == 256
