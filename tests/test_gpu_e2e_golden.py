@@ -1,14 +1,16 @@
-"""The hand-derived end-to-end case (tests/golden/e2e_two_tokens.txt) on the
-GPU through the C ABI: stage 1, then the LM head with its sharded argmax and
-the fused step.  Every value of the case is an exact dyadic number, so the
-GPU must reproduce the hand-derived hidden, codes, scales, tokens, maxima and
-per-shard results bit for bit, whatever its summation order."""
+"""The hand-derived end-to-end cases (tests/golden/e2e_two_tokens.txt and
+tests/golden/nvfp4_e2e_two_tokens.txt) on the GPU through the C ABI: stage 1,
+then the LM head with its sharded argmax, in the FP8 and the NVFP4 forms.
+Every value of the cases is an exact dyadic number, so the GPU must reproduce
+the hand-derived hidden, codes, scales, tokens, maxima and per-shard results
+bit for bit, whatever its summation order."""
 import numpy as np
 import pytest
 import torch
 
 from tests._parity import bf16_host, to_dev, to_dev_bf16
-from tests.test_oracle_pins import e2e_golden_inputs
+from tests.test_oracle_pins import (check_nvfp4_e2e_stage1, e2e_golden_inputs,
+                                    nvfp4_e2e_golden_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,3 +73,22 @@ def test_e2e_golden_step_call(nfq):
     hidden, codes, scales, tok, mx, sidx, sval = out
     _check_stage1(g, bf16_host(hidden), codes.cpu().numpy(), scales.cpu().numpy())
     _check_stage2(g, *[x.cpu().numpy() for x in (tok, mx, sidx, sval)])
+
+
+def test_nvfp4_e2e_golden(nfq):
+    g, p, r, w, qw, sw, gw = nvfp4_e2e_golden_inputs()
+    h, c, bs, gs = nfq.mtp_reduce_norm_quant_nvfp4([to_dev_bf16(x) for x in p], to_dev_bf16(r),
+                                                   to_dev_bf16(w))
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    check_nvfp4_e2e_stage1(g, bf16_host(h), c.cpu().numpy(), bs.cpu().numpy(), gs.cpu().numpy())
+    wp = nfq.pack_lm_head_weights_nvfp4(to_dev(qw), to_dev(sw), gw)
+    tok, mx, sidx, sval = nfq.lm_head_nvfp4_argmax(c, bs, gs, wp, 2, want_max=True,
+                                                   want_shards=True)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    assert tok.cpu().numpy().tolist() == [int(v) for v in g["tokens"]]
+    assert mx.cpu().numpy().tolist() == [float(g["logits_t0"][0]), float(g["logits_t1"][2])]
+    for t in range(2):
+        assert sidx[:, t].cpu().numpy().tolist() == [int(v) for v in g[f"shard_idx_t{t}"]]
+        assert sval[:, t].cpu().numpy().tolist() == [float(v) for v in g[f"shard_val_t{t}"]]

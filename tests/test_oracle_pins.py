@@ -651,3 +651,62 @@ def test_end_to_end_hand_derived_two_tokens():
         assert a["shard_idx"][t].tolist() == [int(v) for v in g[f"shard_idx_t{t}"]]
         assert a["shard_val"][t].tolist() == [float(v) for v in g[f"shard_val_t{t}"]]
     assert H == 256
+
+
+def nvfp4_e2e_golden_inputs():
+    """The inputs of tests/golden/nvfp4_e2e_two_tokens.txt: partials [k][T][H],
+    residual [T][H], norm weight [H] (BF16 bits), the NVFP4 weight codes
+    [V][H/2] (packed), block scales [V][H/16] and its tensor scale."""
+    g = _read_golden("nvfp4_e2e_two_tokens.txt")
+    H, T = int(g["H"][0]), 2
+    k = len(g["partials_t0"])
+    p = np.zeros((k, T, H), np.float32)
+    r = np.zeros((T, H), np.float32)
+    for t in range(T):
+        for j, v in enumerate(g[f"partials_t{t}"]):
+            p[j, t, :] = float(v)
+        r[t, :] = float(g[f"residual_t{t}"][0])
+    w = np.empty(H, np.float32)
+    w[:16] = np.tile([float(v) for v in g["w_block0"]], 4)
+    w[16:] = np.tile([float(v) for v in g["w_rest"]], (H - 16) // 2)
+    qw = np.zeros((4, H // 2), np.uint8)
+    sw = np.full((4, H // 16), 0x38, np.uint8)
+    qw[0, :] = 0x22
+    qw[1, :8] = 0x22
+    sw[1, 0] = 0x40
+    qw[2, :] = 0x99
+    qw[3, H // 2 - 1] = 0x70
+    sw[3, H // 16 - 1] = 0x30
+    return g, bf16_bits_of(p), bf16_bits_of(r), bf16_bits_of(w), qw, sw, float(g["gw"][0])
+
+
+def check_nvfp4_e2e_stage1(g, hidden, codes, block_scales, row_scales):
+    """Stage 1 of the NVFP4 hand-derived case against its expected bytes."""
+    for t in range(2):
+        h = [int(v, 16) for v in g[f"hidden_t{t}"]]
+        assert hidden[t, :16].tolist() == h[:4] * 4
+        assert hidden[t, 16:].tolist() == h[4:6] * 120
+        c = [int(v, 16) for v in g[f"codes_t{t}"]]
+        assert codes[t, :8].tolist() == c[:2] * 4
+        assert np.all(codes[t, 8:] == c[2])
+        b0, b1 = (int(v, 16) for v in g["block_scales"])
+        assert block_scales[t, 0] == b0 and np.all(block_scales[t, 1:] == b1)
+        assert np.float32(row_scales[t]).view(np.uint32) == int(g["row_scale"][0], 16)
+
+
+def test_nvfp4_end_to_end_hand_derived_two_tokens():
+    """The NVFP4 stage 1 into the NVFP4 LM head and the sharded argmax on a case
+    worked by hand (tests/golden/nvfp4_e2e_two_tokens.txt): pins the packing
+    order, which block scale meets which, the row and tensor scales, and the
+    argmax outputs."""
+    g, p, r, w, qw, sw, gw = nvfp4_e2e_golden_inputs()
+    o = oracle.reduce_norm_quant_nvfp4(p, r, w)
+    check_nvfp4_e2e_stage1(g, o["hidden"], o["codes"], o["block_scales"], o["global_scales"])
+    L = oracle.lm_head_logits_nvfp4(o["codes"], o["block_scales"], o["global_scales"], qw, sw, gw)
+    for t in range(2):
+        assert L[t].tolist() == [float(v) for v in g[f"logits_t{t}"]]
+    a = oracle.argmax(L, 2)
+    assert a["tokens"].tolist() == [int(v) for v in g["tokens"]]
+    for t in range(2):
+        assert a["shard_idx"][t].tolist() == [int(v) for v in g[f"shard_idx_t{t}"]]
+        assert a["shard_val"][t].tolist() == [float(v) for v in g[f"shard_val_t{t}"]]
