@@ -92,3 +92,24 @@ def test_nvfp4_e2e_golden(nfq):
     for t in range(2):
         assert sidx[:, t].cpu().numpy().tolist() == [int(v) for v in g[f"shard_idx_t{t}"]]
         assert sval[:, t].cpu().numpy().tolist() == [float(v) for v in g[f"shard_val_t{t}"]]
+
+
+def test_unfused_e2e_golden(nfq):
+    """The unfused arm's five kernels on the hand-derived case: BF16 all-reduce
+    output, hidden, activation, BF16 logits and tokens as worked by hand."""
+    g, p, r, w, qw, sw = e2e_golden_inputs()
+    s = nfq.unfused_allreduce_bf16([to_dev_bf16(x) for x in p])
+    h = nfq.unfused_add_rmsnorm(s, to_dev_bf16(r), to_dev_bf16(w))
+    c, sc = nfq.unfused_quant_fp8(h)
+    logits = nfq.unfused_lm_head_logits(c, sc, nfq.pack_lm_head_weights(to_dev(qw)), to_dev(sw))
+    tok = nfq.unfused_argmax_bf16(logits)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    s_host = bf16_host(s)
+    s0, s1 = (int(v, 16) for v in g["unfused_sum"])
+    assert np.all(s_host[0] == s0) and np.all(s_host[1] == s1)
+    _check_stage1(g, bf16_host(h), c.cpu().numpy(), sc.cpu().numpy())
+    lb = bf16_host(logits)
+    for t in range(2):
+        assert lb[t].tolist() == [int(v, 16) for v in g[f"unfused_logits_t{t}"]]
+    assert tok.cpu().numpy().tolist() == [int(v) for v in g["tokens"]]

@@ -710,3 +710,19 @@ def test_nvfp4_end_to_end_hand_derived_two_tokens():
     for t in range(2):
         assert a["shard_idx"][t].tolist() == [int(v) for v in g[f"shard_idx_t{t}"]]
         assert a["shard_val"][t].tolist() == [float(v) for v in g[f"shard_val_t{t}"]]
+
+
+def test_unfused_end_to_end_hand_derived_two_tokens():
+    """The unfused path on the hand-derived case: the BF16 all-reduce output,
+    the hidden, the activation, the BF16 logits and the tokens are the values
+    worked by hand in tests/golden/e2e_two_tokens.txt."""
+    g, p, r, w, qw, sw = e2e_golden_inputs()
+    u = oracle.unfused_step(p, r, w, qw, sw)
+    s0, s1 = (int(v, 16) for v in g["unfused_sum"])
+    assert np.all(u["sum"][0] == s0) and np.all(u["sum"][1] == s1)
+    fused = oracle.reduce_norm_quant(p, r, w)
+    for key in ("hidden", "codes", "scales"):
+        assert np.array_equal(u[key], fused[key])
+    for t in range(2):
+        assert u["logits"][t].tolist() == [int(v, 16) for v in g[f"unfused_logits_t{t}"]]
+    assert u["tokens"].tolist() == [int(v) for v in g["tokens"]]
