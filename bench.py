@@ -124,11 +124,39 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_comments(text):
+    """C/C++/CUDA source without its comments, trailing blanks and blank lines
+    (string literals kept as they are)."""
+    out, i, n, in_str = [], 0, len(text), False
+    while i < n:
+        c = text[i]
+        if in_str:
+            out.append(text[i:i + 2] if c == "\\" else c)
+            i += 2 if c == "\\" else 1
+            in_str = c != '"'
+            continue
+        if c == '"':
+            in_str = True
+            out.append(c)
+            i += 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_source_hash(files):
+    """Hash of the kernel sources' code: a change to comments alone keeps it."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "norm_fp8_quant_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "norm_fp8_quant_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

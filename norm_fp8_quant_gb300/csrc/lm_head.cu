@@ -8,8 +8,7 @@
 // full-vocab logits; Accuracy: ties at shard boundaries are decided by the
 // local-argmax rule (here: the lowest global vocab index).
 //
-// Formulation (swap-AB): the weight is the MMA's M operand (128 vocab rows =
-// one 128x128 scale block row) and the tokens are N.  Per 128-wide K block:
+// Per 128-wide K block kb, with the products summed by the tensor cores:
 //   P[v][n] = sum_{k in block} qw[v][k] * qa[n][k]     tcgen05.mma kind::f8f6f4,
 //                                                      fp32 accumulator in TMEM
 //   acc[v][n] += P[v][n] * (sw[v/128][kb] * sa[n][kb]) fp32, in registers
@@ -17,7 +16,17 @@
 // scaling (power-of-two scale factors) cannot express, hence the per-block
 // promotion out of TMEM.
 //
-// Warp roles (one CTA per SM, persistent over contiguous vocab tiles):
+// Two kernel families:
+//  - lm_head_small_kernel (the default, up to 256 tokens a launch): the tokens
+//    are the MMA's M operand (64 or 128) and 256 weight rows (two scale blocks)
+//    are N, so each MMA consumes twice the weight bytes; 129..256 tokens run
+//    as two token groups over one weight stream.  Described before the kernel.
+//  - lm_head_argmax_kernel (weight-major, below; selected with
+//    nfq_lm_head_small_batch(0)): the weight is M (128 vocab rows = one scale
+//    block row) and up to 256 tokens are N.
+//
+// Warp roles of the weight-major kernel (one CTA per SM, persistent over
+// contiguous vocab tiles):
 //   warps 0 .. 4*EPI-1   epilogue: TMEM -> registers, promotion, argmax
 //   warp  4*EPI          TMA producer: weight tile 128x128 + activation tile
 //                        Nx128 per K block into a ring of swizzled stages
