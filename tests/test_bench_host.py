@@ -48,3 +48,15 @@ def test_single_rank_and_throughput():
     assert bench.tokens_per_s(2, 64, 100, 20.0) == pytest.approx(640000.0)
     assert bench.stage1_bytes(64, 6144, 8) == 8282112
     assert bench.stage2_bytes(64, 6144, 151552) == 931768576
+
+
+def test_traffic_hash_ignores_comments_only():
+    """The ncu traffic stays attached to a kernel through comment edits and is
+    dropped by any code edit: the hash is over the code without comments."""
+    src = 'asm("mov.b32 %0, %1; // not a comment");  // note\n/* block\n note */ int a = 1;\n\n'
+    code = bench.strip_comments(src)
+    assert code == 'asm("mov.b32 %0, %1; // not a comment");\n int a = 1;'
+    assert bench.strip_comments(src.replace("note", "other words")) == code
+    assert bench.strip_comments(src.replace("a = 1", "a = 2")) != code
+    assert bench.strip_comments('s = "a\\"/*b*/"; /* c */') == 's = "a\\"/*b*/";'
+
