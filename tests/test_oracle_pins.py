@@ -366,6 +366,56 @@ def test_argmax_planted_ties_across_shard_boundaries_and_signed_zero():
     assert r["gap"][0] == 0 and r["gap"][2] == 0 and r["gap"][5] > 0
 
 
+# The relative top-2 gap decides which draft ids must match exactly (gap >= 1e-3
+# or gap == 0) and which are near ties, so its value is pinned, not only its
+# sign: gap = (L1 - L2) / |L1| with L2 the best logit at another index, and
+# L1 - L2 when L1 == 0.  Each row below is built so that one plausible slip
+# gives a different value: dividing by L2 ([4, 2] -> 1.0), dropping the
+# absolute value ([-2, -3] -> -0.5), taking L2 as the second-largest distinct
+# value ([3, 3, 1] -> 2/3), or dividing by zero when L1 == 0.
+GAP_ROWS = [
+    ([4.0, 3.0, -1.0, 0.0], 0.25),
+    ([4.0, 2.0], 0.5),
+    ([-2.0, -3.0, -7.0], 0.5),
+    ([0.0, -0.5, -4.0], 0.5),
+    ([-0.0, -0.25], 0.25),
+    ([3.0, 3.0, 1.0], 0.0),
+    ([1.0, 5.0, 2.0, 5.0, 4.0], 0.0),
+    ([-1.0, 0.5, 0.25, -3.0], 0.5),
+    ([8.0, 6.0, 7.0, 1.0], 0.125),
+]
+
+
+@pytest.mark.parametrize("row,gap", GAP_ROWS)
+def test_argmax_gap_value_hand_computed(row, gap):
+    L = np.array([row], np.float32)
+    r = oracle.argmax(L, 1)
+    assert r["gap"][0] == gap
+
+
+def test_argmax_gap_value_is_placed_by_row_not_shard():
+    """The gap is taken over the whole vocabulary; the runner-up may sit in
+    another shard than the maximum."""
+    L = np.full((1, 16), -9.0, np.float32)
+    L[0, 2] = 10.0
+    L[0, 13] = 8.0                     # shard 3 of 4
+    assert oracle.argmax(L, 4)["gap"][0] == 0.2
+
+
+def test_argmax_gap_value_matches_a_sorted_copy():
+    """Brute force on random rows with repeated values: sort a copy in
+    descending order, L1 the first element and L2 the second (which equals L1
+    when the maximum is repeated), gap in fp64 from the fp32 values."""
+    for n, V, lo, hi in ((40, 9, -4, 5), (40, 33, -2, 3), (20, 200, -50, 50)):
+        L = (rng.integers(lo, hi, (n, V)) / 4.0).astype(np.float32)
+        L[:5] += rng.normal(0, 1, (5, V)).astype(np.float32)
+        r = oracle.argmax(L, 1)
+        for i in range(n):
+            s = np.sort(L[i].astype(np.float64))[::-1]
+            want = (s[0] - s[1]) if s[0] == 0 else (s[0] - s[1]) / abs(s[0])
+            assert r["gap"][i] == want, (i, L[i], r["gap"][i], want)
+
+
 # ----------------------------------------------------------- tie stress --
 
 def test_tie_stress_construction_is_reproduced_by_the_oracle():
