@@ -230,9 +230,12 @@ int nfq_mtp_draft_chain(int positions, const void *const *partials, int k,
  *
  * Instead of a caller workspace it uses a scratch array of 131,088 bytes that
  * the library keeps in device memory for the life of the process on every GPU
- * that loads it; calls needing more (more than 64 shards) return
- * NFQ_ERR_WORKSPACE.  It allocates nothing and frees nothing.  Arguments,
+ * that loads it.  That is the workspace of the largest shard count any LM-head
+ * call accepts (64); S outside 1..64 returns NFQ_ERR_SHAPE, as it does for
+ * nfq_lm_head_fp8_argmax.  It allocates nothing and frees nothing.  Arguments,
  * outputs and errors are those of nfq_lm_head_fp8_argmax minus the workspace.
+ * - Every argument is checked before the array is touched: a rejected call
+ *   queues nothing.
  * - The first call on a device looks up the array's device address for that
  *   device (the current one); make that first call before any stream capture.
  * - Each call clears the part of the array it uses with an asynchronous memset

@@ -178,7 +178,7 @@ int nfq_mtp_reduce_norm_quant_nvfp4(const void *const *partials, int k, const vo
 
 size_t nfq_lm_head_workspace_bytes(int T, int S) {
   (void)T;
-  if (S < 1 || S > 64) return 0;
+  if (S < 1 || S > kMaxShards) return 0;
   return stage2_workspace_bytes(S);
 }
 
@@ -190,26 +190,49 @@ int nfq_lm_head_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
 
 }  // extern "C"
 
+namespace nfq {
+
+// Every argument of an FP8 LM-head call except the workspace: NULL pointers,
+// shapes and alignment.  Queues nothing.
+int lm_head_check_args(const nfq_quant_act *a, const uint8_t *w, const float *w_scales, int V,
+                       int S, const int32_t *tokens_out, const float *max_logit_out,
+                       const int32_t *shard_idx_out, const float *shard_val_out) {
+  if (!a || !w || !w_scales || !tokens_out) return NFQ_ERR_NULL;
+  if (!a->codes || !a->scales) return NFQ_ERR_NULL;
+  const int T = a->tokens, H = a->hidden;
+  if (a->group != 128 || H < 128 || H > 16384 || H % 128 != 0 || T < 0) return NFQ_ERR_SHAPE;
+  if (V < 1 || S < 1 || S > kMaxShards || V % S != 0) return NFQ_ERR_SHAPE;
+  // the per-token outputs are written with 4-byte stores
+  if (!aligned16(a->codes) || !aligned16(a->scales) || !aligned16(w) || !aligned16(w_scales) ||
+      !aligned4(tokens_out) || (max_logit_out && !aligned4(max_logit_out)) ||
+      (shard_idx_out && !aligned4(shard_idx_out)) ||
+      (shard_val_out && !aligned4(shard_val_out)))
+    return NFQ_ERR_ALIGN;
+  return NFQ_OK;
+}
+
+// NFQ_OK when the current device runs this library's kernels (looked up once
+// per device).
+int current_device_supported() {
+  DeviceInfo *d = nullptr;
+  return device_info(&d);
+}
+
+}  // namespace nfq
+
 namespace {
 
 int lm_head_common(const nfq_quant_act *a, const uint8_t *w, bool packed, const float *w_scales,
                    int V, int S, int32_t *tokens_out, float *max_logit_out,
                    int32_t *shard_idx_out, float *shard_val_out, void *workspace,
                    size_t ws_bytes, void *stream) {
-  if (!a || !w || !w_scales || !tokens_out) return NFQ_ERR_NULL;
-  if (!a->codes || !a->scales) return NFQ_ERR_NULL;
-  const int T = a->tokens, H = a->hidden;
-  if (a->group != 128 || H < 128 || H > 16384 || H % 128 != 0 || T < 0) return NFQ_ERR_SHAPE;
-  if (V < 1 || S < 1 || S > 64 || V % S != 0) return NFQ_ERR_SHAPE;
+  const int chk = lm_head_check_args(a, w, w_scales, V, S, tokens_out, max_logit_out,
+                                     shard_idx_out, shard_val_out);
+  if (chk != NFQ_OK) return chk;
   if (!workspace) return NFQ_ERR_WORKSPACE;
   if (ws_bytes < stage2_workspace_bytes(S)) return NFQ_ERR_WORKSPACE;
-  // the per-token outputs are written with 4-byte stores
-  if (!aligned16(a->codes) || !aligned16(a->scales) || !aligned16(w) || !aligned16(w_scales) ||
-      !aligned4(tokens_out) || !aligned16(workspace) ||
-      (max_logit_out && !aligned4(max_logit_out)) ||
-      (shard_idx_out && !aligned4(shard_idx_out)) ||
-      (shard_val_out && !aligned4(shard_val_out)))
-    return NFQ_ERR_ALIGN;
+  if (!aligned16(workspace)) return NFQ_ERR_ALIGN;
+  const int T = a->tokens, H = a->hidden;
   if (T == 0) return NFQ_OK;
   DeviceInfo *d = nullptr;
   const int st = device_info(&d);
@@ -421,7 +444,7 @@ int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w
   if (!a->codes || !a->block_scales || !a->row_scales) return NFQ_ERR_NULL;
   const int T = a->tokens, H = a->hidden;
   if (a->block != 16 || H < 256 || H > 16384 || H % 256 != 0 || T < 0) return NFQ_ERR_SHAPE;
-  if (V < 1 || S < 1 || S > 64 || V % S != 0) return NFQ_ERR_SHAPE;
+  if (V < 1 || S < 1 || S > kMaxShards || V % S != 0) return NFQ_ERR_SHAPE;
   if (!workspace) return NFQ_ERR_WORKSPACE;
   if (ws_bytes < stage2_workspace_bytes(S)) return NFQ_ERR_WORKSPACE;
   if (!aligned16(a->codes) || !aligned16(a->block_scales) || !aligned16(a->row_scales) ||
@@ -513,7 +536,7 @@ int nfq_mtp_step_fp8(const void *const *partials, int k, const void *residual,
   if (T < 0 || H < 128 || H > 16384 || H % 128 != 0) return NFQ_ERR_SHAPE;
   if (!(eps >= 0.0f) || eps > 1.0f) return NFQ_ERR_SHAPE;
   if (q->group != 128 || q->tokens != T || q->hidden != H) return NFQ_ERR_SHAPE;
-  if (V < 1 || S < 1 || S > 64 || V % S != 0) return NFQ_ERR_SHAPE;
+  if (V < 1 || S < 1 || S > kMaxShards || V % S != 0) return NFQ_ERR_SHAPE;
   if (!workspace || ws_bytes < stage2_workspace_bytes(S)) return NFQ_ERR_WORKSPACE;
   if (!aligned16(residual) || !aligned16(norm_w) || !aligned16(hidden_out) ||
       !aligned16(q->codes) || !aligned16(q->scales) || !aligned16(w_packed) ||

@@ -1013,9 +1013,7 @@ __global__ void __launch_bounds__(256) pack_weights_kernel(const uint8_t *__rest
 
 }  // namespace
 
-size_t stage2_workspace_bytes(int S) {
-  return (size_t)S * kKeyStride * sizeof(unsigned long long) + 16u;
-}
+size_t stage2_workspace_bytes(int S) { return stage2_workspace_bytes_for(S); }
 
 template <int MT, bool kPacked, bool kLogits = false, bool kFused = false>
 cudaError_t launch_small(const Stage2Params &p_in, const void *act_codes, const void *w,

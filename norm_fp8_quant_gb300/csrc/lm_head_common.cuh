@@ -16,7 +16,7 @@ namespace nfq {
 namespace {
 
 constexpr int kErrBitStage2 = 2;
-constexpr int kKeyStride = 256;   // keys per shard in the workspace
+constexpr int kKeyStride = kArgmaxKeysPerShard;   // keys per shard in the workspace
 constexpr uint32_t kWTileBytes = 128 * 128;
 
 // Ordered 64-bit key: larger value first, then lower index; -0 counts as +0.

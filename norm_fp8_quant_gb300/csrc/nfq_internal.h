@@ -9,6 +9,15 @@
 namespace nfq {
 
 constexpr int kMaxPartials = 16;
+constexpr int kMaxShards = 64;          // vocabulary shards of one LM-head call
+constexpr int kArgmaxKeysPerShard = 256; // argmax keys per shard: one per token of a launch
+
+// Bytes of the LM head's scratch for S shards: S x 256 packed 64-bit argmax
+// keys, then a 16-byte block holding the CTA-done counter (and the fused
+// step's row counter).
+__host__ __device__ constexpr size_t stage2_workspace_bytes_for(int S) {
+  return (size_t)S * kArgmaxKeysPerShard * 8u + 16u;
+}
 
 // Stage 1 launch parameters (passed by value to the kernel).
 struct Stage1Params {

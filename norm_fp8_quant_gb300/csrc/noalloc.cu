@@ -3,10 +3,20 @@
 // fixed array in this library's device memory, so the call allocates nothing.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
 #include "../../include/nfq.h"
+#include "nfq_internal.h"
+
+namespace nfq {
+// Defined with the other entry points (abi.cu).
+int lm_head_check_args(const nfq_quant_act *a, const uint8_t *w, const float *w_scales, int V,
+                       int S, const int32_t *tokens_out, const float *max_logit_out,
+                       const int32_t *shard_idx_out, const float *shard_val_out);
+int current_device_supported();
+}  // namespace nfq
 
 namespace {
 
@@ -14,11 +24,16 @@ namespace {
 // the 16-byte counter block (128 KiB + 16 B).  Every GPU that loads the
 // library holds this array until the process exits.
 constexpr size_t kNoAllocScratchBytes = 64u * 256u * 8u + 16u;
+static_assert(kNoAllocScratchBytes == nfq::stage2_workspace_bytes_for(nfq::kMaxShards),
+              "the array must hold the workspace of the largest shard count a call accepts");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices];   // device address of the array, per device
+// Device address of the array, per device.  Two host threads making their
+// first call on one device at the same time may both look it up; they store
+// the same value, and the atomic makes that race well defined.
+std::atomic<void *> g_scratch_ptr[kMaxDevices];
 
 // Once per device, with that device current: look up where the array lives.
 // In host code the array's name is only a host-side stand-in, so its device
@@ -26,12 +41,12 @@ void *g_scratch_ptr[kMaxDevices];   // device address of the array, per device
 int scratch_for_current_device(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NFQ_ERR_CUDA;
-  if (!g_scratch_ptr[dev]) {
-    void *ptr = nullptr;
+  void *ptr = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+  if (!ptr) {
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return NFQ_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
+    g_scratch_ptr[dev].store(ptr, std::memory_order_relaxed);
   }
-  *out = g_scratch_ptr[dev];
+  *out = ptr;
   return NFQ_OK;
 }
 
@@ -42,10 +57,15 @@ extern "C" int nfq_lm_head_fp8_argmax_noalloc(const nfq_quant_act *a, const uint
                                               int32_t *tokens_out, float *max_logit_out,
                                               int32_t *shard_idx_out, float *shard_val_out,
                                               void *stream) {
-  if (!a) return NFQ_ERR_NULL;
-  const size_t need = nfq_lm_head_workspace_bytes(a->tokens, S);
-  if (need == 0) return NFQ_ERR_SHAPE;
-  if (need > kNoAllocScratchBytes) return NFQ_ERR_WORKSPACE;
+  // every argument is checked before the shared array is touched, so a
+  // rejected call cannot disturb another call in flight
+  const int chk = nfq::lm_head_check_args(a, w, w_scales, V, S, tokens_out, max_logit_out,
+                                          shard_idx_out, shard_val_out);
+  if (chk != NFQ_OK) return chk;
+  if (a->tokens == 0) return NFQ_OK;
+  const int dv = nfq::current_device_supported();
+  if (dv != NFQ_OK) return dv;
+  const size_t need = nfq_lm_head_workspace_bytes(a->tokens, S);   // S <= 64: fits the array
   void *scratch = nullptr;
   const int st = scratch_for_current_device(&scratch);
   if (st != NFQ_OK) return st;
