@@ -50,7 +50,7 @@ def test_random_shapes_fp8(nfq, seed):
     assert nfq.device_error() == 0
     ref = oracle.reduce_norm_quant(inp["partials"], inp["residual"], inp["norm_w"], w.eps)
     check_stage1(bf16_host(h), c.cpu().numpy(), s.cpu().numpy(), ref)
-    sample = sorted(set([0, T - 1] + list(np.random.default_rng(seed).integers(0, T, 4))))
+    sample = list(range(T))
     check_stage2(t.cpu().numpy(), c.cpu().numpy(), s.cpu().numpy(), qw, sw, S, sample,
                  mx.cpu().numpy(), si.cpu().numpy(), sv.cpu().numpy())
 
@@ -73,7 +73,7 @@ def test_random_shapes_nvfp4(nfq, seed):
            "global_scales": g.cpu().numpy()}
     check_stage1_fp4(bf16_host(h), act["codes"], act["block_scales"], act["global_scales"],
                      ref["hidden"])
-    sample = sorted(set([0, T - 1] + list(np.random.default_rng(seed).integers(0, T, 4))))
+    sample = list(range(T))
     check_stage2_fp4(t.cpu().numpy(), act["codes"], act["block_scales"], act["global_scales"],
                      qw, sw, gw, S, sample, mx.cpu().numpy(), si.cpu().numpy(),
                      sv.cpu().numpy())

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import synth
-from tests._parity import U, abs_dot, bf16_host, check_stage1, to_dev, to_dev_bf16
+from tests._parity import U, abs_dot, bf16_host, check_stage1, oracle_logits, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -67,8 +67,8 @@ def test_unfused_logits_and_argmax(nfq, T, H, V):
     logits = nfq.unfused_lm_head_logits(to_dev(ref["codes"]), to_dev(ref["scales"]), wp, to_dev(sw))
     torch.cuda.synchronize()
     Lg = bf16_host(logits)
-    sample = sorted(set([0, T - 1, T // 2]))
-    L32 = oracle.lm_head_logits(ref["codes"], ref["scales"], qw, sw, tokens=sample)
+    sample = list(range(T))                   # every token's whole logits row
+    L32 = oracle_logits(ref["codes"], ref["scales"], qw, sw, sample)
     Lb = oracle.f32_to_bf16(L32.ravel()).reshape(L32.shape)
     # BF16 of fp32 logits that agree within the summation bound: equal almost
     # everywhere; elsewhere within the fp32 bound plus one BF16 rounding (near
