@@ -9,9 +9,13 @@ FP8 LM head over vocab 151552 in 8 shards with the fused greedy argmax.
 
 Prints one JSON line (rank 0).  `value` is draft tokens/s of K steps run one
 after another on one stream with inputs resident in HBM, timed by CUDA events
-at the two ends; the per-kernel durations behind `norm_quant`, `lm_head` and
-`roofline` come from a second run of the K steps with CUDA events around every
-launch (`instrumented_ms_per_step`).  `e2e` repeats the measurement through the public API
+at the two ends; the K-step run is repeated (`repeats`: by default enough
+repeats for about 0.4 s of timed steps, 5 to 200) and `value` is the median,
+with the spread in `repeats`.  The per-kernel durations behind
+`norm_quant`, `lm_head` and `roofline` come from a further run of the K steps
+with CUDA events around every launch (`instrumented_ms_per_step`);
+`norm_quant.graph_us` times stage 1 alone from a CUDA graph of back-to-back
+launches over the rotating inputs.  `e2e` repeats the measurement through the public API
 with each step's stage-1 inputs copied from pinned host memory (on a copy
 stream, overlapping the previous step's kernels) and its tokens read back.  Each step reads the
 932 MB FP8 LM-head weight (> L2) and a different one of 40 rotating stage-1
@@ -21,9 +25,13 @@ With N > 1 (torchrun) every rank runs the same workload on its own GPU
 (independent replicas, weak scaling; the only collectives are the timing
 barrier and the max over ranks).
 
---impl reference times the CPU oracle instead (rank 0 only): each step is a
-bounded sample (stage 1 on all 64 rows, the LM head for all 64 tokens over 32
-vocab rows), scaled to the whole workload.
+--impl reference times the CPU oracle instead (rank 0 only): each step is the
+whole workload (stage 1 on every row, the LM head for every token over the
+full vocabulary), its independent outputs split over the host's cores.
+
+--stage1-sweep times stage 1 alone from CUDA graphs at T = 1 .. 8192 rows of
+the decode c=64 shape and prints one JSON line with GB/s and the fraction of
+the measured HBM peak per batch size.
 """
 from __future__ import annotations
 
@@ -62,6 +70,11 @@ def parse():
     ap.add_argument("--variant", choices=["fp8", "nvfp4", "unfused"], default="fp8",
                     help="packed FP8 path (default), its NVFP4 form, or the unfused "
                          "reference arm (separate kernels, BF16 logits, full-vocab argmax)")
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="times the K-step run is repeated, value being the median "
+                         "(0: enough repeats for about 0.4 s of timed steps, 5 to 200)")
+    ap.add_argument("--stage1-sweep", action="store_true",
+                    help="stage 1 alone, CUDA-graph timed, at T = 1 .. 8192 (c=64 shape)")
     return ap.parse_args()
 
 
@@ -267,6 +280,34 @@ WORKLOAD_TEXT = {
 }
 
 
+def rotation_sets(w):
+    """Stage-1 input sets rotated over the timed steps (> 2 x L2 in all)."""
+    set_bytes = (w.k + 1) * w.T * w.H * 2
+    return int(min(64, max(2, -(-ROTATION_BYTES // set_bytes)))), set_bytes
+
+
+def bench_config(args, w, world):
+    """The `config` object of the JSON line; both arms print the same one."""
+    fp4 = args.variant == "nvfp4"
+    unfused = args.variant == "unfused"
+    nsets, set_bytes = rotation_sets(w)
+    cfg = {"workload": WORKLOAD_TEXT.get(args.workload, args.workload)
+                       + ("; NVFP4 activation and LM head" if fp4 else
+                          "; unfused reference arm: BF16 all-reduce, add+RMSNorm, "
+                          "quant, BF16 logits, full-vocab argmax" if unfused else ""),
+           "variant": args.variant,
+           "draft_positions_per_step": max(1, args.mtp) if w.V > 0 and not unfused else 1,
+           "l2": f"inputs larger than L2: {nsets} rotating stage-1 input sets "
+                 f"({nsets * set_bytes / 1e6:.0f} MB)"
+                 + (f", {(stage2_bytes_nvfp4(w.T, w.H, w.V) if fp4 else stage2_bytes(w.T, w.H, w.V)) / 1e6:.0f}"
+                    f" MB {'NVFP4' if fp4 else 'FP8'} weight read every step" if w.V > 0 else ""),
+           "parallelism": f"replicas x{world}"}
+    if w.V > 0:
+        cfg["weight_layout"] = ("packed once at load: tile-contiguous, pre-swizzled 16 KB blocks "
+                                "of 128 rows x 128 bytes" + (" + 2 KB block-scale blocks" if fp4 else ""))
+    return cfg
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -290,8 +331,7 @@ def run_ours(args, rank, world, local):
     host_parts = [to_bf16(p).pin_memory() for p in inp["partials"]]
     host_res = to_bf16(inp["residual"]).pin_memory()
     norm_w = to_bf16(inp["norm_w"]).to(dev)
-    set_bytes = (k + 1) * T * H * 2
-    nsets = int(min(64, max(2, -(-ROTATION_BYTES // set_bytes))))
+    nsets, set_bytes = rotation_sets(w)
     sets = [([p.to(dev) for p in host_parts], host_res.to(dev)) for _ in range(nsets)]
     fp4 = args.variant == "nvfp4"
     unfused = args.variant == "unfused"
@@ -405,22 +445,32 @@ def run_ours(args, rank, world, local):
                                     tokens_out=chain_tokens, workspace=ws)
         for i in range(max(1, args.warmup // P)):
             chain(i)
-    barrier()
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_start.record(stream)
-    for i in range(K):
-        if P > 1:
-            chain(i)
-        else:
-            stage1(*sets[i % nsets])
-            if has_lm:
-                stage2()
-    e_end.record(stream)
-    barrier()
-    total_ms = e_start.elapsed_time(e_end)
-    if nfq.device_error() != nfq.NFQ_OK:
-        raise RuntimeError("a kernel reported an expired wait during the timed steps")
+    # the K-step run, repeated: each repeat times exactly K steps between
+    # barriers; the reported value is the median repeat
+    rep_ms = []
+    n_rep = max(1, args.repeats) if args.repeats > 0 else 200
+    while len(rep_ms) < n_rep:
+        barrier()
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        e_start.record(stream)
+        for i in range(K):
+            if P > 1:
+                chain(i)
+            else:
+                stage1(*sets[i % nsets])
+                if has_lm:
+                    stage2()
+        e_end.record(stream)
+        barrier()
+        rep_ms.append(e_start.elapsed_time(e_end))
+        if nfq.device_error() != nfq.NFQ_OK:
+            raise RuntimeError("a kernel reported an expired wait during the timed steps")
+        if args.repeats <= 0 and len(rep_ms) == 1:   # about 0.4 s of timed steps in all
+            n_rep = int(min(200, max(5, -(-400.0 // max(rep_ms[0], 1e-3)))))
+            if world > 1:                            # every rank runs the same count
+                n_rep = int(max_over_ranks([float(n_rep)], world, dev)[0])
+    total_ms = sorted(rep_ms)[len(rep_ms) // 2]
 
     # (2) the same K steps with CUDA events around every launch: per-kernel
     # durations for the roofline
@@ -443,18 +493,19 @@ def run_ours(args, rank, world, local):
     s2_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
 
     # (3) the same steps replayed from one CUDA graph (one step per rotating
-    # input set): the step time without host launch overhead
-    graph_ms = None
-    if P == 1:
+    # input set; with --mtp P one chained P-position step per capture): the
+    # step time without host launch overhead
+    launches_per_step = ((5 if has_lm else 3) if unfused else (2 if has_lm else 1)) * P
+
+    def graph_time(body, n_bodies):
+        """ms per body of a CUDA graph holding n_bodies calls, replayed."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            for i in range(nsets):
-                stage1(*sets[i])
-                if has_lm:
-                    stage2()
+            for j in range(n_bodies):
+                body(j)
         g.replay()
         barrier()
-        reps = max(1, -(-K // nsets))
+        reps = max(3, -(-K // n_bodies))
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
         g0.record(stream)
@@ -462,12 +513,24 @@ def run_ours(args, rank, world, local):
             g.replay()
         g1.record(stream)
         barrier()
-        graph_ms = g0.elapsed_time(g1) / (reps * nsets)
-        gpu_launches_graph = ((5 if has_lm else 3) if unfused else (2 if has_lm else 1)) * reps * nsets
         del g
         if nfq.device_error() != nfq.NFQ_OK:
-            raise RuntimeError("a kernel reported an expired wait in the graph replay")
-    gpu_launches = ((5 if has_lm else 3) if unfused else (2 if has_lm else 1)) * K * P
+            raise RuntimeError("a kernel reported an expired wait in a graph replay")
+        return g0.elapsed_time(g1) / (reps * n_bodies), reps * n_bodies
+
+    def one_step(j):
+        if P > 1:
+            chain(j)
+        else:
+            stage1(*sets[j])
+            if has_lm:
+                stage2()
+    n_graph = nsets if P == 1 else max(1, nsets // P)
+    graph_ms, graph_steps = graph_time(one_step, n_graph)
+    gpu_launches_graph = launches_per_step * graph_steps
+    # stage 1 alone from a graph of back-to-back launches
+    s1_graph_ms, _ = graph_time(lambda j: stage1(*sets[j]), nsets)
+    gpu_launches = launches_per_step * K
 
     # end to end through the public API: every step copies its stage-1 inputs
     # (one pinned host batch holding the k partials and the residual) to the
@@ -545,8 +608,9 @@ def run_ours(args, rank, world, local):
     e2e_ms = (time.perf_counter() - c0) * 1e3
     barrier()
 
-    total_ms, e2e_ms, graph_max = max_over_ranks([total_ms, e2e_ms, graph_ms or 0.0], world, dev)
-    graph_ms = graph_max if graph_ms is not None else None
+    total_ms, e2e_ms, graph_ms, s1_graph_ms = max_over_ranks(
+        [total_ms, e2e_ms, graph_ms, s1_graph_ms], world, dev)
+    rep_ms = max_over_ranks(rep_ms, world, dev)
 
     result = None
     if rank == 0:
@@ -555,6 +619,8 @@ def run_ours(args, rank, world, local):
               stage1_bytes_unfused(T, H, k) if unfused else stage1_bytes(T, H, k))
         gbs1 = b1 / (s1_ms * 1e-3) / 1e9
         value = tokens_per_s(world, T * P, K, total_ms)
+        gbs1g = b1 / (s1_graph_ms * 1e-3) / 1e9
+        rep_steps = sorted(x / K for x in rep_ms)
         result = {
             "metric": METRIC,
             "value": round(value, 1),
@@ -563,6 +629,11 @@ def run_ours(args, rank, world, local):
             "steps": K,
             "warmup": args.warmup,
             "ms_per_step": round(total_ms / K, 5),
+            "repeats": {"n": len(rep_ms), "ms_per_step_median": round(total_ms / K, 5),
+                        "ms_per_step_min": round(rep_steps[0], 5),
+                        "ms_per_step_max": round(rep_steps[-1], 5),
+                        "value_min": round(tokens_per_s(world, T * P, K, rep_steps[-1] * K), 1),
+                        "value_max": round(tokens_per_s(world, T * P, K, rep_steps[0] * K), 1)},
             "draft_positions_per_step": P,
             "instrumented_ms_per_step": round(instrumented_ms / K, 5),
             "higher_is_better": True,
@@ -571,19 +642,11 @@ def run_ours(args, rank, world, local):
             "dtype": ("e2m1 MMA with e4m3 block-16 scales (NVFP4), fp32 accumulate; bf16 in, "
                       "fp32 norm" if fp4 else "e4m3 MMA, fp32 accumulate; bf16 in, fp32 norm"),
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload)
-                                   + ("; NVFP4 activation and LM head" if fp4 else
-                                      "; unfused reference arm: BF16 all-reduce, add+RMSNorm, "
-                                      "quant, BF16 logits, full-vocab argmax" if unfused else ""),
-                       "variant": args.variant,
-                       "l2": f"inputs larger than L2: {nsets} rotating stage-1 input sets "
-                             f"({nsets * set_bytes / 1e6:.0f} MB)"
-                             + (f", {(stage2_bytes_nvfp4(T, H, V) if fp4 else stage2_bytes(T, H, V)) / 1e6:.0f}"
-                                f" MB {'NVFP4' if fp4 else 'FP8'} weight read every step"
-                                if has_lm else ""),
-                       "parallelism": f"replicas x{world}"},
+            "config": bench_config(args, w, world),
             "norm_quant": {"us": round(s1_ms * 1e3, 3), "GB/s": round(gbs1, 1),
                            "frac": round(gbs1 / peak, 4), "bytes": b1,
+                           "graph_us": round(s1_graph_ms * 1e3, 3),
+                           "graph_GB/s": round(gbs1g, 1), "graph_frac": round(gbs1g / peak, 4),
                            "traffic": (ncu_traffic("norm_quant_nvfp4" if fp4 else "norm_quant")
                                        if args.workload == WORKLOAD and not unfused else None)},
             "e2e": {"value": round(tokens_per_s(world, T, e2e_steps, e2e_ms), 1),
@@ -592,19 +655,15 @@ def run_ours(args, rank, world, local):
             "gpu_launches": gpu_launches,
             "clocks": clocks,
         }
-        if graph_ms is not None:
-            result["graph"] = {"ms_per_step": round(graph_ms, 5),
-                               "value": round(tokens_per_s(world, T, 1, graph_ms), 1),
-                               # positive: what host launches cost over a graph replay
-                               "stream_minus_graph_us_per_step": round((total_ms / K - graph_ms) * 1e3, 2),
-                               "gpu_launches": gpu_launches_graph}
+        result["graph"] = {"ms_per_step": round(graph_ms, 5),
+                           "value": round(tokens_per_s(world, T * P, 1, graph_ms), 1),
+                           # positive: what host launches cost over a graph replay
+                           "stream_minus_graph_us_per_step": round((total_ms / K - graph_ms) * 1e3, 2),
+                           "gpu_launches": gpu_launches_graph}
         if has_lm:
             b2 = (stage2_bytes_nvfp4(T, H, V) if fp4 else
                   stage2_bytes_unfused(T, H, V) if unfused else stage2_bytes(T, H, V))
             gbs2 = b2 / (s2_ms * 1e-3) / 1e9
-            result["config"]["weight_layout"] = ("packed once at load: tile-contiguous, "
-                                                 "pre-swizzled 16 KB blocks of 128 rows x 128 bytes"
-                                                 + (" + 2 KB block-scale blocks" if fp4 else ""))
             result["lm_head"] = {"us": round(s2_ms * 1e3, 3), "GB/s": round(gbs2, 1),
                                  "frac": round(gbs2 / peak, 4), "bytes": b2,
                                  "draft_tokens_per_s": round(T / (s2_ms * 1e-3), 1)}
@@ -731,6 +790,10 @@ def cpu_baseline(name, variant="fp8"):
 
 
 def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host's cores over the whole
+    workload every step: stage 1 on every row, then the LM head for every token
+    over the full vocabulary (outputs split over threads, each in its fixed
+    order), so that ms_per_step x steps is the time the arm ran."""
     if rank != 0:
         return None
     import synth
@@ -738,45 +801,119 @@ def run_reference(args, rank, world):
     has_lm = w.V > 0
     fp4 = args.variant == "nvfp4"
     n = oracle_threads()
+    inp = synth.stage1_inputs(w)
     if has_lm:
-        inp = synth.stage1_inputs(w)
-        rows = min(w.V, 32 * n)                   # 32 vocab rows a host thread per step
-        qw, sw, gw = sample_weights(args.workload, max(128, (rows + 127) // 128 * 128), fp4)
-        sample = (f"per step: stage 1 on all {w.T} rows + LM head for all {w.T} tokens over "
-                  f"{rows} vocab rows, scaled to {w.V} rows")
+        qw, sw, gw = sample_weights(args.workload, w.V, fp4)
+        rows, toks = w.V, list(range(w.T))
+        sample = (f"per step: stage 1 on all {w.T} rows + LM head for all {w.T} tokens over all "
+                  f"{w.V} vocab rows")
     else:
-        inp = synth.stage1_inputs(w, rows=[0])
-        rows, qw, sw, gw = 0, None, None, (1.0 if fp4 else None)
-        sample = f"per step: stage 1 on 1 of {w.T} rows, scaled to all rows"
-    toks = list(range(w.T)) if has_lm else None
+        qw = sw = None
+        gw = 1.0 if fp4 else None
+        rows, toks = 0, None
+        sample = f"per step: stage 1 on all {w.T} rows"
     for _ in range(args.warmup):
         oracle_sample(w, inp, qw, sw, rows, toks, threads=n, gw=gw)
     t0 = time.perf_counter()
-    fulls = [oracle_sample(w, inp, qw, sw, rows, toks, threads=n, gw=gw)[1]
-             for _ in range(args.steps)]
+    for _ in range(args.steps):
+        oracle_sample(w, inp, qw, sw, rows, toks, threads=n, gw=gw)
     elapsed = time.perf_counter() - t0
-    full = sum(fulls) / len(fulls)
-    value = w.T / full
+    full = elapsed / max(1, args.steps)
+    value = w.T / full                    # one draft position per step: T tokens
     unit = "draft tokens/s" if has_lm else "tokens/s"
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4),
             "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(full * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp32 (fp64 norm)", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
-                       "variant": args.variant,
-                       "parallelism": "cpu oracle, rank 0"},
+            "config": bench_config(args, w, world),
             "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": n,
                              "kind": "oracle",
                              "sample": f"{sample}; outputs split over {n} host threads; "
-                                       f"{elapsed:.1f} s timed"},
+                                       f"{args.steps} steps in {elapsed:.1f} s"},
             "e2e": {"value": round(value, 4), "unit": unit,
                     "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+SWEEP_T = [1, 16, 64, 128, 256, 512, 1024, 2048, 4096, 8192]
+
+
+def run_stage1_sweep(args, local):
+    """Stage 1 alone at T = 1 .. 8192 rows of the decode c=64 shape (H = 6144,
+    k = 8 partials with the outlier channels), each batch size timed from a
+    CUDA graph of back-to-back launches over rotating input sets (> 2 x L2)."""
+    import numpy as np
+    import torch
+
+    import norm_fp8_quant_gb300 as nfq
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peak, peak_kind = load_peaks()
+    wmax = synth.workload(WORKLOAD, T=max(SWEEP_T))
+    inp = synth.stage1_inputs(wmax)
+    to_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    norm_w = to_bf16(inp["norm_w"]).to(dev)
+    H, k = wmax.H, wmax.k
+    rows = []
+    for T in SWEEP_T:
+        w = synth.workload(WORKLOAD, T=T)
+        nsets, _ = rotation_sets(w)
+        host = [to_bf16(inp["partials"][i, :T]) for i in range(k)] + [to_bf16(inp["residual"][:T])]
+        sets = [[h.to(dev) for h in host] for _ in range(nsets)]
+        hidden = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        codes = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        scales = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
+        calls = [nfq.prepare_reduce_norm_quant(st[:k], st[k], norm_w, w.eps, hidden, codes, scales)
+                 for st in sets]
+        for c in calls[:3]:
+            c()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in calls:
+                c()
+        g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, -(-max(args.steps, 400) // nsets)) if T <= 1024 else max(3, args.steps // 100)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if nfq.device_error() != nfq.NFQ_OK:
+            raise RuntimeError("a kernel reported an expired wait in the stage-1 sweep")
+        us = e0.elapsed_time(e1) * 1e3 / (reps * nsets)
+        gbs = stage1_bytes(T, H, k) / (us * 1e-6) / 1e9
+        plan = nfq.stage1_split_plan(T, H, torch.cuda.get_device_properties(dev).multi_processor_count)
+        rows.append({"T": T, "us": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "kernel": (f"stage1_split_kernel, {plan['ctas_per_row']} CTAs per row, "
+                                f"{plan['vpt']} vectors per thread" if plan["ctas_per_row"]
+                                else "reduce_norm_quant_kernel (persistent)"),
+                     "launches": reps * nsets})
+        del g, calls, sets
+        torch.cuda.empty_cache()
+    reach = [r["T"] for r in rows if r["frac"] >= 0.75]
+    return {"metric": "norm+FP8-quant GB/s by batch size (stage 1 alone, CUDA-graph timed)",
+            "unit": "GB/s", "peak": peak, "peak_source": peak_kind,
+            "config": {"workload": f"decode c=64 shape: H={H}, k={k} BF16 partials N(0,0.5) with "
+                                   "1% outlier channels x20, residual N(0,1); first T rows",
+                       "l2": "inputs larger than L2: rotating input sets (> 280 MB per batch size)"},
+            "rows": rows, "smallest_T_at_frac_0.75": reach[0] if reach else None}
 
 
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.stage1_sweep:
+        from norm_fp8_quant_gb300 import build
+        if rank == 0:
+            build.build()
+            print(json.dumps(run_stage1_sweep(args, local)), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args, rank, world)
         if res is not None:

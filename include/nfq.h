@@ -402,12 +402,22 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   (0 = as many as fit, at most 5; values below 2 or above what fits fall back).
  * nfq_stage1_grid: at most max_ctas CTAs for later stage-1 launches, each then
  *   taking several rows in turn (0 = one CTA per SM at most).
+ * nfq_stage1_split: batches of at most max_tokens rows (-1 = the default
+ *   limit, 0 = no batch) run on the small-batch stage-1 kernel, one row per
+ *   cluster of ctas_per_row CTAs (0 = automatic) with vpt 16-byte vectors per
+ *   thread (0 = automatic); larger batches run on the persistent kernel that
+ *   nfq_stage1_plan describes.  The results are the same bits either way.
+ * nfq_stage1_split_plan: the small-batch plan for (T, H) on num_sms SMs:
+ *   out4 = {CTAs per row (0: the persistent kernel runs), vectors per thread,
+ *   active threads, block threads}.
  */
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7);
 void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot);
 void nfq_lm_head_small_batch(int enabled);
 void nfq_lm_head_nvfp4_tune(int stages);
 void nfq_stage1_grid(int max_ctas);
+void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt);
+int nfq_stage1_split_plan(int T, int H, int num_sms, int *out4);
 
 #ifdef __cplusplus
 }

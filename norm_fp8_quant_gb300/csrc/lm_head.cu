@@ -446,6 +446,7 @@ __global__ void __launch_bounds__(128 * EPI + 64, 1)
 // weight block is fetched from HBM once and served to the second CTA by L2.
 
 constexpr int kSmallMaxT = 128;                 // tokens per token group of the token-major form
+constexpr int kFusedMaxGroups = 64;             // the fused step's rows: H <= 8192
 constexpr int kSmallEpiWarps = 16;
 template <int MT>
 __host__ __device__ constexpr uint32_t small_stage_bytes() { return 2 * kWTileBytes + MT * 128; }
@@ -504,18 +505,15 @@ __device__ bool fused_stage1(const Stage2Params &p, float *red, int *flag,
         }
       }
     }
-    // sum of squares: thread, warp, then the warps holding data in order
-    float ss = 0.0f;
+    // sum of squares in the canonical order of stage1_math.cuh: group sums
+    // (one per 128 channels) in shared memory, then the row total
 #pragma unroll
-    for (int v = 0; v < 2; ++v)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[v][e], x[v][e], ss);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) red[warp] = ss;
+    for (int v = 0; v < 2; ++v) {
+      const float gsv = group_sum16(vec_sumsq(x[v]));     // all lanes (shuffles)
+      if (active && (tc & 15) == 0) red[(v * NA + tc) / 16] = gsv;
+    }
     named_bar_sync(1, kSmallEpiWarps * 32);
-    float tot = 0.0f;
-    for (int q = 0; q < NA / 32; ++q) tot += red[q];
+    const float tot = row_total(red, p.H / 128);
     const float ms = __fdiv_rn(tot, (float)p.H);
     const float rr = __frsqrt_rn(__fadd_rn(ms, s.eps));
     const uint4 *wsrc = static_cast<const uint4 *>(s.norm_w);
@@ -645,7 +643,7 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   grid_launch_dependents();
   if constexpr (kFused) {
     // stage 1 of the step, then the activation scales, by the epilogue warps
-    __shared__ float s1_red[kSmallEpiWarps];
+    __shared__ float s1_red[kFusedMaxGroups];
     __shared__ int s1_flag;
     if (warp < kSmallEpiWarps && fused_stage1(p, s1_red, &s1_flag, abort_flag)) {
       for (int i = (int)threadIdx.x; i < G * MT; i += kSmallEpiWarps * 32) {

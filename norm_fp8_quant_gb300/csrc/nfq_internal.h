@@ -43,6 +43,11 @@ struct Stage1Params {
 cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream);
 void stage1_set_tuning(int cluster, int vpt, int slots, int per_slot);
 void stage1_set_grid(int max_ctas);   // 0: one CTA (cluster) per SM at most
+// Small batches: batches of at most max_tokens rows (-1: the default limit, 0:
+// none) run one row per cluster of ctas_per_row CTAs (0: automatic) with vpt
+// vectors per thread (0: automatic).
+void stage1_set_split(int max_tokens, int ctas_per_row, int vpt);
+int stage1_split_plan(int T, int H, int num_sms, int *out4);
 int stage1_plan(int T, int H, int k, int num_sms, int *out7);
 bool stage1_fp4_supported(int H);
 

@@ -45,10 +45,11 @@ __host__ __device__ constexpr int stage1_max_threads(int vpt) {
   return vpt == 1 ? 1024 : vpt == 2 ? 544 : 288;
 }
 
+constexpr int kMaxGroups = 256;   // 128-channel groups of the widest row (H = 32768)
+
 struct RowSums {
-  float red[2][32];     // per consumer warp, double-buffered by row parity
-  float cl[2][8];       // per cluster rank, double-buffered by row parity
-  float amx[2][32];     // per consumer warp: row maximum |hidden| (NVFP4 form)
+  float gs[2][kMaxGroups];   // per group: sum of squares, double-buffered by row parity
+  float amx[2][32];          // per consumer warp: row maximum |hidden| (NVFP4 form)
 };
 
 template <int VPT, bool kFp4>
@@ -62,9 +63,8 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
   uint8_t *ring = smem;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)p.nslot * slot_bytes);
   uint64_t *empty = full + p.nslot;
-  uint64_t *ss_bar = empty + p.nslot;               // [2], cluster exchange
-  uint64_t *red_bar = ss_bar + 2;                   // [2], consumer warps of this CTA
-  uint64_t *amx_bar = red_bar + 2;                  // [2], row maximum (NVFP4 form)
+  uint64_t *ss_bar = empty + p.nslot;               // [2], the row's group sums (cluster-wide)
+  uint64_t *amx_bar = ss_bar + 2;                   // [2], row maximum (NVFP4 form)
   RowSums *sums = reinterpret_cast<RowSums *>(amx_bar + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sums + 1);
 
@@ -80,10 +80,11 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), (uint32_t)n_cons_warps);
     }
-    mbar_init(smem_u32(&ss_bar[0]), (uint32_t)C);
-    mbar_init(smem_u32(&ss_bar[1]), (uint32_t)C);
-    mbar_init(smem_u32(&red_bar[0]), (uint32_t)n_cons_warps);
-    mbar_init(smem_u32(&red_bar[1]), (uint32_t)n_cons_warps);
+    // one arrival per consumer warp (one CTA), or per 128-channel group of the
+    // row from whichever CTA of the cluster holds it
+    const uint32_t ss_count = C > 1 ? (uint32_t)(p.H / 128) : (uint32_t)n_cons_warps;
+    mbar_init(smem_u32(&ss_bar[0]), ss_count);
+    mbar_init(smem_u32(&ss_bar[1]), ss_count);
     mbar_init(smem_u32(&amx_bar[0]), (uint32_t)n_cons_warps);
     mbar_init(smem_u32(&amx_bar[1]), (uint32_t)n_cons_warps);
     *abort_flag = 0;
@@ -200,41 +201,36 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
       }
       if (!ok) break;
 
-      // sum of squares: thread -> warp -> CTA -> cluster, fixed orders
-      float ss = 0.0f;
-#pragma unroll
-      for (int v = 0; v < VPT; ++v)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(x[v][e], x[v][e], ss);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      // sum of squares in the canonical order (stage1_math.cuh): each group's
+      // leader lane sends the group sum to every CTA of the cluster, and the
+      // row total is formed from all G group sums
       const int par = row_iter & 1;
       const uint32_t pph = (uint32_t)((row_iter >> 1) & 1);
-      if (lane == 0) {
-        sums->red[par][cw] = ss;
-        mbar_arrive(smem_u32(&red_bar[par]));   // release: the store above is visible
-      }
-      __syncwarp();
-      const bool got_red = mbar_wait(smem_u32(&red_bar[par]), pph, abort_flag, p.err,
-                                     kErrBitStage1);
-      if (!__all_sync(0xffffffffu, got_red)) break;
-      float tot = 0.0f;
-      for (int q = 0; q < n_cons_warps; ++q) tot += sums->red[par][q];
-      if (C > 1) {
-        if (tc == 0) {
-          const uint32_t slot_addr = smem_u32(&sums->cl[par][rank]);
-          for (int q = 0; q < C; ++q) {
-            st_remote_f32(slot_addr, (uint32_t)q, tot);
-            mbar_arrive_remote(smem_u32(&ss_bar[par]), (uint32_t)q);
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const float gsv = group_sum16(vec_sumsq(x[v]));   // all lanes (shuffles)
+        if (active && (tc & 15) == 0) {
+          const int g = (col0 + (v * NA + tc) * 8) / 128;
+          if (C > 1) {
+            const uint32_t a = smem_u32(&sums->gs[par][g]);
+            for (int q = 0; q < C; ++q) {
+              st_remote_f32(a, (uint32_t)q, gsv);
+              mbar_arrive_remote(smem_u32(&ss_bar[par]), (uint32_t)q);
+            }
+          } else {
+            sums->gs[par][g] = gsv;
           }
         }
-        __syncwarp();
-        const bool got_cl =
-            mbar_wait<true>(smem_u32(&ss_bar[par]), pph, abort_flag, p.err, kErrBitStage1);
-        if (!__all_sync(0xffffffffu, got_cl)) break;
-        tot = 0.0f;
-        for (int q = 0; q < C; ++q) tot += sums->cl[par][q];
       }
+      // one CTA: the warp's group sums are ordered before lane 0's release
+      // arrival by the warp barrier
+      __syncwarp();
+      if (C == 1 && lane == 0) mbar_arrive(smem_u32(&ss_bar[par]));
+      const bool got_ss =
+          C > 1 ? mbar_wait<true>(smem_u32(&ss_bar[par]), pph, abort_flag, p.err, kErrBitStage1)
+                : mbar_wait(smem_u32(&ss_bar[par]), pph, abort_flag, p.err, kErrBitStage1);
+      if (!__all_sync(0xffffffffu, got_ss)) break;
+      const float tot = row_total(sums->gs[par], p.H / 128);
       const float ms = __fdiv_rn(tot, (float)p.H);
       const float rr = __frsqrt_rn(__fadd_rn(ms, p.eps));
 
@@ -326,6 +322,187 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
   if (C > 1) cluster_sync_all();   // no CTA leaves while a peer may still write to it
 }
 
+// ------------------------------------------------------ small batches --
+//
+// One row per cluster of R CTAs (R = 1: one CTA per row, no cluster); CTA
+// `rank` of the cluster holds E = H / R consecutive channels, E / 8 vectors,
+// VPT per thread (vector j in thread j mod NA, slot j / NA: the 16 vectors of
+// a group in 16 consecutive lanes).  A CTA handles exactly one row slice, so
+// nothing is pipelined across rows: every thread issues all of its 16-byte
+// loads at once (the k partials, the residual and the norm weight; up to NB
+// inputs per batch), and with T * R CTAs spread over the SMs the whole batch
+// is in flight together.  That is what a latency-bound small batch needs: at
+// T = 64 one CTA per row would leave most SMs idle and each of the others
+// streaming a whole row.
+//
+// The CTAs of a cluster exchange the row's group sums through distributed
+// shared memory: each group's leader lane stores its sum into every CTA's
+// gsum[] (after a cluster barrier whose arrive was issued at the start, so
+// that every peer has begun), then one cluster barrier publishes them.  The
+// NVFP4 form repeats that exchange for the row maximum of |hidden|.  No wait
+// is data-dependent: every thread reaches every barrier.
+constexpr int kSplitMaxThreads = 512;
+
+template <int VPT, bool kFp4>
+__global__ void __launch_bounds__(kSplitMaxThreads)
+    stage1_split_kernel(const Stage1Params p) {
+  constexpr int NB = VPT == 1 ? 17 : VPT == 2 ? 9 : 4;   // inputs per batch of loads
+  __shared__ float gsum[kMaxGroups];
+  __shared__ float gmax[kMaxGroups];
+  const int R = p.C;
+  const uint32_t rank = R > 1 ? cluster_ctarank() : 0u;
+  const int r = R > 1 ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int E = p.E, G = p.H / 128, NA = p.n_active;
+  const int col0 = (int)rank * E;
+  const int tc = (int)threadIdx.x;
+  const bool active = tc < NA;
+  if (R > 1) cluster_arrive_relaxed();   // this CTA has started
+  // the previous kernel on the stream may write this one's inputs, or still
+  // read the buffers this one writes
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  const size_t rowv = ((size_t)r * (size_t)p.H + (size_t)col0) / 8u;   // first vector of the slice
+  const uint64_t pol = policy_evict_first();
+  uint4 wpk[VPT];
+  const uint4 *wsrc = static_cast<const uint4 *>(p.norm_w) + col0 / 8;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v)
+    wpk[v] = active ? __ldg(wsrc + v * NA + tc) : make_uint4(0u, 0u, 0u, 0u);
+  float x[VPT][8];
+  for (int i0 = 0; i0 <= p.k; i0 += NB) {
+    uint4 in[NB][VPT];
+#pragma unroll
+    for (int c = 0; c < NB; ++c) {
+      const int i = i0 + c;
+      const uint4 *src =
+          static_cast<const uint4 *>(i < p.k ? p.partials[i < p.k ? i : 0] : p.residual) + rowv;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v)
+        in[c][v] = (active && i <= p.k) ? ld_stream16(src + v * NA + tc, pol)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int c = 0; c < NB; ++c) {
+      const int i = i0 + c;
+      if (i > p.k) break;
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        if (i == 0) unpack_bf16x8(in[c][v], x[v]);
+        else add_bf16x8(x[v], in[c][v]);   // x += input, fp32, in input order
+      }
+    }
+  }
+
+  // the row's sum of squares in the canonical order (stage1_math.cuh)
+  float lead[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) lead[v] = group_sum16(vec_sumsq(x[v]));   // all lanes
+  if (R > 1) cluster_wait();   // every CTA of the cluster has started
+  if (active && (tc & 15) == 0) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int g = (col0 + (v * NA + tc) * 8) / 128;
+      if (R > 1) {
+        for (int q = 0; q < R; ++q) st_remote_f32(smem_u32(&gsum[g]), (uint32_t)q, lead[v]);
+      } else {
+        gsum[g] = lead[v];
+      }
+    }
+  }
+  if (R > 1) cluster_sync_all();
+  else __syncthreads();
+  const float tot = row_total(gsum, G);
+  const float ms = __fdiv_rn(tot, (float)p.H);
+  const float rr = __frsqrt_rn(__fadd_rn(ms, p.eps));
+
+  uint4 *hid = static_cast<uint4 *>(p.hidden) + rowv;
+  if constexpr (kFp4) {
+    // hidden, then the row maximum |hidden| over the cluster (group maxima
+    // exchanged like the sums), then per 16-element block (two adjacent
+    // lanes) the e4m3 block scale and the e2m1 codes
+    float yv[VPT][8];
+    uint32_t hbv[VPT][4];
+    float gm[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      float wv[8];
+      unpack_bf16x8(wpk[v], wv);
+      float am = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const __nv_bfloat162 h2 =
+            __floats2bfloat162_rn(__fmul_rn(__fmul_rn(x[v][e], rr), wv[e]),
+                                  __fmul_rn(__fmul_rn(x[v][e + 1], rr), wv[e + 1]));
+        const uint32_t hu = *reinterpret_cast<const uint32_t *>(&h2);
+        hbv[v][e / 2] = hu;
+        yv[v][e] = __uint_as_float(hu << 16);
+        yv[v][e + 1] = __uint_as_float(hu & 0xFFFF0000u);
+        am = fmaxf(am, fmaxf(fabsf(yv[v][e]), fabsf(yv[v][e + 1])));
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      gm[v] = am;
+    }
+    if (active && (tc & 15) == 0) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const int g = (col0 + (v * NA + tc) * 8) / 128;
+        if (R > 1) {
+          for (int q = 0; q < R; ++q) st_remote_f32(smem_u32(&gmax[g]), (uint32_t)q, gm[v]);
+        } else {
+          gmax[g] = gm[v];
+        }
+      }
+    }
+    if (R > 1) cluster_sync_all();
+    else __syncthreads();
+    const float amax_row = row_max(gmax, G);
+    const float g = __fdiv_rn(amax_row, 2688.0f);     // 448 * 6
+    const float d = __fmul_rn(6.0f, g);
+    uint32_t *cod4 = reinterpret_cast<uint32_t *>(p.codes) + rowv;
+    uint8_t *bsc = p.bscales + ((size_t)r * (size_t)p.H + (size_t)col0) / 16u;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      float ab = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ab = fmaxf(ab, fabsf(yv[v][e]));
+      ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));   // the block's other half
+      const uint32_t sb = (g != 0.0f) ? (uint32_t)(e4m3x2(__fdiv_rn(ab, d), 0.0f) & 0xFFu) : 0u;
+      const float eff = __fmul_rn(e4m3_value(sb), g);
+      uint32_t packed = 0u;
+      if (eff != 0.0f) {
+#pragma unroll
+        for (int e = 0; e < 8; e += 2)
+          packed |= e2m1x2(__fdiv_rn(yv[v][e], eff), __fdiv_rn(yv[v][e + 1], eff)) << (4 * e);
+      }
+      if (active) {
+        const int j = v * NA + tc;
+        hid[j] = make_uint4(hbv[v][0], hbv[v][1], hbv[v][2], hbv[v][3]);
+        cod4[j] = packed;
+        if ((tc & 1) == 0) bsc[j / 2] = (uint8_t)sb;
+      }
+    }
+    if (active && tc == 0 && rank == 0) p.gscales[r] = g;
+  } else {
+    uint2 *cod = reinterpret_cast<uint2 *>(p.codes) + rowv;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      uint4 hv;
+      uint2 cv;
+      float scale;
+      fp8_vector_epilogue(x[v], wpk[v], rr, hv, cv, scale);   // all lanes (group shuffles)
+      if (active) {
+        const int j = v * NA + tc;
+        hid[j] = hv;
+        cod[j] = cv;
+        if ((tc & 15) == 0)
+          p.scales[(size_t)r * (size_t)G + (size_t)((col0 + j * 8) / 128)] = scale;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------- host --
@@ -338,6 +515,111 @@ struct Stage1Choice {
 };
 
 int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0, g_tune_per_slot = 0, g_tune_ctas = 0;
+
+// ---- small batches: which rows go to stage1_split_kernel, and its shape --
+
+constexpr int kSplitDefaultMaxT = 512;   // largest batch run by the small-batch kernel
+int g_split_max_T = -1;                  // tuning: -1 automatic, 0 never, else the limit
+int g_split_R = 0, g_split_vpt = 0;      // tuning: 0 automatic
+
+struct SplitChoice {
+  int R, VPT, NA, threads;
+};
+
+// R CTAs per row and VPT vectors per thread: whole groups per CTA, whole
+// 16-lane groups per vector slot, at most kSplitMaxThreads threads.
+bool split_shape(int G, int R, int vpt, SplitChoice &c) {
+  if (R < 1 || R > 8 || G % R != 0) return false;
+  const int gc = G / R;
+  if (gc % vpt != 0) return false;
+  const int na = 16 * gc / vpt;
+  const int threads = (na + 31) / 32 * 32;
+  if (threads > kSplitMaxThreads) return false;
+  c = SplitChoice{R, vpt, na, threads};
+  return true;
+}
+
+// R = 0 when the batch goes to the persistent kernel.  The defaults follow a
+// CUDA-graph sweep on GB300 (H = 6144 and 7168, k = 8):
+//  - T <= 24: one vector per thread, the smallest R with T * R >= 64 (or the
+//    largest R): at T = 1 eight CTAs per row take 2.8 us against 3.5 us for one;
+//  - T <= 96: one vector per thread, the smallest R with T * R >= 256 (T = 64:
+//    R = 4, 4.4 us; one CTA per row with two vectors per thread: 4.5 us);
+//  - T <= 160: one CTA per row, two vectors per thread (T = 128: 5.6 us);
+//  - T <= 512: one CTA per row, four vectors per thread, so that two CTAs fit
+//    on an SM (T = 256: 9.2 us, the persistent kernel 10.5 us);
+//  - above: the persistent kernel (T = 1024: 29.0 us against 30.0 us).
+// A shape the width does not allow falls back to the next vectors-per-thread
+// choice, then to the next R.
+SplitChoice choose_split(int T, int H, int num_sms) {
+  (void)num_sms;
+  SplitChoice none{0, 0, 0, 0};
+  const int max_T = g_split_max_T >= 0 ? g_split_max_T : kSplitDefaultMaxT;
+  if (T < 1 || T > max_T) return none;
+  const int G = H / 128;
+  int target;   // CTAs the batch should reach
+  int order[3];
+  if (T <= 24) {
+    target = 64; order[0] = 1; order[1] = 2; order[2] = 4;
+  } else if (T <= 96) {
+    target = 256; order[0] = 1; order[1] = 2; order[2] = 4;
+  } else if (T <= 160) {
+    target = 1; order[0] = 2; order[1] = 1; order[2] = 4;
+  } else {
+    target = 1; order[0] = 4; order[1] = 2; order[2] = 1;
+  }
+  SplitChoice best = none;
+  for (int R = 1; R <= 8; ++R) {
+    if (g_split_R > 0 && R != g_split_R) continue;
+    SplitChoice c = none;
+    for (int v : order) {
+      if (g_split_vpt > 0 && v != g_split_vpt) continue;
+      if (split_shape(G, R, v, c)) break;
+      c = none;
+    }
+    if (!c.R) continue;
+    best = c;
+    if ((long)T * R >= target) break;
+  }
+  return best;
+}
+
+template <int VPT>
+cudaError_t launch_split_vpt(const Stage1Params &p, const SplitChoice &c, cudaStream_t stream) {
+  auto kern = p.fp4 ? stage1_split_kernel<VPT, true> : stage1_split_kernel<VPT, false>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.T * c.R));
+  cfg.blockDim = dim3((unsigned)c.threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (c.R > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = (unsigned)c.R;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_split(Stage1Params p, const SplitChoice &c, cudaStream_t stream) {
+  p.C = c.R;
+  p.E = p.H / c.R;
+  p.n_active = c.NA;
+  switch (c.VPT) {
+    case 1: return launch_split_vpt<1>(p, c, stream);
+    case 2: return launch_split_vpt<2>(p, c, stream);
+    case 4: return launch_split_vpt<4>(p, c, stream);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
 
 size_t stage1_smem_bytes(int nslot, int per_slot, int E) {
   return (size_t)nslot * (size_t)per_slot * (size_t)E * 2u + (size_t)nslot * 16u + 48u +
@@ -465,7 +747,24 @@ bool stage1_fp4_supported(int H) {
   return H % 256 == 0 && H >= 256 && H <= 16384 && choose_stage1(1, H, 1, 1, true).VPT != 0;
 }
 
+void stage1_set_split(int max_tokens, int ctas_per_row, int vpt) {
+  g_split_max_T = max_tokens;
+  g_split_R = ctas_per_row;
+  g_split_vpt = vpt;
+}
+
+int stage1_split_plan(int T, int H, int num_sms, int *out4) {
+  const SplitChoice c = choose_split(T, H, num_sms);
+  out4[0] = c.R;
+  out4[1] = c.VPT;
+  out4[2] = c.NA;
+  out4[3] = c.threads;
+  return 0;
+}
+
 cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream) {
+  const SplitChoice sc = choose_split(p.T, p.H, num_sms);
+  if (sc.R > 0) return launch_split(p, sc, stream);
   Stage1Choice ch = choose_stage1(p.T, p.H, p.k, num_sms, p.fp4 != 0);
   if (ch.VPT == 0) return cudaErrorInvalidConfiguration;
   p.C = ch.C;

@@ -144,6 +144,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+// 16-byte global load through the non-coherent path, not kept in L1, with an
+// L2 eviction policy.  Only for data no kernel writes while this one runs.
+__device__ __forceinline__ uint4 ld_stream16(const void *p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -248,6 +258,16 @@ __device__ __forceinline__ uint32_t nclusters_x() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
   return r;
+}
+
+// Split cluster barrier: arrive early (relaxed: orders nothing), wait later
+// (acquire).  Every thread of every CTA of the cluster executes both.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {

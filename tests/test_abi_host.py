@@ -110,6 +110,51 @@ def test_stage1_plans_cover_the_workload_shapes(lib):
         assert p["threads"] <= 1024 and p["smem"] <= 227 * 1024
 
 
+def _split_valid(G, r, u):
+    return G % r == 0 and (G // r) % u == 0 and -(-(16 * (G // r) // u) // 32) * 32 <= 512
+
+
+def test_stage1_split_plans(lib):
+    """The small-batch kernel: whole groups per CTA, whole 16-lane groups per
+    vector slot, at most 512 threads; R and vectors per thread by batch size
+    as documented (T <= 24: T*R >= 64, one vector; T <= 96: T*R >= 256, one
+    vector; T <= 160: R = 1, two vectors; T <= 512: R = 1, four vectors);
+    larger batches go to the persistent kernel (R = 0)."""
+    for (T, H) in [(1, 7168), (4, 1024), (16, 6144), (64, 6144), (64, 7168), (128, 6144),
+                   (256, 6144), (300, 7168), (3, 128), (2, 16384), (1, 32768), (17, 896),
+                   (512, 2048)]:
+        p = nfq.stage1_split_plan(T, H, 152)
+        G = H // 128
+        R, v = p["ctas_per_row"], p["vpt"]
+        assert R >= 1 and _split_valid(G, R, v), (T, H)
+        assert p["active_threads"] == 16 * (G // R) // v and p["threads"] <= 512
+        target, order = ((64, (1, 2, 4)) if T <= 24 else (256, (1, 2, 4)) if T <= 96 else
+                         (1, (2, 1, 4)) if T <= 160 else (1, (4, 2, 1)))
+        want = None
+        for r in range(1, 9):
+            u = next((u for u in order if _split_valid(G, r, u)), None)
+            if u is None:
+                continue
+            want = (r, u)
+            if T * r >= target:
+                break
+        assert (R, v) == want, (T, H, R, v, want)
+    assert nfq.stage1_split_plan(64, 6144, 152)["ctas_per_row"] == 4
+    assert nfq.stage1_split_plan(513, 6144, 152)["ctas_per_row"] == 0
+    assert nfq.stage1_split_plan(8192, 7168, 152)["ctas_per_row"] == 0
+    nfq.stage1_split(0)
+    try:
+        assert nfq.stage1_split_plan(64, 6144, 152)["ctas_per_row"] == 0
+    finally:
+        nfq.stage1_split()
+    nfq.stage1_split(-1, 4, 2)
+    try:
+        p = nfq.stage1_split_plan(64, 6144, 152)
+        assert (p["ctas_per_row"], p["vpt"], p["threads"]) == (4, 2, 96)
+    finally:
+        nfq.stage1_split()
+
+
 def test_chain_argument_validation(lib):
     import ctypes as C
     q = nfq.QuantAct(FAKE, FAKE, 4, 1024, 128)

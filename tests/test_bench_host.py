@@ -60,3 +60,24 @@ def test_traffic_hash_ignores_comments_only():
     assert bench.strip_comments(src.replace("a = 1", "a = 2")) != code
     assert bench.strip_comments('s = "a\\"/*b*/"; /* c */') == 's = "a\\"/*b*/";'
 
+
+
+def test_reference_arm_times_the_whole_workload_and_shares_the_config():
+    """The reference arm (the oracle on the host's cores) computes the whole
+    workload every step, so ms_per_step x steps is time it actually ran, and it
+    prints the same config object as the GPU arm."""
+    import argparse
+    import time
+
+    import synth
+    args = argparse.Namespace(workload="tiny", variant="fp8", steps=2, warmup=1, mtp=1)
+    t0 = time.perf_counter()
+    r = bench.run_reference(args, 0, 1)
+    wall = time.perf_counter() - t0
+    w = synth.workload("tiny")
+    assert r["impl"] == "reference" and r["steps"] == 2
+    assert r["config"] == bench.bench_config(args, w, 1)
+    assert set(r["config"]) >= {"workload", "variant", "l2", "parallelism", "weight_layout"}
+    assert r["ms_per_step"] * r["steps"] <= wall * 1e3
+    assert r["value"] == pytest.approx(w.T / (r["ms_per_step"] * 1e-3), rel=1e-3)
+    assert "all 4096 vocab rows" in r["cpu_baseline"]["sample"]

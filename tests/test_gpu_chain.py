@@ -113,3 +113,69 @@ def test_nvfp4_chain_matches_oracle(nfq, name, P):
         act = oracle.nvfp4_quant(gh[p])
         check_stage2_fp4(toks[p], act["codes"], act["block_scales"], act["global_scales"], qw, sw,
                          gw, w.S, sample)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_chain_under_one_cuda_graph(nfq, fmt):
+    """Five chained draft positions captured in one CUDA graph: every replay
+    gives the bytes of the eager chain (tokens, every position's hidden, the
+    activation), the argmax workspace returns to zero, and every link matches
+    the oracle fed the previous link's hidden."""
+    from tests._parity import check_stage2_fp4
+    P = 5
+    w = synth.workload("decode_c64", V=32768, S=8)
+    base = synth.stage1_inputs(w)
+    pos = [synth.stage1_inputs(synth.workload("decode_c64", seed=p + 1))["partials"] for p in range(P)]
+    parts = [[to_dev_bf16(x) for x in part] for part in pos]
+    res0, nw = to_dev_bf16(base["residual"]), to_dev_bf16(base["norm_w"])
+    T, H = w.T, w.H
+    hidden = [torch.empty((T, H), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    toks = torch.empty((P, T), dtype=torch.int32, device="cuda")
+    ws = nfq.lm_head_workspace(T, w.S, "cuda")
+    if fmt == "fp8":
+        qw, sw = synth.lm_head_weights(w)
+        wp, swd = nfq.pack_lm_head_weights(to_dev(qw)), to_dev(sw)
+        codes = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+        scales = torch.empty((T, H // 128), dtype=torch.float32, device="cuda")
+        act = (codes, scales)
+        run = lambda: nfq.mtp_draft_chain(parts, res0, nw, wp, swd, w.S, w.eps, hidden_bufs=hidden,
+                                          codes=codes, scales=scales, tokens_out=toks, workspace=ws)
+    else:
+        qw, sw, gw = synth.lm_head_weights_nvfp4(w)
+        wp = nfq.pack_lm_head_weights_nvfp4(to_dev(qw), to_dev(sw), gw)
+        codes = torch.empty((T, H // 2), dtype=torch.uint8, device="cuda")
+        bs = torch.empty((T, H // 16), dtype=torch.uint8, device="cuda")
+        gs = torch.empty(T, dtype=torch.float32, device="cuda")
+        act = (codes, bs, gs)
+        run = lambda: nfq.mtp_draft_chain_nvfp4(parts, res0, nw, wp, w.S, w.eps, hidden_bufs=hidden,
+                                                codes=codes, block_scales=bs, row_scales=gs,
+                                                tokens_out=toks, workspace=ws)
+    outs = [toks, *hidden, *act]
+    run()
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    eager = [o.clone() for o in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        for o in outs:
+            o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert nfq.device_error() == 0
+        assert torch.count_nonzero(ws).item() == 0
+        for a, b in zip(eager, outs):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    tk = toks.cpu().numpy()
+    gh = [bf16_host(h) for h in hidden]
+    for p in range(P):
+        res = base["residual"] if p == 0 else gh[p - 1]
+        ref = oracle.reduce_norm_quant(pos[p], res, base["norm_w"], w.eps)
+        _hidden_within_one_ulp(gh[p], ref["hidden"])
+        if fmt == "fp8":
+            check_stage2(tk[p], ref["codes"], ref["scales"], qw, sw, w.S, list(range(T)))
+        else:
+            a = oracle.nvfp4_quant(gh[p])
+            check_stage2_fp4(tk[p], a["codes"], a["block_scales"], a["global_scales"], qw, sw, gw,
+                             w.S, list(range(T)))

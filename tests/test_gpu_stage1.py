@@ -133,3 +133,75 @@ def test_stage1_row_ranges_compose(nfq, cuts):
     assert torch.equal(hid.view(torch.int16), whole[0].view(torch.int16))
     assert torch.equal(cod, whole[1]) and torch.equal(sca, whole[2])
     check_stage1(bf16_host(hid), cod.cpu().numpy(), sca.cpu().numpy(), run_oracle(inp))
+
+
+def _stage1_bytes(nfq, parts, res, nw, fp4=False):
+    if fp4:
+        out = nfq.mtp_reduce_norm_quant_nvfp4(parts, res, nw)
+    else:
+        out = nfq.mtp_reduce_norm_quant(parts, res, nw)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    return [o.view(torch.uint8).cpu().numpy() if o.dtype != torch.float32 else
+            o.cpu().numpy().view(np.uint32) for o in out]
+
+
+@pytest.mark.parametrize("fp4", [False, True])
+@pytest.mark.parametrize("T,H,k", [(64, 6144, 8), (1, 7168, 8), (256, 6144, 4), (5, 1024, 3),
+                                   (2, 16384, 2), (300, 2048, 5)])
+def test_stage1_kernels_and_shapes_give_the_same_bits(nfq, fp4, T, H, k):
+    """The small-batch kernel (every valid CTAs-per-row and vectors-per-thread
+    shape) and the persistent kernel take the row's sum of squares in one
+    order, so they return the same bytes; all of them match the oracle."""
+    w = synth.workload("tiny", T=T, H=H, k=k, seed=T + H + k)
+    inp = synth.stage1_inputs(w)
+    parts = [to_dev_bf16(p) for p in inp["partials"]]
+    res, nw = to_dev_bf16(inp["residual"]), to_dev_bf16(inp["norm_w"])
+    G = H // 128
+    try:
+        nfq.stage1_split(0)                       # the persistent kernel
+        base = _stage1_bytes(nfq, parts, res, nw, fp4)
+        shapes = [(R, v) for R in range(1, 9) for v in (1, 2, 4)
+                  if G % R == 0 and (G // R) % v == 0 and -(-(16 * (G // R) // v) // 32) * 32 <= 512]
+        assert shapes
+        for R, v in shapes:
+            nfq.stage1_split(1 << 20, R, v)
+            got = _stage1_bytes(nfq, parts, res, nw, fp4)
+            for a, b in zip(base, got):
+                assert np.array_equal(a, b), (R, v)
+    finally:
+        nfq.stage1_split()
+    ref = run_oracle(inp)
+    if fp4:
+        from tests._parity import check_stage1_fp4
+        hid = base[0].view(np.uint16).reshape(T, H)
+        check_stage1_fp4(hid, base[1].reshape(T, H // 2), base[2].reshape(T, H // 16),
+                         base[3].view(np.float32), ref["hidden"])
+    else:
+        check_stage1(base[0].view(np.uint16).reshape(T, H), base[1].reshape(T, H),
+                     base[2].view(np.float32).reshape(T, G), ref)
+
+
+def test_stage1_wide_row_persistent_cluster(nfq):
+    """H = 32768 with more rows than the small-batch limit: the persistent
+    kernel splits each row over a two-CTA cluster and exchanges the group sums
+    through distributed shared memory; same bytes as the small-batch kernel."""
+    w = synth.workload("tiny", T=600, H=32768, k=2, seed=31)
+    inp = synth.stage1_inputs(w)
+    parts = [to_dev_bf16(p) for p in inp["partials"]]
+    res, nw = to_dev_bf16(inp["residual"]), to_dev_bf16(inp["norm_w"])
+    assert nfq.stage1_plan(600, 32768, 2)["cluster"] == 2
+    persistent = _stage1_bytes(nfq, parts, res, nw)
+    try:
+        nfq.stage1_split(1 << 20)
+        split = _stage1_bytes(nfq, parts, res, nw)
+    finally:
+        nfq.stage1_split()
+    for a, b in zip(persistent, split):
+        assert np.array_equal(a, b)
+    rows = [0, 1, 299, 598, 599]
+    sub = synth.stage1_inputs(w, rows=rows)
+    h = persistent[0].view(np.uint16).reshape(600, 32768)
+    c = persistent[1].reshape(600, 32768)
+    s = persistent[2].view(np.float32).reshape(600, 256)
+    check_stage1(h[rows], c[rows], s[rows], run_oracle(sub))
