@@ -75,6 +75,8 @@ def parse():
                          "(0: enough repeats for about 0.4 s of timed steps, 5 to 200)")
     ap.add_argument("--stage1-sweep", action="store_true",
                     help="stage 1 alone, CUDA-graph timed, at T = 1 .. 8192 (c=64 shape)")
+    ap.add_argument("--probe-mma", action="store_true",
+                    help="FP8 tcgen05 MMA rate from shared memory (the tensor roofline)")
     return ap.parse_args()
 
 
@@ -678,7 +680,7 @@ def run_ours(args, rank, world, local):
                                              "lm_head_small_kernel (BF16 logits) + "
                                              "unfused_argmax_kernel" if unfused else
                                              "lm_head_small_kernel" if T <= 128 else
-                                             "lm_head_small_kernel, two token groups"
+                                             "lm_head_pair_kernel (CTA pairs, cta_group::2)"
                                              if T <= 256 else
                                              f"lm_head_small_kernel x {(T + 255) // 256}"),
                                   "peak_source": peak_kind}
@@ -905,9 +907,76 @@ def run_stage1_sweep(args, local):
             "rows": rows, "smallest_T_at_frac_0.75": reach[0] if reach else None}
 
 
+def run_probe_mma(args, local):
+    """The FP8 dense tensor rate on this GPU: every SM (or SM pair) issuing
+    back-to-back tcgen05.mma kind::f8f6f4 from shared memory in the LM head's
+    shapes, timed with CUDA events (the measurement kernel of nfq_probe_fp8_mma)."""
+    import torch
+
+    import norm_fp8_quant_gb300 as nfq
+
+    torch.cuda.set_device(local)
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    rows = []
+    for pair in (False, True):
+        ctas = sms // 2 if pair else sms
+        iters = 2048
+        for _ in range(3):
+            nfq.probe_fp8_mma(pair, ctas, iters)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n = max(5, min(50, args.steps))
+        flops = 0.0
+        e0.record()
+        for _ in range(n):
+            flops += nfq.probe_fp8_mma(pair, ctas, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        if nfq.device_error() != nfq.NFQ_OK:
+            raise RuntimeError("the MMA probe reported an expired wait")
+        ms = e0.elapsed_time(e1)
+        mma_ns = ms * 1e6 / (n * iters * 4)
+        rows.append({"shape": ("cta_group::2, M=256 x N=256 x K=32 per CTA pair" if pair else
+                               "cta_group::1, M=128 x N=256 x K=32 per CTA"),
+                     "ctas": 2 * ctas if pair else ctas, "launches": n,
+                     "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
+                     "ns_per_mma": round(mma_ns, 2)})
+    tmem = []
+    for batched in (False, True):
+        iters = 4096
+        for _ in range(3):
+            nfq.probe_tmem_ld(batched, sms, iters)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n = max(5, min(50, args.steps))
+        nbytes = 0.0
+        e0.record()
+        for _ in range(n):
+            nbytes += nfq.probe_tmem_ld(batched, sms, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        tmem.append({"pattern": ("four 16-column loads, one wait" if batched else
+                                 "16-column loads, a wait after each (the LM head epilogue)"),
+                     "ctas": sms, "launches": n,
+                     "TB/s": round(nbytes / (ms * 1e-3) / 1e12, 2)})
+    return {"metric": "FP8 dense tensor rate (tcgen05.mma kind::f8f6f4 from shared memory)",
+            "unit": "TFLOP/s", "rows": rows, "tmem_read": tmem,
+            "config": {"workload": "every SM issues 2048 K blocks of four back-to-back MMAs into "
+                                   "one TMEM accumulator from zeroed shared-memory tiles"}}
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.probe_mma:
+        from norm_fp8_quant_gb300 import build
+        if rank == 0:
+            build.build()
+            print(json.dumps(run_probe_mma(args, local)), flush=True)
+        return
     if args.stage1_sweep:
         from norm_fp8_quant_gb300 import build
         if rank == 0:

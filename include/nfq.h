@@ -396,8 +396,12 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   inputs per slot of later stage-1 launches (0 = automatic; invalid choices
  *   fall back).
  * nfq_lm_head_small_batch: 1 (default) runs the FP8 LM head on the token-major
- *   kernel (up to 256 tokens per launch, as two 128-token groups above 128);
- *   0 forces the weight-major kernel for every batch size.
+ *   kernels (up to 256 tokens per launch); 0 forces the weight-major kernel for
+ *   every batch size.
+ * nfq_lm_head_pair: 1 (default) runs 129..256 tokens on CTA pairs that issue
+ *   cta_group::2 MMAs (M = 256 tokens, each CTA holding half of the weight
+ *   tile); 0 runs them as two independent 128-token groups over one weight
+ *   stream.  The results are the same either way.
  * nfq_lm_head_nvfp4_tune: pipeline stages of later NVFP4 LM-head launches
  *   (0 = as many as fit, at most 5; values below 2 or above what fits fall back).
  * nfq_stage1_grid: at most max_ctas CTAs for later stage-1 launches, each then
@@ -407,6 +411,19 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   cluster of ctas_per_row CTAs (0 = automatic) with vpt 16-byte vectors per
  *   thread (0 = automatic); larger batches run on the persistent kernel that
  *   nfq_stage1_plan describes.  The results are the same bits either way.
+ * nfq_probe_fp8_mma: a measurement kernel, not part of the path.  `ctas`
+ *   CTAs (pair != 0: `ctas` CTA pairs issuing cta_group::2 MMAs) each issue
+ *   `iters` K blocks of four back-to-back tcgen05.mma kind::f8f6f4 from zeroed
+ *   shared-memory tiles, M = 128 (pairs: 256) x N = 256 x K = 32 each, into
+ *   TMEM; 2 * M * 256 * 128 * iters flops per CTA (per pair).  Asynchronous on
+ *   `stream`; time it with events.  NFQ_ERR_SHAPE for ctas outside 1..4096 or
+ *   iters outside 1..2^20.
+ * nfq_probe_tmem_ld: a measurement kernel, not part of the path.  `ctas` CTAs
+ *   of 16 warps each read a 128-lane x 256-column TMEM accumulator into
+ *   registers `iters` times, in the LM head epilogue's pattern (each warp 32
+ *   lanes x 64 columns as four 16-column loads; batched != 0: one wait for
+ *   the four instead of one each): 128 KiB per CTA per iteration.
+ *   Asynchronous on `stream`; NFQ_ERR_SHAPE as for nfq_probe_fp8_mma.
  * nfq_stage1_split_plan: the small-batch plan for (T, H) on num_sms SMs:
  *   out4 = {CTAs per row (0: the persistent kernel runs), vectors per thread,
  *   active threads, block threads}.
@@ -414,9 +431,12 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7);
 void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot);
 void nfq_lm_head_small_batch(int enabled);
+void nfq_lm_head_pair(int enabled);
 void nfq_lm_head_nvfp4_tune(int stages);
 void nfq_stage1_grid(int max_ctas);
 void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt);
+int nfq_probe_fp8_mma(int pair, int ctas, int iters, void *stream);
+int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_stage1_split_plan(int T, int H, int num_sms, int *out4);
 
 #ifdef __cplusplus

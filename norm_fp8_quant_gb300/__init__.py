@@ -100,6 +100,12 @@ def load(path: str = LIB_PATH):
     lib.nfq_stage1_tune.restype = None
     lib.nfq_lm_head_small_batch.argtypes = [ctypes.c_int]
     lib.nfq_lm_head_small_batch.restype = None
+    lib.nfq_lm_head_pair.argtypes = [ctypes.c_int]
+    lib.nfq_lm_head_pair.restype = None
+    lib.nfq_probe_fp8_mma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_probe_fp8_mma.restype = ctypes.c_int
+    lib.nfq_probe_tmem_ld.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_probe_tmem_ld.restype = ctypes.c_int
     lib.nfq_mtp_reduce_norm_quant_nvfp4.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
                                                     ctypes.c_int, ctypes.c_int, _P,
                                                     ctypes.POINTER(Fp4Act), _P]
@@ -381,6 +387,34 @@ def lm_head_small_batch(enabled: bool = True):
     """Choose the FP8 LM-head kernel family: the token-major kernel (default;
     up to 256 tokens per launch) or the weight-major kernel."""
     load().nfq_lm_head_small_batch(1 if enabled else 0)
+
+
+def probe_fp8_mma(pair: bool, ctas: int, iters: int, stream=None):
+    """Launch the FP8 MMA-rate measurement kernel (not part of the path):
+    `ctas` CTAs (or CTA pairs) each issuing `iters` K blocks of four MMAs.
+    Returns the flops the launch performs."""
+    import torch
+    dev = torch.cuda.current_device()
+    _check(_on_device(dev, load().nfq_probe_fp8_mma, 1 if pair else 0, ctas, iters,
+                      _raw_stream(dev, stream)), "nfq_probe_fp8_mma")
+    M = 256 if pair else 128
+    return 2.0 * M * 256 * 128 * iters * ctas
+
+
+def probe_tmem_ld(batched: bool, ctas: int, iters: int, stream=None):
+    """Launch the TMEM read-rate measurement kernel (not part of the path).
+    Returns the bytes the launch reads from TMEM."""
+    import torch
+    dev = torch.cuda.current_device()
+    _check(_on_device(dev, load().nfq_probe_tmem_ld, 1 if batched else 0, ctas, iters,
+                      _raw_stream(dev, stream)), "nfq_probe_tmem_ld")
+    return 128.0 * 256 * 4 * iters * ctas
+
+
+def lm_head_pair(enabled: bool = True):
+    """129..256 tokens: CTA pairs with cta_group::2 MMAs (default) or two
+    independent 128-token groups."""
+    load().nfq_lm_head_pair(1 if enabled else 0)
 
 
 # ------------------------------------------------------------ NVFP4 form --

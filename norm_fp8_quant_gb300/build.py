@@ -10,8 +10,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libnfq.so")
-SOURCES = ["abi.cu", "norm_quant.cu", "lm_head.cu", "lm_head_fp4.cu", "unfused.cu", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "nfq_internal.h", "lm_head_common.cuh"]
+SOURCES = ["abi.cu", "norm_quant.cu", "lm_head.cu", "lm_head_fp4.cu", "unfused.cu", "noalloc.cu",
+           "probe.cu"]
+HEADERS = ["ptx.cuh", "nfq_internal.h", "lm_head_common.cuh", "stage1_math.cuh"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo",
               "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", os.path.join(ROOT, "include")]

@@ -663,4 +663,27 @@ void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot) {
 // small-batch kernel, 0 the weight-major kernel used for larger batches.
 void nfq_lm_head_small_batch(int enabled) { stage2_set_small(enabled); }
 
+int nfq_probe_fp8_mma(int pair, int ctas, int iters, void *stream) {
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20)) return NFQ_ERR_SHAPE;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_probe_fp8_mma(pair ? 1 : 0, ctas, iters, d->err,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream) {
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20)) return NFQ_ERR_SHAPE;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(
+      launch_probe_tmem_ld(batched ? 1 : 0, ctas, iters, static_cast<cudaStream_t>(stream)));
+}
+
+// Selects the form of the token-major FP8 LM head for 129..256 tokens: 1
+// (default) CTA pairs issuing cta_group::2 MMAs, 0 two independent 128-token
+// groups over one weight stream.
+void nfq_lm_head_pair(int enabled) { stage2_set_pair(enabled); }
+
 }  // extern "C"

@@ -507,10 +507,12 @@ __device__ bool fused_stage1(const Stage2Params &p, float *red, int *flag,
     }
     // sum of squares in the canonical order of stage1_math.cuh: group sums
     // (one per 128 channels) in shared memory, then the row total
+    float gsv[2];
 #pragma unroll
-    for (int v = 0; v < 2; ++v) {
-      const float gsv = group_sum16(vec_sumsq(x[v]));     // all lanes (shuffles)
-      if (active && (tc & 15) == 0) red[(v * NA + tc) / 16] = gsv;
+    for (int v = 0; v < 2; ++v) gsv[v] = group_sum16(vec_sumsq(x[v]));   // all lanes (shuffles)
+    if (active && (tc & 15) == 0) {
+#pragma unroll
+      for (int v = 0; v < 2; ++v) red[(v * NA + tc) / 16] = gsv[v];
     }
     named_bar_sync(1, kSmallEpiWarps * 32);
     const float tot = row_total(red, p.H / 128);
@@ -948,6 +950,344 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
   if constexpr (!kLogits) finish_launch(p, &sh->last);
 }
 
+// ------------------------------------------------ CTA pairs, 129..256 tokens --
+//
+// Batches of 129..256 tokens run on CTA pairs (clusters of two) with
+// cta_group::2 MMAs of M = 256 tokens: the even CTA holds tokens 0..127 and
+// the odd one tokens 128.. as the A operand, and each holds HALF of the tile's
+// weight rows as the B operand (block blk0 + rank of a two-block tile, or rows
+// 64*rank.. of a one-block tile).  The even CTA's single MMA thread issues the
+// MMAs; each CTA's TMEM receives its 128 tokens x the tile's 256 columns.
+// Against two independent 128-token CTAs streaming the same weight, a stage
+// moves 32 KB per CTA through shared memory instead of 48 KB (and the MMAs
+// read 32 KB instead of 48 KB), which is what bounds that form.
+//
+// Hand-offs between the two CTAs:
+//  - both CTAs' tensor copies of a stage complete on the EVEN CTA's full
+//    barrier (cta_group::2 copies may signal the peer's barrier); the even
+//    producer's arrive.expect_tx carries the stage's bytes of both CTAs;
+//  - the MMA commits arrive, multicast, on both CTAs' empty (stage reusable)
+//    and tfull (accumulator ready) barriers;
+//  - both CTAs' epilogue warps arrive on the even CTA's tempty barriers.
+// A cluster barrier after the set-up (barriers initialised, TMEM allocated)
+// and one before the teardown (every MMA, copy and remote arrival done) bound
+// every cross-CTA access.  The barriers carry no generic-memory data between
+// the CTAs (copies and MMAs complete through the async proxy, TMEM reads and
+// writes are ordered by the tcgen05 fences), so every wait is the CTA-scope
+// one.
+
+constexpr uint32_t kPairATile = 128 * 128;         // 128 tokens x 128 K bytes
+constexpr uint32_t kPairStage = 2 * kPairATile;    // A tile + half of the tile's weight rows
+
+struct PairSmem {
+  uint64_t full[kMaxStages];   // even CTA: both CTAs' bytes of a stage have landed
+  uint64_t empty[kMaxStages];  // each CTA: its part of the stage may be refilled
+  uint64_t tfull[2];           // each CTA: accumulator b is ready
+  uint64_t tempty[2];          // even CTA: both CTAs' epilogues are done with accumulator b
+  uint32_t tmem_base;
+  int abort;
+  int last;
+};
+
+template <bool kPacked>
+__global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
+    lm_head_pair_kernel(const __grid_constant__ CUtensorMap tmap_w128,
+                        const __grid_constant__ CUtensorMap tmap_w64,
+                        const __grid_constant__ CUtensorMap tmap_a0,
+                        const __grid_constant__ CUtensorMap tmap_a1, const Stage2Params p,
+                        int nstage) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  const int G = p.G;
+  float *sa_s = reinterpret_cast<float *>(smem + (size_t)nstage * kPairStage);  // [G][128]
+  PairSmem *sh = reinterpret_cast<PairSmem *>(sa_s + (size_t)G * 128);
+  volatile int *abort_flag = &sh->abort;
+
+  const int warp = (int)(threadIdx.x / 32);
+  const int lane = (int)(threadIdx.x % 32);
+  constexpr int kProducer = kSmallEpiWarps, kMma = kSmallEpiWarps + 1;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const int pair = (int)cluster_id_x(), n_pair = (int)nclusters_x();
+  const int t_base = (int)rank * 128;
+  const int Tc = min(p.T - t_base, 128);                    // this CTA's tokens (>= 1)
+  const int Tc_pair = p.T;                                   // both CTAs' tokens
+  const CUtensorMap *tmap_act = rank ? &tmap_a1 : &tmap_a0;
+  const int b_begin = (int)(((long)pair * p.n_vtiles) / n_pair);
+  const int b_end = (int)(((long)(pair + 1) * p.n_vtiles) / n_pair);
+  const int n_tiles = (b_end - b_begin + 1) / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh->tfull[b]), 1);
+      mbar_init(smem_u32(&sh->tempty[b]), 2 * kSmallEpiWarps);
+    }
+    sh->abort = 0;
+    sh->last = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kProducer && lane == 0) {
+    if constexpr (!kPacked) {
+      prefetch_tmap(&tmap_w128);
+      prefetch_tmap(&tmap_w64);
+    }
+    prefetch_tmap(tmap_act);
+  }
+  if (warp == kMma) {
+    tmem_alloc_pair(smem_u32(&sh->tmem_base), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist and the TMEM columns are allocated
+  tc_fence_after();
+  // everything below reads memory the previous kernel on the stream may write
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int i = (int)threadIdx.x; i < G * 128; i += (int)blockDim.x) {
+    const int kb = i / 128, n = i % 128;
+    sa_s[i] = (n < Tc) ? p.act_scales[(size_t)(t_base + n) * G + kb] : 0.0f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  // the even CTA's full barriers, as seen from this CTA
+  const uint32_t full0 = mapa_shared(smem_u32(&sh->full[0]), 0u);
+
+  if (warp == kProducer) {
+    // -------------------------------------------------------------- producer --
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err,
+                                kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t *st = smem + (size_t)s * kPairStage;
+          const uint32_t fb = full0 + 8u * s;
+          if (even)   // the stage's bytes of both CTAs: two activation tiles, the weight rows
+            mbar_arrive_expect_tx(smem_u32(&sh->full[s]),
+                                  (uint32_t)Tc_pair * 128u + (uint32_t)nb * kWTileBytes);
+          tma_load_2d_pair(smem_u32(st), tmap_act, kb * 128, 0, fb, pol_a);
+          if (nb == 2) {
+            if constexpr (kPacked)
+              tma_load_2d_pair(smem_u32(st + kPairATile), &tmap_w128, 0,
+                               ((blk0 + (int)rank) * G + kb) * 128, fb, pol_w);
+            else
+              tma_load_2d_pair(smem_u32(st + kPairATile), &tmap_w128, kb * 128,
+                               (blk0 + (int)rank) * 128, fb, pol_w);
+          } else {
+            if constexpr (kPacked)
+              tma_load_2d_pair(smem_u32(st + kPairATile), &tmap_w64, 0,
+                               (blk0 * G + kb) * 128 + 64 * (int)rank, fb, pol_w);
+            else
+              tma_load_2d_pair(smem_u32(st + kPairATile), &tmap_w64, kb * 128,
+                               blk0 * 128 + 64 * (int)rank, fb, pol_w);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && even) {
+      // the even CTA counts both CTAs' copies: wait until every stage issued has landed
+      const uint32_t issued = it;
+      const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
+      for (uint32_t j = first; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kMma) {
+    // ------------------------------------------------------------------- MMA --
+    uint32_t it = 0;
+    bool ok = even;                 // the even CTA issues for the pair
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
+      const uint32_t idesc = idesc_e4m3_f32(256, (uint32_t)(nb * 128));
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const uint32_t s = it % (uint32_t)nstage;
+        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+        const uint32_t b = it & 1u;
+        const uint32_t bph = (it >> 1) & 1u;
+        int got = 1;
+        if (lane == 0)
+          got = mbar_wait(smem_u32(&sh->tempty[b]), bph ^ 1u, abort_flag, p.err,
+                                kErrBitStage2) &&
+                mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint8_t *st = smem + (size_t)s * kPairStage;
+          const uint32_t a_addr = smem_u32(st);
+          const uint32_t w_addr = smem_u32(st + kPairATile);
+          const uint32_t d_tmem = tmem_base + b * 256u;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_pair(d_tmem, sw128_kmajor_desc(a_addr + kk * 32),
+                        sw128_kmajor_desc(w_addr + kk * 32), idesc, kk > 0 ? 1u : 0u);
+          mma_commit_pair(smem_u32(&sh->empty[s]), (uint16_t)3);
+          mma_commit_pair(smem_u32(&sh->tfull[b]), (uint16_t)3);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0 && even && it > 0) {
+      const uint32_t last = it - 1;
+      mbar_wait_drain(smem_u32(&sh->tfull[last & 1u]), (last >> 1) & 1u);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue --
+    // Token r of this CTA is TMEM lane r; thread t of warp w holds token
+    // 32 (w%4) + t and the tile columns 64 (w/4) .. +63, read 16 at a time.
+    const int q = warp & 3;
+    const int g = warp >> 2;
+    const int tok = 32 * q + lane;
+    const bool quad_active = 32 * q < Tc;
+    const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
+      const bool active = quad_active && (g < 2 * nb);
+      const int blk = blk0 + (g >> 1);
+      float swr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kk = 32 * i + lane;
+        swr[i] = (active && kk < G) ? __ldg(p.w_scales + (size_t)blk * G + kk) : 0.0f;
+      }
+      float acc[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < G; ++kb, ++it) {
+        const uint32_t b = it & 1u;
+        const bool got = mbar_wait(smem_u32(&sh->tfull[b]), (it >> 1) & 1u, abort_flag,
+                                         p.err, kErrBitStage2);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float src = kb < 32 ? swr[0] : kb < 64 ? swr[1] : kb < 96 ? swr[2] : swr[3];
+        const float swv = __shfl_sync(0xffffffffu, src, kb & 31);
+        const float sc = active ? sa_s[kb * 128 + tok] * swv : 0.0f;
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t r[16];
+          if (active) {
+            tmem_ld16(taddr0 + b * 256u + (uint32_t)c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) asm volatile("" : "+r"(r[j]));
+          }
+          if (c == 48) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {   // the even CTA's tempty: an execution dependency only
+              if (even) mbar_arrive(smem_u32(&sh->tempty[b]));
+              else mbar_arrive_remote_cta(smem_u32(&sh->tempty[b]), 0u);
+            }
+          }
+          if (active) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 2)
+              fma2(acc[c + j], acc[c + j + 1], __uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                   sc, sc);
+          }
+        }
+      }
+      if (!ok) break;
+      if (!active) continue;
+
+      // argmax over this thread's 64 columns (ascending rows), merged per shard
+      const int row0 = blk0 * 128 + 64 * g;
+      const int last_row = min(row0 + 63, p.V - 1);
+      const bool tok_ok = tok < Tc;
+      const int key = t_base + tok;
+      if (row0 / p.shard_width == last_row / p.shard_width) {
+        float best = -INFINITY;
+        int bi = -1;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int v = row0 + j;
+          if (v < p.V && (bi < 0 || acc[j] > best)) {
+            best = acc[j];
+            bi = v;
+          }
+        }
+        if (tok_ok && bi >= 0)
+          atomicMax(&p.keys[(size_t)(row0 / p.shard_width) * kKeyStride + key],
+                    pack_key(best, (uint32_t)bi));
+      } else {
+        float best = -INFINITY;
+        int bi = -1, cur = -1;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int v = row0 + j;
+          if (v >= p.V) break;
+          const int sv = v / p.shard_width;
+          if (sv != cur) {
+            if (bi >= 0 && tok_ok)
+              atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
+            cur = sv;
+            bi = -1;
+          }
+          if (bi < 0 || acc[j] > best) {
+            best = acc[j];
+            bi = v;
+          }
+        }
+        if (bi >= 0 && tok_ok)
+          atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
+      }
+    }
+    __threadfence();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------- teardown --
+  // After an expired wait the odd CTA cannot see its copies complete (they
+  // count on the even CTA's barriers, which may never have been armed for
+  // them): it gives copies in flight 50 us to land before leaving.
+  if (!even && threadIdx.x == 0 && *abort_flag) {
+    const unsigned long long t0 = globaltimer();
+    while (globaltimer() - t0 < 50000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // every MMA, copy and remote arrival of the pair is done
+  tc_fence_after();
+  if (warp == kMma) tmem_dealloc_pair(tmem_base, 512);
+  finish_launch(p, &sh->last);
+}
+
 // ------------------------------------------------------------------- host --
 
 
@@ -1052,8 +1392,69 @@ cudaError_t launch_small(const Stage2Params &p_in, const void *act_codes, const 
                     ta[1], p, nstage);
 }
 
+bool g_pair_enabled = true;
+
+// 129..256 tokens on CTA pairs (cta_group::2).  Weight tiles come through 2-D
+// tensor maps with boxes of 128 and 64 rows: over the row-major [V][H] weight
+// (128-byte swizzle), or over the packed layout seen as [blocks x 128][128]
+// bytes (already swizzled, copied as is).
+template <bool kPacked>
+cudaError_t launch_pair(const Stage2Params &p_in, const void *act_codes, const void *w,
+                        int num_sms, cudaStream_t stream) {
+  if (p_in.T <= kSmallMaxT || p_in.T > 2 * kSmallMaxT || num_sms < 2)
+    return cudaErrorInvalidConfiguration;
+  Stage2Params p = p_in;
+  p.n_groups = 2;
+  CUtensorMap tw128, tw64, ta[2];
+  if constexpr (kPacked) {
+    const uint64_t rows = (uint64_t)p.n_vtiles * (uint64_t)p.G * 128u;
+    if (!encode_u8_map_plain(&tw128, w, rows, 128, 128, 128) ||
+        !encode_u8_map_plain(&tw64, w, rows, 128, 128, 64))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!encode_u8_map(&tw128, w, (uint64_t)p.V, (uint64_t)p.H, 128) ||
+        !encode_u8_map(&tw64, w, (uint64_t)p.V, (uint64_t)p.H, 64))
+      return cudaErrorInvalidValue;
+  }
+  for (int g = 0; g < 2; ++g) {
+    const int Tg = (p.T - g * 128) < 128 ? (p.T - g * 128) : 128;
+    if (!encode_u8_map(&ta[g], static_cast<const uint8_t *>(act_codes) + (size_t)g * 128 * p.H,
+                       (uint64_t)Tg, (uint64_t)p.H, (uint32_t)Tg))
+      return cudaErrorInvalidValue;
+  }
+  const size_t fixed = 1024 /*align pad*/ + (size_t)p.G * 128 * 4 + sizeof(PairSmem) + 64;
+  const size_t budget = 227u * 1024u;
+  int nstage = (int)((budget - fixed) / kPairStage);
+  if (nstage > kMaxStages) nstage = kMaxStages;
+  if (nstage < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + (size_t)nstage * kPairStage;
+  auto kern = lm_head_pair_kernel<kPacked>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int pairs = (num_sms / 2) < p.n_vtiles ? (num_sms / 2) : p.n_vtiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.blockDim = dim3((unsigned)(kSmallEpiWarps * 32 + 64));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tw128, tw64, ta[0], ta[1], p, nstage);
+}
+
 cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const void *w,
                           int num_sms, cudaStream_t stream) {
+  if (p.T > kSmallMaxT && p.T <= 2 * kSmallMaxT && g_small_enabled && g_pair_enabled)
+    return p.w_packed ? launch_pair<true>(p, act_codes, w, num_sms, stream)
+                      : launch_pair<false>(p, act_codes, w, num_sms, stream);
   if (p.T <= 2 * kSmallMaxT && g_small_enabled) {
     if (p.T <= 64)
       return p.w_packed ? launch_small<64, true>(p, act_codes, w, num_sms, stream)
@@ -1066,6 +1467,8 @@ cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes, const vo
 }
 
 void stage2_set_small(int enabled) { g_small_enabled = enabled != 0; }
+
+void stage2_set_pair(int enabled) { g_pair_enabled = enabled != 0; }
 
 // The fused step: batches of at most 64 tokens (one CTA per row among the
 // grid), rows whose H/16 data-holding threads are whole warps within the 512

@@ -99,6 +99,7 @@ cudaError_t launch_stage2(const Stage2Params &p, const void *act_codes_base, con
 
 size_t stage2_workspace_bytes(int S);
 void stage2_set_small(int enabled);   // 0: always use the wide-batch kernel (tests, tuning)
+void stage2_set_pair(int enabled);    // 0: 129..256 tokens as two independent token groups
 int stage2_token_chunk();             // tokens per LM-head launch
 size_t packed_weight_bytes(int V, int H);
 cudaError_t launch_pack_weights(const uint8_t *w, int V, int H, uint8_t *out, cudaStream_t stream);
@@ -131,5 +132,12 @@ void stage2_fp4_set_stages(int n);   // 0: as many pipeline stages as fit
 size_t fp4_packed_weight_bytes(int V, int H);
 cudaError_t launch_pack_fp4_weights(const uint8_t *codes, const uint8_t *bscales, int V, int H,
                                     uint8_t *out, cudaStream_t stream);
+
+// Measurement: `ctas` CTAs (pair: CTA pairs) each issue `iters` K blocks of
+// four FP8 MMAs from shared memory (probe.cu).
+cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err, cudaStream_t stream);
+// Measurement: `ctas` CTAs of 16 warps each read 64 TMEM columns x 32 lanes
+// per warp, `iters` times (probe.cu).
+cudaError_t launch_probe_tmem_ld(int batched, int ctas, int iters, cudaStream_t stream);
 
 }  // namespace nfq

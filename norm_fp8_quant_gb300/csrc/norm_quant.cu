@@ -206,9 +206,12 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
       // row total is formed from all G group sums
       const int par = row_iter & 1;
       const uint32_t pph = (uint32_t)((row_iter >> 1) & 1);
+      float gsv_[VPT];
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) gsv_[v] = group_sum16(vec_sumsq(x[v]));   // all lanes
 #pragma unroll
       for (int v = 0; v < VPT; ++v) {
-        const float gsv = group_sum16(vec_sumsq(x[v]));   // all lanes (shuffles)
+        const float gsv = gsv_[v];
         if (active && (tc & 15) == 0) {
           const int g = (col0 + (v * NA + tc) * 8) / 128;
           if (C > 1) {
@@ -672,13 +675,17 @@ Stage1Choice choose_stage1(int T, int H, int k, int num_sms, bool fp4 = false) {
   ch.threads = 32 + ((ch.NA + 31) / 32) * 32;
   const int E = H / C;
   const size_t in_bytes = (size_t)E * 2u;
-  // inputs per slot: about 42 KB per barrier round trip (three inputs of a
-  // 6144- or 7168-wide row measured best), at most a whole row
-  int m = (int)((42u * 1024u) / in_bytes);
-  if (m < 1) m = 1;
-  if (m > k + 1) m = k + 1;
-  if (g_tune_per_slot > 0) m = g_tune_per_slot < k + 1 ? g_tune_per_slot : k + 1;
+  // inputs per slot: a row's k + 1 inputs in as few slots as leave room for
+  // two slots in the ring, split evenly (k = 8: two slots of 5 and 4 inputs
+  // for H = 6144 and 7168; a CUDA-graph sweep at T = 2048 and 8192 found this
+  // 3-5 % faster than three slots of 3, and far faster than smaller slots)
   const size_t budget = 200u * 1024u;
+  int per_row = 1;
+  while ((k + per_row) / per_row > 1 &&
+         2u * in_bytes * (size_t)((k + per_row) / per_row) > budget)
+    ++per_row;
+  int m = (k + per_row) / per_row;   // ceil((k + 1) / per_row)
+  if (g_tune_per_slot > 0) m = g_tune_per_slot < k + 1 ? g_tune_per_slot : k + 1;
   while (m > 1 && 2u * in_bytes * (size_t)m > budget) --m;   // room for two slots
   const int slots_per_row = (k + 1 + m - 1) / m;
   int nslot = (int)(budget / (in_bytes * (size_t)m));

@@ -1,0 +1,191 @@
+// Measurement kernels (not on the hot path): the rate at which tcgen05 FP8
+// MMAs run when nothing else competes for the SM (the FP8 tensor roofline
+// that the LM head's tensor-pipe figures are read against), and the rate at
+// which TMEM accumulators can be read into registers (what bounds the LM
+// head's per-K-block promotion when it holds 128 tokens per SM).
+//
+// fp8_mma_rate_kernel<kPair>: every CTA (kPair: every CTA pair, cta_group::2)
+// zeroes an A tile and a B tile in shared memory, allocates one 256-column
+// TMEM accumulator and has one thread issue `iters` K blocks of four
+// back-to-back tcgen05.mma kind::f8f6f4 (K = 32 bytes each) with the shapes
+// the LM head uses: M = 128 tokens x N = 256 weight rows per CTA, or M = 256 x
+// N = 256 per pair (each CTA holding 128 A rows and 128 B rows).  A commit at
+// the end arrives on an mbarrier, waited for with the usual time limit.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "nfq_internal.h"
+#include "ptx.cuh"
+
+namespace nfq {
+
+namespace {
+
+constexpr int kProbeErrBit = 4;
+
+template <bool kPair>
+__global__ void __launch_bounds__(128, 1) fp8_mma_rate_kernel(int iters, unsigned *err) {
+  // A: 128 rows x 128 bytes; B: 256 rows (one CTA) or 128 rows (each CTA of a pair)
+  constexpr uint32_t kA = 128 * 128, kB = (kPair ? 128 : 256) * 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  __shared__ uint64_t done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  const int warp = (int)(threadIdx.x / 32), lane = (int)(threadIdx.x % 32);
+  const bool issuer = !kPair || cluster_ctarank() == 0;
+
+  uint4 *z = reinterpret_cast<uint4 *>(smem);
+  for (uint32_t i = threadIdx.x; i < (kA + kB) / 16; i += blockDim.x)
+    z[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&done), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(&tmem_base), 256);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&tmem_base), 256);
+      tmem_relinquish();
+    }
+  }
+  // the zeroed tiles are read by the tensor cores (async proxy)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  tc_fence_after();
+
+  if (warp == 0) {
+    if (issuer && lane == 0) {
+      const uint32_t a = smem_u32(smem), b = smem_u32(smem + kA);
+      const uint32_t idesc = idesc_e4m3_f32(kPair ? 256 : 128, 256);
+      for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if constexpr (kPair)
+            mma_f8_pair(tmem_base, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32),
+                        idesc, (it | kk) ? 1u : 0u);
+          else
+            mma_f8(tmem_base, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32),
+                   idesc, (it | kk) ? 1u : 0u);
+        }
+      }
+      if constexpr (kPair)
+        mma_commit_pair(smem_u32(&done), (uint16_t)3);
+      else
+        mma_commit(smem_u32(&done));
+    }
+    __syncwarp();
+    // every CTA waits for the last MMAs (a pair's commit arrives on both CTAs)
+    if (lane == 0 &&
+        !mbar_wait(smem_u32(&done), 0u, (volatile int *)&abort_flag, err, kProbeErrBit)) {
+      // gave up: the MMAs still in flight are waited for, again with a limit
+      mbar_wait_drain(smem_u32(&done), 0u);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) {
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, 256);
+    else
+      tmem_dealloc(tmem_base, 256);
+  }
+}
+
+// tmem_ld_rate_kernel: the rate at which 16 warps of one CTA per SM read a
+// 128-lane x 512-column TMEM allocation into registers with the LM head
+// epilogue's access pattern: warp w reads lane quadrant w % 4, columns
+// 64 (w / 4) .. +63 of one of two 256-column accumulators (alternating), as
+// four 32x32b.x16 loads, waiting for each (kBatched: for all four at once).
+__device__ unsigned g_tmem_probe_sink;   // bumped only by an (unexpected) checksum match
+
+template <bool kBatched>
+__global__ void __launch_bounds__(512, 1) tmem_ld_rate_kernel(int iters) {
+  __shared__ uint32_t tmem_base;
+  const int warp = (int)(threadIdx.x / 32);
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t t0 = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(64 * (warp >> 2));
+  uint32_t x = 0;
+  for (int it = 0; it < iters; ++it) {
+    const uint32_t ta = t0 + (uint32_t)(it & 1) * 256u;
+    if constexpr (kBatched) {
+      uint32_t r0[16], r1[16], r2[16], r3[16];
+      tmem_ld16(ta, r0);
+      tmem_ld16(ta + 16, r1);
+      tmem_ld16(ta + 32, r2);
+      tmem_ld16(ta + 48, r3);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x ^= r0[j] ^ r1[j] ^ r2[j] ^ r3[j];
+    } else {
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(ta + (uint32_t)c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x ^= r[j];
+      }
+    }
+  }
+  if (x == 0x9E3779B9u) atomicAdd(&g_tmem_probe_sink, 1u);   // keeps the loads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem_base, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_probe_tmem_ld(int batched, int ctas, int iters, cudaStream_t stream) {
+  // the whole TMEM (512 columns) and most of shared memory: one CTA per SM
+  const size_t smem = 120u * 1024u;
+  auto kern = batched ? tmem_ld_rate_kernel<true> : tmem_ld_rate_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)ctas, 512, smem, stream>>>(iters);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,
+                                 cudaStream_t stream) {
+  // the tiles need at most 49 KB; asking for 120 KB keeps one CTA per SM
+  const size_t smem = 120u * 1024u;
+  auto kern = pair ? fp8_mma_rate_kernel<true> : fp8_mma_rate_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pair ? 2 * ctas : ctas));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, iters, err);
+}
+
+}  // namespace nfq

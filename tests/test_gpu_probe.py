@@ -1,0 +1,35 @@
+"""The measurement kernels run to completion and leave no error: the FP8
+MMA-rate kernel in both shapes (one CTA, and CTA pairs issuing cta_group::2
+MMAs) and the TMEM read-rate kernel in both load patterns."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nfq():
+    import norm_fp8_quant_gb300 as m
+    from norm_fp8_quant_gb300 import build
+    build.build()
+    m.load()
+    assert torch.cuda.is_available()
+    return m
+
+
+@pytest.mark.parametrize("pair", [False, True])
+def test_probe_fp8_mma_runs(nfq, pair):
+    flops = nfq.probe_fp8_mma(pair, 4, 16)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    assert flops == 2.0 * (256 if pair else 128) * 256 * 128 * 16 * 4
+    with pytest.raises(nfq.NfqError):
+        nfq.probe_fp8_mma(pair, 0, 16)
+
+
+@pytest.mark.parametrize("batched", [False, True])
+def test_probe_tmem_ld_runs(nfq, batched):
+    nbytes = nfq.probe_tmem_ld(batched, 4, 8)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    assert nbytes == 128.0 * 256 * 4 * 8 * 4

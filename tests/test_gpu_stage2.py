@@ -187,3 +187,27 @@ def test_pack_weights_layout(nfq, V, H):
     expect = np.empty_like(blocks)
     expect[:, :, r, c ^ (r % 8)] = blocks[:, :, r, c]
     assert np.array_equal(packed, expect.reshape(-1))
+
+
+@pytest.mark.parametrize("T,H,V,S", [(129, 256, 1024, 8), (200, 1024, 5000, 5),
+                                     (256, 512, 128, 1), (160, 16384, 3000, 3),
+                                     (255, 1024, 151552, 8)])
+def test_stage2_cta_pairs_equal_two_token_groups(nfq, T, H, V, S, layout):
+    """129..256 tokens: the CTA-pair kernel (cta_group::2 MMAs, each CTA
+    holding half of every weight tile) and two independent 128-token groups
+    give the same bytes; both match the oracle on every token.  Ragged second
+    halves, a single 128-row block (one-block tiles, 64 weight rows per CTA),
+    the widest rows and a full vocabulary are covered."""
+    w = synth.workload("tiny", T=T, H=H, k=2, V=V, S=S, seed=T * 3 + V)
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    pair = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, S, layout=layout)
+    nfq.lm_head_pair(False)
+    try:
+        groups = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, S, layout=layout)
+    finally:
+        nfq.lm_head_pair(True)
+    for a, b in zip(pair, groups):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    check_stage2(pair[0], ref["codes"], ref["scales"], qw, sw, S, list(range(T)), *pair[1:],
+                 cache_key=("pair", T, H, V, S))
