@@ -686,8 +686,13 @@ def run_ours(args, rank, world, local):
                                   "peak_source": peak_kind}
         else:
             result["roofline"] = {"bound": "hbm", "achieved": round(gbs1, 1), "peak": peak,
-                                  "unit": "GB/s", "frac": round(gbs1 / peak, 4), "traffic": None,
-                                  "kernel": "reduce_norm_quant_kernel", "peak_source": peak_kind}
+                                  "unit": "GB/s", "frac": round(gbs1 / peak, 4),
+                                  "traffic": (ncu_traffic("norm_quant_prefill")
+                                              if args.workload == "prefill" and not fp4
+                                              and not unfused else None),
+                                  "kernel": ("reduce_norm_quant_kernel (persistent)" if T > 512
+                                             else "stage1_split_kernel"),
+                                  "peak_source": peak_kind}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -843,7 +848,9 @@ SWEEP_T = [1, 16, 64, 128, 256, 512, 1024, 2048, 4096, 8192]
 def run_stage1_sweep(args, local):
     """Stage 1 alone at T = 1 .. 8192 rows of the decode c=64 shape (H = 6144,
     k = 8 partials with the outlier channels), each batch size timed from a
-    CUDA graph of back-to-back launches over rotating input sets (> 2 x L2)."""
+    CUDA graph of back-to-back launches over rotating input sets (> 2 x L2).
+    `read_floor_us` times the small-batch kernel's loads alone (the same grid,
+    no arithmetic, no stores: nfq_probe_stage1_reads) the same way."""
     import numpy as np
     import torch
 
@@ -889,9 +896,25 @@ def run_stage1_sweep(args, local):
         if nfq.device_error() != nfq.NFQ_OK:
             raise RuntimeError("a kernel reported an expired wait in the stage-1 sweep")
         us = e0.elapsed_time(e1) * 1e3 / (reps * nsets)
+        # the floor: the small-batch kernel's loads alone, same grid, same graph
+        reads = [nfq.prepare_probe_stage1_reads(st[:k], st[k]) for st in sets]
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2):
+            for c in reads:
+                c()
+        g2.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            g2.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        floor_us = e0.elapsed_time(e1) * 1e3 / (reps * nsets)
+        del g2, reads
         gbs = stage1_bytes(T, H, k) / (us * 1e-6) / 1e9
         plan = nfq.stage1_split_plan(T, H, torch.cuda.get_device_properties(dev).multi_processor_count)
         rows.append({"T": T, "us": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "read_floor_us": round(floor_us, 3),
                      "kernel": (f"stage1_split_kernel, {plan['ctas_per_row']} CTAs per row, "
                                 f"{plan['vpt']} vectors per thread" if plan["ctas_per_row"]
                                 else "reduce_norm_quant_kernel (persistent)"),

@@ -424,6 +424,11 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   lanes x 64 columns as four 16-column loads; batched != 0: one wait for
  *   the four instead of one each): 128 KiB per CTA per iteration.
  *   Asynchronous on `stream`; NFQ_ERR_SHAPE as for nfq_probe_fp8_mma.
+ * nfq_probe_stage1_reads: a measurement kernel, not part of the path: the
+ *   loads of the small-batch stage-1 kernel alone (the k partials and the
+ *   residual, BF16 [T][H]) in the grid that kernel uses at this size, without
+ *   arithmetic or stores; the floor under stage 1's time.  Asynchronous on
+ *   `stream`.
  * nfq_stage1_split_plan: the small-batch plan for (T, H) on num_sms SMs:
  *   out4 = {CTAs per row (0: the persistent kernel runs), vectors per thread,
  *   active threads, block threads}.
@@ -437,6 +442,8 @@ void nfq_stage1_grid(int max_ctas);
 void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt);
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
+int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,
+                           int H, void *stream);
 int nfq_stage1_split_plan(int T, int H, int num_sms, int *out4);
 
 #ifdef __cplusplus

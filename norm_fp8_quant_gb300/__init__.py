@@ -106,6 +106,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_probe_fp8_mma.restype = ctypes.c_int
     lib.nfq_probe_tmem_ld.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_tmem_ld.restype = ctypes.c_int
+    lib.nfq_probe_stage1_reads.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_probe_stage1_reads.restype = ctypes.c_int
     lib.nfq_mtp_reduce_norm_quant_nvfp4.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
                                                     ctypes.c_int, ctypes.c_int, _P,
                                                     ctypes.POINTER(Fp4Act), _P]
@@ -409,6 +411,21 @@ def probe_tmem_ld(batched: bool, ctas: int, iters: int, stream=None):
     _check(_on_device(dev, load().nfq_probe_tmem_ld, 1 if batched else 0, ctas, iters,
                       _raw_stream(dev, stream)), "nfq_probe_tmem_ld")
     return 128.0 * 256 * 4 * iters * ctas
+
+
+def prepare_probe_stage1_reads(partials, residual) -> "PreparedCall":
+    """The small-batch stage-1 kernel's loads alone (a measurement kernel, not
+    part of the path), as a PreparedCall."""
+    import torch
+    T, H = residual.shape
+    _need_cuda(residual, *partials)
+    if residual.dtype != torch.bfloat16 or any(p.dtype != torch.bfloat16 or p.shape != (T, H)
+                                               for p in partials):
+        raise ValueError("partials and residual must be bf16 [T][H]")
+    arr = (ctypes.c_void_p * len(partials))(*[p.data_ptr() for p in partials])
+    args = (arr, len(partials), residual.data_ptr(), T, H)
+    return PreparedCall(load().nfq_probe_stage1_reads, args, residual.device.index,
+                        "nfq_probe_stage1_reads", (partials, residual, arr))
 
 
 def lm_head_pair(enabled: bool = True):

@@ -672,6 +672,31 @@ int nfq_probe_fp8_mma(int pair, int ctas, int iters, void *stream) {
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,
+                           int H, void *stream) {
+  if (!partials || !residual) return NFQ_ERR_NULL;
+  if (k < 1 || k > kMaxPartials || T < 1 || H < 128 || H > 32768 || H % 128 != 0)
+    return NFQ_ERR_SHAPE;
+  for (int i = 0; i < k; ++i) {
+    if (!partials[i]) return NFQ_ERR_NULL;
+    if (!aligned16(partials[i])) return NFQ_ERR_ALIGN;
+  }
+  if (!aligned16(residual)) return NFQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  Stage1Params p;
+  std::memset(&p, 0, sizeof(p));
+  for (int i = 0; i < k; ++i) p.partials[i] = partials[i];
+  p.residual = residual;
+  p.k = k;
+  p.T = T;
+  p.H = H;
+  const cudaError_t e = launch_stage1_reads(p, d->num_sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
+  return map_cuda(e);
+}
+
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream) {
   if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20)) return NFQ_ERR_SHAPE;
   DeviceInfo *d = nullptr;

@@ -48,6 +48,8 @@ void stage1_set_grid(int max_ctas);   // 0: one CTA (cluster) per SM at most
 // vectors per thread (0: automatic).
 void stage1_set_split(int max_tokens, int ctas_per_row, int vpt);
 int stage1_split_plan(int T, int H, int num_sms, int *out4);
+// Measurement: the small-batch kernel's loads alone (its grid at this size).
+cudaError_t launch_stage1_reads(Stage1Params p, int num_sms, cudaStream_t stream);
 int stage1_plan(int T, int H, int k, int num_sms, int *out7);
 bool stage1_fp4_supported(int H);
 

@@ -33,3 +33,12 @@ def test_probe_tmem_ld_runs(nfq, batched):
     torch.cuda.synchronize()
     assert nfq.device_error() == 0
     assert nbytes == 128.0 * 256 * 4 * 8 * 4
+
+
+@pytest.mark.parametrize("T,H,k", [(64, 6144, 8), (1, 7168, 8), (700, 1024, 3)])
+def test_probe_stage1_reads_runs(nfq, T, H, k):
+    parts = [torch.randn(T, H, device="cuda").to(torch.bfloat16) for _ in range(k)]
+    res = torch.randn(T, H, device="cuda").to(torch.bfloat16)
+    nfq.prepare_probe_stage1_reads(parts, res)()
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
