@@ -474,8 +474,8 @@ int nfq_lm_head_nvfp4_argmax(const nfq_fp4_act *a, const void *w_packed, float w
   p.S = S;
   p.shard_width = V / S;
   p.n_vtiles = (V + 127) / 128;
-  for (int t0 = 0; t0 < T; t0 += kFp4MaxT) {
-    const int Tc = (T - t0) < kFp4MaxT ? (T - t0) : kFp4MaxT;
+  for (int t0 = 0; t0 < T; t0 += kFp4LaunchMaxT) {
+    const int Tc = (T - t0) < kFp4LaunchMaxT ? (T - t0) : kFp4LaunchMaxT;
     p.tok0 = t0;
     p.T = Tc;
     p.act_codes = a->codes + (size_t)t0 * (size_t)(H / 2);

@@ -15,7 +15,12 @@
 //
 // Token-major, as the FP8 small-batch form: a tile is 256 vocab rows (two
 // 128-row blocks, the MMA's N), the tokens (up to 128, zero-padded; MT = 64
-// rows loaded for batches of at most 64) are M.
+// rows loaded for batches of at most 64) are M.  129..256 tokens run in one
+// launch as two token groups: CTAs 2i and 2i+1 stream the same block range for
+// tokens 0..127 and 128.., the weight with the normal L2 policy so that the
+// second request for every block is served from L2.  Without a per-K-block
+// promotion the epilogue reads each tile once, so the second group costs the
+// SM little more than the weight stream it shares.
 // One K step is 128 code bytes = 256 elements = four MMAs of K = 64.
 //
 // Warps (704 threads):
@@ -92,7 +97,9 @@ struct Fp4Smem {
 template <int MT>
 __global__ void __launch_bounds__(kF4Threads, 1)
     lm_head_fp4_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                       const __grid_constant__ CUtensorMap tmap_sa, const Stage2Params p,
+                       const __grid_constant__ CUtensorMap tmap_sa,
+                       const __grid_constant__ CUtensorMap tmap_a2,
+                       const __grid_constant__ CUtensorMap tmap_sa2, const Stage2Params p,
                        int nstage) {
   using L = Fp4Layout<MT>;
   extern __shared__ uint8_t smem_raw[];
@@ -108,8 +115,16 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int G = p.G;                                           // K steps of 256 elements
   const size_t scale_region = (size_t)p.n_vtiles * (size_t)G * kWTileBytes;
 
-  const int b_begin = (int)(((long)blockIdx.x * p.n_vtiles) / gridDim.x);
-  const int b_end = (int)(((long)(blockIdx.x + 1) * p.n_vtiles) / gridDim.x);
+  // token group: tokens t_base .. t_base + Tc - 1 of the launch
+  const int n_grp = p.n_groups;
+  const int grp = (int)blockIdx.x % n_grp;
+  const int cta = (int)blockIdx.x / n_grp, n_cta = (int)gridDim.x / n_grp;
+  const int t_base = grp * kFp4MaxT;
+  const int Tc = min(p.T - t_base, kFp4MaxT);
+  const CUtensorMap *tm_a = grp ? &tmap_a2 : &tmap_a;
+  const CUtensorMap *tm_sa = grp ? &tmap_sa2 : &tmap_sa;
+  const int b_begin = (int)(((long)cta * p.n_vtiles) / n_cta);
+  const int b_end = (int)(((long)(cta + 1) * p.n_vtiles) / n_cta);
   const int n_tiles = (b_end - b_begin + 1) / 2;
 
   if (threadIdx.x == 0) {
@@ -125,8 +140,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     fence_mbarrier_init();
   }
   if (warp == kF4Producer && lane == 0) {
-    prefetch_tmap(&tmap_a);
-    prefetch_tmap(&tmap_sa);
+    prefetch_tmap(tm_a);
+    prefetch_tmap(tm_sa);
   }
   if (warp == kF4Mma) {
     tmem_alloc(smem_u32(&sh->tmem_base), 512);
@@ -140,7 +155,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int total_steps = n_tiles * G;
   const int npre = total_steps < nstage ? total_steps : nstage;
   if (warp == kF4Producer && lane == 0) {
-    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_w = n_grp > 1 ? policy_evict_normal() : policy_evict_first();
     for (int it = 0; it < npre; ++it) {
       int blk0, nb;
       small_tile(b_begin, b_end, it / G, blk0, nb);
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
   for (int i = (int)threadIdx.x; i < kFp4MaxT; i += (int)blockDim.x)
-    gs_s[i] = (i < p.T) ? __fmul_rn(p.act_gscales[i], p.w_scale) : 0.0f;
+    gs_s[i] = (i < Tc) ? __fmul_rn(p.act_gscales[t_base + i], p.w_scale) : 0.0f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -169,7 +184,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 
   if (warp == kF4Producer) {
     // -------------------------------------------------------------- producer --
-    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_w = n_grp > 1 ? policy_evict_normal() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     uint32_t it = 0;
     bool ok = true;
@@ -191,9 +206,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         if (lane == 0) {
           uint8_t *st = smem + (size_t)s * L::kStage;
           const uint32_t fb = smem_u32(&sh->full[s]);
-          // the activation boxes hold exactly the T token rows (no out-of-range rows)
+          // the activation boxes hold exactly the group's Tc token rows
           mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * (kWTileBytes + kF4ScaleBlock)) +
-                                        (uint32_t)p.T * (128u + 16u));
+                                        (uint32_t)Tc * (128u + 16u));
           for (int h = 0; h < nb && !pre; ++h) {
             const size_t blk = (size_t)(blk0 + h) * (size_t)G + (size_t)ks;
             bulk_g2s(smem_u32(st + L::kW + h * kWTileBytes), p.w_packed + blk * kWTileBytes,
@@ -201,8 +216,8 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             bulk_g2s(smem_u32(st + L::kSfb + h * kF4ScaleBlock),
                      p.w_packed + scale_region + blk * kF4ScaleBlock, kF4ScaleBlock, fb, pol_w);
           }
-          tma_load_2d(smem_u32(st + L::kA), &tmap_a, ks * 128, 0, fb, pol_a);
-          tma_load_2d(smem_u32(st + L::kSfa), &tmap_sa, ks * 16, 0, fb, pol_a);
+          tma_load_2d(smem_u32(st + L::kA), tm_a, ks * 128, 0, fb, pol_a);
+          tma_load_2d(smem_u32(st + L::kSfa), tm_sa, ks * 16, 0, fb, pol_a);
         }
         __syncwarp();
       }
@@ -288,7 +303,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         for (int c = 0; c < 4; ++c) {
           // token row 32c + lane: its 16 scale bytes = words for MMAs 0..3
           // (rows past MT feed accumulator rows that are never read)
-          const uint4 v = (32 * c + lane < p.T)
+          const uint4 v = (32 * c + lane < Tc)
                               ? *reinterpret_cast<const uint4 *>(sfa_s + (32 * c + lane) * 16)
                               : make_uint4(0u, 0u, 0u, 0u);
           ra[0 + c] = v.x;
@@ -328,8 +343,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     const int q = warp & 3;
     const int g = warp >> 2;
     const int tok = 32 * q + lane;
-    const bool quad_active = 32 * q < p.T && 32 * q < MT;
-    const bool tok_ok = tok < p.T;
+    const bool quad_active = 32 * q < Tc && 32 * q < MT;
+    const bool tok_ok = tok < Tc;
+    const int key = t_base + tok;                   // the token's index in the launch
     const float sc = gs_s[tok];
     const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
     for (int ti = 0; ti < n_tiles; ++ti) {
@@ -367,7 +383,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
             if (v >= p.V) break;
             if (v >= next_bound) {
               if (bi >= 0 && tok_ok)
-                atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+                atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
               cur = v / p.shard_width;
               next_bound = (cur + 1) * p.shard_width;
               bi = -1;
@@ -381,7 +397,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         }
       }
       if (active && bi >= 0 && tok_ok)
-        atomicMax(&p.keys[(size_t)cur * kKeyStride + tok], pack_key(best, (uint32_t)bi));
+        atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
     }
     __threadfence();
     __syncwarp();
@@ -437,16 +453,29 @@ namespace {
 int g_fp4_stages = 0;   // 0: as many as fit
 
 template <int MT>
-cudaError_t launch_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) {
+cudaError_t launch_fp4(const Stage2Params &p_in, int num_sms, cudaStream_t stream) {
   using L = Fp4Layout<MT>;
-  CUtensorMap ta, tsa;
-  // boxes of exactly T rows: a box reaching past the tensor's last row is
-  // filled with zeros by the copy engine, which measured slow for tiny T
-  if (!encode_u8_map(&ta, p.act_codes, (uint64_t)p.T, (uint64_t)(p.H / 2), (uint32_t)p.T))
-    return cudaErrorInvalidValue;
-  if (!encode_u8_map_plain(&tsa, p.act_bscales, (uint64_t)p.T, (uint64_t)(p.H / 16), 16u,
-                           (uint32_t)p.T))
-    return cudaErrorInvalidValue;
+  Stage2Params p = p_in;
+  const int n_grp = (MT == kFp4MaxT && p.T > kFp4MaxT) ? 2 : 1;
+  if (p.T < 1 || p.T > n_grp * MT || num_sms < n_grp) return cudaErrorInvalidConfiguration;
+  p.n_groups = n_grp;
+  CUtensorMap ta[2], tsa[2];
+  // per group, boxes of exactly its token rows: a box reaching past the
+  // tensor's last row is filled with zeros by the copy engine, which measured
+  // slow for tiny T
+  for (int g = 0; g < n_grp; ++g) {
+    const int Tg = (p.T - g * MT) < MT ? (p.T - g * MT) : MT;
+    if (!encode_u8_map(&ta[g], p.act_codes + (size_t)g * MT * (size_t)(p.H / 2), (uint64_t)Tg,
+                       (uint64_t)(p.H / 2), (uint32_t)Tg))
+      return cudaErrorInvalidValue;
+    if (!encode_u8_map_plain(&tsa[g], p.act_bscales + (size_t)g * MT * (size_t)(p.H / 16),
+                             (uint64_t)Tg, (uint64_t)(p.H / 16), 16u, (uint32_t)Tg))
+      return cudaErrorInvalidValue;
+  }
+  if (n_grp == 1) {
+    ta[1] = ta[0];
+    tsa[1] = tsa[0];
+  }
   const size_t fixed = 1024 /*align pad*/ + kFp4MaxT * sizeof(float) + sizeof(Fp4Smem) + 64;
   const size_t budget = 227u * 1024u;
   int nstage = (int)((budget - fixed) / L::kStage);
@@ -458,8 +487,9 @@ cudaError_t launch_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) 
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int grid = num_sms < p.n_vtiles ? num_sms : p.n_vtiles;
-  return launch_pdl(kern, grid, kF4Threads, smem, stream, ta, tsa, p, nstage);
+  const int per_grp = (num_sms / n_grp) < p.n_vtiles ? (num_sms / n_grp) : p.n_vtiles;
+  return launch_pdl(kern, per_grp * n_grp, kF4Threads, smem, stream, ta[0], tsa[0], ta[1],
+                    tsa[1], p, nstage);
 }
 
 }  // namespace
@@ -467,7 +497,7 @@ cudaError_t launch_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) 
 void stage2_fp4_set_stages(int n) { g_fp4_stages = n; }
 
 cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) {
-  if (p.T < 1 || p.T > kFp4MaxT) return cudaErrorInvalidConfiguration;
+  if (p.T < 1 || p.T > kFp4LaunchMaxT) return cudaErrorInvalidConfiguration;
   return p.T <= 64 ? launch_fp4<64>(p, num_sms, stream) : launch_fp4<128>(p, num_sms, stream);
 }
 

@@ -127,8 +127,10 @@ cudaError_t launch_unfused_quant(const void *hidden, int T, int H, uint8_t *code
 cudaError_t launch_unfused_argmax(const void *logits, int T, int V, int32_t *tokens,
                                   cudaStream_t stream);
 
-// NVFP4 LM head (token-major, block-scaled tensor cores), T <= 128 per launch
+// NVFP4 LM head (token-major, block-scaled tensor cores): up to 128 tokens per
+// token group, two groups (256 tokens) per launch
 constexpr int kFp4MaxT = 128;
+constexpr int kFp4LaunchMaxT = 2 * kFp4MaxT;
 cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream);
 void stage2_fp4_set_stages(int n);   // 0: as many pipeline stages as fit
 size_t fp4_packed_weight_bytes(int V, int H);

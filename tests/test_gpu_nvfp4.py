@@ -146,10 +146,12 @@ def test_nvfp4_lm_head_decode_c64_all_tokens(nfq):
                                      (33, 256, 4100, 4), (64, 768, 2048, 64),
                                      (100, 512, 3000, 3), (128, 256, 1536, 6),
                                      (129, 256, 1024, 8), (250, 512, 640, 5),
-                                     (7, 16384, 1000, 4)])
+                                     (256, 256, 128, 1), (300, 512, 2000, 4),
+                                     (513, 256, 1024, 2), (7, 16384, 1000, 4)])
 def test_nvfp4_lm_head_edge_shapes(nfq, T, H, V, S):
     """Ragged vocab tails, one-block tiles, shards narrower than a warp's
-    columns, every lane quadrant and the 128-token chunks."""
+    columns, every lane quadrant, two token groups in one launch (129..256
+    tokens, ragged second group) and several launches (300, 513 tokens)."""
     w = synth.workload("tiny", T=T, H=H, k=2, V=V, S=S, seed=T + H + V + S)
     act = oracle_stage1(synth.stage1_inputs(w))
     qw, sw, gw = fp4_weights(w)
@@ -248,3 +250,14 @@ def test_nvfp4_pack_layout(nfq, V, H):
     words = sp.reshape(nvt, 4, 32, G, 4, 4)            # vt, c, i, s, kk, byte
     want = words.transpose(0, 3, 4, 2, 1, 5)           # vt, s, kk, i, c, byte
     assert np.array_equal(packed[nvt * G * 16384:], want.reshape(-1))
+
+
+@pytest.mark.parametrize("T", [136, 256])
+def test_nvfp4_two_token_groups_full_vocab(nfq, T):
+    """129..256 tokens in one launch over a full-size vocabulary: every CTA pair
+    of the grid shares a weight stream; every token against the oracle."""
+    w = synth.workload("tiny", T=T, H=1024, k=2, V=151552, S=8, seed=T + 3)
+    act = oracle_stage1(synth.stage1_inputs(w))
+    qw, sw, gw = synth.lm_head_weights_nvfp4(w)
+    out = run_lm(nfq, act, qw, sw, gw, w.S)
+    check(*out, act, qw, sw, gw, w.S, list(range(T)), cache_key=("nvfp4_two", T))
