@@ -912,11 +912,14 @@ def run_stage1_sweep(args, local):
         floor_us = e0.elapsed_time(e1) * 1e3 / (reps * nsets)
         del g2, reads
         gbs = stage1_bytes(T, H, k) / (us * 1e-6) / 1e9
-        plan = nfq.stage1_split_plan(T, H, torch.cuda.get_device_properties(dev).multi_processor_count)
+        plan = nfq.stage1_split_plan(T, H, k,
+                                     torch.cuda.get_device_properties(dev).multi_processor_count)
         rows.append({"T": T, "us": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
                      "read_floor_us": round(floor_us, 3),
                      "kernel": (f"stage1_split_kernel, {plan['ctas_per_row']} CTAs per row, "
-                                f"{plan['vpt']} vectors per thread" if plan["ctas_per_row"]
+                                f"{plan['vpt']} vectors per thread, inputs "
+                                + ("copied into shared memory" if plan["tma"] else
+                                   "loaded into registers") if plan["ctas_per_row"]
                                 else "reduce_norm_quant_kernel (persistent)"),
                      "launches": reps * nsets})
         del g, calls, sets

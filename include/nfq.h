@@ -409,8 +409,10 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  * nfq_stage1_split: batches of at most max_tokens rows (-1 = the default
  *   limit, 0 = no batch) run on the small-batch stage-1 kernel, one row per
  *   cluster of ctas_per_row CTAs (0 = automatic) with vpt 16-byte vectors per
- *   thread (0 = automatic); larger batches run on the persistent kernel that
- *   nfq_stage1_plan describes.  The results are the same bits either way.
+ *   thread (0 = automatic), its inputs loaded into registers (tma = 0) or
+ *   copied into shared memory by bulk copies (tma = 1; -1 = automatic);
+ *   larger batches run on the persistent kernel that nfq_stage1_plan
+ *   describes.  The results are the same bits either way.
  * nfq_probe_fp8_mma: a measurement kernel, not part of the path.  `ctas`
  *   CTAs (pair != 0: `ctas` CTA pairs issuing cta_group::2 MMAs) each issue
  *   `iters` K blocks of four back-to-back tcgen05.mma kind::f8f6f4 from zeroed
@@ -429,9 +431,9 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   residual, BF16 [T][H]) in the grid that kernel uses at this size, without
  *   arithmetic or stores; the floor under stage 1's time.  Asynchronous on
  *   `stream`.
- * nfq_stage1_split_plan: the small-batch plan for (T, H) on num_sms SMs:
- *   out4 = {CTAs per row (0: the persistent kernel runs), vectors per thread,
- *   active threads, block threads}.
+ * nfq_stage1_split_plan: the small-batch plan for (T, H, k) on num_sms SMs:
+ *   out5 = {CTAs per row (0: the persistent kernel runs), vectors per thread,
+ *   active threads, block threads, 1 if the inputs go through shared memory}.
  */
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7);
 void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot);
@@ -439,12 +441,12 @@ void nfq_lm_head_small_batch(int enabled);
 void nfq_lm_head_pair(int enabled);
 void nfq_lm_head_nvfp4_tune(int stages);
 void nfq_stage1_grid(int max_ctas);
-void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt);
+void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma);
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,
                            int H, void *stream);
-int nfq_stage1_split_plan(int T, int H, int num_sms, int *out4);
+int nfq_stage1_split_plan(int T, int H, int k, int num_sms, int *out5);
 
 #ifdef __cplusplus
 }

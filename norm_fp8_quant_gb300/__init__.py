@@ -125,9 +125,10 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_nvfp4_tune.restype = None
     lib.nfq_stage1_grid.argtypes = [ctypes.c_int]
     lib.nfq_stage1_grid.restype = None
-    lib.nfq_stage1_split.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.nfq_stage1_split.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
     lib.nfq_stage1_split.restype = None
-    lib.nfq_stage1_split_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_stage1_split_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          _P]
     lib.nfq_stage1_split_plan.restype = ctypes.c_int
     lib.nfq_mtp_draft_chain_nvfp4.argtypes = [ctypes.c_int, _P, ctypes.c_int, _P, _P,
                                               ctypes.c_float, ctypes.c_int, ctypes.c_int, _P,
@@ -642,17 +643,18 @@ def stage1_grid(max_ctas: int = 0):
     load().nfq_stage1_grid(max_ctas)
 
 
-def stage1_split(max_tokens: int = -1, ctas_per_row: int = 0, vpt: int = 0):
+def stage1_split(max_tokens: int = -1, ctas_per_row: int = 0, vpt: int = 0, tma: int = -1):
     """Small-batch stage-1 kernel: batches of at most max_tokens rows (-1 the
     default limit, 0 none), ctas_per_row CTAs per row and vpt vectors per
-    thread (0 = automatic); for tuning sweeps and tests."""
-    load().nfq_stage1_split(max_tokens, ctas_per_row, vpt)
+    thread (0 = automatic), inputs through registers (tma 0) or shared memory
+    (tma 1; -1 automatic); for tuning sweeps and tests."""
+    load().nfq_stage1_split(max_tokens, ctas_per_row, vpt, tma)
 
 
-def stage1_split_plan(T: int, H: int, num_sms: int = 152):
-    out = (ctypes.c_int * 4)()
-    _check(load().nfq_stage1_split_plan(T, H, num_sms, out), "nfq_stage1_split_plan")
-    return dict(zip(["ctas_per_row", "vpt", "active_threads", "threads"], list(out)))
+def stage1_split_plan(T: int, H: int, k: int = 8, num_sms: int = 152):
+    out = (ctypes.c_int * 5)()
+    _check(load().nfq_stage1_split_plan(T, H, k, num_sms, out), "nfq_stage1_split_plan")
+    return dict(zip(["ctas_per_row", "vpt", "active_threads", "threads", "tma"], list(out)))
 
 
 # ---------------------------------------------------- unfused reference arm --

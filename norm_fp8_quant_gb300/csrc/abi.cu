@@ -639,14 +639,15 @@ void nfq_lm_head_nvfp4_tune(int stages) { stage2_fp4_set_stages(stages); }
 
 void nfq_stage1_grid(int max_ctas) { stage1_set_grid(max_ctas); }
 
-void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt) {
-  stage1_set_split(max_tokens, ctas_per_row, vpt);
+void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma) {
+  stage1_set_split(max_tokens, ctas_per_row, vpt, tma);
 }
 
-int nfq_stage1_split_plan(int T, int H, int num_sms, int *out4) {
-  if (!out4) return NFQ_ERR_NULL;
-  if (H < 128 || H % 128 || T < 1 || num_sms < 1) return NFQ_ERR_SHAPE;
-  return stage1_split_plan(T, H, num_sms, out4);
+int nfq_stage1_split_plan(int T, int H, int k, int num_sms, int *out5) {
+  if (!out5) return NFQ_ERR_NULL;
+  if (H < 128 || H % 128 || T < 1 || k < 1 || k > kMaxPartials || num_sms < 1)
+    return NFQ_ERR_SHAPE;
+  return stage1_split_plan(T, H, k, num_sms, out5);
 }
 
 int nfq_stage1_plan(int T, int H, int k, int num_sms, int *out7) {

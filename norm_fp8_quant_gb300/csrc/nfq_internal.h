@@ -45,9 +45,10 @@ void stage1_set_tuning(int cluster, int vpt, int slots, int per_slot);
 void stage1_set_grid(int max_ctas);   // 0: one CTA (cluster) per SM at most
 // Small batches: batches of at most max_tokens rows (-1: the default limit, 0:
 // none) run one row per cluster of ctas_per_row CTAs (0: automatic) with vpt
-// vectors per thread (0: automatic).
-void stage1_set_split(int max_tokens, int ctas_per_row, int vpt);
-int stage1_split_plan(int T, int H, int num_sms, int *out4);
+// vectors per thread (0: automatic), the inputs loaded into registers (tma 0)
+// or copied into shared memory (tma 1; -1: automatic).
+void stage1_set_split(int max_tokens, int ctas_per_row, int vpt, int tma);
+int stage1_split_plan(int T, int H, int k, int num_sms, int *out5);
 // Measurement: the small-batch kernel's loads alone (its grid at this size).
 cudaError_t launch_stage1_reads(Stage1Params p, int num_sms, cudaStream_t stream);
 int stage1_plan(int T, int H, int k, int num_sms, int *out7);

@@ -344,14 +344,23 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
 // that every peer has begun), then one cluster barrier publishes them.  The
 // NVFP4 form repeats that exchange for the row maximum of |hidden|.  No wait
 // is data-dependent: every thread reaches every barrier.
+//
+// kTma (batches above 96 rows with more than 9 inputs): the slice's k + 1
+// inputs are instead copied into shared memory by 1-D bulk copies, all
+// requested at once under one mbarrier, and the threads add from there, so
+// registers do not split the loads into several rounds.  Two CTAs of up to
+// 112 KB of slices fit on an SM.
 constexpr int kSplitMaxThreads = 512;
 
-template <int VPT, bool kFp4>
+template <int VPT, bool kFp4, bool kTma>
 __global__ void __launch_bounds__(kSplitMaxThreads)
     stage1_split_kernel(const Stage1Params p) {
   constexpr int NB = VPT == 1 ? 17 : VPT == 2 ? 9 : 4;   // inputs per batch of loads
   __shared__ float gsum[kMaxGroups];
   __shared__ float gmax[kMaxGroups];
+  __shared__ uint64_t in_full;        // kTma: every input slice has landed
+  __shared__ int abort_word;
+  extern __shared__ __align__(128) uint8_t in_slices[];   // kTma: [k + 1][E] BF16
   const int R = p.C;
   const uint32_t rank = R > 1 ? cluster_ctarank() : 0u;
   const int r = R > 1 ? (int)cluster_id_x() : (int)blockIdx.x;
@@ -359,6 +368,14 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
   const int col0 = (int)rank * E;
   const int tc = (int)threadIdx.x;
   const bool active = tc < NA;
+  if constexpr (kTma) {
+    if (tc == 0) {
+      mbar_init(smem_u32(&in_full), 1);
+      abort_word = 0;
+      fence_mbarrier_init();
+    }
+    __syncthreads();
+  }
   if (R > 1) cluster_arrive_relaxed();   // this CTA has started
   // the previous kernel on the stream may write this one's inputs, or still
   // read the buffers this one writes
@@ -367,13 +384,40 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
 
   const size_t rowv = ((size_t)r * (size_t)p.H + (size_t)col0) / 8u;   // first vector of the slice
   const uint64_t pol = policy_evict_first();
+  if constexpr (kTma) {
+    if (tc == 0) {
+      const uint32_t in_bytes = (uint32_t)E * 2u;
+      mbar_arrive_expect_tx(smem_u32(&in_full), in_bytes * (uint32_t)(p.k + 1));
+      for (int i = 0; i <= p.k; ++i)
+        bulk_g2s(smem_u32(in_slices + (size_t)i * in_bytes),
+                 static_cast<const uint4 *>(i < p.k ? p.partials[i] : p.residual) + rowv,
+                 in_bytes, smem_u32(&in_full), pol);
+    }
+  }
   uint4 wpk[VPT];
   const uint4 *wsrc = static_cast<const uint4 *>(p.norm_w) + col0 / 8;
 #pragma unroll
   for (int v = 0; v < VPT; ++v)
     wpk[v] = active ? __ldg(wsrc + v * NA + tc) : make_uint4(0u, 0u, 0u, 0u);
   float x[VPT][8];
-  for (int i0 = 0; i0 <= p.k; i0 += NB) {
+  if constexpr (kTma) {
+    // every thread waits (bounded); after an expired wait the copies still in
+    // flight are waited for, again with a limit, and the results are garbage
+    // (the device error word says so) but every barrier below is still reached
+    if (!mbar_wait(smem_u32(&in_full), 0u, &abort_word, p.err, kErrBitStage1))
+      mbar_wait_drain(smem_u32(&in_full), 0u);
+    const uint4 *sl = reinterpret_cast<const uint4 *>(in_slices);
+    const int vecs = E / 8;
+    for (int i = 0; i <= p.k; ++i) {
+#pragma unroll
+      for (int v = 0; v < VPT; ++v) {
+        const uint4 d = active ? sl[(size_t)i * vecs + v * NA + tc] : make_uint4(0u, 0u, 0u, 0u);
+        if (i == 0) unpack_bf16x8(d, x[v]);
+        else add_bf16x8(x[v], d);   // x += input, fp32, in input order
+      }
+    }
+  }
+  for (int i0 = 0; i0 <= p.k && !kTma; i0 += NB) {
     uint4 in[NB][VPT];
 #pragma unroll
     for (int c = 0; c < NB; ++c) {
@@ -575,9 +619,11 @@ int g_tune_C = 0, g_tune_vpt = 0, g_tune_slots = 0, g_tune_per_slot = 0, g_tune_
 constexpr int kSplitDefaultMaxT = 512;   // largest batch run by the small-batch kernel
 int g_split_max_T = -1;                  // tuning: -1 automatic, 0 never, else the limit
 int g_split_R = 0, g_split_vpt = 0;      // tuning: 0 automatic
+int g_split_tma = -1;                    // tuning: -1 automatic, 0 register loads, 1 bulk copies
+constexpr size_t kTmaSliceMax = 112u * 1024u;   // input slices of a CTA: two CTAs per SM
 
 struct SplitChoice {
-  int R, VPT, NA, threads;
+  int R, VPT, NA, threads, tma;
 };
 
 // R CTAs per row and VPT vectors per thread: whole groups per CTA, whole
@@ -589,7 +635,7 @@ bool split_shape(int G, int R, int vpt, SplitChoice &c) {
   const int na = 16 * gc / vpt;
   const int threads = (na + 31) / 32 * 32;
   if (threads > kSplitMaxThreads) return false;
-  c = SplitChoice{R, vpt, na, threads};
+  c = SplitChoice{R, vpt, na, threads, 0};
   return true;
 }
 
@@ -605,12 +651,35 @@ bool split_shape(int G, int R, int vpt, SplitChoice &c) {
 //  - above: the persistent kernel (T = 1024: 29.0 us against 30.0 us).
 // A shape the width does not allow falls back to the next vectors-per-thread
 // choice, then to the next R.
-SplitChoice choose_split(int T, int H, int num_sms) {
+SplitChoice choose_split(int T, int H, int k, int num_sms) {
   (void)num_sms;
-  SplitChoice none{0, 0, 0, 0};
+  SplitChoice none{0, 0, 0, 0, 0};
   const int max_T = g_split_max_T >= 0 ? g_split_max_T : kSplitDefaultMaxT;
   if (T < 1 || T > max_T) return none;
   const int G = H / 128;
+  // Above 96 rows with more than 9 inputs (more than a register batch of two
+  // vectors a thread): the inputs through shared memory (bulk copies), the
+  // smallest R whose slices of the k + 1 inputs leave room for two CTAs an
+  // SM.  With k <= 8 the register loads measured as fast or faster (T = 128:
+  // 5.6 against 6.1 us; T = 256: 9.4 against 9.1 us; tie stress, k = 4: 7.5
+  // against 7.8 us).
+  const bool want_tma = g_split_tma >= 0 ? g_split_tma != 0 : (T > 96 && k > 8);
+  if (want_tma) {
+    const int order[3] = {2, 1, 4};
+    for (int R = 1; R <= 8; ++R) {
+      if (g_split_R > 0 && R != g_split_R) continue;
+      if (G % R != 0 || (size_t)(k + 1) * (size_t)(H / R) * 2u > kTmaSliceMax) continue;
+      for (int v : order) {
+        if (g_split_vpt > 0 && v != g_split_vpt) continue;
+        SplitChoice c = none;
+        if (split_shape(G, R, v, c)) {
+          c.tma = 1;
+          return c;
+        }
+      }
+    }
+    if (g_split_tma > 0) return none;   // forced, but no shape fits: the persistent kernel
+  }
   int target;   // CTAs the batch should reach
   int order[3];
   if (T <= 24) {
@@ -640,11 +709,20 @@ SplitChoice choose_split(int T, int H, int num_sms) {
 
 template <int VPT>
 cudaError_t launch_split_vpt(const Stage1Params &p, const SplitChoice &c, cudaStream_t stream) {
-  auto kern = p.fp4 ? stage1_split_kernel<VPT, true> : stage1_split_kernel<VPT, false>;
+  auto kern = c.tma ? (p.fp4 ? stage1_split_kernel<VPT, true, true>
+                             : stage1_split_kernel<VPT, false, true>)
+                    : (p.fp4 ? stage1_split_kernel<VPT, true, false>
+                             : stage1_split_kernel<VPT, false, false>);
+  const size_t smem = c.tma ? (size_t)(p.k + 1) * (size_t)p.E * 2u : 0u;
+  if (c.tma) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.T * c.R));
   cfg.blockDim = dim3((unsigned)c.threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int n = 0;
@@ -805,28 +883,32 @@ bool stage1_fp4_supported(int H) {
   return H % 256 == 0 && H >= 256 && H <= 16384 && choose_stage1(1, H, 1, 1, true).VPT != 0;
 }
 
-void stage1_set_split(int max_tokens, int ctas_per_row, int vpt) {
+void stage1_set_split(int max_tokens, int ctas_per_row, int vpt, int tma) {
   g_split_max_T = max_tokens;
   g_split_R = ctas_per_row;
   g_split_vpt = vpt;
+  g_split_tma = tma;
 }
 
-int stage1_split_plan(int T, int H, int num_sms, int *out4) {
-  const SplitChoice c = choose_split(T, H, num_sms);
-  out4[0] = c.R;
-  out4[1] = c.VPT;
-  out4[2] = c.NA;
-  out4[3] = c.threads;
+int stage1_split_plan(int T, int H, int k, int num_sms, int *out5) {
+  const SplitChoice c = choose_split(T, H, k, num_sms);
+  out5[0] = c.R;
+  out5[1] = c.VPT;
+  out5[2] = c.NA;
+  out5[3] = c.threads;
+  out5[4] = c.tma;
   return 0;
 }
 
 // The small-batch kernel's loads alone, in the grid launch_stage1 would use
 // for the small-batch kernel at this size (forced for any T).
 cudaError_t launch_stage1_reads(Stage1Params p, int num_sms, cudaStream_t stream) {
-  const int saved = g_split_max_T;
+  const int saved = g_split_max_T, saved_tma = g_split_tma;
   g_split_max_T = 1 << 30;
-  const SplitChoice c = choose_split(p.T, p.H, num_sms);
+  g_split_tma = 0;   // the register-load form: its loads are what the probe mirrors
+  const SplitChoice c = choose_split(p.T, p.H, p.k, num_sms);
   g_split_max_T = saved;
+  g_split_tma = saved_tma;
   if (c.R == 0) return cudaErrorInvalidConfiguration;
   p.C = c.R;
   p.E = p.H / c.R;
@@ -858,7 +940,7 @@ cudaError_t launch_stage1_reads(Stage1Params p, int num_sms, cudaStream_t stream
 }
 
 cudaError_t launch_stage1(Stage1Params p, int num_sms, cudaStream_t stream) {
-  const SplitChoice sc = choose_split(p.T, p.H, num_sms);
+  const SplitChoice sc = choose_split(p.T, p.H, p.k, num_sms);
   if (sc.R > 0) return launch_split(p, sc, stream);
   Stage1Choice ch = choose_stage1(p.T, p.H, p.k, num_sms, p.fp4 != 0);
   if (ch.VPT == 0) return cudaErrorInvalidConfiguration;

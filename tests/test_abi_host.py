@@ -116,41 +116,63 @@ def _split_valid(G, r, u):
 
 def test_stage1_split_plans(lib):
     """The small-batch kernel: whole groups per CTA, whole 16-lane groups per
-    vector slot, at most 512 threads; R and vectors per thread by batch size
-    as documented (T <= 24: T*R >= 64, one vector; T <= 96: T*R >= 256, one
-    vector; T <= 160: R = 1, two vectors; T <= 512: R = 1, four vectors);
-    larger batches go to the persistent kernel (R = 0)."""
-    for (T, H) in [(1, 7168), (4, 1024), (16, 6144), (64, 6144), (64, 7168), (128, 6144),
-                   (256, 6144), (300, 7168), (3, 128), (2, 16384), (1, 32768), (17, 896),
-                   (512, 2048)]:
-        p = nfq.stage1_split_plan(T, H, 152)
+    vector slot, at most 512 threads.  Batches above 96 rows copy the inputs
+    into shared memory when k > 8, with the smallest R whose (k+1) input
+    slices fit in 112 KB (two CTAs an SM); the rest load into registers, with R and the
+    vectors per thread by batch size (T <= 24: T*R >= 64, one vector; T <= 96:
+    T*R >= 256, one vector); batches above 512 rows go to the persistent
+    kernel (R = 0)."""
+    for (T, H, k) in [(1, 7168, 8), (4, 1024, 2), (16, 6144, 8), (64, 6144, 8), (64, 7168, 8),
+                      (128, 6144, 8), (256, 6144, 4), (256, 6144, 8), (300, 7168, 8),
+                      (3, 128, 1), (2, 16384, 4), (1, 32768, 2), (17, 896, 3), (512, 2048, 16),
+                      (200, 16384, 16)]:
+        p = nfq.stage1_split_plan(T, H, k, num_sms=152)
         G = H // 128
         R, v = p["ctas_per_row"], p["vpt"]
         assert R >= 1 and _split_valid(G, R, v), (T, H)
         assert p["active_threads"] == 16 * (G // R) // v and p["threads"] <= 512
-        target, order = ((64, (1, 2, 4)) if T <= 24 else (256, (1, 2, 4)) if T <= 96 else
-                         (1, (2, 1, 4)) if T <= 160 else (1, (4, 2, 1)))
         want = None
-        for r in range(1, 9):
-            u = next((u for u in order if _split_valid(G, r, u)), None)
-            if u is None:
-                continue
-            want = (r, u)
-            if T * r >= target:
-                break
-        assert (R, v) == want, (T, H, R, v, want)
-    assert nfq.stage1_split_plan(64, 6144, 152)["ctas_per_row"] == 4
-    assert nfq.stage1_split_plan(513, 6144, 152)["ctas_per_row"] == 0
-    assert nfq.stage1_split_plan(8192, 7168, 152)["ctas_per_row"] == 0
+        if T > 96 and k > 8:
+            for r in range(1, 9):
+                if G % r or (k + 1) * (H // r) * 2 > 112 * 1024:
+                    continue
+                u = next((u for u in (2, 1, 4) if _split_valid(G, r, u)), None)
+                if u is not None:
+                    want = (r, u, 1)
+                    break
+        if want is None:
+            target, order = ((64, (1, 2, 4)) if T <= 24 else (256, (1, 2, 4)) if T <= 96 else
+                             (1, (2, 1, 4)) if T <= 160 else (1, (4, 2, 1)))
+            for r in range(1, 9):
+                u = next((u for u in order if _split_valid(G, r, u)), None)
+                if u is None:
+                    continue
+                want = (r, u, 0)
+                if T * r >= target:
+                    break
+        assert (R, v, p["tma"]) == want, (T, H, k, R, v, p["tma"], want)
+    assert nfq.stage1_split_plan(64, 6144, 8)["ctas_per_row"] == 4
+    assert nfq.stage1_split_plan(256, 6144, 8)["tma"] == 0
+    assert nfq.stage1_split_plan(256, 6144, 16)["tma"] == 1
+    assert nfq.stage1_split_plan(513, 6144, 8)["ctas_per_row"] == 0
+    assert nfq.stage1_split_plan(8192, 7168, 8)["ctas_per_row"] == 0
     nfq.stage1_split(0)
     try:
-        assert nfq.stage1_split_plan(64, 6144, 152)["ctas_per_row"] == 0
+        assert nfq.stage1_split_plan(64, 6144, 8)["ctas_per_row"] == 0
     finally:
         nfq.stage1_split()
-    nfq.stage1_split(-1, 4, 2)
+    nfq.stage1_split(-1, 4, 2, 0)
     try:
-        p = nfq.stage1_split_plan(64, 6144, 152)
-        assert (p["ctas_per_row"], p["vpt"], p["threads"]) == (4, 2, 96)
+        p = nfq.stage1_split_plan(64, 6144, 8)
+        assert (p["ctas_per_row"], p["vpt"], p["threads"], p["tma"]) == (4, 2, 96, 0)
+        p = nfq.stage1_split_plan(256, 6144, 8)
+        assert (p["ctas_per_row"], p["tma"]) == (4, 0)
+    finally:
+        nfq.stage1_split()
+    nfq.stage1_split(-1, 0, 0, 1)
+    try:
+        p = nfq.stage1_split_plan(16, 6144, 8)
+        assert (p["ctas_per_row"], p["vpt"], p["tma"]) == (1, 2, 1)
     finally:
         nfq.stage1_split()
 

@@ -148,11 +148,12 @@ def _stage1_bytes(nfq, parts, res, nw, fp4=False):
 
 @pytest.mark.parametrize("fp4", [False, True])
 @pytest.mark.parametrize("T,H,k", [(64, 6144, 8), (1, 7168, 8), (256, 6144, 4), (5, 1024, 3),
-                                   (2, 16384, 2), (300, 2048, 5)])
+                                   (2, 16384, 2), (300, 2048, 5), (160, 7168, 16)])
 def test_stage1_kernels_and_shapes_give_the_same_bits(nfq, fp4, T, H, k):
     """The small-batch kernel (every valid CTAs-per-row and vectors-per-thread
-    shape) and the persistent kernel take the row's sum of squares in one
-    order, so they return the same bytes; all of them match the oracle."""
+    shape, inputs through registers or through shared memory) and the
+    persistent kernel take the row's sum of squares in one order, so they
+    return the same bytes; all of them match the oracle."""
     w = synth.workload("tiny", T=T, H=H, k=k, seed=T + H + k)
     inp = synth.stage1_inputs(w)
     parts = [to_dev_bf16(p) for p in inp["partials"]]
@@ -165,10 +166,15 @@ def test_stage1_kernels_and_shapes_give_the_same_bits(nfq, fp4, T, H, k):
                   if G % R == 0 and (G // R) % v == 0 and -(-(16 * (G // R) // v) // 32) * 32 <= 512]
         assert shapes
         for R, v in shapes:
-            nfq.stage1_split(1 << 20, R, v)
-            got = _stage1_bytes(nfq, parts, res, nw, fp4)
-            for a, b in zip(base, got):
-                assert np.array_equal(a, b), (R, v)
+            # inputs through registers, then through shared memory (bulk copies)
+            for tma in (0, 1):
+                if tma and (k + 1) * (H // R) * 2 > 112 * 1024:
+                    continue
+                nfq.stage1_split(1 << 20, R, v, tma)
+                assert nfq.stage1_split_plan(T, H, k)["tma"] == tma
+                got = _stage1_bytes(nfq, parts, res, nw, fp4)
+                for a, b in zip(base, got):
+                    assert np.array_equal(a, b), (R, v, tma)
     finally:
         nfq.stage1_split()
     ref = run_oracle(inp)
