@@ -359,6 +359,7 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
   __shared__ float gsum[kMaxGroups];
   __shared__ float gmax[kMaxGroups];
   __shared__ uint64_t in_full;        // kTma: every input slice has landed
+  __shared__ uint64_t xch[2];         // R > 1: the row's group sums / maxima have landed
   __shared__ int abort_word;
   extern __shared__ __align__(128) uint8_t in_slices[];   // kTma: [k + 1][E] BF16
   const int R = p.C;
@@ -368,15 +369,27 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
   const int col0 = (int)rank * E;
   const int tc = (int)threadIdx.x;
   const bool active = tc < NA;
-  if constexpr (kTma) {
+  if (kTma || R > 1) {
     if (tc == 0) {
-      mbar_init(smem_u32(&in_full), 1);
+      if (kTma) mbar_init(smem_u32(&in_full), 1);
+      if (R > 1) {
+        // the exchanges: each group's value arrives from the CTA that holds it
+        // as 4 bytes counted on these barriers (st.async)
+        mbar_init(smem_u32(&xch[0]), 1);
+        mbar_init(smem_u32(&xch[1]), 1);
+      }
       abort_word = 0;
       fence_mbarrier_init();
+      if (R > 1) {
+        mbar_arrive_expect_tx(smem_u32(&xch[0]), (uint32_t)G * 4u);
+        if (kFp4) mbar_arrive_expect_tx(smem_u32(&xch[1]), (uint32_t)G * 4u);
+      }
     }
     __syncthreads();
   }
-  if (R > 1) cluster_arrive_relaxed();   // this CTA has started
+  // this CTA has started and its exchange barriers exist (release: the peers
+  // see them initialised once their wait returns)
+  if (R > 1) cluster_arrive_release();
   // the previous kernel on the stream may write this one's inputs, or still
   // read the buffers this one writes
   grid_dependency_wait();
@@ -451,14 +464,21 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
     for (int v = 0; v < VPT; ++v) {
       const int g = (col0 + (v * NA + tc) * 8) / 128;
       if (R > 1) {
-        for (int q = 0; q < R; ++q) st_remote_f32(smem_u32(&gsum[g]), (uint32_t)q, lead[v]);
+        for (int q = 0; q < R; ++q)
+          st_async_remote_f32(smem_u32(&gsum[g]), smem_u32(&xch[0]), (uint32_t)q, lead[v]);
       } else {
         gsum[g] = lead[v];
       }
     }
   }
-  if (R > 1) cluster_sync_all();
-  else __syncthreads();
+  if (R > 1) {
+    // all G group sums are in this CTA's gsum once the barrier has counted
+    // their bytes; after an expired wait the results are garbage (the device
+    // error word says so) but every barrier below is still reached
+    mbar_wait(smem_u32(&xch[0]), 0u, &abort_word, p.err, kErrBitStage1);
+  } else {
+    __syncthreads();
+  }
   const float tot = row_total(gsum, G);
   const float ms = __fdiv_rn(tot, (float)p.H);
   const float rr = __frsqrt_rn(__fadd_rn(ms, p.eps));
@@ -496,13 +516,14 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
       for (int v = 0; v < VPT; ++v) {
         const int g = (col0 + (v * NA + tc) * 8) / 128;
         if (R > 1) {
-          for (int q = 0; q < R; ++q) st_remote_f32(smem_u32(&gmax[g]), (uint32_t)q, gm[v]);
+          for (int q = 0; q < R; ++q)
+            st_async_remote_f32(smem_u32(&gmax[g]), smem_u32(&xch[1]), (uint32_t)q, gm[v]);
         } else {
           gmax[g] = gm[v];
         }
       }
     }
-    if (R > 1) cluster_sync_all();
+    if (R > 1) mbar_wait(smem_u32(&xch[1]), 0u, &abort_word, p.err, kErrBitStage1);
     else __syncthreads();
     const float amax_row = row_max(gmax, G);
     const float g = __fdiv_rn(amax_row, 2688.0f);     // 448 * 6

@@ -280,6 +280,27 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
+// Arrive on the cluster barrier with release semantics (publishes this CTA's
+// earlier writes, such as mbarrier initialisation, to the CTAs that wait).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// 4-byte store into the shared memory of CTA `rank` that counts its bytes on
+// the mbarrier at offset `bar` of that CTA (complete_tx): the receiver learns
+// of the value by waiting on its own barrier, no cluster-wide barrier needed.
+__device__ __forceinline__ void st_async_remote_f32(uint32_t local_addr, uint32_t bar,
+                                                    uint32_t rank, float v) {
+  asm volatile(
+      "{\n\t.reg .b32 ra, rb;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, %2;\n\t"
+      "mapa.shared::cluster.u32 rb, %1, %2;\n\t"
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [ra], %3, [rb];\n\t}" ::"r"(
+          local_addr),
+      "r"(bar), "r"(rank), "r"(__float_as_uint(v))
+      : "memory");
+}
+
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
