@@ -944,11 +944,11 @@ def run_probe_mma(args, local):
     torch.cuda.set_device(local)
     sms = torch.cuda.get_device_properties(local).multi_processor_count
     rows = []
-    for pair in (False, True):
+    for pair, stages in ((False, 1), (True, 1), (False, 4), (True, 4)):
         ctas = sms // 2 if pair else sms
         iters = 2048
         for _ in range(3):
-            nfq.probe_fp8_mma(pair, ctas, iters)
+            nfq.probe_fp8_mma(pair, ctas, iters, stages)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -956,7 +956,7 @@ def run_probe_mma(args, local):
         flops = 0.0
         e0.record()
         for _ in range(n):
-            flops += nfq.probe_fp8_mma(pair, ctas, iters)
+            flops += nfq.probe_fp8_mma(pair, ctas, iters, stages)
         e1.record()
         torch.cuda.synchronize()
         if nfq.device_error() != nfq.NFQ_OK:
@@ -965,6 +965,7 @@ def run_probe_mma(args, local):
         mma_ns = ms * 1e6 / (n * iters * 4)
         rows.append({"shape": ("cta_group::2, M=256 x N=256 x K=32 per CTA pair" if pair else
                                "cta_group::1, M=128 x N=256 x K=32 per CTA"),
+                     "operand_sets": stages,
                      "ctas": 2 * ctas if pair else ctas, "launches": n,
                      "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
                      "ns_per_mma": round(mma_ns, 2)})

@@ -417,9 +417,11 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   CTAs (pair != 0: `ctas` CTA pairs issuing cta_group::2 MMAs) each issue
  *   `iters` K blocks of four back-to-back tcgen05.mma kind::f8f6f4 from zeroed
  *   shared-memory tiles, M = 128 (pairs: 256) x N = 256 x K = 32 each, into
- *   TMEM; 2 * M * 256 * 128 * iters flops per CTA (per pair).  Asynchronous on
- *   `stream`; time it with events.  NFQ_ERR_SHAPE for ctas outside 1..4096 or
- *   iters outside 1..2^20.
+ *   TMEM; 2 * M * 256 * 128 * iters flops per CTA (per pair).  K block i reads
+ *   the tiles of set i % stages (1..4 sets: with more than one, every K block
+ *   reads operands the previous one did not).  Asynchronous on `stream`; time
+ *   it with events.  NFQ_ERR_SHAPE for ctas outside 1..4096, iters outside
+ *   1..2^20 or stages outside 1..4.
  * nfq_probe_tmem_ld: a measurement kernel, not part of the path.  `ctas` CTAs
  *   of 16 warps each read a 128-lane x 256-column TMEM accumulator into
  *   registers `iters` times, in the LM head epilogue's pattern (each warp 32
@@ -442,7 +444,7 @@ void nfq_lm_head_pair(int enabled);
 void nfq_lm_head_nvfp4_tune(int stages);
 void nfq_stage1_grid(int max_ctas);
 void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma);
-int nfq_probe_fp8_mma(int pair, int ctas, int iters, void *stream);
+int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,
                            int H, void *stream);

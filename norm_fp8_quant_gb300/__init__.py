@@ -102,7 +102,7 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_small_batch.restype = None
     lib.nfq_lm_head_pair.argtypes = [ctypes.c_int]
     lib.nfq_lm_head_pair.restype = None
-    lib.nfq_probe_fp8_mma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_probe_fp8_mma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_fp8_mma.restype = ctypes.c_int
     lib.nfq_probe_tmem_ld.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_tmem_ld.restype = ctypes.c_int
@@ -392,13 +392,13 @@ def lm_head_small_batch(enabled: bool = True):
     load().nfq_lm_head_small_batch(1 if enabled else 0)
 
 
-def probe_fp8_mma(pair: bool, ctas: int, iters: int, stream=None):
+def probe_fp8_mma(pair: bool, ctas: int, iters: int, stages: int = 1, stream=None):
     """Launch the FP8 MMA-rate measurement kernel (not part of the path):
-    `ctas` CTAs (or CTA pairs) each issuing `iters` K blocks of four MMAs.
-    Returns the flops the launch performs."""
+    `ctas` CTAs (or CTA pairs) each issuing `iters` K blocks of four MMAs, K
+    block i on operand set i % stages.  Returns the flops the launch performs."""
     import torch
     dev = torch.cuda.current_device()
-    _check(_on_device(dev, load().nfq_probe_fp8_mma, 1 if pair else 0, ctas, iters,
+    _check(_on_device(dev, load().nfq_probe_fp8_mma, 1 if pair else 0, ctas, iters, stages,
                       _raw_stream(dev, stream)), "nfq_probe_fp8_mma")
     M = 256 if pair else 128
     return 2.0 * M * 256 * 128 * iters * ctas

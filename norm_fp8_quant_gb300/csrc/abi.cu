@@ -192,6 +192,10 @@ int nfq_lm_head_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
 
 namespace nfq {
 
+// The MMA-rate probe with `stages` sets of operand tiles (probe.cu).
+cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stages,
+                                        unsigned *err, cudaStream_t stream);
+
 // Every argument of an FP8 LM-head call except the workspace: NULL pointers,
 // shapes and alignment.  Queues nothing.
 int lm_head_check_args(const nfq_quant_act *a, const uint8_t *w, const float *w_scales, int V,
@@ -664,13 +668,14 @@ void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot) {
 // small-batch kernel, 0 the weight-major kernel used for larger batches.
 void nfq_lm_head_small_batch(int enabled) { stage2_set_small(enabled); }
 
-int nfq_probe_fp8_mma(int pair, int ctas, int iters, void *stream) {
-  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20)) return NFQ_ERR_SHAPE;
+int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream) {
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || stages < 1 || stages > 4)
+    return NFQ_ERR_SHAPE;
   DeviceInfo *d = nullptr;
   const int st = device_info(&d);
   if (st != NFQ_OK) return st;
-  return map_cuda(launch_probe_fp8_mma(pair ? 1 : 0, ctas, iters, d->err,
-                                       static_cast<cudaStream_t>(stream)));
+  return map_cuda(launch_probe_fp8_mma_stages(pair ? 1 : 0, ctas, iters, stages, d->err,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,

@@ -5,12 +5,13 @@
 // head's per-K-block promotion when it holds 128 tokens per SM).
 //
 // fp8_mma_rate_kernel<kPair>: every CTA (kPair: every CTA pair, cta_group::2)
-// zeroes an A tile and a B tile in shared memory, allocates one 256-column
-// TMEM accumulator and has one thread issue `iters` K blocks of four
-// back-to-back tcgen05.mma kind::f8f6f4 (K = 32 bytes each) with the shapes
-// the LM head uses: M = 128 tokens x N = 256 weight rows per CTA, or M = 256 x
-// N = 256 per pair (each CTA holding 128 A rows and 128 B rows).  A commit at
-// the end arrives on an mbarrier, waited for with the usual time limit.
+// zeroes `stages` pairs of A and B tiles in shared memory, allocates one
+// 256-column TMEM accumulator and has one thread issue `iters` K blocks of
+// four back-to-back tcgen05.mma kind::f8f6f4 (K = 32 bytes each), K block i
+// reading the tiles of stage i % stages, with the shapes the LM head uses:
+// M = 128 tokens x N = 256 weight rows per CTA, or M = 256 x N = 256 per pair
+// (each CTA holding 128 A rows and 128 B rows).  A commit at the end arrives
+// on an mbarrier, waited for with the usual time limit.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -25,7 +26,8 @@ namespace {
 constexpr int kProbeErrBit = 4;
 
 template <bool kPair>
-__global__ void __launch_bounds__(128, 1) fp8_mma_rate_kernel(int iters, unsigned *err) {
+__global__ void __launch_bounds__(128, 1)
+    fp8_mma_rate_kernel(int iters, int stages, unsigned *err) {
   // A: 128 rows x 128 bytes; B: 256 rows (one CTA) or 128 rows (each CTA of a pair)
   constexpr uint32_t kA = 128 * 128, kB = (kPair ? 128 : 256) * 128;
   extern __shared__ uint8_t smem_raw[];
@@ -39,7 +41,7 @@ __global__ void __launch_bounds__(128, 1) fp8_mma_rate_kernel(int iters, unsigne
   const bool issuer = !kPair || cluster_ctarank() == 0;
 
   uint4 *z = reinterpret_cast<uint4 *>(smem);
-  for (uint32_t i = threadIdx.x; i < (kA + kB) / 16; i += blockDim.x)
+  for (uint32_t i = threadIdx.x; i < (uint32_t)stages * (kA + kB) / 16; i += blockDim.x)
     z[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&done), 1);
@@ -64,9 +66,11 @@ __global__ void __launch_bounds__(128, 1) fp8_mma_rate_kernel(int iters, unsigne
 
   if (warp == 0) {
     if (issuer && lane == 0) {
-      const uint32_t a = smem_u32(smem), b = smem_u32(smem + kA);
       const uint32_t idesc = idesc_e4m3_f32(kPair ? 256 : 128, 256);
+      int st = 0;
       for (int it = 0; it < iters; ++it) {
+        const uint32_t a = smem_u32(smem + (size_t)st * (kA + kB)), b = a + kA;
+        st = (st + 1 == stages) ? 0 : st + 1;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           if constexpr (kPair)
@@ -165,10 +169,14 @@ cudaError_t launch_probe_tmem_ld(int batched, int ctas, int iters, cudaStream_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,
-                                 cudaStream_t stream) {
-  // the tiles need at most 49 KB; asking for 120 KB keeps one CTA per SM
-  const size_t smem = 120u * 1024u;
+// `stages` sets of tiles (1..4): each K block reads fresh operands from shared
+// memory, as the LM head's pipeline does, instead of the same tiles again.
+cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stages,
+                                        unsigned *err, cudaStream_t stream) {
+  if (stages < 1 || stages > 4) return cudaErrorInvalidValue;
+  // the tiles need at most 4 x 48 KB; at least 120 KB keeps one CTA per SM
+  const size_t tiles = 1024 + (size_t)stages * (128 * 128 + (pair ? 128 : 256) * 128);
+  const size_t smem = tiles > 120u * 1024u ? tiles : 120u * 1024u;
   auto kern = pair ? fp8_mma_rate_kernel<true> : fp8_mma_rate_kernel<false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -185,7 +193,12 @@ cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, iters, err);
+  return cudaLaunchKernelEx(&cfg, kern, iters, stages, err);
+}
+
+cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,
+                                 cudaStream_t stream) {
+  return launch_probe_fp8_mma_stages(pair, ctas, iters, 1, err, stream);
 }
 
 }  // namespace nfq

@@ -147,7 +147,8 @@ def test_nvfp4_lm_head_decode_c64_all_tokens(nfq):
                                      (100, 512, 3000, 3), (128, 256, 1536, 6),
                                      (129, 256, 1024, 8), (250, 512, 640, 5),
                                      (256, 256, 128, 1), (300, 512, 2000, 4),
-                                     (513, 256, 1024, 2), (7, 16384, 1000, 4)])
+                                     (513, 256, 1024, 2), (7, 16384, 1000, 4),
+                                     (200, 16384, 700, 7)])
 def test_nvfp4_lm_head_edge_shapes(nfq, T, H, V, S):
     """Ragged vocab tails, one-block tiles, shards narrower than a warp's
     columns, every lane quadrant, two token groups in one launch (129..256

@@ -18,13 +18,16 @@ def nfq():
 
 
 @pytest.mark.parametrize("pair", [False, True])
-def test_probe_fp8_mma_runs(nfq, pair):
-    flops = nfq.probe_fp8_mma(pair, 4, 16)
+@pytest.mark.parametrize("stages", [1, 4])
+def test_probe_fp8_mma_runs(nfq, pair, stages):
+    flops = nfq.probe_fp8_mma(pair, 4, 16, stages)
     torch.cuda.synchronize()
     assert nfq.device_error() == 0
     assert flops == 2.0 * (256 if pair else 128) * 256 * 128 * 16 * 4
     with pytest.raises(nfq.NfqError):
         nfq.probe_fp8_mma(pair, 0, 16)
+    with pytest.raises(nfq.NfqError):
+        nfq.probe_fp8_mma(pair, 4, 16, 5)
 
 
 @pytest.mark.parametrize("batched", [False, True])

@@ -211,3 +211,16 @@ def test_stage2_cta_pairs_equal_two_token_groups(nfq, T, H, V, S, layout):
         assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
     check_stage2(pair[0], ref["codes"], ref["scales"], qw, sw, S, list(range(T)), *pair[1:],
                  cache_key=("pair", T, H, V, S))
+
+
+@pytest.mark.parametrize("T", [64, 200])
+def test_stage2_large_vocab_max_shards(nfq, T, layout):
+    """A 262144-row vocabulary in the largest shard count (64 shards of 4096
+    rows, boundaries inside CTA ranges and tiles): every token, every shard's
+    result and the maxima against the oracle; 200 tokens run on CTA pairs."""
+    w = synth.workload("tiny", T=T, H=256, k=2, V=262144, S=64, seed=T + 7)
+    ref = stage1_ref(w)
+    qw, sw = synth.lm_head_weights(w)
+    tok, mx, sidx, sval = run_gpu(nfq, ref["codes"], ref["scales"], qw, sw, w.S, layout=layout)
+    check_stage2(tok, ref["codes"], ref["scales"], qw, sw, w.S, list(range(T)), mx, sidx, sval,
+                 cache_key=("large_vocab", T))
