@@ -944,7 +944,7 @@ def run_probe_mma(args, local):
     torch.cuda.set_device(local)
     sms = torch.cuda.get_device_properties(local).multi_processor_count
     rows = []
-    for pair, stages in ((False, 1), (True, 1), (False, 4), (True, 4)):
+    for pair, stages in ((False, 1), (True, 1), (False, 4), (True, 4), (False, 0)):
         ctas = sms // 2 if pair else sms
         iters = 2048
         for _ in range(3):
@@ -965,7 +965,9 @@ def run_probe_mma(args, local):
         mma_ns = ms * 1e6 / (n * iters * 4)
         rows.append({"shape": ("cta_group::2, M=256 x N=256 x K=32 per CTA pair" if pair else
                                "cta_group::1, M=128 x N=256 x K=32 per CTA"),
-                     "operand_sets": stages,
+                     "operand_sets": max(1, stages),
+                     "tmem_readers": ("16 warps reading TMEM meanwhile (the epilogue's pattern)"
+                                      if stages == 0 else None),
                      "ctas": 2 * ctas if pair else ctas, "launches": n,
                      "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
                      "ns_per_mma": round(mma_ns, 2)})

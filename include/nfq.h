@@ -419,9 +419,11 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   shared-memory tiles, M = 128 (pairs: 256) x N = 256 x K = 32 each, into
  *   TMEM; 2 * M * 256 * 128 * iters flops per CTA (per pair).  K block i reads
  *   the tiles of set i % stages (1..4 sets: with more than one, every K block
- *   reads operands the previous one did not).  Asynchronous on `stream`; time
- *   it with events.  NFQ_ERR_SHAPE for ctas outside 1..4096, iters outside
- *   1..2^20 or stages outside 1..4.
+ *   reads operands the previous one did not).  stages = 0 (one CTA, not
+ *   pairs): one operand set, while 16 other warps of the CTA read TMEM with
+ *   the LM head epilogue's pattern until the MMAs are done.  Asynchronous on
+ *   `stream`; time it with events.  NFQ_ERR_SHAPE for ctas outside 1..4096,
+ *   iters outside 1..2^20, stages outside 0..4, or pairs with stages = 0.
  * nfq_probe_tmem_ld: a measurement kernel, not part of the path.  `ctas` CTAs
  *   of 16 warps each read a 128-lane x 256-column TMEM accumulator into
  *   registers `iters` times, in the LM head epilogue's pattern (each warp 32

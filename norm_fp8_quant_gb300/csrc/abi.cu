@@ -192,9 +192,12 @@ int nfq_lm_head_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
 
 namespace nfq {
 
-// The MMA-rate probe with `stages` sets of operand tiles (probe.cu).
+// The MMA-rate probe with `stages` sets of operand tiles, and with 16 warps
+// reading TMEM meanwhile (probe.cu).
 cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stages,
                                         unsigned *err, cudaStream_t stream);
+cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
+                                          cudaStream_t stream);
 
 // Every argument of an FP8 LM-head call except the workspace: NULL pointers,
 // shapes and alignment.  Queues nothing.
@@ -669,11 +672,15 @@ void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot) {
 void nfq_lm_head_small_batch(int enabled) { stage2_set_small(enabled); }
 
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream) {
-  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || stages < 1 || stages > 4)
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || stages < 0 || stages > 4)
     return NFQ_ERR_SHAPE;
   DeviceInfo *d = nullptr;
   const int st = device_info(&d);
   if (st != NFQ_OK) return st;
+  if (stages == 0)   // one CTA per SM, with 16 warps reading TMEM during the MMAs
+    return pair ? NFQ_ERR_SHAPE
+                : map_cuda(launch_probe_mma_with_readers(ctas, iters, d->err,
+                                                         static_cast<cudaStream_t>(stream)));
   return map_cuda(launch_probe_fp8_mma_stages(pair ? 1 : 0, ctas, iters, stages, d->err,
                                               static_cast<cudaStream_t>(stream)));
 }

@@ -156,7 +156,90 @@ __global__ void __launch_bounds__(512, 1) tmem_ld_rate_kernel(int iters) {
   if (warp == 0) tmem_dealloc(tmem_base, 512);
 }
 
+// mma_with_readers_kernel: fp8_mma_rate_kernel's issue loop (one CTA, one
+// operand set, accumulator in TMEM columns 0..255) while 16 other warps read
+// TMEM columns 256..511 with the LM head epilogue's pattern, as long as the
+// MMAs run: the MMA rate the LM head's promotion leaves.  The readers stop
+// when the issuing thread's last MMA has completed (a flag in shared memory),
+// or after a fixed number of passes.
+__global__ void __launch_bounds__(17 * 32, 1) mma_with_readers_kernel(int iters, unsigned *err) {
+  constexpr uint32_t kA = 128 * 128, kB = 256 * 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  __shared__ uint64_t done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  __shared__ volatile int finished;
+  const int warp = (int)(threadIdx.x / 32), lane = (int)(threadIdx.x % 32);
+  uint4 *z = reinterpret_cast<uint4 *>(smem);
+  for (uint32_t i = threadIdx.x; i < (kA + kB) / 16; i += blockDim.x)
+    z[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&done), 1);
+    abort_flag = 0;
+    finished = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 16) {
+    tmem_alloc(smem_u32(&tmem_base), 512);
+    tmem_relinquish();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 16) {
+    if (lane == 0) {
+      const uint32_t a = smem_u32(smem), b = smem_u32(smem + kA);
+      const uint32_t idesc = idesc_e4m3_f32(128, 256);
+      for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8(tmem_base, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32),
+                 idesc, (it | kk) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&done));
+      if (!mbar_wait(smem_u32(&done), 0u, (volatile int *)&abort_flag, err, kProbeErrBit))
+        mbar_wait_drain(smem_u32(&done), 0u);
+      finished = 1;
+    }
+    __syncwarp();
+  } else {
+    const uint32_t ta = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + 256u +
+                        (uint32_t)(64 * (warp >> 2));
+    uint32_t x = 0;
+    for (int pass = 0; pass < (1 << 22); ++pass) {
+      if (__shfl_sync(0xffffffffu, finished, 0)) break;
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(ta + (uint32_t)c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x ^= r[j];
+      }
+    }
+    if (x == 0x9E3779B9u) atomicAdd(&g_tmem_probe_sink, 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 16) tmem_dealloc(tmem_base, 512);
+}
+
 }  // namespace
+
+cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
+                                          cudaStream_t stream) {
+  const size_t smem = 120u * 1024u;
+  cudaError_t e = cudaFuncSetAttribute(mma_with_readers_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  mma_with_readers_kernel<<<(unsigned)ctas, 17 * 32, smem, stream>>>(iters, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_probe_tmem_ld(int batched, int ctas, int iters, cudaStream_t stream) {
   // the whole TMEM (512 columns) and most of shared memory: one CTA per SM

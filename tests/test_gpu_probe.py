@@ -30,6 +30,15 @@ def test_probe_fp8_mma_runs(nfq, pair, stages):
         nfq.probe_fp8_mma(pair, 4, 16, 5)
 
 
+def test_probe_mma_with_tmem_readers_runs(nfq):
+    flops = nfq.probe_fp8_mma(False, 4, 64, 0)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    assert flops == 2.0 * 128 * 256 * 128 * 64 * 4
+    with pytest.raises(nfq.NfqError):
+        nfq.probe_fp8_mma(True, 4, 16, 0)
+
+
 @pytest.mark.parametrize("batched", [False, True])
 def test_probe_tmem_ld_runs(nfq, batched):
     nbytes = nfq.probe_tmem_ld(batched, 4, 8)
