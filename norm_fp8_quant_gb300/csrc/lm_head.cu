@@ -1063,26 +1063,20 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
 
   if (warp == kProducer) {
     // -------------------------------------------------------------- producer --
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_a = policy_evict_last();
-    uint32_t it = 0;
-    bool ok = true;
-    for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      int blk0, nb;
-      small_tile(b_begin, b_end, ti, blk0, nb);
-      for (int kb = 0; kb < G; ++kb, ++it) {
-        const uint32_t s = it % (uint32_t)nstage;
-        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-        int got = 1;
-        if (lane == 0)
-          got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err,
-                                kErrBitStage2);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
+    // One thread waits for free stages and issues both CTAs' copies.
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t it = 0, s = 0, ph = 0;
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        for (int kb = 0; kb < G; ++kb, ++it) {
+          if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
           uint8_t *st = smem + (size_t)s * kPairStage;
           const uint32_t fb = full0 + 8u * s;
           if (even)   // the stage's bytes of both CTAs: two activation tiles, the weight rows
@@ -1104,60 +1098,61 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
               tma_load_2d_pair(smem_u32(st + kPairATile), &tmap_w64, kb * 128,
                                blk0 * 128 + 64 * (int)rank, fb, pol_w);
           }
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        __syncwarp();
       }
-    }
-    if (lane == 0 && even) {
-      // the even CTA counts both CTAs' copies: wait until every stage issued has landed
-      const uint32_t issued = it;
-      const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
-      for (uint32_t j = first; j < issued; ++j)
-        mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
+      if (even) {
+        // the even CTA counts both CTAs' copies: wait until every stage issued has landed
+        const uint32_t first = it > (uint32_t)nstage ? it - (uint32_t)nstage : 0u;
+        for (uint32_t q = first; q < it; ++q)
+          mbar_wait_drain(smem_u32(&sh->full[q % (uint32_t)nstage]), (q / (uint32_t)nstage) & 1u);
+      }
     }
     __syncwarp();
   } else if (warp == kMma) {
     // ------------------------------------------------------------------- MMA --
-    uint32_t it = 0;
-    bool ok = even;                 // the even CTA issues for the pair
-    for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      int blk0, nb;
-      small_tile(b_begin, b_end, ti, blk0, nb);
-      const uint32_t idesc = idesc_e4m3_f32(256, (uint32_t)(nb * 128));
-      for (int kb = 0; kb < G; ++kb, ++it) {
-        const uint32_t s = it % (uint32_t)nstage;
-        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-        const uint32_t b = it & 1u;
-        const uint32_t bph = (it >> 1) & 1u;
-        int got = 1;
-        if (lane == 0)
-          got = mbar_wait(smem_u32(&sh->tempty[b]), bph ^ 1u, abort_flag, p.err,
-                                kErrBitStage2) &&
-                mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          tc_fence_after();
-          const uint8_t *st = smem + (size_t)s * kPairStage;
-          const uint32_t a_addr = smem_u32(st);
-          const uint32_t w_addr = smem_u32(st + kPairATile);
+    // One thread of the even CTA issues for the pair.  The descriptors of
+    // stage s are the stage-0 ones advanced by s stages; K step kk adds 32 bytes
+    // (2 in the descriptor's address field).
+    if (lane == 0 && even) {
+      const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(smem));
+      const uint64_t w_desc0 = sw128_kmajor_desc(smem_u32(smem + kPairATile));
+      constexpr uint64_t kStageDesc = kPairStage >> 4;
+      uint32_t it = 0, s = 0, ph = 0;
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        const uint32_t idesc = idesc_e4m3_f32(256, (uint32_t)(nb * 128));
+        for (int kb = 0; kb < G; ++kb, ++it) {
+          const uint32_t b = it & 1u;
+          const uint64_t ad = a_desc0 + kStageDesc * s, wd = w_desc0 + kStageDesc * s;
           const uint32_t d_tmem = tmem_base + b * 256u;
+          if (!mbar_wait(smem_u32(&sh->tempty[b]), ((it >> 1) & 1u) ^ 1u, abort_flag, p.err,
+                         kErrBitStage2) ||
+              !mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8_pair(d_tmem, sw128_kmajor_desc(a_addr + kk * 32),
-                        sw128_kmajor_desc(w_addr + kk * 32), idesc, kk > 0 ? 1u : 0u);
+            mma_f8_pair(d_tmem, ad + 2u * kk, wd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
           mma_commit_pair(smem_u32(&sh->empty[s]), (uint16_t)3);
           mma_commit_pair(smem_u32(&sh->tfull[b]), (uint16_t)3);
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        __syncwarp();
       }
-    }
-    if (lane == 0 && even && it > 0) {
-      const uint32_t last = it - 1;
-      mbar_wait_drain(smem_u32(&sh->tfull[last & 1u]), (last >> 1) & 1u);
+      if (it > 0) {
+        const uint32_t last = it - 1;
+        mbar_wait_drain(smem_u32(&sh->tfull[last & 1u]), (last >> 1) & 1u);
+      }
     }
     __syncwarp();
   } else {
@@ -1187,6 +1182,10 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
       for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < G; ++kb, ++it) {
         const uint32_t b = it & 1u;
+        // this K block's scale does not depend on the accumulator: taken while the MMAs run
+        const float src = kb < 32 ? swr[0] : kb < 64 ? swr[1] : kb < 96 ? swr[2] : swr[3];
+        const float swv = __shfl_sync(0xffffffffu, src, kb & 31);
+        const float sc = active ? sa_s[kb * 128 + tok] * swv : 0.0f;
         const bool got = mbar_wait(smem_u32(&sh->tfull[b]), (it >> 1) & 1u, abort_flag,
                                          p.err, kErrBitStage2);
         if (!__all_sync(0xffffffffu, got)) {
@@ -1194,9 +1193,6 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
           break;
         }
         tc_fence_after();
-        const float src = kb < 32 ? swr[0] : kb < 64 ? swr[1] : kb < 96 ? swr[2] : swr[3];
-        const float swv = __shfl_sync(0xffffffffu, src, kb & 31);
-        const float sc = active ? sa_s[kb * 128 + tok] * swv : 0.0f;
 #pragma unroll
         for (int c = 0; c < 64; c += 16) {
           uint32_t r[16];
@@ -1227,23 +1223,22 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
 
       // argmax over this thread's 64 columns (ascending rows), merged per shard
       const int row0 = blk0 * 128 + 64 * g;
-      const int last_row = min(row0 + 63, p.V - 1);
       const bool tok_ok = tok < Tc;
       const int key = t_base + tok;
-      if (row0 / p.shard_width == last_row / p.shard_width) {
-        float best = -INFINITY;
-        int bi = -1;
+      const int shard0 = row0 / p.shard_width;
+      if (row0 + 63 < p.V && (row0 + 63) / p.shard_width == shard0) {
+        // all 64 rows valid and in one shard: first maximum in ascending row order
+        float best = acc[0];
+        int bj = 0;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int v = row0 + j;
-          if (v < p.V && (bi < 0 || acc[j] > best)) {
+        for (int j = 1; j < 64; ++j)
+          if (acc[j] > best) {
             best = acc[j];
-            bi = v;
+            bj = j;
           }
-        }
-        if (tok_ok && bi >= 0)
-          atomicMax(&p.keys[(size_t)(row0 / p.shard_width) * kKeyStride + key],
-                    pack_key(best, (uint32_t)bi));
+        if (tok_ok)
+          atomicMax(&p.keys[(size_t)shard0 * kKeyStride + key],
+                    pack_key(best, (uint32_t)(row0 + bj)));
       } else {
         float best = -INFINITY;
         int bi = -1, cur = -1;
