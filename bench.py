@@ -991,8 +991,38 @@ def run_probe_mma(args, local):
                                  "16-column loads, a wait after each (the LM head epilogue)"),
                      "ctas": sms, "launches": n,
                      "TB/s": round(nbytes / (ms * 1e-3) / 1e12, 2)})
+    hand = []
+    for pair, buffers, mode in ((False, 2, 2), (False, 2, 0), (False, 2, 1), (True, 2, 2),
+                                (True, 2, 0), (True, 2, 1), (False, 4, 1), (False, 8, 1)):
+        ctas = sms // 2 if pair else sms
+        iters = 2048
+        for _ in range(3):
+            nfq.probe_handshake(pair, buffers, mode, ctas, iters)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n = max(5, min(50, args.steps))
+        e0.record()
+        for _ in range(n):
+            nfq.probe_handshake(pair, buffers, mode, ctas, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        if nfq.device_error() != nfq.NFQ_OK:
+            raise RuntimeError("the hand-off probe reported an expired wait")
+        ms = e0.elapsed_time(e1)
+        hand.append({"shape": ("CTA pairs, M=256" if pair else "single CTAs, M=128"),
+                     "buffers": buffers, "N": 512 // buffers,
+                     "epilogue": {0: "16 warps release each buffer unread",
+                                  1: "16 warps read their columns (16 at a time), then release",
+                                  2: "none: each group of MMAs waited for before the next"}[mode],
+                     "ctas": 2 * ctas if pair else ctas, "launches": n,
+                     "ns_per_k_block": round(ms * 1e6 / (n * iters), 1)})
     return {"metric": "FP8 dense tensor rate (tcgen05.mma kind::f8f6f4 from shared memory)",
             "unit": "TFLOP/s", "rows": rows, "tmem_read": tmem,
+            "handshake": {"rows": hand,
+                          "what": "the LM head's accumulator hand-off without data: per K block "
+                                  "(128 deep, 256 weight columns) four MMAs per N-column group, "
+                                  "one TMEM buffer per group"},
             "config": {"workload": "every SM issues 2048 K blocks of four back-to-back MMAs into "
                                    "one TMEM accumulator from zeroed shared-memory tiles"}}
 

@@ -430,6 +430,19 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   lanes x 64 columns as four 16-column loads; batched != 0: one wait for
  *   the four instead of one each): 128 KiB per CTA per iteration.
  *   Asynchronous on `stream`; NFQ_ERR_SHAPE as for nfq_probe_fp8_mma.
+ * nfq_probe_handshake: a measurement kernel, not part of the path: the FP8
+ *   LM head's accumulator hand-off with no data to stream.  `ctas` CTAs
+ *   (pair != 0: `ctas` CTA pairs, cta_group::2, M = 256) run `iters` K blocks;
+ *   one thread issues each K block as buffers / 2 groups of four MMAs of
+ *   M = 128 x N = 512 / buffers x K = 32, each group into its own TMEM buffer
+ *   (buffers = 2, 4 or 8 fill the 512 columns; pairs: 2), and 16 epilogue
+ *   warps per CTA wait for each buffer and release it, after reading their
+ *   N / 4 columns 16 at a time (mode 1) or at once (mode 0); mode 2: no
+ *   epilogue, the issuing thread waits for each group to complete before the
+ *   next.  Asynchronous on `stream`; time it with events: the time per K block
+ *   is what one K block of the LM head's K loop costs before any data moves.
+ *   NFQ_ERR_SHAPE for ctas outside 1..4096, iters outside 1..2^20, mode
+ *   outside 0..2, buffers other than 2, 4, 8, or pairs with buffers != 2.
  * nfq_probe_stage1_reads: a measurement kernel, not part of the path: the
  *   loads of the small-batch stage-1 kernel alone (the k partials and the
  *   residual, BF16 [T][H]) in the grid that kernel uses at this size, without
@@ -448,6 +461,7 @@ void nfq_stage1_grid(int max_ctas);
 void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma);
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
+int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream);
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,
                            int H, void *stream);
 int nfq_stage1_split_plan(int T, int H, int k, int num_sms, int *out5);

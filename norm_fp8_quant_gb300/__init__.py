@@ -106,6 +106,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_probe_fp8_mma.restype = ctypes.c_int
     lib.nfq_probe_tmem_ld.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_tmem_ld.restype = ctypes.c_int
+    lib.nfq_probe_handshake.argtypes = [ctypes.c_int] * 5 + [_P]
+    lib.nfq_probe_handshake.restype = ctypes.c_int
     lib.nfq_probe_stage1_reads.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_stage1_reads.restype = ctypes.c_int
     lib.nfq_mtp_reduce_norm_quant_nvfp4.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
@@ -412,6 +414,19 @@ def probe_tmem_ld(batched: bool, ctas: int, iters: int, stream=None):
     _check(_on_device(dev, load().nfq_probe_tmem_ld, 1 if batched else 0, ctas, iters,
                       _raw_stream(dev, stream)), "nfq_probe_tmem_ld")
     return 128.0 * 256 * 4 * iters * ctas
+
+
+def probe_handshake(pair: bool, buffers: int, mode: int, ctas: int, iters: int, stream=None):
+    """Launch the accumulator hand-off measurement kernel (not part of the path):
+    `ctas` CTAs (or CTA pairs) run `iters` K blocks through `buffers` TMEM
+    buffers; mode 0 / 1: 16 epilogue warps release each buffer without / after
+    reading it; mode 2: each group of MMAs waited for before the next.
+    Returns the number of K blocks each CTA (pair) runs."""
+    import torch
+    dev = torch.cuda.current_device()
+    _check(_on_device(dev, load().nfq_probe_handshake, 1 if pair else 0, buffers, mode, ctas,
+                      iters, _raw_stream(dev, stream)), "nfq_probe_handshake")
+    return iters
 
 
 def prepare_probe_stage1_reads(partials, residual) -> "PreparedCall":

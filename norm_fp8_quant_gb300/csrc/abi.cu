@@ -198,6 +198,9 @@ cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stage
                                         unsigned *err, cudaStream_t stream);
 cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
                                           cudaStream_t stream);
+// The LM head's accumulator hand-off without data (probe.cu).
+cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, int iters,
+                                   unsigned *err, cudaStream_t stream);
 
 // Every argument of an FP8 LM-head call except the workspace: NULL pointers,
 // shapes and alignment.  Queues nothing.
@@ -672,15 +675,15 @@ void nfq_stage1_tune(int cluster, int vpt, int slots, int per_slot) {
 void nfq_lm_head_small_batch(int enabled) { stage2_set_small(enabled); }
 
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream) {
-  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || stages < 0 || stages > 4)
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || stages < 0 || stages > 4 ||
+      (pair && stages == 0))
     return NFQ_ERR_SHAPE;
   DeviceInfo *d = nullptr;
   const int st = device_info(&d);
   if (st != NFQ_OK) return st;
   if (stages == 0)   // one CTA per SM, with 16 warps reading TMEM during the MMAs
-    return pair ? NFQ_ERR_SHAPE
-                : map_cuda(launch_probe_mma_with_readers(ctas, iters, d->err,
-                                                         static_cast<cudaStream_t>(stream)));
+    return map_cuda(launch_probe_mma_with_readers(ctas, iters, d->err,
+                                                  static_cast<cudaStream_t>(stream)));
   return map_cuda(launch_probe_fp8_mma_stages(pair ? 1 : 0, ctas, iters, stages, d->err,
                                               static_cast<cudaStream_t>(stream)));
 }
@@ -708,6 +711,17 @@ int nfq_probe_stage1_reads(const void *const *partials, int k, const void *resid
   const cudaError_t e = launch_stage1_reads(p, d->num_sms, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorInvalidConfiguration) return NFQ_ERR_SHAPE;
   return map_cuda(e);
+}
+
+int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream) {
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || mode < 0 || mode > 2)
+    return NFQ_ERR_SHAPE;
+  if (!(buffers == 2 || (!pair && (buffers == 4 || buffers == 8)))) return NFQ_ERR_SHAPE;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_probe_handshake(pair ? 1 : 0, buffers, mode, ctas, iters, d->err,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream) {

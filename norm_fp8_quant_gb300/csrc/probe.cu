@@ -1,8 +1,9 @@
 // Measurement kernels (not on the hot path): the rate at which tcgen05 FP8
 // MMAs run when nothing else competes for the SM (the FP8 tensor roofline
-// that the LM head's tensor-pipe figures are read against), and the rate at
-// which TMEM accumulators can be read into registers (what bounds the LM
-// head's per-K-block promotion when it holds 128 tokens per SM).
+// that the LM head's tensor-pipe figures are read against), the rate at
+// which TMEM accumulators can be read into registers, and the time of the
+// LM head's accumulator hand-off between the MMA thread and the epilogue
+// warps through two (or more) TMEM buffers, with no data to stream.
 //
 // fp8_mma_rate_kernel<kPair>: every CTA (kPair: every CTA pair, cta_group::2)
 // zeroes `stages` pairs of A and B tiles in shared memory, allocates one
@@ -229,6 +230,147 @@ __global__ void __launch_bounds__(17 * 32, 1) mma_with_readers_kernel(int iters,
   if (warp == 16) tmem_dealloc(tmem_base, 512);
 }
 
+// handshake_kernel<kPair, NB>: the LM head's accumulator hand-off without
+// any data to stream.  One thread (of the even CTA) issues, per K block, NB / 2
+// groups of four MMAs (M = 128 per CTA, 256 per pair, x N = 512 / NB x K = 32,
+// from one zeroed operand set), each group into its own N-column TMEM buffer
+// (NB buffers fill the 512 columns), and commits each group to that buffer's
+// full barrier.  16 epilogue warps per CTA wait for each buffer, read their
+// N / 4 columns of it 16 at a time with a wait after each (mode 1; mode 0:
+// no reads) and arrive on its empty barrier (CTA pairs: 16 local and 16
+// remote arrivals on the even CTA's barrier), which the issuing thread waits
+// for before it reuses the buffer.  mode 2: no epilogue; the issuing thread
+// waits for each group to complete before it issues the next (the MMAs'
+// issue-to-completion latency).
+template <bool kPair, int NB>
+__global__ void __launch_bounds__(17 * 32, 1) handshake_kernel(int iters, int mode, unsigned *err) {
+  constexpr int N = 512 / NB, GROUPS = NB / 2, C = N / 4;
+  static_assert(!kPair || NB == 2, "CTA pairs: two 256-column buffers only");
+  constexpr uint32_t kA = 128 * 128, kB = (kPair ? 128 : 256) * 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  __shared__ uint64_t full[NB], empty[NB], fin;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  const int warp = (int)(threadIdx.x / 32), lane = (int)(threadIdx.x % 32);
+  const bool even = !kPair || cluster_ctarank() == 0;
+
+  uint4 *z = reinterpret_cast<uint4 *>(smem);
+  for (uint32_t i = threadIdx.x; i < (kA + kB) / 16; i += blockDim.x)
+    z[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(smem_u32(&full[b]), 1);
+      mbar_init(smem_u32(&empty[b]), kPair ? 32 : 16);
+    }
+    mbar_init(smem_u32(&fin), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 16) {
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(&tmem_base), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&tmem_base), 512);
+      tmem_relinquish();
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  tc_fence_after();
+  volatile int *ab = &abort_flag;
+  const int total = iters * GROUPS;
+
+  if (warp == 16) {
+    if (lane == 0 && even) {
+      const uint64_t a_desc = sw128_kmajor_desc(smem_u32(smem));
+      const uint64_t b_desc = sw128_kmajor_desc(smem_u32(smem + kA));
+      const uint32_t idesc = idesc_e4m3_f32(kPair ? 256 : 128, (uint32_t)N);
+      for (int i = 0; i < total; ++i) {
+        const int buf = i % NB, use = i / NB, grp = i % GROUPS;
+        if (mode != 2) {
+          if (!mbar_wait(smem_u32(&empty[buf]), (uint32_t)(use & 1) ^ 1u, ab, err, kProbeErrBit))
+            break;
+          tc_fence_after();
+        }
+        // group grp multiplies B rows grp * N .. + N - 1 (128 bytes each)
+        const uint64_t bd = b_desc + (uint64_t)((grp * N * 128) >> 4);
+        const uint32_t d = tmem_base + (uint32_t)(buf * N);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if constexpr (kPair)
+            mma_f8_pair(d, a_desc + 2u * kk, bd + 2u * kk, idesc, kk ? 1u : 0u);
+          else
+            mma_f8(d, a_desc + 2u * kk, bd + 2u * kk, idesc, kk ? 1u : 0u);
+        }
+        if (mode == 2) {
+          if constexpr (kPair)
+            mma_commit_pair(smem_u32(&full[buf]), (uint16_t)1);
+          else
+            mma_commit(smem_u32(&full[buf]));
+          if (!mbar_wait(smem_u32(&full[buf]), (uint32_t)(use & 1), ab, err, kProbeErrBit)) break;
+        } else {
+          if constexpr (kPair)
+            mma_commit_pair(smem_u32(&full[buf]), (uint16_t)3);
+          else
+            mma_commit(smem_u32(&full[buf]));
+        }
+      }
+      // every MMA issued has completed before the TMEM is given back
+      if constexpr (kPair)
+        mma_commit_pair(smem_u32(&fin), (uint16_t)1);
+      else
+        mma_commit(smem_u32(&fin));
+      mbar_wait_drain(smem_u32(&fin), 0u);
+    }
+    __syncwarp();
+  } else if (mode != 2) {
+    const uint32_t t0 =
+        tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(C * (warp >> 2));
+    uint32_t x = 0;
+    for (int i = 0; i < total; ++i) {
+      const int buf = i % NB, use = i / NB;
+      const bool got = mbar_wait(smem_u32(&full[buf]), (uint32_t)(use & 1), ab, err, kProbeErrBit);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      if (mode == 1) {
+#pragma unroll
+        for (int c = 0; c < C; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(t0 + (uint32_t)(buf * N + c), r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x ^= r[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (even)
+          mbar_arrive(smem_u32(&empty[buf]));
+        else
+          mbar_arrive_remote_cta(smem_u32(&empty[buf]), 0u);
+      }
+    }
+    if (x == 0x9E3779B9u) atomicAdd(&g_tmem_probe_sink, 1u);   // keeps the loads
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  tc_fence_after();
+  if (warp == 16) {
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, 512);
+    else
+      tmem_dealloc(tmem_base, 512);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
@@ -282,6 +424,35 @@ cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stage
 cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,
                                  cudaStream_t stream) {
   return launch_probe_fp8_mma_stages(pair, ctas, iters, 1, err, stream);
+}
+
+// The accumulator hand-off probe: `ctas` CTAs (pair: `ctas` CTA pairs) with
+// `buffers` TMEM buffers (2, 4 or 8; pairs: 2), `iters` K blocks each.
+cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, int iters,
+                                   unsigned *err, cudaStream_t stream) {
+  void (*kern)(int, int, unsigned *) = nullptr;
+  if (pair && buffers == 2) kern = handshake_kernel<true, 2>;
+  else if (!pair && buffers == 2) kern = handshake_kernel<false, 2>;
+  else if (!pair && buffers == 4) kern = handshake_kernel<false, 4>;
+  else if (!pair && buffers == 8) kern = handshake_kernel<false, 8>;
+  if (!kern || mode < 0 || mode > 2) return cudaErrorInvalidValue;
+  // 48 KB of tiles; 120 KB keeps one CTA per SM
+  const size_t smem = 120u * 1024u;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pair ? 2 * ctas : ctas));
+  cfg.blockDim = dim3(17 * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, iters, mode, err);
 }
 
 }  // namespace nfq

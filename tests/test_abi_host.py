@@ -246,3 +246,17 @@ def test_stage2_nvfp4_argument_validation(lib):
     assert pk(H=1000) == nfq.NFQ_ERR_SHAPE
     assert pk(n=16) == nfq.NFQ_ERR_WORKSPACE
     assert pk(bs=MIS) == nfq.NFQ_ERR_ALIGN
+
+
+def test_probe_argument_validation(lib):
+    """The measurement kernels reject their out-of-range arguments before any
+    device call (so these run without a GPU)."""
+    shape = nfq.NFQ_ERR_SHAPE
+    assert lib.nfq_probe_handshake(0, 3, 1, 4, 16, None) == shape     # 3 buffers
+    assert lib.nfq_probe_handshake(1, 4, 1, 4, 16, None) == shape     # pairs: 2 buffers only
+    assert lib.nfq_probe_handshake(0, 2, 3, 4, 16, None) == shape     # mode 3
+    assert lib.nfq_probe_handshake(0, 2, 1, 0, 16, None) == shape     # no CTAs
+    assert lib.nfq_probe_handshake(0, 2, 1, 4, 0, None) == shape      # no K blocks
+    assert lib.nfq_probe_fp8_mma(1, 4, 16, 0, None) == shape          # readers: one CTA only
+    assert lib.nfq_probe_fp8_mma(0, 4, 16, 5, None) == shape
+    assert lib.nfq_probe_tmem_ld(0, 0, 8, None) == shape

@@ -54,3 +54,15 @@ def test_probe_stage1_reads_runs(nfq, T, H, k):
     nfq.prepare_probe_stage1_reads(parts, res)()
     torch.cuda.synchronize()
     assert nfq.device_error() == 0
+
+
+@pytest.mark.parametrize("pair,buffers", [(False, 2), (False, 4), (False, 8), (True, 2)])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_probe_handshake_runs(nfq, pair, buffers, mode):
+    """The accumulator hand-off probe runs every K block through its buffers and
+    leaves no expired wait, with and without an epilogue."""
+    assert nfq.probe_handshake(pair, buffers, mode, 4, 64) == 64
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    with pytest.raises(nfq.NfqError):
+        nfq.probe_handshake(pair, 6, mode, 4, 64)
