@@ -443,6 +443,18 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   is what one K block of the LM head's K loop costs before any data moves.
  *   NFQ_ERR_SHAPE for ctas outside 1..4096, iters outside 1..2^20, mode
  *   outside 0..2, buffers other than 2, 4, 8, or pairs with buffers != 2.
+ * nfq_check_fp8_quotient: a verification kernel, not part of the path.  Stage
+ *   1 forms each FP8 code from RN(hidden / scale) without a division per
+ *   element (one correctly rounded reciprocal per group and two FMAs, used
+ *   where the scale lies in [2^-40, 2^40); IEEE division elsewhere).  This
+ *   runs through every positive finite bf16 group maximum amax, its scale
+ *   RN(amax / 448), and every bf16 hidden value y with |y| <= amax and every
+ *   NaN, comparing the e4m3 code of that quotient with the code of IEEE
+ *   y / scale.  `mismatches` (device, 8-byte aligned) is incremented per
+ *   difference and `first_bad` (device, 4-byte aligned) receives
+ *   (amax bits << 16) | y bits of one of them if it holds 0xFFFFFFFF; the
+ *   caller sets both first.  Asynchronous on `stream`.  NFQ_ERR_NULL /
+ *   NFQ_ERR_ALIGN for bad pointers.
  * nfq_probe_stage1_reads: a measurement kernel, not part of the path: the
  *   loads of the small-batch stage-1 kernel alone (the k partials and the
  *   residual, BF16 [T][H]) in the grid that kernel uses at this size, without
@@ -462,6 +474,7 @@ void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma);
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream);
+int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, void *stream);
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,
                            int H, void *stream);
 int nfq_stage1_split_plan(int T, int H, int k, int num_sms, int *out5);

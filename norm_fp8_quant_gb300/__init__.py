@@ -108,6 +108,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_probe_tmem_ld.restype = ctypes.c_int
     lib.nfq_probe_handshake.argtypes = [ctypes.c_int] * 5 + [_P]
     lib.nfq_probe_handshake.restype = ctypes.c_int
+    lib.nfq_check_fp8_quotient.argtypes = [_P, _P, _P]
+    lib.nfq_check_fp8_quotient.restype = ctypes.c_int
     lib.nfq_probe_stage1_reads.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_stage1_reads.restype = ctypes.c_int
     lib.nfq_mtp_reduce_norm_quant_nvfp4.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
@@ -427,6 +429,22 @@ def probe_handshake(pair: bool, buffers: int, mode: int, ctas: int, iters: int, 
     _check(_on_device(dev, load().nfq_probe_handshake, 1 if pair else 0, buffers, mode, ctas,
                       iters, _raw_stream(dev, stream)), "nfq_probe_handshake")
     return iters
+
+
+def check_fp8_quotient(stream=None):
+    """Run the exhaustive check of stage 1's division-free FP8 codes against
+    those of IEEE division (a verification kernel, not part of the path).
+    Returns (mismatches, first mismatch as (amax bits << 16) | hidden bits, or
+    None)."""
+    import torch
+    dev = torch.cuda.current_device()
+    count = torch.zeros(1, dtype=torch.int64, device=dev)
+    first = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    _check(_on_device(dev, load().nfq_check_fp8_quotient, count.data_ptr(), first.data_ptr(),
+                      _raw_stream(dev, stream)), "nfq_check_fp8_quotient")
+    torch.cuda.synchronize(dev)
+    f = int(first.item()) & 0xFFFFFFFF
+    return int(count.item()), (None if f == 0xFFFFFFFF else f)
 
 
 def prepare_probe_stage1_reads(partials, residual) -> "PreparedCall":

@@ -201,6 +201,9 @@ cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
 // The LM head's accumulator hand-off without data (probe.cu).
 cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, int iters,
                                    unsigned *err, cudaStream_t stream);
+// Stage 1's division-free quotient against IEEE division (probe.cu).
+cudaError_t launch_check_fp8_quotient(unsigned long long *count, unsigned *first,
+                                      cudaStream_t stream);
 
 // Every argument of an FP8 LM-head call except the workspace: NULL pointers,
 // shapes and alignment.  Queues nothing.
@@ -722,6 +725,17 @@ int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, vo
   if (st != NFQ_OK) return st;
   return map_cuda(launch_probe_handshake(pair ? 1 : 0, buffers, mode, ctas, iters, d->err,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, void *stream) {
+  if (!mismatches || !first_bad) return NFQ_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(mismatches) & 7u) || (reinterpret_cast<uintptr_t>(first_bad) & 3u))
+    return NFQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(
+      launch_check_fp8_quotient(mismatches, first_bad, static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream) {

@@ -1,9 +1,10 @@
 // Measurement kernels (not on the hot path): the rate at which tcgen05 FP8
 // MMAs run when nothing else competes for the SM (the FP8 tensor roofline
 // that the LM head's tensor-pipe figures are read against), the rate at
-// which TMEM accumulators can be read into registers, and the time of the
+// which TMEM accumulators can be read into registers, the time of the
 // LM head's accumulator hand-off between the MMA thread and the epilogue
-// warps through two (or more) TMEM buffers, with no data to stream.
+// warps through two (or more) TMEM buffers, with no data to stream; and an
+// exhaustive check of stage 1's division-free quotient.
 //
 // fp8_mma_rate_kernel<kPair>: every CTA (kPair: every CTA pair, cta_group::2)
 // zeroes `stages` pairs of A and B tiles in shared memory, allocates one
@@ -19,6 +20,7 @@
 
 #include "nfq_internal.h"
 #include "ptx.cuh"
+#include "stage1_math.cuh"
 
 namespace nfq {
 
@@ -371,6 +373,29 @@ __global__ void __launch_bounds__(17 * 32, 1) handshake_kernel(int iters, int mo
   }
 }
 
+// quotient_check_kernel: block a (1 + blockIdx.x) takes the bf16 pattern a as
+// the group maximum amax and the scale s = RN(amax / 448) that stage 1 forms;
+// where quot_rn stands for the division (quot_rn_ok), its threads run through
+// every bf16 pattern y with |y| <= amax, and every NaN, and compare the e4m3
+// code of quot_rn(y, s, RN(1/s)) with that of IEEE y / s.  Mismatches are
+// counted and the first one kept as (a << 16) | y.
+__global__ void __launch_bounds__(256) quotient_check_kernel(unsigned long long *count,
+                                                             unsigned *first) {
+  const uint32_t a = 1u + blockIdx.x;
+  const float amax = __uint_as_float(a << 16);
+  const float s = __fdiv_rn(amax, 448.0f);
+  if (!quot_rn_ok(s)) return;
+  const float r = __frcp_rn(s);
+  for (uint32_t yb = threadIdx.x; yb < 65536u; yb += blockDim.x) {
+    const float y = __uint_as_float(yb << 16);
+    if (!isnan(y) && !(fabsf(y) <= amax)) continue;
+    if (e4m3x2(quot_rn(y, s, r), 0.0f) != e4m3x2(__fdiv_rn(y, s), 0.0f)) {
+      atomicAdd(count, 1ull);
+      atomicCAS(first, 0xFFFFFFFFu, (a << 16) | yb);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
@@ -453,6 +478,13 @@ cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, in
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, iters, mode, err);
+}
+
+// Every positive finite bf16 group maximum (0x0001 .. 0x7F7F), one block each.
+cudaError_t launch_check_fp8_quotient(unsigned long long *count, unsigned *first,
+                                      cudaStream_t stream) {
+  quotient_check_kernel<<<0x7F7Fu, 256, 0, stream>>>(count, first);
+  return cudaGetLastError();
 }
 
 }  // namespace nfq

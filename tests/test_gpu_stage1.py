@@ -211,3 +211,12 @@ def test_stage1_wide_row_persistent_cluster(nfq):
     c = persistent[1].reshape(600, 32768)
     s = persistent[2].view(np.float32).reshape(600, 256)
     check_stage1(h[rows], c[rows], s[rows], run_oracle(sub))
+
+
+def test_fp8_quotient_matches_ieee_division_exhaustively(nfq):
+    """Stage 1 forms each FP8 code from RN(hidden / scale) by one reciprocal per
+    group and two FMAs.  Over every bf16 group maximum, the scale stage 1 derives
+    from it and every bf16 hidden value the group can hold (and every NaN), the
+    code equals the one IEEE division gives."""
+    count, first = nfq.check_fp8_quotient()
+    assert count == 0, f"{count} mismatches, first amax/hidden bits {first:#010x}"
