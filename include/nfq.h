@@ -444,16 +444,20 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   NFQ_ERR_SHAPE for ctas outside 1..4096, iters outside 1..2^20, mode
  *   outside 0..2, buffers other than 2, 4, 8, or pairs with buffers != 2.
  * nfq_check_fp8_quotient: a verification kernel, not part of the path.  Stage
- *   1 forms each FP8 code from RN(hidden / scale) without a division per
- *   element (one correctly rounded reciprocal per group and two FMAs, used
- *   where the scale lies in [2^-40, 2^40); IEEE division elsewhere).  This
- *   runs through every positive finite bf16 group maximum amax, its scale
- *   RN(amax / 448), and every bf16 hidden value y with |y| <= amax and every
- *   NaN, comparing the e4m3 code of that quotient with the code of IEEE
- *   y / scale.  `mismatches` (device, 8-byte aligned) is incremented per
- *   difference and `first_bad` (device, 4-byte aligned) receives
- *   (amax bits << 16) | y bits of one of them if it holds 0xFFFFFFFF; the
- *   caller sets both first.  Asynchronous on `stream`.  NFQ_ERR_NULL /
+ *   1 forms each group's FP8 scale RN(amax / 448) and codes e4m3(RN(hidden /
+ *   scale)) without IEEE divisions: the scale from the constant RN(1 / 448)
+ *   and a correction FMA, the scale's reciprocal from the hardware
+ *   approximation and one Newton step, each code from that reciprocal and
+ *   two FMAs (where the scale lies in [2^-40, 2^40); IEEE division
+ *   elsewhere).  This runs through every bf16 group maximum amax from 0 to
+ *   +inf, and for each every bf16 hidden value y with |y| <= amax and every
+ *   NaN, and counts in mismatches[0] the scales that differ from IEEE
+ *   amax / 448, in mismatches[1] the reciprocals that differ from the IEEE
+ *   reciprocal, in mismatches[2] the codes that differ from those of IEEE
+ *   y / scale.  `mismatches` (device, 3 counters, 8-byte aligned) must be
+ *   zeroed and `first_bad` (device, 4-byte aligned) set to 0xFFFFFFFF by the
+ *   caller; it receives (amax bits << 16) | y bits of one difference (y bits
+ *   0 for a scale or reciprocal).  Asynchronous on `stream`.  NFQ_ERR_NULL /
  *   NFQ_ERR_ALIGN for bad pointers.
  * nfq_probe_stage1_reads: a measurement kernel, not part of the path: the
  *   loads of the small-batch stage-1 kernel alone (the k partials and the

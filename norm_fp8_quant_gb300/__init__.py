@@ -432,19 +432,19 @@ def probe_handshake(pair: bool, buffers: int, mode: int, ctas: int, iters: int, 
 
 
 def check_fp8_quotient(stream=None):
-    """Run the exhaustive check of stage 1's division-free FP8 codes against
-    those of IEEE division (a verification kernel, not part of the path).
-    Returns (mismatches, first mismatch as (amax bits << 16) | hidden bits, or
-    None)."""
+    """Run the exhaustive check of stage 1's division-free FP8 scales,
+    reciprocals and codes against IEEE arithmetic (a verification kernel, not
+    part of the path).  Returns ([scale, reciprocal, code mismatches], first
+    mismatch as (amax bits << 16) | hidden bits, or None)."""
     import torch
     dev = torch.cuda.current_device()
-    count = torch.zeros(1, dtype=torch.int64, device=dev)
+    count = torch.zeros(3, dtype=torch.int64, device=dev)
     first = torch.full((1,), -1, dtype=torch.int32, device=dev)
     _check(_on_device(dev, load().nfq_check_fp8_quotient, count.data_ptr(), first.data_ptr(),
                       _raw_stream(dev, stream)), "nfq_check_fp8_quotient")
     torch.cuda.synchronize(dev)
     f = int(first.item()) & 0xFFFFFFFF
-    return int(count.item()), (None if f == 0xFFFFFFFF else f)
+    return [int(c) for c in count.tolist()], (None if f == 0xFFFFFFFF else f)
 
 
 def prepare_probe_stage1_reads(partials, residual) -> "PreparedCall":

@@ -373,24 +373,36 @@ __global__ void __launch_bounds__(17 * 32, 1) handshake_kernel(int iters, int mo
   }
 }
 
-// quotient_check_kernel: block a (1 + blockIdx.x) takes the bf16 pattern a as
-// the group maximum amax and the scale s = RN(amax / 448) that stage 1 forms;
-// where quot_rn stands for the division (quot_rn_ok), its threads run through
-// every bf16 pattern y with |y| <= amax, and every NaN, and compare the e4m3
-// code of quot_rn(y, s, RN(1/s)) with that of IEEE y / s.  Mismatches are
-// counted and the first one kept as (a << 16) | y.
+// quotient_check_kernel: block a takes the bf16 pattern a (0 .. +inf) as the
+// group maximum amax and checks stage 1's division-free steps against IEEE
+// arithmetic: the scale fp8_scale(amax) against RN(amax / 448) bit for bit;
+// where quot_rn stands for the division (quot_rn_ok), recip_rn(scale)
+// against the IEEE reciprocal bit for bit, and for every bf16 pattern y with
+// |y| <= amax, and every NaN, the e4m3 code of quot_rn(y, scale, recip_rn)
+// against that of IEEE y / scale.  Differences are counted in count[0]
+// (scales), count[1] (reciprocals) and count[2] (codes); the first one seen
+// is kept as (a << 16) | y (y = 0 for a scale or reciprocal).
 __global__ void __launch_bounds__(256) quotient_check_kernel(unsigned long long *count,
                                                              unsigned *first) {
-  const uint32_t a = 1u + blockIdx.x;
+  const uint32_t a = blockIdx.x;
   const float amax = __uint_as_float(a << 16);
-  const float s = __fdiv_rn(amax, 448.0f);
-  if (!quot_rn_ok(s)) return;
-  const float r = __frcp_rn(s);
+  const float s = fp8_scale(amax);
+  const float s_ieee = __fdiv_rn(amax, 448.0f);
+  if (threadIdx.x == 0 && __float_as_uint(s) != __float_as_uint(s_ieee)) {
+    atomicAdd(&count[0], 1ull);
+    atomicCAS(first, 0xFFFFFFFFu, a << 16);
+  }
+  if (!quot_rn_ok(s_ieee)) return;
+  const float r = recip_rn(s);
+  if (threadIdx.x == 0 && __float_as_uint(r) != __float_as_uint(__frcp_rn(s_ieee))) {
+    atomicAdd(&count[1], 1ull);
+    atomicCAS(first, 0xFFFFFFFFu, a << 16);
+  }
   for (uint32_t yb = threadIdx.x; yb < 65536u; yb += blockDim.x) {
     const float y = __uint_as_float(yb << 16);
     if (!isnan(y) && !(fabsf(y) <= amax)) continue;
-    if (e4m3x2(quot_rn(y, s, r), 0.0f) != e4m3x2(__fdiv_rn(y, s), 0.0f)) {
-      atomicAdd(count, 1ull);
+    if (e4m3x2(quot_rn(y, s, r), 0.0f) != e4m3x2(__fdiv_rn(y, s_ieee), 0.0f)) {
+      atomicAdd(&count[2], 1ull);
       atomicCAS(first, 0xFFFFFFFFu, (a << 16) | yb);
     }
   }
@@ -480,10 +492,11 @@ cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, in
   return cudaLaunchKernelEx(&cfg, kern, iters, mode, err);
 }
 
-// Every positive finite bf16 group maximum (0x0001 .. 0x7F7F), one block each.
+// Every bf16 group maximum from 0 to +inf (0x0000 .. 0x7F80), one block each;
+// count holds three counters.
 cudaError_t launch_check_fp8_quotient(unsigned long long *count, unsigned *first,
                                       cudaStream_t stream) {
-  quotient_check_kernel<<<0x7F7Fu, 256, 0, stream>>>(count, first);
+  quotient_check_kernel<<<0x7F81u, 256, 0, stream>>>(count, first);
   return cudaGetLastError();
 }
 

@@ -214,9 +214,11 @@ def test_stage1_wide_row_persistent_cluster(nfq):
 
 
 def test_fp8_quotient_matches_ieee_division_exhaustively(nfq):
-    """Stage 1 forms each FP8 code from RN(hidden / scale) by one reciprocal per
-    group and two FMAs.  Over every bf16 group maximum, the scale stage 1 derives
-    from it and every bf16 hidden value the group can hold (and every NaN), the
-    code equals the one IEEE division gives."""
-    count, first = nfq.check_fp8_quotient()
-    assert count == 0, f"{count} mismatches, first amax/hidden bits {first:#010x}"
+    """Stage 1 forms each group's FP8 scale and codes without IEEE divisions.
+    Over every bf16 group maximum (0 to +inf) the scale equals RN(amax / 448),
+    its reciprocal equals the IEEE reciprocal, and for every bf16 hidden value
+    the group can hold (and every NaN) the code equals the one IEEE division
+    gives."""
+    counts, first = nfq.check_fp8_quotient()
+    assert counts == [0, 0, 0], (
+        f"scale/reciprocal/code mismatches {counts}, first amax/hidden bits {first:#010x}")
