@@ -459,6 +459,22 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   caller; it receives (amax bits << 16) | y bits of one difference (y bits
  *   0 for a scale or reciprocal).  Asynchronous on `stream`.  NFQ_ERR_NULL /
  *   NFQ_ERR_ALIGN for bad pointers.
+ * nfq_check_fp4_quotient: a verification kernel, not part of the path.  The
+ *   NVFP4 stage 1 forms each 16-element block's e4m3 scale code
+ *   e4m3(RN(ab / d)), d = RN(6 g), g = RN(amax_row / 2688), and each e2m1 code
+ *   e2m1(RN(y / eff)), eff = RN(value(scale code) g), without IEEE divisions
+ *   (a reciprocal from the hardware approximation and one Newton step, then
+ *   two FMAs per quotient, where the divisor lies in [2^-40, 2^40); IEEE
+ *   division elsewhere).  This runs through every bf16 row maximum from 0 to
+ *   +inf and every finite e4m3 block scale and counts: mismatches[0] the
+ *   reciprocals of d, mismatches[1] the block-scale codes (every bf16 block
+ *   maximum ab <= amax_row), mismatches[2] the reciprocals of eff,
+ *   mismatches[3] the e2m1 codes (every bf16 y with |y| <= amax_row, and every
+ *   NaN) that differ from IEEE arithmetic's.  `mismatches` (device, 4
+ *   counters) must be zeroed and `first_bad` (device, one 64-bit word) set to
+ *   all ones by the caller; it receives (scale code << 32) | (amax_row bits
+ *   << 16) | value bits of one difference.  Both 8-byte aligned.
+ *   Asynchronous on `stream`.  NFQ_ERR_NULL / NFQ_ERR_ALIGN for bad pointers.
  * nfq_probe_stage1_reads: a measurement kernel, not part of the path: the
  *   loads of the small-batch stage-1 kernel alone (the k partials and the
  *   residual, BF16 [T][H]) in the grid that kernel uses at this size, without
@@ -479,6 +495,8 @@ int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream);
 int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, void *stream);
+int nfq_check_fp4_quotient(unsigned long long *mismatches, unsigned long long *first_bad,
+                           void *stream);
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,
                            int H, void *stream);
 int nfq_stage1_split_plan(int T, int H, int k, int num_sms, int *out5);

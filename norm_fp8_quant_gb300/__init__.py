@@ -110,6 +110,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_probe_handshake.restype = ctypes.c_int
     lib.nfq_check_fp8_quotient.argtypes = [_P, _P, _P]
     lib.nfq_check_fp8_quotient.restype = ctypes.c_int
+    lib.nfq_check_fp4_quotient.argtypes = [_P, _P, _P]
+    lib.nfq_check_fp4_quotient.restype = ctypes.c_int
     lib.nfq_probe_stage1_reads.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_stage1_reads.restype = ctypes.c_int
     lib.nfq_mtp_reduce_norm_quant_nvfp4.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
@@ -445,6 +447,23 @@ def check_fp8_quotient(stream=None):
     torch.cuda.synchronize(dev)
     f = int(first.item()) & 0xFFFFFFFF
     return [int(c) for c in count.tolist()], (None if f == 0xFFFFFFFF else f)
+
+
+def check_fp4_quotient(stream=None):
+    """Run the exhaustive check of the NVFP4 stage 1's division-free block-scale
+    and e2m1 codes against IEEE arithmetic (a verification kernel, not part of
+    the path).  Returns ([reciprocal of d, block-scale code, reciprocal of eff,
+    e2m1 code mismatches], first mismatch as (scale code << 32) | (row max bits
+    << 16) | value bits, or None)."""
+    import torch
+    dev = torch.cuda.current_device()
+    count = torch.zeros(4, dtype=torch.int64, device=dev)
+    first = torch.full((1,), -1, dtype=torch.int64, device=dev)
+    _check(_on_device(dev, load().nfq_check_fp4_quotient, count.data_ptr(), first.data_ptr(),
+                      _raw_stream(dev, stream)), "nfq_check_fp4_quotient")
+    torch.cuda.synchronize(dev)
+    f = int(first.item()) & 0xFFFFFFFFFFFFFFFF
+    return [int(c) for c in count.tolist()], (None if f == 0xFFFFFFFFFFFFFFFF else f)
 
 
 def prepare_probe_stage1_reads(partials, residual) -> "PreparedCall":

@@ -204,6 +204,8 @@ cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, in
 // Stage 1's division-free quotient against IEEE division (probe.cu).
 cudaError_t launch_check_fp8_quotient(unsigned long long *count, unsigned *first,
                                       cudaStream_t stream);
+cudaError_t launch_check_fp4_quotient(unsigned long long *count, unsigned long long *first,
+                                      cudaStream_t stream);
 
 // Every argument of an FP8 LM-head call except the workspace: NULL pointers,
 // shapes and alignment.  Queues nothing.
@@ -736,6 +738,18 @@ int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, 
   if (st != NFQ_OK) return st;
   return map_cuda(
       launch_check_fp8_quotient(mismatches, first_bad, static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_check_fp4_quotient(unsigned long long *mismatches, unsigned long long *first_bad,
+                           void *stream) {
+  if (!mismatches || !first_bad) return NFQ_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(mismatches) & 7u) || (reinterpret_cast<uintptr_t>(first_bad) & 7u))
+    return NFQ_ERR_ALIGN;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(
+      launch_check_fp4_quotient(mismatches, first_bad, static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream) {

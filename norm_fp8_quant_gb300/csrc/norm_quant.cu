@@ -276,6 +276,8 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
         for (int q = 0; q < n_cons_warps; ++q) amax_row = fmaxf(amax_row, sums->amx[par][q]);
         const float g = __fdiv_rn(amax_row, 2688.0f);     // 448 * 6
         const float d = __fmul_rn(6.0f, g);
+        const bool d_fast = quot_rn_ok(d);
+        const float rd = d_fast ? recip_rn(d) : 0.0f;
         uint32_t *cod4 = reinterpret_cast<uint32_t *>(p.codes + rowbase / 2u);
         uint8_t *bsc = p.bscales + (size_t)r * (size_t)(p.H / 16);
 #pragma unroll
@@ -284,14 +286,8 @@ __global__ void __launch_bounds__(stage1_max_threads(VPT), 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) ab = fmaxf(ab, fabsf(yv[v][e]));
           ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));   // the block's other half
-          const uint32_t sb = (g != 0.0f) ? (uint32_t)(e4m3x2(__fdiv_rn(ab, d), 0.0f) & 0xFFu) : 0u;
-          const float eff = __fmul_rn(e4m3_value(sb), g);
-          uint32_t packed = 0u;
-          if (eff != 0.0f) {
-#pragma unroll
-            for (int e = 0; e < 8; e += 2)
-              packed |= e2m1x2(__fdiv_rn(yv[v][e], eff), __fdiv_rn(yv[v][e + 1], eff)) << (4 * e);
-          }
+          uint32_t sb;
+          const uint32_t packed = fp4_vector_codes(yv[v], ab, g, d, rd, d_fast, sb);
           if (active) {
             const int j = v * NA + tc;
             hid[j] = make_uint4(hbv[v][0], hbv[v][1], hbv[v][2], hbv[v][3]);
@@ -528,6 +524,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
     const float amax_row = row_max(gmax, G);
     const float g = __fdiv_rn(amax_row, 2688.0f);     // 448 * 6
     const float d = __fmul_rn(6.0f, g);
+    const bool d_fast = quot_rn_ok(d);
+    const float rd = d_fast ? recip_rn(d) : 0.0f;
     uint32_t *cod4 = reinterpret_cast<uint32_t *>(p.codes) + rowv;
     uint8_t *bsc = p.bscales + ((size_t)r * (size_t)p.H + (size_t)col0) / 16u;
 #pragma unroll
@@ -536,14 +534,8 @@ __global__ void __launch_bounds__(kSplitMaxThreads)
 #pragma unroll
       for (int e = 0; e < 8; ++e) ab = fmaxf(ab, fabsf(yv[v][e]));
       ab = fmaxf(ab, __shfl_xor_sync(0xffffffffu, ab, 1));   // the block's other half
-      const uint32_t sb = (g != 0.0f) ? (uint32_t)(e4m3x2(__fdiv_rn(ab, d), 0.0f) & 0xFFu) : 0u;
-      const float eff = __fmul_rn(e4m3_value(sb), g);
-      uint32_t packed = 0u;
-      if (eff != 0.0f) {
-#pragma unroll
-        for (int e = 0; e < 8; e += 2)
-          packed |= e2m1x2(__fdiv_rn(yv[v][e], eff), __fdiv_rn(yv[v][e + 1], eff)) << (4 * e);
-      }
+      uint32_t sb;
+      const uint32_t packed = fp4_vector_codes(yv[v], ab, g, d, rd, d_fast, sb);
       if (active) {
         const int j = v * NA + tc;
         hid[j] = make_uint4(hbv[v][0], hbv[v][1], hbv[v][2], hbv[v][3]);

@@ -3,8 +3,8 @@
 // that the LM head's tensor-pipe figures are read against), the rate at
 // which TMEM accumulators can be read into registers, the time of the
 // LM head's accumulator hand-off between the MMA thread and the epilogue
-// warps through two (or more) TMEM buffers, with no data to stream; and an
-// exhaustive check of stage 1's division-free quotient.
+// warps through two (or more) TMEM buffers, with no data to stream; and
+// exhaustive checks of stage 1's division-free FP8 and NVFP4 quotients.
 //
 // fp8_mma_rate_kernel<kPair>: every CTA (kPair: every CTA pair, cta_group::2)
 // zeroes `stages` pairs of A and B tiles in shared memory, allocates one
@@ -408,6 +408,55 @@ __global__ void __launch_bounds__(256) quotient_check_kernel(unsigned long long 
   }
 }
 
+// quotient_check_fp4_kernel: block (a, c) takes the bf16 pattern a (0 .. +inf)
+// as the row maximum, g = RN(amax_row / 2688), d = RN(6 g), and the e4m3 code
+// c (0 .. 0x7E) as a block scale, eff = RN(value(c) g); it checks stage 1's
+// division-free NVFP4 steps against IEEE arithmetic: (c = 0 only) recip_rn(d)
+// against the IEEE reciprocal, counted in count[0], and for every bf16 block
+// maximum ab <= amax_row the block-scale code e4m3(RN(ab / d)), count[1];
+// recip_rn(eff) against the IEEE reciprocal, count[2]; for every bf16 y with
+// |y| <= amax_row, and every NaN, the e2m1 code of RN(y / eff), count[3].
+// The first difference seen is kept as (c << 32) | (a << 16) | y.
+__global__ void __launch_bounds__(256) quotient_check_fp4_kernel(unsigned long long *count,
+                                                                 unsigned long long *first) {
+  const uint32_t a = blockIdx.x, c = blockIdx.y;
+  const float amax_row = __uint_as_float(a << 16);
+  const float g = __fdiv_rn(amax_row, 2688.0f);
+  if (g == 0.0f) return;
+  const float d = __fmul_rn(6.0f, g);
+  const unsigned long long tag = ((unsigned long long)c << 32) | ((unsigned long long)a << 16);
+  if (c == 0 && quot_rn_ok(d)) {
+    const float rd = recip_rn(d);
+    if (threadIdx.x == 0 && __float_as_uint(rd) != __float_as_uint(__frcp_rn(d))) {
+      atomicAdd(&count[0], 1ull);
+      atomicCAS(first, ~0ull, tag);
+    }
+    for (uint32_t ab_bits = threadIdx.x; ab_bits <= 0x7F80u; ab_bits += blockDim.x) {
+      const float ab = __uint_as_float(ab_bits << 16);
+      if (!(ab <= amax_row)) continue;
+      if ((e4m3x2(quot_rn(ab, d, rd), 0.0f) & 0xFFu) != (e4m3x2(__fdiv_rn(ab, d), 0.0f) & 0xFFu)) {
+        atomicAdd(&count[1], 1ull);
+        atomicCAS(first, ~0ull, tag | ab_bits);
+      }
+    }
+  }
+  const float eff = __fmul_rn(e4m3_value(c), g);
+  if (!quot_rn_ok(eff)) return;
+  const float re = recip_rn(eff);
+  if (threadIdx.x == 0 && __float_as_uint(re) != __float_as_uint(__frcp_rn(eff))) {
+    atomicAdd(&count[2], 1ull);
+    atomicCAS(first, ~0ull, tag);
+  }
+  for (uint32_t yb = threadIdx.x; yb < 65536u; yb += blockDim.x) {
+    const float y = __uint_as_float(yb << 16);
+    if (!isnan(y) && !(fabsf(y) <= amax_row)) continue;
+    if (e2m1x2(quot_rn(y, eff, re), 0.0f) != e2m1x2(__fdiv_rn(y, eff), 0.0f)) {
+      atomicAdd(&count[3], 1ull);
+      atomicCAS(first, ~0ull, tag | yb);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
@@ -497,6 +546,14 @@ cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, in
 cudaError_t launch_check_fp8_quotient(unsigned long long *count, unsigned *first,
                                       cudaStream_t stream) {
   quotient_check_kernel<<<0x7F81u, 256, 0, stream>>>(count, first);
+  return cudaGetLastError();
+}
+
+// Every bf16 row maximum from 0 to +inf times every finite e4m3 block scale;
+// count holds four counters.
+cudaError_t launch_check_fp4_quotient(unsigned long long *count, unsigned long long *first,
+                                      cudaStream_t stream) {
+  quotient_check_fp4_kernel<<<dim3(0x7F81u, 0x7Fu), 256, 0, stream>>>(count, first);
   return cudaGetLastError();
 }
 

@@ -261,5 +261,8 @@ def test_probe_argument_validation(lib):
     assert lib.nfq_probe_fp8_mma(0, 4, 16, 5, None) == shape
     assert lib.nfq_probe_tmem_ld(0, 0, 8, None) == shape
     assert lib.nfq_check_fp8_quotient(None, None, None) == nfq.NFQ_ERR_NULL
+    assert lib.nfq_check_fp4_quotient(None, None, None) == nfq.NFQ_ERR_NULL
+    assert lib.nfq_check_fp4_quotient(ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4),
+                                      None) == nfq.NFQ_ERR_ALIGN
     assert lib.nfq_check_fp8_quotient(ctypes.c_void_p(FAKE + 4), ctypes.c_void_p(FAKE),
                                       None) == nfq.NFQ_ERR_ALIGN

@@ -262,3 +262,14 @@ def test_nvfp4_two_token_groups_full_vocab(nfq, T):
     qw, sw, gw = synth.lm_head_weights_nvfp4(w)
     out = run_lm(nfq, act, qw, sw, gw, w.S)
     check(*out, act, qw, sw, gw, w.S, list(range(T)), cache_key=("nvfp4_two", T))
+
+
+def test_fp4_quotients_match_ieee_division_exhaustively(nfq):
+    """The NVFP4 stage 1 forms each block-scale code and each e2m1 code without
+    IEEE divisions.  Over every bf16 row maximum and every finite e4m3 block
+    scale, the reciprocals equal the IEEE reciprocals, and for every bf16 block
+    maximum and value the row can hold (and every NaN) both codes equal the
+    ones IEEE division gives."""
+    counts, first = nfq.check_fp4_quotient()
+    assert counts == [0, 0, 0, 0], (
+        f"mismatches (rcp d, scale code, rcp eff, e2m1 code) {counts}, first {first:#014x}")
