@@ -670,43 +670,43 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     const uint64_t pol_a = policy_evict_last();
     // the fused step's activation was written by other CTAs' generic stores
     if constexpr (kFused) fence_proxy_async_global();
-    uint32_t it = 0;
-    bool ok = !(kFused && *abort_flag);
-    for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      int blk0, nb;
-      small_tile(b_begin, b_end, ti, blk0, nb);
-      for (int kb = 0; kb < G; ++kb, ++it) {
-        const uint32_t s = it % (uint32_t)nstage;
-        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-        const bool pre = (int)it < npre;           // weight part already requested
-        int got = 1;
-        if (lane == 0 && !pre)
-          got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          uint8_t *st = smem + (size_t)s * kStage;
-          const uint32_t fb = smem_u32(&sh->full[s]);
-          mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * kWTileBytes) + (uint32_t)Tc * 128u);
-          for (int h = 0; h < nb && !pre; ++h) {
-            if constexpr (kPacked) {
-              bulk_g2s(smem_u32(st + h * kWTileBytes),
-                       p.w_packed + ((size_t)(blk0 + h) * G + kb) * kWTileBytes, kWTileBytes, fb,
-                       pol_w);
-            } else {
-              tma_load_2d(smem_u32(st + h * kWTileBytes), &tmap_w, kb * 128, (blk0 + h) * 128, fb,
-                          pol_w);
-            }
-          }
-          tma_load_2d(smem_u32(st + 2 * kWTileBytes), tmap_act, kb * 128, 0, fb, pol_a);
-        }
-        __syncwarp();
-      }
-    }
+    // One thread waits for free stages and issues the copies.
     if (lane == 0) {
+      uint32_t it = 0, s = 0, ph = 0;
+      bool ok = !(kFused && *abort_flag);
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        for (int kb = 0; kb < G; ++kb, ++it) {
+          const bool pre = (int)it < npre;           // weight part already requested
+          if (!pre &&
+              !mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
+          {
+            uint8_t *st = smem + (size_t)s * kStage;
+            const uint32_t fb = smem_u32(&sh->full[s]);
+            mbar_arrive_expect_tx(fb,
+                                  (pre ? 0u : (uint32_t)nb * kWTileBytes) + (uint32_t)Tc * 128u);
+            for (int h = 0; h < nb && !pre; ++h) {
+              if constexpr (kPacked) {
+                bulk_g2s(smem_u32(st + h * kWTileBytes),
+                         p.w_packed + ((size_t)(blk0 + h) * G + kb) * kWTileBytes, kWTileBytes, fb,
+                         pol_w);
+              } else {
+                tma_load_2d(smem_u32(st + h * kWTileBytes), &tmap_w, kb * 128, (blk0 + h) * 128,
+                            fb, pol_w);
+              }
+            }
+            tma_load_2d(smem_u32(st + 2 * kWTileBytes), tmap_act, kb * 128, 0, fb, pol_a);
+          }
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
       // stages whose weight was requested but which the loop never reached:
       // arrive, so their phase completes once those bytes have landed
       for (uint32_t j = it; j < (uint32_t)npre; ++j) mbar_arrive(smem_u32(&sh->full[j]));
@@ -718,45 +718,44 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
     __syncwarp();
   } else if (warp == kMma) {
     // ------------------------------------------------------------------- MMA --
-    uint32_t it = 0;
-    bool ok = true;
-    for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      int blk0, nb;
-      small_tile(b_begin, b_end, ti, blk0, nb);
-      const uint32_t idesc = idesc_e4m3_f32(MT, (uint32_t)(nb * 128));
-      for (int kb = 0; kb < G; ++kb, ++it) {
-        const uint32_t s = it % (uint32_t)nstage;
-        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-        const uint32_t b = it & 1u;
-        const uint32_t bph = (it >> 1) & 1u;
-        int got = 1;
-        if (lane == 0)
-          got = mbar_wait(smem_u32(&sh->tempty[b]), bph ^ 1u, abort_flag, p.err, kErrBitStage2) &&
-                mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          tc_fence_after();
-          const uint8_t *st = smem + (size_t)s * kStage;
-          const uint32_t w_addr = smem_u32(st);
-          const uint32_t a_addr = smem_u32(st + 2 * kWTileBytes);
+    // One thread issues; the descriptors of stage s are the stage-0 ones
+    // advanced by s stages, K step kk adds 32 bytes (2 in the address field).
+    if (lane == 0) {
+      const uint64_t w_desc0 = sw128_kmajor_desc(smem_u32(smem));
+      const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(smem + 2 * kWTileBytes));
+      constexpr uint64_t kStageDesc = kStage >> 4;
+      uint32_t it = 0, s = 0, ph = 0;
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        const uint32_t idesc = idesc_e4m3_f32(MT, (uint32_t)(nb * 128));
+        for (int kb = 0; kb < G; ++kb, ++it) {
+          const uint32_t b = it & 1u;
+          const uint64_t ad = a_desc0 + kStageDesc * s, wd = w_desc0 + kStageDesc * s;
           const uint32_t d_tmem = tmem_base + b * 256u;
+          if (!mbar_wait(smem_u32(&sh->tempty[b]), ((it >> 1) & 1u) ^ 1u, abort_flag, p.err,
+                         kErrBitStage2) ||
+              !mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8(d_tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(w_addr + kk * 32),
-                   idesc, kk > 0 ? 1u : 0u);
+            mma_f8(d_tmem, ad + 2u * kk, wd + 2u * kk, idesc, kk > 0 ? 1u : 0u);
           mma_commit(smem_u32(&sh->empty[s]));
           mma_commit(smem_u32(&sh->tfull[b]));
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        __syncwarp();
       }
-    }
-    if (lane == 0 && it > 0) {
-      const uint32_t last = it - 1;
-      mbar_wait_drain(smem_u32(&sh->tfull[last & 1u]), (last >> 1) & 1u);
+      if (it > 0) {
+        const uint32_t last = it - 1;
+        mbar_wait_drain(smem_u32(&sh->tfull[last & 1u]), (last >> 1) & 1u);
+      }
     }
     __syncwarp();
   } else {

@@ -184,45 +184,44 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 
   if (warp == kF4Producer) {
     // -------------------------------------------------------------- producer --
-    const uint64_t pol_w = n_grp > 1 ? policy_evict_normal() : policy_evict_first();
-    const uint64_t pol_a = policy_evict_last();
-    uint32_t it = 0;
-    bool ok = true;
-    for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      int blk0, nb;
-      small_tile(b_begin, b_end, ti, blk0, nb);
-      for (int ks = 0; ks < G; ++ks, ++it) {
-        const uint32_t s = it % (uint32_t)nstage;
-        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-        const bool pre = (int)it < npre;           // weight part already requested
-        int got = 1;
-        if (lane == 0 && !pre)
-          got = mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          uint8_t *st = smem + (size_t)s * L::kStage;
-          const uint32_t fb = smem_u32(&sh->full[s]);
-          // the activation boxes hold exactly the group's Tc token rows
-          mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * (kWTileBytes + kF4ScaleBlock)) +
-                                        (uint32_t)Tc * (128u + 16u));
-          for (int h = 0; h < nb && !pre; ++h) {
-            const size_t blk = (size_t)(blk0 + h) * (size_t)G + (size_t)ks;
-            bulk_g2s(smem_u32(st + L::kW + h * kWTileBytes), p.w_packed + blk * kWTileBytes,
-                     kWTileBytes, fb, pol_w);
-            bulk_g2s(smem_u32(st + L::kSfb + h * kF4ScaleBlock),
-                     p.w_packed + scale_region + blk * kF4ScaleBlock, kF4ScaleBlock, fb, pol_w);
-          }
-          tma_load_2d(smem_u32(st + L::kA), tm_a, ks * 128, 0, fb, pol_a);
-          tma_load_2d(smem_u32(st + L::kSfa), tm_sa, ks * 16, 0, fb, pol_a);
-        }
-        __syncwarp();
-      }
-    }
+    // One thread waits for free stages and issues the copies.
     if (lane == 0) {
+      const uint64_t pol_w = n_grp > 1 ? policy_evict_normal() : policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t it = 0, s = 0, ph = 0;
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        for (int ks = 0; ks < G; ++ks, ++it) {
+          const bool pre = (int)it < npre;           // weight part already requested
+          if (!pre &&
+              !mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
+          {
+            uint8_t *st = smem + (size_t)s * L::kStage;
+            const uint32_t fb = smem_u32(&sh->full[s]);
+            // the activation boxes hold exactly the group's Tc token rows
+            mbar_arrive_expect_tx(fb, (pre ? 0u : (uint32_t)nb * (kWTileBytes + kF4ScaleBlock)) +
+                                          (uint32_t)Tc * (128u + 16u));
+            for (int h = 0; h < nb && !pre; ++h) {
+              const size_t blk = (size_t)(blk0 + h) * (size_t)G + (size_t)ks;
+              bulk_g2s(smem_u32(st + L::kW + h * kWTileBytes), p.w_packed + blk * kWTileBytes,
+                       kWTileBytes, fb, pol_w);
+              bulk_g2s(smem_u32(st + L::kSfb + h * kF4ScaleBlock),
+                       p.w_packed + scale_region + blk * kF4ScaleBlock, kF4ScaleBlock, fb, pol_w);
+            }
+            tma_load_2d(smem_u32(st + L::kA), tm_a, ks * 128, 0, fb, pol_a);
+            tma_load_2d(smem_u32(st + L::kSfa), tm_sa, ks * 16, 0, fb, pol_a);
+          }
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
       // stages whose weight was requested but which the loop never reached:
       // arrive, so their phase completes once those bytes have landed
       for (uint32_t j = it; j < (uint32_t)npre; ++j) mbar_arrive(smem_u32(&sh->full[j]));
@@ -234,53 +233,46 @@ __global__ void __launch_bounds__(kF4Threads, 1)
     __syncwarp();
   } else if (warp == kF4Mma) {
     // ------------------------------------------------------------------- MMA --
-    uint32_t it = 0;
-    int committed = 0;                             // tiles whose last MMA was committed
-    bool ok = true;
-    for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      int blk0, nb;
-      small_tile(b_begin, b_end, ti, blk0, nb);
-      const uint32_t idesc = idesc_nvfp4(128, (uint32_t)(nb * 128));
-      // the single accumulator is free once the epilogue has read tile ti-1
-      int got = 1;
-      if (lane == 0)
-        got = mbar_wait(smem_u32(&sh->tempty), (uint32_t)(ti & 1) ^ 1u, abort_flag, p.err,
-                        kErrBitStage2);
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) break;
-      for (int ks = 0; ks < G; ++ks, ++it) {
-        const uint32_t s = it % (uint32_t)nstage;
-        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
-        got = 1;
-        if (lane == 0)
-          got = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2) &&
-                mbar_wait(smem_u32(&sh->sfready[s]), ph, abort_flag, p.err, kErrBitStage2);
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
+    // One thread issues; the descriptors of stage s are the stage-0 ones
+    // advanced by s stages, K step kk adds 32 bytes (2 in the address field).
+    if (lane == 0) {
+      const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(smem + L::kA));
+      const uint64_t w_desc0 = sw128_kmajor_desc(smem_u32(smem + L::kW));
+      constexpr uint64_t kStageDesc = L::kStage >> 4;
+      uint32_t s = 0, ph = 0;
+      int committed = 0;
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        const uint32_t idesc = idesc_nvfp4(128, (uint32_t)(nb * 128));
+        if (!mbar_wait(smem_u32(&sh->tempty), (uint32_t)(ti & 1) ^ 1u, abort_flag, p.err,
+                       kErrBitStage2))
           break;
-        }
-        if (lane == 0) {
-          tc_fence_after();
-          const uint8_t *st = smem + (size_t)s * L::kStage;
-          const uint32_t w_addr = smem_u32(st + L::kW);
-          const uint32_t a_addr = smem_u32(st + L::kA);
+        for (int ks = 0; ks < G; ++ks) {
+          const uint64_t ad = a_desc0 + kStageDesc * s, wd = w_desc0 + kStageDesc * s;
           const uint32_t sfa = tmem_base + kF4SfBase + s * kF4SfCols;
-          const uint32_t sfb = sfa + 16u;
+          if (!mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2) ||
+              !mbar_wait(smem_u32(&sh->sfready[s]), ph, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_fp4_block16(tmem_base, sw128_kmajor_desc(a_addr + kk * 32),
-                            sw128_kmajor_desc(w_addr + kk * 32), idesc, sfa + 4u * kk,
-                            sfb + 8u * kk, (ks > 0 || kk > 0) ? 1u : 0u);
+            mma_fp4_block16(tmem_base, ad + 2u * kk, wd + 2u * kk, idesc, sfa + 4u * kk,
+                            sfa + 16u + 8u * kk, (ks > 0 || kk > 0) ? 1u : 0u);
           mma_commit(smem_u32(&sh->empty[s]));
           if (ks == G - 1) mma_commit(smem_u32(&sh->tfull));
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        __syncwarp();
+        if (ok) committed = ti + 1;
       }
-      if (ok) committed = ti + 1;
+      if (committed > 0) mbar_wait_drain(smem_u32(&sh->tfull), (uint32_t)((committed - 1) & 1));
     }
-    if (lane == 0 && committed > 0)
-      mbar_wait_drain(smem_u32(&sh->tfull), (uint32_t)((committed - 1) & 1));
     __syncwarp();
   } else if (warp >= kF4SfWarp0) {
     // --------------------------------------------------------- scale writers --
