@@ -792,6 +792,10 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
       for (int j = 0; j < CPT; ++j) acc[j] = 0.0f;
       for (int kb = 0; kb < G; ++kb, ++it) {
         const uint32_t b = it & 1u;
+        // this K block's scale does not depend on the accumulator: taken while the MMAs run
+        const float src = kb < 32 ? swr[0] : kb < 64 ? swr[1] : kb < 96 ? swr[2] : swr[3];
+        const float swv = __shfl_sync(0xffffffffu, src, kb & 31);
+        const float sc = active ? sa_s[kb * MT + tok] * swv : 0.0f;
         const bool got = mbar_wait(smem_u32(&sh->tfull[b]), (it >> 1) & 1u, abort_flag, p.err,
                                    kErrBitStage2);
         if (!__all_sync(0xffffffffu, got)) {
@@ -799,9 +803,6 @@ __global__ void __launch_bounds__(kSmallEpiWarps * 32 + 64, 1)
           break;
         }
         tc_fence_after();
-        const float src = kb < 32 ? swr[0] : kb < 64 ? swr[1] : kb < 96 ? swr[2] : swr[3];
-        const float swv = __shfl_sync(0xffffffffu, src, kb & 31);
-        const float sc = active ? sa_s[kb * MT + tok] * swv : 0.0f;
         if constexpr (MT == 64) {
           uint32_t r[32];
           if (active) {
