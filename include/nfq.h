@@ -475,6 +475,11 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   all ones by the caller; it receives (scale code << 32) | (amax_row bits
  *   << 16) | value bits of one difference.  Both 8-byte aligned.
  *   Asynchronous on `stream`.  NFQ_ERR_NULL / NFQ_ERR_ALIGN for bad pointers.
+ * nfq_probe_wait_timeout: a failure-detection check, not part of the path.
+ *   One thread waits, with the bounded wait every kernel of the path uses, on
+ *   a barrier nothing arrives on; after the wait's time limit (2 s) it sets the
+ *   device error word, which nfq_device_error then reports as
+ *   NFQ_ERR_TIMEOUT, and the kernel returns.  Asynchronous on `stream`.
  * nfq_probe_stage1_reads: a measurement kernel, not part of the path: the
  *   loads of the small-batch stage-1 kernel alone (the k partials and the
  *   residual, BF16 [T][H]) in the grid that kernel uses at this size, without
@@ -495,6 +500,7 @@ int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream);
 int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, void *stream);
+int nfq_probe_wait_timeout(void *stream);
 int nfq_check_fp4_quotient(unsigned long long *mismatches, unsigned long long *first_bad,
                            void *stream);
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,

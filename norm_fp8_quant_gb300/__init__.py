@@ -112,6 +112,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_check_fp8_quotient.restype = ctypes.c_int
     lib.nfq_check_fp4_quotient.argtypes = [_P, _P, _P]
     lib.nfq_check_fp4_quotient.restype = ctypes.c_int
+    lib.nfq_probe_wait_timeout.argtypes = [_P]
+    lib.nfq_probe_wait_timeout.restype = ctypes.c_int
     lib.nfq_probe_stage1_reads.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_stage1_reads.restype = ctypes.c_int
     lib.nfq_mtp_reduce_norm_quant_nvfp4.argtypes = [_P, ctypes.c_int, _P, _P, ctypes.c_float,
@@ -447,6 +449,16 @@ def check_fp8_quotient(stream=None):
     torch.cuda.synchronize(dev)
     f = int(first.item()) & 0xFFFFFFFF
     return [int(c) for c in count.tolist()], (None if f == 0xFFFFFFFF else f)
+
+
+def probe_wait_timeout(stream=None):
+    """Launch a kernel whose bounded wait runs out (about 2 s): afterwards
+    device_error() reports NFQ_ERR_TIMEOUT.  A failure-detection check, not
+    part of the path."""
+    import torch
+    dev = torch.cuda.current_device()
+    _check(_on_device(dev, load().nfq_probe_wait_timeout, _raw_stream(dev, stream)),
+           "nfq_probe_wait_timeout")
 
 
 def check_fp4_quotient(stream=None):

@@ -206,6 +206,8 @@ cudaError_t launch_check_fp8_quotient(unsigned long long *count, unsigned *first
                                       cudaStream_t stream);
 cudaError_t launch_check_fp4_quotient(unsigned long long *count, unsigned long long *first,
                                       cudaStream_t stream);
+// A bounded wait on a barrier nothing arrives on (probe.cu).
+cudaError_t launch_probe_wait_timeout(unsigned *err, cudaStream_t stream);
 
 // Every argument of an FP8 LM-head call except the workspace: NULL pointers,
 // shapes and alignment.  Queues nothing.
@@ -750,6 +752,13 @@ int nfq_check_fp4_quotient(unsigned long long *mismatches, unsigned long long *f
   if (st != NFQ_OK) return st;
   return map_cuda(
       launch_check_fp4_quotient(mismatches, first_bad, static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_probe_wait_timeout(void *stream) {
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_probe_wait_timeout(d->err, static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream) {

@@ -3,8 +3,9 @@
 // that the LM head's tensor-pipe figures are read against), the rate at
 // which TMEM accumulators can be read into registers, the time of the
 // LM head's accumulator hand-off between the MMA thread and the epilogue
-// warps through two (or more) TMEM buffers, with no data to stream; and
-// exhaustive checks of stage 1's division-free FP8 and NVFP4 quotients.
+// warps through two (or more) TMEM buffers, with no data to stream;
+// exhaustive checks of stage 1's division-free FP8 and NVFP4 quotients; and a
+// bounded wait that is made to run out.
 //
 // fp8_mma_rate_kernel<kPair>: every CTA (kPair: every CTA pair, cta_group::2)
 // zeroes `stages` pairs of A and B tiles in shared memory, allocates one
@@ -457,6 +458,25 @@ __global__ void __launch_bounds__(256) quotient_check_fp4_kernel(unsigned long l
   }
 }
 
+// wait_timeout_kernel: one thread waits, with the bounded wait every kernel
+// of the path uses, on an mbarrier that nothing arrives on.  The wait gives
+// up after its time limit, sets the device error word's probe bit and the
+// kernel returns: the failure a stuck peer would cause, made on purpose
+// without faulting or hanging anything.
+__global__ void __launch_bounds__(32) wait_timeout_kernel(unsigned *err) {
+  __shared__ uint64_t never;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&never), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0)
+    (void)mbar_wait(smem_u32(&never), 0u, (volatile int *)&abort_flag, err, kProbeErrBit);
+  __syncwarp();
+}
+
 }  // namespace
 
 cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
@@ -554,6 +574,11 @@ cudaError_t launch_check_fp8_quotient(unsigned long long *count, unsigned *first
 cudaError_t launch_check_fp4_quotient(unsigned long long *count, unsigned long long *first,
                                       cudaStream_t stream) {
   quotient_check_fp4_kernel<<<dim3(0x7F81u, 0x7Fu), 256, 0, stream>>>(count, first);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_probe_wait_timeout(unsigned *err, cudaStream_t stream) {
+  wait_timeout_kernel<<<1, 32, 0, stream>>>(err);
   return cudaGetLastError();
 }
 

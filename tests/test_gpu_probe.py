@@ -66,3 +66,22 @@ def test_probe_handshake_runs(nfq, pair, buffers, mode):
     assert nfq.device_error() == 0
     with pytest.raises(nfq.NfqError):
         nfq.probe_handshake(pair, 6, mode, 4, 64)
+
+
+def test_expired_wait_sets_the_error_word_and_the_context_stays_usable(nfq):
+    """Failure detection without a fault: a kernel's bounded wait on a barrier
+    nothing arrives on gives up after its limit, the host reads
+    NFQ_ERR_TIMEOUT from the device error word (cleared by the read), and the
+    next launches run normally on the same context."""
+    import time
+    assert nfq.device_error() == nfq.NFQ_OK
+    t0 = time.time()
+    nfq.probe_wait_timeout()
+    assert nfq.device_error() == nfq.NFQ_ERR_TIMEOUT
+    waited = time.time() - t0
+    assert 1.5 < waited < 30.0, waited
+    assert nfq.device_error() == nfq.NFQ_OK           # the read cleared it
+    # the context still runs tensor-core work afterwards and leaves no error
+    assert nfq.probe_fp8_mma(False, 4, 16) > 0
+    torch.cuda.synchronize()
+    assert nfq.device_error() == nfq.NFQ_OK
