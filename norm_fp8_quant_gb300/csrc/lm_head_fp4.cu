@@ -277,12 +277,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   } else if (warp >= kF4SfWarp0) {
     // --------------------------------------------------------- scale writers --
     const int q = warp & 3;                        // this warp's TMEM lane quadrant
-    uint32_t it = 0;
+    uint32_t s = 0, ph = 0;
     bool ok = true;
     for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      for (int ks = 0; ks < G; ++ks, ++it) {
-        const uint32_t s = it % (uint32_t)nstage;
-        const uint32_t ph = (it / (uint32_t)nstage) & 1u;
+      for (int ks = 0; ks < G; ++ks) {
         const bool got = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
@@ -324,6 +322,10 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh->sfready[s]));
+        if (++s == (uint32_t)nstage) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
     __syncwarp();
