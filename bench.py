@@ -676,7 +676,10 @@ def run_ours(args, rank, world, local):
                                               else ncu_traffic("lm_head_tie_stress")
                                               if args.workload == "tie_stress" and not fp4
                                               and not unfused else None),
-                                  "kernel": ("lm_head_fp4_kernel" if fp4 else
+                                  "kernel": ("lm_head_fp4_kernel" if fp4 and T <= 128 else
+                                             "lm_head_fp4_pair_kernel (CTA pairs, cta_group::2)"
+                                             if fp4 and T <= 256 else
+                                             f"lm_head_fp4 x {(T + 255) // 256}" if fp4 else
                                              "lm_head_small_kernel (BF16 logits) + "
                                              "unfused_argmax_kernel" if unfused else
                                              "lm_head_small_kernel" if T <= 128 else

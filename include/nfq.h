@@ -398,10 +398,11 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  * nfq_lm_head_small_batch: 1 (default) runs the FP8 LM head on the token-major
  *   kernels (up to 256 tokens per launch); 0 forces the weight-major kernel for
  *   every batch size.
- * nfq_lm_head_pair: 1 (default) runs 129..256 tokens on CTA pairs that issue
- *   cta_group::2 MMAs (M = 256 tokens, each CTA holding half of the weight
- *   tile); 0 runs them as two independent 128-token groups over one weight
- *   stream.  The results are the same either way.
+ * nfq_lm_head_pair: 1 (default) runs 129..256 tokens of the FP8 and the NVFP4
+ *   LM heads on CTA pairs that issue cta_group::2 MMAs (M = 256 tokens, each
+ *   CTA holding half of the weight tile); 0 runs them as two independent
+ *   128-token groups over one weight stream.  The results are the same either
+ *   way.
  * nfq_lm_head_nvfp4_tune: pipeline stages of later NVFP4 LM-head launches
  *   (0 = as many as fit, at most 5; values below 2 or above what fits fall back).
  * nfq_stage1_grid: at most max_ctas CTAs for later stage-1 launches, each then

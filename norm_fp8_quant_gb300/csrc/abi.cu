@@ -208,6 +208,8 @@ cudaError_t launch_check_fp4_quotient(unsigned long long *count, unsigned long l
                                       cudaStream_t stream);
 // A bounded wait on a barrier nothing arrives on (probe.cu).
 cudaError_t launch_probe_wait_timeout(unsigned *err, cudaStream_t stream);
+// The form of the NVFP4 LM head for 129..256 tokens (lm_head_fp4.cu).
+void stage2_fp4_set_pair(int enabled);
 
 // Every argument of an FP8 LM-head call except the workspace: NULL pointers,
 // shapes and alignment.  Queues nothing.
@@ -770,9 +772,12 @@ int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream) {
       launch_probe_tmem_ld(batched ? 1 : 0, ctas, iters, static_cast<cudaStream_t>(stream)));
 }
 
-// Selects the form of the token-major FP8 LM head for 129..256 tokens: 1
+// Selects the form of the FP8 and NVFP4 LM heads for 129..256 tokens: 1
 // (default) CTA pairs issuing cta_group::2 MMAs, 0 two independent 128-token
 // groups over one weight stream.
-void nfq_lm_head_pair(int enabled) { stage2_set_pair(enabled); }
+void nfq_lm_head_pair(int enabled) {
+  stage2_set_pair(enabled);
+  stage2_fp4_set_pair(enabled);
+}
 
 }  // extern "C"

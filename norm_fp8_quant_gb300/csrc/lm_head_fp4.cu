@@ -404,6 +404,382 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   finish_launch(p, &sh->last);
 }
 
+// ------------------------------------------------ CTA pairs, 129..256 tokens --
+//
+// 129..256 tokens on CTA pairs (clusters of two) with cta_group::2 block-scaled
+// MMAs of M = 256 tokens: the even CTA holds tokens 0..127 and the odd one
+// tokens 128.. as the A operand, and each holds HALF of the tile's weight
+// codes as the B operand (block blk0 + rank of a two-block tile, rows
+// 64*rank.. of a one-block tile).  The pair streams every weight block once,
+// and a CTA moves 38 KB per K step through shared memory where a 128-token
+// CTA holding the whole tile moves 54 KB: the per-SM ingest that bounds the
+// two-group form.
+//
+// Both CTAs keep the single-CTA layout of the block scales in TMEM: the
+// activation scales of the CTA's own 128 tokens (column 4kk + c: rows
+// 32c + lane) and the weight scales of ALL the tile's rows (column 8kk + c),
+// which is what the pair MMA reads from each CTA.  Each CTA therefore loads the
+// scale blocks of the whole tile (4 KB per K step; the second request of each
+// is served from L2).
+//
+// Hand-offs between the two CTAs:
+//  - each CTA's copies complete on its own full barrier; its scale writers
+//    wait there, store the stage's scales into TMEM and arrive on the EVEN
+//    CTA's sfready barrier (release at cluster scope).  That barrier completes
+//    once both CTAs' bytes have landed and both CTAs' scales are in TMEM, so
+//    the MMA thread waits on it alone (acquire at cluster scope);
+//  - the MMA commits arrive, multicast, on both CTAs' empty and tfull barriers;
+//  - both CTAs' epilogue warps arrive on the even CTA's tempty barrier (an
+//    execution dependency only, as in the FP8 pair kernel).
+// A cluster barrier after the set-up (barriers initialised, TMEM allocated)
+// and one before the teardown (every MMA, copy and remote arrival done) bound
+// every cross-CTA access.  Each CTA drains its own copies, so neither needs
+// to outwait the other's after an expired wait.
+
+constexpr uint32_t kP4A = 0;                               // 128 tokens x 128 code bytes
+constexpr uint32_t kP4W = 128 * 128;                       // this CTA's weight rows
+constexpr uint32_t kP4Sfb = kP4W + kWTileBytes;            // the whole tile's weight scales
+constexpr uint32_t kP4Sfa = kP4Sfb + kF4SfbBytes;          // this CTA's activation scales
+constexpr uint32_t kP4Stage = kP4Sfa + 128 * 16;
+static_assert(kP4Stage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+
+__device__ __forceinline__ void mma_fp4_block16_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t sfa, uint32_t sfb,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+// The copies of K step ks of tile (blk0, nb) that do not depend on the
+// activation: this CTA's weight codes and the tile's weight scales.
+__device__ __forceinline__ void issue_pair_weight(const Stage2Params &p, size_t scale_region,
+                                                  uint8_t *st, uint32_t fb, int blk0, int nb,
+                                                  int ks, uint32_t rank, uint64_t pol_w,
+                                                  uint64_t pol_s) {
+  const size_t G = (size_t)p.G;
+  const uint8_t *codes =
+      nb == 2 ? p.w_packed + ((size_t)(blk0 + (int)rank) * G + (size_t)ks) * kWTileBytes
+              : p.w_packed + ((size_t)blk0 * G + (size_t)ks) * kWTileBytes +
+                    (size_t)rank * (kWTileBytes / 2);
+  bulk_g2s(smem_u32(st + kP4W), codes, nb == 2 ? kWTileBytes : kWTileBytes / 2, fb, pol_w);
+  for (int h = 0; h < nb; ++h)
+    bulk_g2s(smem_u32(st + kP4Sfb + h * kF4ScaleBlock),
+             p.w_packed + scale_region + ((size_t)(blk0 + h) * G + (size_t)ks) * kF4ScaleBlock,
+             kF4ScaleBlock, fb, pol_s);
+}
+
+__device__ __forceinline__ uint32_t pair_weight_bytes(int nb) {
+  return (nb == 2 ? kWTileBytes : kWTileBytes / 2) + (uint32_t)nb * kF4ScaleBlock;
+}
+
+__global__ void __launch_bounds__(kF4Threads, 1)
+    lm_head_fp4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a0,
+                            const __grid_constant__ CUtensorMap tmap_sa0,
+                            const __grid_constant__ CUtensorMap tmap_a1,
+                            const __grid_constant__ CUtensorMap tmap_sa1, const Stage2Params p,
+                            int nstage) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  float *gs_s = reinterpret_cast<float *>(smem + (size_t)nstage * kP4Stage);   // [128]
+  Fp4Smem *sh = reinterpret_cast<Fp4Smem *>(gs_s + kFp4MaxT);
+  volatile int *abort_flag = &sh->abort;
+
+  const int warp = (int)(threadIdx.x / 32);
+  const int lane = (int)(threadIdx.x % 32);
+  const int G = p.G;                                           // K steps of 256 elements
+  const size_t scale_region = (size_t)p.n_vtiles * (size_t)G * kWTileBytes;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const int pair = (int)cluster_id_x(), n_pair = (int)nclusters_x();
+  const int t_base = (int)rank * kFp4MaxT;
+  const int Tc = min(p.T - t_base, kFp4MaxT);                  // this CTA's tokens (>= 1)
+  const CUtensorMap *tm_a = rank ? &tmap_a1 : &tmap_a0;
+  const CUtensorMap *tm_sa = rank ? &tmap_sa1 : &tmap_sa0;
+  const int b_begin = (int)(((long)pair * p.n_vtiles) / n_pair);
+  const int b_end = (int)(((long)(pair + 1) * p.n_vtiles) / n_pair);
+  const int n_tiles = (b_end - b_begin + 1) / 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nstage; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+      mbar_init(smem_u32(&sh->sfready[s]), 2 * kF4SfWarps);
+    }
+    mbar_init(smem_u32(&sh->tfull), 1);
+    mbar_init(smem_u32(&sh->tempty), 2 * kF4EpiWarps);
+    sh->abort = 0;
+    sh->last = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kF4Producer && lane == 0) {
+    prefetch_tmap(tm_a);
+    prefetch_tmap(tm_sa);
+  }
+  if (warp == kF4Mma) {
+    tmem_alloc_pair(smem_u32(&sh->tmem_base), 512);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();   // this CTA's barriers exist
+  // The weight part of the first stages is requested before the wait for the
+  // previous kernel (see the single-CTA kernel); it completes on this CTA's
+  // own barriers only.
+  const int total_steps = n_tiles * G;
+  const int npre = total_steps < nstage ? total_steps : nstage;
+  if (warp == kF4Producer) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_s = policy_evict_normal();
+      for (int it = 0; it < npre; ++it) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, it / G, blk0, nb);
+        const uint32_t fb = smem_u32(&sh->full[it]);
+        mbar_expect_tx(fb, pair_weight_bytes(nb));
+        issue_pair_weight(p, scale_region, smem + (size_t)it * kP4Stage, fb, blk0, nb, it % G,
+                          rank, pol_w, pol_s);
+      }
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  cluster_sync_all();   // both CTAs' barriers exist and the TMEM columns are allocated
+  tc_fence_after();
+  // everything below reads memory the previous kernel on the stream may write
+  grid_dependency_wait();
+  grid_launch_dependents();
+  for (int i = (int)threadIdx.x; i < kFp4MaxT; i += (int)blockDim.x)
+    gs_s[i] = (i < Tc) ? __fmul_rn(p.act_gscales[t_base + i], p.w_scale) : 0.0f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+
+  if (warp == kF4Producer) {
+    // -------------------------------------------------------------- producer --
+    // One thread of each CTA waits for its free stages and issues its copies.
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_s = policy_evict_normal();
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t it = 0, s = 0, ph = 0;
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        for (int ks = 0; ks < G; ++ks, ++it) {
+          const bool pre = (int)it < npre;           // weight part already requested
+          if (!pre &&
+              !mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = smem + (size_t)s * kP4Stage;
+          const uint32_t fb = smem_u32(&sh->full[s]);
+          mbar_arrive_expect_tx(fb, (pre ? 0u : pair_weight_bytes(nb)) + (uint32_t)Tc * (128u + 16u));
+          if (!pre) issue_pair_weight(p, scale_region, st, fb, blk0, nb, ks, rank, pol_w, pol_s);
+          tma_load_2d(smem_u32(st + kP4A), tm_a, ks * 128, 0, fb, pol_a);
+          tma_load_2d(smem_u32(st + kP4Sfa), tm_sa, ks * 16, 0, fb, pol_a);
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      for (uint32_t j = it; j < (uint32_t)npre; ++j) mbar_arrive(smem_u32(&sh->full[j]));
+      const uint32_t issued = it > (uint32_t)npre ? it : (uint32_t)npre;
+      const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
+      for (uint32_t j = first; j < issued; ++j)
+        mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kF4Mma) {
+    // ------------------------------------------------------------------- MMA --
+    // One thread of the even CTA issues for the pair.  The last commit on an
+    // empty barrier covers every MMA issued before it: the thread waits for it
+    // before the teardown, also when it gave up in the middle of a tile.
+    if (lane == 0 && even) {
+      const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(smem + kP4A));
+      const uint64_t w_desc0 = sw128_kmajor_desc(smem_u32(smem + kP4W));
+      constexpr uint64_t kStageDesc = kP4Stage >> 4;
+      uint32_t s = 0, ph = 0, n_issued = 0, s_last = 0, ph_last = 0;
+      bool ok = true;
+      for (int ti = 0; ti < n_tiles && ok; ++ti) {
+        int blk0, nb;
+        small_tile(b_begin, b_end, ti, blk0, nb);
+        const uint32_t idesc = idesc_nvfp4(256, (uint32_t)(nb * 128));
+        if (!mbar_wait(smem_u32(&sh->tempty), (uint32_t)(ti & 1) ^ 1u, abort_flag, p.err,
+                       kErrBitStage2))
+          break;
+        for (int ks = 0; ks < G; ++ks) {
+          const uint64_t ad = a_desc0 + kStageDesc * s, wd = w_desc0 + kStageDesc * s;
+          const uint32_t sfa = tmem_base + kF4SfBase + s * kF4SfCols;
+          if (!mbar_wait(smem_u32(&sh->sfready[s]), ph, abort_flag, p.err, kErrBitStage2)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_fp4_block16_pair(tmem_base, ad + 2u * kk, wd + 2u * kk, idesc, sfa + 4u * kk,
+                                 sfa + 16u + 8u * kk, (ks > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_pair(smem_u32(&sh->empty[s]), (uint16_t)3);
+          if (ks == G - 1) mma_commit_pair(smem_u32(&sh->tfull), (uint16_t)3);
+          ++n_issued;
+          s_last = s;
+          ph_last = ph;
+          if (++s == (uint32_t)nstage) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (n_issued > 0) mbar_wait_drain(smem_u32(&sh->empty[s_last]), ph_last);
+    }
+    __syncwarp();
+  } else if (warp >= kF4SfWarp0) {
+    // --------------------------------------------------------- scale writers --
+    const int q = warp & 3;                        // this warp's TMEM lane quadrant
+    uint32_t s = 0, ph = 0;
+    bool ok = true;
+    for (int ti = 0; ti < n_tiles && ok; ++ti) {
+      for (int ks = 0; ks < G; ++ks) {
+        const bool got = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t *sfb_s = smem + (size_t)s * kP4Stage + kP4Sfb;
+        const uint8_t *sfa_s = smem + (size_t)s * kP4Stage + kP4Sfa;
+        uint32_t ra[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // this CTA's token row 32c + lane (rows past Tc feed accumulator
+          // rows that are never read)
+          const uint4 v = (32 * c + lane < Tc)
+                              ? *reinterpret_cast<const uint4 *>(sfa_s + (32 * c + lane) * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+          ra[0 + c] = v.x;
+          ra[4 + c] = v.y;
+          ra[8 + c] = v.z;
+          ra[12 + c] = v.w;
+        }
+        uint32_t rb[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // the tile's rows 128h + 32c + lane (block h of a one-block tile:
+            // columns the MMA of N = 128 does not read)
+            const uint4 v = *reinterpret_cast<const uint4 *>(sfb_s + h * kF4ScaleBlock +
+                                                             (kk * 32 + lane) * 16);
+            rb[kk * 8 + h * 4 + 0] = v.x;
+            rb[kk * 8 + h * 4 + 1] = v.y;
+            rb[kk * 8 + h * 4 + 2] = v.z;
+            rb[kk * 8 + h * 4 + 3] = v.w;
+          }
+        const uint32_t col =
+            tmem_base + ((uint32_t)(32 * q) << 16) + kF4SfBase + s * kF4SfCols;
+        tmem_st16(col, ra);
+        tmem_st32(col + 16u, rb);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (even) mbar_arrive(smem_u32(&sh->sfready[s]));
+          else mbar_arrive_remote_cta(smem_u32(&sh->sfready[s]), 0u);
+        }
+        if (++s == (uint32_t)nstage) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue --
+    // Token 32q + lane of this CTA is TMEM lane 32q + lane; column n of the
+    // accumulator is row n of the tile.  Each thread reads its 64 columns at
+    // once, releases the accumulator and then takes their argmax per shard.
+    const int q = warp & 3;
+    const int g = warp >> 2;
+    const int tok = 32 * q + lane;
+    const bool quad_active = 32 * q < Tc;
+    const bool tok_ok = tok < Tc;
+    const int key = t_base + tok;                   // the token's index in the launch
+    const float sc = gs_s[tok];
+    const uint32_t taddr0 = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * g);
+    for (int ti = 0; ti < n_tiles; ++ti) {
+      int blk0, nb;
+      small_tile(b_begin, b_end, ti, blk0, nb);
+      const bool got = mbar_wait(smem_u32(&sh->tfull), (uint32_t)(ti & 1), abort_flag, p.err,
+                                 kErrBitStage2);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const bool active = quad_active && (g < 2 * nb);
+      uint32_t r0[32], r1[32];
+      if (active) {
+        tmem_ld32(taddr0, r0);
+        tmem_ld32(taddr0 + 32u, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) asm volatile("" : "+r"(r0[j]), "+r"(r1[j]));
+      }
+      // every TMEM read of this tile is complete: the MMA may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {   // the even CTA's tempty: an execution dependency only
+        if (even) mbar_arrive(smem_u32(&sh->tempty));
+        else mbar_arrive_remote_cta(smem_u32(&sh->tempty), 0u);
+      }
+      if (!active) continue;
+      const int row0 = blk0 * 128 + 64 * g;
+      int cur = row0 / p.shard_width;                 // shard of the running maximum
+      int next_bound = (cur + 1) * p.shard_width;     // first row of the next shard
+      float best = -INFINITY;
+      int bi = -1;
+#pragma unroll
+      for (int c4 = 0; c4 < 2; ++c4) {
+        const uint32_t(&r)[32] = c4 ? r1 : r0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int v = row0 + 32 * c4 + j;
+          if (v >= p.V) break;
+          if (v >= next_bound) {
+            if (bi >= 0 && tok_ok)
+              atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
+            cur = v / p.shard_width;
+            next_bound = (cur + 1) * p.shard_width;
+            bi = -1;
+          }
+          const float logit = __fmul_rn(__uint_as_float(r[j]), sc);
+          if (bi < 0 || logit > best) {
+            best = logit;
+            bi = v;
+          }
+        }
+      }
+      if (bi >= 0 && tok_ok)
+        atomicMax(&p.keys[(size_t)cur * kKeyStride + key], pack_key(best, (uint32_t)bi));
+    }
+    __threadfence();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------- teardown --
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // every MMA, copy and remote arrival of the pair is done
+  tc_fence_after();
+  if (warp == kF4Mma) tmem_dealloc_pair(tmem_base, 512);
+  finish_launch(p, &sh->last);
+}
+
 // Scale blocks of the packed NVFP4 weight: block (vt, s) holds, at word
 // (kk * 32 + i) * 4 + c, the four block scales 4kk .. 4kk+3 of K step s for
 // row vt * 128 + 32c + i (zero past V).
@@ -486,12 +862,61 @@ cudaError_t launch_fp4(const Stage2Params &p_in, int num_sms, cudaStream_t strea
                     tsa[1], p, nstage);
 }
 
+bool g_fp4_pair = true;  // 129..256 tokens on CTA pairs (false: two token groups)
+
+cudaError_t launch_fp4_pair(const Stage2Params &p_in, int num_sms, cudaStream_t stream) {
+  Stage2Params p = p_in;
+  if (p.T <= kFp4MaxT || p.T > 2 * kFp4MaxT || num_sms < 2) return cudaErrorInvalidConfiguration;
+  p.n_groups = 1;
+  CUtensorMap ta[2], tsa[2];
+  // per CTA of the pair, boxes of exactly its token rows
+  for (int r = 0; r < 2; ++r) {
+    const int Tr = (p.T - r * kFp4MaxT) < kFp4MaxT ? (p.T - r * kFp4MaxT) : kFp4MaxT;
+    if (!encode_u8_map(&ta[r], p.act_codes + (size_t)r * kFp4MaxT * (size_t)(p.H / 2),
+                       (uint64_t)Tr, (uint64_t)(p.H / 2), (uint32_t)Tr))
+      return cudaErrorInvalidValue;
+    if (!encode_u8_map_plain(&tsa[r], p.act_bscales + (size_t)r * kFp4MaxT * (size_t)(p.H / 16),
+                             (uint64_t)Tr, (uint64_t)(p.H / 16), 16u, (uint32_t)Tr))
+      return cudaErrorInvalidValue;
+  }
+  const size_t fixed = 1024 /*align pad*/ + kFp4MaxT * sizeof(float) + sizeof(Fp4Smem) + 64;
+  const size_t budget = 227u * 1024u;
+  int nstage = (int)((budget - fixed) / kP4Stage);
+  if (nstage > kF4MaxStages) nstage = kF4MaxStages;
+  if (g_fp4_stages >= 2 && g_fp4_stages < nstage) nstage = g_fp4_stages;
+  if (nstage < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + (size_t)nstage * kP4Stage;
+  cudaError_t e = cudaFuncSetAttribute(lm_head_fp4_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int pairs = (num_sms / 2) < p.n_vtiles ? (num_sms / 2) : p.n_vtiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.blockDim = dim3((unsigned)kF4Threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, lm_head_fp4_pair_kernel, ta[0], tsa[0], ta[1], tsa[1], p,
+                            nstage);
+}
+
 }  // namespace
 
 void stage2_fp4_set_stages(int n) { g_fp4_stages = n; }
 
+void stage2_fp4_set_pair(int enabled) { g_fp4_pair = enabled != 0; }
+
 cudaError_t launch_stage2_fp4(const Stage2Params &p, int num_sms, cudaStream_t stream) {
   if (p.T < 1 || p.T > kFp4LaunchMaxT) return cudaErrorInvalidConfiguration;
+  if (p.T > kFp4MaxT && g_fp4_pair) return launch_fp4_pair(p, num_sms, stream);
   return p.T <= 64 ? launch_fp4<64>(p, num_sms, stream) : launch_fp4<128>(p, num_sms, stream);
 }
 

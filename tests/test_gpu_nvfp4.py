@@ -255,13 +255,37 @@ def test_nvfp4_pack_layout(nfq, V, H):
 
 @pytest.mark.parametrize("T", [136, 256])
 def test_nvfp4_two_token_groups_full_vocab(nfq, T):
-    """129..256 tokens in one launch over a full-size vocabulary: every CTA pair
-    of the grid shares a weight stream; every token against the oracle."""
+    """129..256 tokens in one launch over a full-size vocabulary, on CTA pairs
+    (the default form): every token against the oracle."""
     w = synth.workload("tiny", T=T, H=1024, k=2, V=151552, S=8, seed=T + 3)
     act = oracle_stage1(synth.stage1_inputs(w))
     qw, sw, gw = synth.lm_head_weights_nvfp4(w)
     out = run_lm(nfq, act, qw, sw, gw, w.S)
     check(*out, act, qw, sw, gw, w.S, list(range(T)), cache_key=("nvfp4_two", T))
+
+
+@pytest.mark.parametrize("T,H,V,S", [(129, 256, 1024, 8), (200, 1024, 5000, 5),
+                                     (256, 512, 128, 1), (160, 16384, 3000, 3),
+                                     (255, 1024, 151552, 8)])
+def test_nvfp4_cta_pairs_equal_two_token_groups(nfq, T, H, V, S):
+    """129..256 tokens: the CTA-pair kernel (cta_group::2 block-scaled MMAs,
+    each CTA holding half of every weight tile and the scales of all of it)
+    and two independent 128-token groups give the same bytes; both match the
+    oracle on every token.  Ragged second halves, one-block tiles (64 weight
+    rows per CTA, N = 128), a single block, the widest rows and a full
+    vocabulary are covered."""
+    w = synth.workload("tiny", T=T, H=H, k=2, V=V, S=S, seed=T * 5 + V)
+    act = oracle_stage1(synth.stage1_inputs(w))
+    qw, sw, gw = fp4_weights(w)
+    pair = run_lm(nfq, act, qw, sw, gw, S)
+    nfq.lm_head_pair(False)
+    try:
+        groups = run_lm(nfq, act, qw, sw, gw, S)
+    finally:
+        nfq.lm_head_pair(True)
+    for a, b in zip(pair, groups):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    check(*pair, act, qw, sw, gw, S, list(range(T)), cache_key=("nvfp4_pair", T, H, V, S))
 
 
 def test_fp4_quotients_match_ieee_division_exhaustively(nfq):
