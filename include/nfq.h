@@ -404,7 +404,8 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   128-token groups over one weight stream.  The results are the same either
  *   way.
  * nfq_lm_head_nvfp4_tune: pipeline stages of later NVFP4 LM-head launches
- *   (0 = as many as fit, at most 5; values below 2 or above what fits fall back).
+ *   (0 = as many as fit, at most 5; values below 2, or below 4 for the CTA-pair
+ *   form of 129..256 tokens, or above what fits fall back).
  * nfq_stage1_grid: at most max_ctas CTAs for later stage-1 launches, each then
  *   taking several rows in turn (0 = one CTA per SM at most).
  * nfq_stage1_split: batches of at most max_tokens rows (-1 = the default

@@ -422,26 +422,73 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 // scale blocks of the whole tile (4 KB per K step; the second request of each
 // is served from L2).
 //
+// Two rings per CTA.  The weight ring holds this CTA's codes and the tile's
+// scales (20 KB a K step, streamed from HBM).  The activation ring holds this
+// CTA's tokens' codes and scales (18 KB a step, served from L2 for every
+// tile).  Each weight slot owns one TMEM scale slot, so the weight ring is 5
+// deep, as many slots as TMEM holds beside the accumulator; the activation
+// ring is 4 deep (2 slots measured 25 % slower, 3 slots 4 %, more nothing).
+// Both producers arrive on one full barrier per step, so the scale writers
+// wait once per step: their loop, not the copies, is what bounded the step
+// time while they waited on three barriers (the K loop ran at about 0.53 us a
+// step with the copies switched off altogether).  The activation ring must
+// not be deeper than the weight ring: the activation producer may run as many
+// steps ahead as it has slots, and it must never arrive on a full barrier
+// whose previous phase (nw steps back) is still pending.  A build that broke
+// this rule (6 activation slots, 5 full barriers) let a CTA exit with copies
+// still in flight and faulted the GPU; the launcher enforces it.
+//
+// Warps (736 threads):
+//   0 .. 15   epilogue: warp w reads TMEM lane quadrant w%4 (tokens
+//             32(w%4) .. +31 of this CTA), tile columns 64(w/4) .. +63
+//   16 .. 19  scale writers: per K step, the step's activation and weight
+//             scales from shared memory into its TMEM scale slot
+//   20        weight producer (1-D bulk copies)
+//   21        TMEM allocator and, in the even CTA, the MMA issuer
+//   22        activation producer (2-D tensor copies)
+//
 // Hand-offs between the two CTAs:
 //  - each CTA's copies complete on its own full barrier; its scale writers
-//    wait there, store the stage's scales into TMEM and arrive on the EVEN
-//    CTA's sfready barrier (release at cluster scope).  That barrier completes
-//    once both CTAs' bytes have landed and both CTAs' scales are in TMEM, so
-//    the MMA thread waits on it alone (acquire at cluster scope);
-//  - the MMA commits arrive, multicast, on both CTAs' empty and tfull barriers;
-//  - both CTAs' epilogue warps arrive on the even CTA's tempty barrier (an
-//    execution dependency only, as in the FP8 pair kernel).
+//    wait there, store the step's scales into TMEM and arrive on the EVEN
+//    CTA's sfready barrier, which therefore completes once both CTAs' bytes
+//    have landed and both CTAs' scales are in TMEM: the MMA thread waits on it
+//    alone;
+//  - the MMA commits arrive, multicast, on both CTAs' empty barriers of the
+//    two rings and on both tfull barriers;
+//  - both CTAs' epilogue warps arrive on the even CTA's tempty barrier.
+// The remote arrivals carry execution dependencies only (the copies and the
+// MMAs go through the async proxy, TMEM accesses are ordered by the tcgen05
+// fences), so they and the waits use the CTA scope: a cluster-scope release
+// and acquire per K step measured about 1 us each, a step's whole budget.
 // A cluster barrier after the set-up (barriers initialised, TMEM allocated)
 // and one before the teardown (every MMA, copy and remote arrival done) bound
-// every cross-CTA access.  Each CTA drains its own copies, so neither needs
-// to outwait the other's after an expired wait.
+// every cross-CTA access.  Each CTA drains its own copies.
 
-constexpr uint32_t kP4A = 0;                               // 128 tokens x 128 code bytes
-constexpr uint32_t kP4W = 128 * 128;                       // this CTA's weight rows
-constexpr uint32_t kP4Sfb = kP4W + kWTileBytes;            // the whole tile's weight scales
-constexpr uint32_t kP4Sfa = kP4Sfb + kF4SfbBytes;          // this CTA's activation scales
-constexpr uint32_t kP4Stage = kP4Sfa + 128 * 16;
-static_assert(kP4Stage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+constexpr int kP4WProducer = kF4Producer;
+constexpr int kP4Mma = kF4Mma;
+constexpr int kP4AProducer = kF4Mma + 1;
+constexpr int kP4Threads = (kP4AProducer + 1) * 32;
+constexpr int kP4MaxW = kF4MaxStages;                       // weight ring depth (at most)
+constexpr int kP4NA = 4;                                    // activation ring depth
+constexpr uint32_t kP4WStage = kWTileBytes + kF4SfbBytes;   // codes (or half), the tile's scales
+constexpr uint32_t kP4WSfb = kWTileBytes;
+constexpr uint32_t kP4AStage = 128 * 128 + 128 * 16;        // 128 tokens' codes, then scales
+constexpr uint32_t kP4ASfa = 128 * 128;
+static_assert(kP4WStage % 1024 == 0 && kP4AStage % 1024 == 0,
+              "ring slots keep the 1024-byte swizzle alignment");
+static_assert(kP4NA <= kP4MaxW, "the activation producer stays within the full-barrier ring");
+
+struct Fp4PairSmem {
+  uint64_t full[kP4MaxW];         // this CTA's weight and activation bytes of a step have landed
+  uint64_t wempty[kP4MaxW];       // the step's MMAs are done: weight slot (and TMEM slot) free
+  uint64_t aempty[kP4NA];
+  uint64_t sfready[kF4MaxStages]; // even CTA: both CTAs' bytes landed, scales in TMEM
+  uint64_t tfull;
+  uint64_t tempty;                // even CTA: both CTAs' epilogues are done with the tile
+  uint32_t tmem_base;
+  int abort;
+  int last;
+};
 
 __device__ __forceinline__ void mma_fp4_block16_pair(uint32_t d_tmem, uint64_t a_desc,
                                                      uint64_t b_desc, uint32_t idesc,
@@ -456,8 +503,8 @@ __device__ __forceinline__ void mma_fp4_block16_pair(uint32_t d_tmem, uint64_t a
       : "memory");
 }
 
-// The copies of K step ks of tile (blk0, nb) that do not depend on the
-// activation: this CTA's weight codes and the tile's weight scales.
+// The weight copies of K step ks of tile (blk0, nb) into weight slot st: this
+// CTA's codes and the tile's scales.
 __device__ __forceinline__ void issue_pair_weight(const Stage2Params &p, size_t scale_region,
                                                   uint8_t *st, uint32_t fb, int blk0, int nb,
                                                   int ks, uint32_t rank, uint64_t pol_w,
@@ -467,9 +514,9 @@ __device__ __forceinline__ void issue_pair_weight(const Stage2Params &p, size_t 
       nb == 2 ? p.w_packed + ((size_t)(blk0 + (int)rank) * G + (size_t)ks) * kWTileBytes
               : p.w_packed + ((size_t)blk0 * G + (size_t)ks) * kWTileBytes +
                     (size_t)rank * (kWTileBytes / 2);
-  bulk_g2s(smem_u32(st + kP4W), codes, nb == 2 ? kWTileBytes : kWTileBytes / 2, fb, pol_w);
+  bulk_g2s(smem_u32(st), codes, nb == 2 ? kWTileBytes : kWTileBytes / 2, fb, pol_w);
   for (int h = 0; h < nb; ++h)
-    bulk_g2s(smem_u32(st + kP4Sfb + h * kF4ScaleBlock),
+    bulk_g2s(smem_u32(st + kP4WSfb + h * kF4ScaleBlock),
              p.w_packed + scale_region + ((size_t)(blk0 + h) * G + (size_t)ks) * kF4ScaleBlock,
              kF4ScaleBlock, fb, pol_s);
 }
@@ -478,18 +525,20 @@ __device__ __forceinline__ uint32_t pair_weight_bytes(int nb) {
   return (nb == 2 ? kWTileBytes : kWTileBytes / 2) + (uint32_t)nb * kF4ScaleBlock;
 }
 
-__global__ void __launch_bounds__(kF4Threads, 1)
+// nw: weight ring depth = TMEM scale slots
+__global__ void __launch_bounds__(kP4Threads, 1)
     lm_head_fp4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a0,
                             const __grid_constant__ CUtensorMap tmap_sa0,
                             const __grid_constant__ CUtensorMap tmap_a1,
                             const __grid_constant__ CUtensorMap tmap_sa1, const Stage2Params p,
-                            int nstage) {
+                            int nw) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  uint8_t *smem = smem_raw + pad;
-  float *gs_s = reinterpret_cast<float *>(smem + (size_t)nstage * kP4Stage);   // [128]
-  Fp4Smem *sh = reinterpret_cast<Fp4Smem *>(gs_s + kFp4MaxT);
+  uint8_t *aring = smem_raw + pad;                              // kP4NA activation slots
+  uint8_t *wring = aring + (size_t)kP4NA * kP4AStage;           // nw weight slots
+  float *gs_s = reinterpret_cast<float *>(wring + (size_t)nw * kP4WStage);   // [128]
+  Fp4PairSmem *sh = reinterpret_cast<Fp4PairSmem *>(gs_s + kFp4MaxT);
   volatile int *abort_flag = &sh->abort;
 
   const int warp = (int)(threadIdx.x / 32);
@@ -506,43 +555,48 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   const int b_begin = (int)(((long)pair * p.n_vtiles) / n_pair);
   const int b_end = (int)(((long)(pair + 1) * p.n_vtiles) / n_pair);
   const int n_tiles = (b_end - b_begin + 1) / 2;
+  const uint32_t total = (uint32_t)(n_tiles * G);              // K steps of the pair
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < nstage; ++s) {
-      mbar_init(smem_u32(&sh->full[s]), 1);
-      mbar_init(smem_u32(&sh->empty[s]), 1);
-      mbar_init(smem_u32(&sh->sfready[s]), 2 * kF4SfWarps);
+    for (int s = 0; s < nw; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 2);      // the two producers
+      mbar_init(smem_u32(&sh->wempty[s]), 1);
     }
+    for (int s = 0; s < kP4NA; ++s) mbar_init(smem_u32(&sh->aempty[s]), 1);
+    for (int s = 0; s < nw; ++s) mbar_init(smem_u32(&sh->sfready[s]), 2 * kF4SfWarps);
     mbar_init(smem_u32(&sh->tfull), 1);
     mbar_init(smem_u32(&sh->tempty), 2 * kF4EpiWarps);
     sh->abort = 0;
     sh->last = 0;
     fence_mbarrier_init();
   }
-  if (warp == kF4Producer && lane == 0) {
+  if (warp == kP4AProducer && lane == 0) {
     prefetch_tmap(tm_a);
     prefetch_tmap(tm_sa);
   }
-  if (warp == kF4Mma) {
+  if (warp == kP4Mma) {
     tmem_alloc_pair(smem_u32(&sh->tmem_base), 512);
     tmem_relinquish_pair();
   }
   __syncthreads();   // this CTA's barriers exist
-  // The weight part of the first stages is requested before the wait for the
-  // previous kernel (see the single-CTA kernel); it completes on this CTA's
-  // own barriers only.
-  const int total_steps = n_tiles * G;
-  const int npre = total_steps < nstage ? total_steps : nstage;
-  if (warp == kF4Producer) {
+  // The weight does not depend on the previous kernel on the stream: the
+  // first nw weight steps are requested before the wait for it.  They
+  // complete on this CTA's own barriers only.
+  const uint32_t npre = total < (uint32_t)nw ? total : (uint32_t)nw;
+  if (warp == kP4WProducer) {
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_s = policy_evict_normal();
-      for (int it = 0; it < npre; ++it) {
-        int blk0, nb;
-        small_tile(b_begin, b_end, it / G, blk0, nb);
+      int ti = 0, ks = 0, blk0 = 0, nb = 0;
+      if (n_tiles > 0) small_tile(b_begin, b_end, 0, blk0, nb);
+      for (uint32_t it = 0; it < npre; ++it) {
         const uint32_t fb = smem_u32(&sh->full[it]);
-        mbar_expect_tx(fb, pair_weight_bytes(nb));
-        issue_pair_weight(p, scale_region, smem + (size_t)it * kP4Stage, fb, blk0, nb, it % G,
-                          rank, pol_w, pol_s);
+        mbar_arrive_expect_tx(fb, pair_weight_bytes(nb));
+        issue_pair_weight(p, scale_region, wring + (size_t)it * kP4WStage, fb, blk0, nb, ks, rank,
+                          pol_w, pol_s);
+        if (++ks == G) {
+          ks = 0;
+          if (++ti < n_tiles) small_tile(b_begin, b_end, ti, blk0, nb);
+        }
       }
     }
     __syncwarp();
@@ -560,53 +614,80 @@ __global__ void __launch_bounds__(kF4Threads, 1)
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
 
-  if (warp == kF4Producer) {
-    // -------------------------------------------------------------- producer --
-    // One thread of each CTA waits for its free stages and issues its copies.
+  if (warp == kP4WProducer) {
+    // ------------------------------------------------------- weight producer --
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_s = policy_evict_normal();
-      const uint64_t pol_a = policy_evict_last();
-      uint32_t it = 0, s = 0, ph = 0;
-      bool ok = true;
-      for (int ti = 0; ti < n_tiles && ok; ++ti) {
-        int blk0, nb;
-        small_tile(b_begin, b_end, ti, blk0, nb);
-        for (int ks = 0; ks < G; ++ks, ++it) {
-          const bool pre = (int)it < npre;           // weight part already requested
-          if (!pre &&
-              !mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2)) {
-            ok = false;
-            break;
-          }
-          uint8_t *st = smem + (size_t)s * kP4Stage;
-          const uint32_t fb = smem_u32(&sh->full[s]);
-          mbar_arrive_expect_tx(fb, (pre ? 0u : pair_weight_bytes(nb)) + (uint32_t)Tc * (128u + 16u));
-          if (!pre) issue_pair_weight(p, scale_region, st, fb, blk0, nb, ks, rank, pol_w, pol_s);
-          tma_load_2d(smem_u32(st + kP4A), tm_a, ks * 128, 0, fb, pol_a);
-          tma_load_2d(smem_u32(st + kP4Sfa), tm_sa, ks * 16, 0, fb, pol_a);
-          if (++s == (uint32_t)nstage) {
-            s = 0;
-            ph ^= 1u;
-          }
+      uint32_t s = npre % (uint32_t)nw, ph = (npre / (uint32_t)nw) & 1u;
+      int ti = (int)npre / G, ks = (int)npre % G, blk0 = 0, nb = 0;
+      if (ti < n_tiles) small_tile(b_begin, b_end, ti, blk0, nb);
+      uint32_t it = npre;
+      for (; it < total; ++it) {
+        if (!mbar_wait(smem_u32(&sh->wempty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2))
+          break;
+        const uint32_t fb = smem_u32(&sh->full[s]);
+        mbar_arrive_expect_tx(fb, pair_weight_bytes(nb));
+        issue_pair_weight(p, scale_region, wring + (size_t)s * kP4WStage, fb, blk0, nb, ks, rank,
+                          pol_w, pol_s);
+        if (++s == (uint32_t)nw) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++ks == G) {
+          ks = 0;
+          if (++ti < n_tiles) small_tile(b_begin, b_end, ti, blk0, nb);
         }
       }
-      for (uint32_t j = it; j < (uint32_t)npre; ++j) mbar_arrive(smem_u32(&sh->full[j]));
-      const uint32_t issued = it > (uint32_t)npre ? it : (uint32_t)npre;
-      const uint32_t first = issued > (uint32_t)nstage ? issued - (uint32_t)nstage : 0u;
-      for (uint32_t j = first; j < issued; ++j)
-        mbar_wait_drain(smem_u32(&sh->full[j % (uint32_t)nstage]), (j / (uint32_t)nstage) & 1u);
+      // the steps whose weight copies may still be in flight (their full
+      // barrier also needs the activation producer's arrival: after an
+      // expired wait that may never come, and the drain gives up in time)
+      const uint32_t first = it > (uint32_t)nw ? it - (uint32_t)nw : 0u;
+      bool drained = true;
+      for (uint32_t j = first; j < it && drained; ++j)
+        drained = mbar_wait(smem_u32(&sh->full[j % (uint32_t)nw]), (j / (uint32_t)nw) & 1u,
+                            abort_flag, p.err, 0u);
+      if (!drained) {   // after an expired wait: give copies in flight 50 us to land
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 50000ull) {
+        }
+      }
     }
     __syncwarp();
-  } else if (warp == kF4Mma) {
+  } else if (warp == kP4AProducer) {
+    // --------------------------------------------------- activation producer --
+    // The activation boxes hold exactly this CTA's Tc token rows.
+    if (lane == 0) {
+      const uint64_t pol_a = policy_evict_last();
+      uint32_t s = 0, ph = 0, f = 0, it = 0;   // activation slot, its phase; full barrier
+      int ks = 0;
+      for (; it < total; ++it) {
+        if (!mbar_wait(smem_u32(&sh->aempty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2))
+          break;
+        uint8_t *st = aring + (size_t)s * kP4AStage;
+        const uint32_t fb = smem_u32(&sh->full[f]);
+        mbar_arrive_expect_tx(fb, (uint32_t)Tc * (128u + 16u));
+        tma_load_2d(smem_u32(st), tm_a, ks * 128, 0, fb, pol_a);
+        tma_load_2d(smem_u32(st + kP4ASfa), tm_sa, ks * 16, 0, fb, pol_a);
+        if (++s == (uint32_t)kP4NA) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++f == (uint32_t)nw) f = 0;
+        if (++ks == G) ks = 0;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kP4Mma) {
     // ------------------------------------------------------------------- MMA --
-    // One thread of the even CTA issues for the pair.  The last commit on an
-    // empty barrier covers every MMA issued before it: the thread waits for it
-    // before the teardown, also when it gave up in the middle of a tile.
+    // One thread of the even CTA issues for the pair.  The last commit on a
+    // weight-ring empty barrier covers every MMA issued before it: the thread
+    // waits for it before the teardown, also when it gave up within a tile.
     if (lane == 0 && even) {
-      const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(smem + kP4A));
-      const uint64_t w_desc0 = sw128_kmajor_desc(smem_u32(smem + kP4W));
-      constexpr uint64_t kStageDesc = kP4Stage >> 4;
-      uint32_t s = 0, ph = 0, n_issued = 0, s_last = 0, ph_last = 0;
+      const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(aring));
+      const uint64_t w_desc0 = sw128_kmajor_desc(smem_u32(wring));
+      constexpr uint64_t kADesc = kP4AStage >> 4, kWDesc = kP4WStage >> 4;
+      uint32_t ws = 0, wph = 0, as = 0;
+      uint32_t n_issued = 0, ws_last = 0, wph_last = 0;
       bool ok = true;
       for (int ti = 0; ti < n_tiles && ok; ++ti) {
         int blk0, nb;
@@ -616,89 +697,89 @@ __global__ void __launch_bounds__(kF4Threads, 1)
                        kErrBitStage2))
           break;
         for (int ks = 0; ks < G; ++ks) {
-          const uint64_t ad = a_desc0 + kStageDesc * s, wd = w_desc0 + kStageDesc * s;
-          const uint32_t sfa = tmem_base + kF4SfBase + s * kF4SfCols;
-          if (!mbar_wait(smem_u32(&sh->sfready[s]), ph, abort_flag, p.err, kErrBitStage2)) {
+          if (!mbar_wait(smem_u32(&sh->sfready[ws]), wph, abort_flag, p.err, kErrBitStage2)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint64_t ad = a_desc0 + kADesc * as, wd = w_desc0 + kWDesc * ws;
+          const uint32_t sf = tmem_base + kF4SfBase + ws * kF4SfCols;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_fp4_block16_pair(tmem_base, ad + 2u * kk, wd + 2u * kk, idesc, sfa + 4u * kk,
-                                 sfa + 16u + 8u * kk, (ks > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_pair(smem_u32(&sh->empty[s]), (uint16_t)3);
+            mma_fp4_block16_pair(tmem_base, ad + 2u * kk, wd + 2u * kk, idesc, sf + 4u * kk,
+                                 sf + 16u + 8u * kk, (ks > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_pair(smem_u32(&sh->wempty[ws]), (uint16_t)3);
+          mma_commit_pair(smem_u32(&sh->aempty[as]), (uint16_t)3);
           if (ks == G - 1) mma_commit_pair(smem_u32(&sh->tfull), (uint16_t)3);
           ++n_issued;
-          s_last = s;
-          ph_last = ph;
-          if (++s == (uint32_t)nstage) {
-            s = 0;
-            ph ^= 1u;
+          ws_last = ws;
+          wph_last = wph;
+          if (++ws == (uint32_t)nw) {
+            ws = 0;
+            wph ^= 1u;
           }
+          if (++as == (uint32_t)kP4NA) as = 0;
         }
       }
-      if (n_issued > 0) mbar_wait_drain(smem_u32(&sh->empty[s_last]), ph_last);
+      if (n_issued > 0) mbar_wait_drain(smem_u32(&sh->wempty[ws_last]), wph_last);
     }
     __syncwarp();
   } else if (warp >= kF4SfWarp0) {
     // --------------------------------------------------------- scale writers --
+    // Step it takes TMEM slot it % nw (as many slots as weight slots): its full
+    // barrier completes only after the weight producer waited for the MMAs of
+    // step it - nw, the slot's previous user.  One wait per step: the loop of
+    // these four warps is on the K loop's critical path.
     const int q = warp & 3;                        // this warp's TMEM lane quadrant
-    uint32_t s = 0, ph = 0;
-    bool ok = true;
-    for (int ti = 0; ti < n_tiles && ok; ++ti) {
-      for (int ks = 0; ks < G; ++ks) {
-        const bool got = mbar_wait(smem_u32(&sh->full[s]), ph, abort_flag, p.err, kErrBitStage2);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint8_t *sfb_s = smem + (size_t)s * kP4Stage + kP4Sfb;
-        const uint8_t *sfa_s = smem + (size_t)s * kP4Stage + kP4Sfa;
-        uint32_t ra[16];
+    uint32_t ws = 0, wph = 0, as = 0;
+    for (uint32_t it = 0; it < total; ++it) {
+      const bool got = mbar_wait(smem_u32(&sh->full[ws]), wph, abort_flag, p.err, kErrBitStage2);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const uint8_t *sfb_s = wring + (size_t)ws * kP4WStage + kP4WSfb;
+      const uint8_t *sfa_s = aring + (size_t)as * kP4AStage + kP4ASfa;
+      uint32_t ra[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          // this CTA's token row 32c + lane (rows past Tc feed accumulator
-          // rows that are never read)
-          const uint4 v = (32 * c + lane < Tc)
-                              ? *reinterpret_cast<const uint4 *>(sfa_s + (32 * c + lane) * 16)
-                              : make_uint4(0u, 0u, 0u, 0u);
-          ra[0 + c] = v.x;
-          ra[4 + c] = v.y;
-          ra[8 + c] = v.z;
-          ra[12 + c] = v.w;
-        }
-        uint32_t rb[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // the tile's rows 128h + 32c + lane (block h of a one-block tile:
-            // columns the MMA of N = 128 does not read)
-            const uint4 v = *reinterpret_cast<const uint4 *>(sfb_s + h * kF4ScaleBlock +
-                                                             (kk * 32 + lane) * 16);
-            rb[kk * 8 + h * 4 + 0] = v.x;
-            rb[kk * 8 + h * 4 + 1] = v.y;
-            rb[kk * 8 + h * 4 + 2] = v.z;
-            rb[kk * 8 + h * 4 + 3] = v.w;
-          }
-        const uint32_t col =
-            tmem_base + ((uint32_t)(32 * q) << 16) + kF4SfBase + s * kF4SfCols;
-        tmem_st16(col, ra);
-        tmem_st32(col + 16u, rb);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (even) mbar_arrive(smem_u32(&sh->sfready[s]));
-          else mbar_arrive_remote_cta(smem_u32(&sh->sfready[s]), 0u);
-        }
-        if (++s == (uint32_t)nstage) {
-          s = 0;
-          ph ^= 1u;
-        }
+      for (int c = 0; c < 4; ++c) {
+        // this CTA's token row 32c + lane (rows past Tc feed accumulator rows
+        // that are never read)
+        const uint4 v = (32 * c + lane < Tc)
+                            ? *reinterpret_cast<const uint4 *>(sfa_s + (32 * c + lane) * 16)
+                            : make_uint4(0u, 0u, 0u, 0u);
+        ra[0 + c] = v.x;
+        ra[4 + c] = v.y;
+        ra[8 + c] = v.z;
+        ra[12 + c] = v.w;
       }
+      uint32_t rb[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // the tile's rows 128h + 32c + lane (for a one-block tile, h = 1
+          // fills columns the MMA of N = 128 does not read)
+          const uint4 v = *reinterpret_cast<const uint4 *>(sfb_s + h * kF4ScaleBlock +
+                                                           (kk * 32 + lane) * 16);
+          rb[kk * 8 + h * 4 + 0] = v.x;
+          rb[kk * 8 + h * 4 + 1] = v.y;
+          rb[kk * 8 + h * 4 + 2] = v.z;
+          rb[kk * 8 + h * 4 + 3] = v.w;
+        }
+      const uint32_t col = tmem_base + ((uint32_t)(32 * q) << 16) + kF4SfBase + ws * kF4SfCols;
+      tmem_st16(col, ra);
+      tmem_st32(col + 16u, rb);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (even) mbar_arrive(smem_u32(&sh->sfready[ws]));
+        else mbar_arrive_remote_cta(smem_u32(&sh->sfready[ws]), 0u);
+      }
+      if (++ws == (uint32_t)nw) {
+        ws = 0;
+        wph ^= 1u;
+      }
+      if (++as == (uint32_t)kP4NA) as = 0;
     }
     __syncwarp();
   } else {
@@ -879,20 +960,23 @@ cudaError_t launch_fp4_pair(const Stage2Params &p_in, int num_sms, cudaStream_t 
                              (uint64_t)Tr, (uint64_t)(p.H / 16), 16u, (uint32_t)Tr))
       return cudaErrorInvalidValue;
   }
-  const size_t fixed = 1024 /*align pad*/ + kFp4MaxT * sizeof(float) + sizeof(Fp4Smem) + 64;
+  // the weight ring (and the TMEM scale slots) as deep as shared memory and
+  // TMEM allow
+  const size_t fixed = 1024 /*align pad*/ + (size_t)kP4NA * kP4AStage +
+                       kFp4MaxT * sizeof(float) + sizeof(Fp4PairSmem) + 64;
   const size_t budget = 227u * 1024u;
-  int nstage = (int)((budget - fixed) / kP4Stage);
-  if (nstage > kF4MaxStages) nstage = kF4MaxStages;
-  if (g_fp4_stages >= 2 && g_fp4_stages < nstage) nstage = g_fp4_stages;
-  if (nstage < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = fixed + (size_t)nstage * kP4Stage;
+  int nw = (int)((budget - fixed) / kP4WStage);
+  if (nw > kP4MaxW) nw = kP4MaxW;
+  if (g_fp4_stages >= kP4NA && g_fp4_stages < nw) nw = g_fp4_stages;
+  if (nw < kP4NA) return cudaErrorInvalidConfiguration;   // see the activation ring's rule
+  const size_t smem = fixed + (size_t)nw * kP4WStage;
   cudaError_t e = cudaFuncSetAttribute(lm_head_fp4_pair_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int pairs = (num_sms / 2) < p.n_vtiles ? (num_sms / 2) : p.n_vtiles;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * pairs));
-  cfg.blockDim = dim3((unsigned)kF4Threads);
+  cfg.blockDim = dim3((unsigned)kP4Threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -904,8 +988,7 @@ cudaError_t launch_fp4_pair(const Stage2Params &p_in, int num_sms, cudaStream_t 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, lm_head_fp4_pair_kernel, ta[0], tsa[0], ta[1], tsa[1], p,
-                            nstage);
+  return cudaLaunchKernelEx(&cfg, lm_head_fp4_pair_kernel, ta[0], tsa[0], ta[1], tsa[1], p, nw);
 }
 
 }  // namespace
