@@ -673,9 +673,10 @@ def run_ours(args, rank, world, local):
                                   "unit": "GB/s", "frac": round(gbs2 / peak, 4),
                                   "traffic": (ncu_traffic("lm_head_nvfp4" if fp4 else "lm_head")
                                               if args.workload == WORKLOAD and not unfused
-                                              else ncu_traffic("lm_head_tie_stress")
-                                              if args.workload == "tie_stress" and not fp4
-                                              and not unfused else None),
+                                              else ncu_traffic("lm_head_nvfp4_tie_stress"
+                                                               if fp4 else "lm_head_tie_stress")
+                                              if args.workload == "tie_stress" and not unfused
+                                              else None),
                                   "kernel": ("lm_head_fp4_kernel" if fp4 and T <= 128 else
                                              "lm_head_fp4_pair_kernel (CTA pairs, cta_group::2)"
                                              if fp4 and T <= 256 else
@@ -974,6 +975,32 @@ def run_probe_mma(args, local):
                      "ctas": 2 * ctas if pair else ctas, "launches": n,
                      "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
                      "ns_per_mma": round(mma_ns, 2)})
+    for pair in (False, True):
+        # the NVFP4 LM head's block-scaled MMA (K = 64 e2m1 elements each)
+        ctas = sms // 2 if pair else sms
+        iters = 2048
+        for _ in range(3):
+            nfq.probe_nvfp4_mma(pair, ctas, iters)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n = max(5, min(50, args.steps))
+        flops = 0.0
+        e0.record()
+        for _ in range(n):
+            flops += nfq.probe_nvfp4_mma(pair, ctas, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        if nfq.device_error() != nfq.NFQ_OK:
+            raise RuntimeError("the MMA probe reported an expired wait")
+        ms = e0.elapsed_time(e1)
+        rows.append({"shape": ("NVFP4 block-scaled, cta_group::2, M=256 x N=256 x K=64 per CTA pair"
+                               if pair else
+                               "NVFP4 block-scaled, cta_group::1, M=128 x N=256 x K=64 per CTA"),
+                     "operand_sets": 1, "tmem_readers": None,
+                     "ctas": 2 * ctas if pair else ctas, "launches": n,
+                     "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
+                     "ns_per_mma": round(ms * 1e6 / (n * iters * 4), 2)})
     tmem = []
     for batched in (False, True):
         iters = 4096

@@ -426,6 +426,13 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   the LM head epilogue's pattern until the MMAs are done.  Asynchronous on
  *   `stream`; time it with events.  NFQ_ERR_SHAPE for ctas outside 1..4096,
  *   iters outside 1..2^20, stages outside 0..4, or pairs with stages = 0.
+ * nfq_probe_nvfp4_mma: a measurement kernel, not part of the path.  As
+ *   nfq_probe_fp8_mma (one operand set) with the NVFP4 LM head's block-scaled
+ *   MMA: `iters` K steps of four tcgen05.mma kind::mxf4nvf4.block_scale
+ *   .scale_vec::4X, M = 128 (pairs: 256) x N = 256 x K = 64 each, block scales
+ *   of 1.0 in TMEM; 2 * M * 256 * 256 * iters flops per CTA (per pair).
+ *   Asynchronous on `stream`; NFQ_ERR_SHAPE for ctas outside 1..4096 or iters
+ *   outside 1..2^20.
  * nfq_probe_tmem_ld: a measurement kernel, not part of the path.  `ctas` CTAs
  *   of 16 warps each read a 128-lane x 256-column TMEM accumulator into
  *   registers `iters` times, in the LM head epilogue's pattern (each warp 32
@@ -499,6 +506,7 @@ void nfq_lm_head_nvfp4_tune(int stages);
 void nfq_stage1_grid(int max_ctas);
 void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma);
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
+int nfq_probe_nvfp4_mma(int pair, int ctas, int iters, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream);
 int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, void *stream);

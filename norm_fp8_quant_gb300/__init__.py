@@ -104,6 +104,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_lm_head_pair.restype = None
     lib.nfq_probe_fp8_mma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_fp8_mma.restype = ctypes.c_int
+    lib.nfq_probe_nvfp4_mma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_probe_nvfp4_mma.restype = ctypes.c_int
     lib.nfq_probe_tmem_ld.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_tmem_ld.restype = ctypes.c_int
     lib.nfq_probe_handshake.argtypes = [ctypes.c_int] * 5 + [_P]
@@ -410,6 +412,18 @@ def probe_fp8_mma(pair: bool, ctas: int, iters: int, stages: int = 1, stream=Non
                       _raw_stream(dev, stream)), "nfq_probe_fp8_mma")
     M = 256 if pair else 128
     return 2.0 * M * 256 * 128 * iters * ctas
+
+
+def probe_nvfp4_mma(pair: bool, ctas: int, iters: int, stream=None):
+    """Launch the block-scaled NVFP4 MMA-rate measurement kernel (not part of
+    the path): `ctas` CTAs (or CTA pairs) each issuing `iters` K steps of four
+    MMAs of K = 64.  Returns the flops the launch performs."""
+    import torch
+    dev = torch.cuda.current_device()
+    _check(_on_device(dev, load().nfq_probe_nvfp4_mma, 1 if pair else 0, ctas, iters,
+                      _raw_stream(dev, stream)), "nfq_probe_nvfp4_mma")
+    M = 256 if pair else 128
+    return 2.0 * M * 256 * 256 * iters * ctas
 
 
 def probe_tmem_ld(batched: bool, ctas: int, iters: int, stream=None):

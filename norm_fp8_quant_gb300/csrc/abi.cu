@@ -198,6 +198,8 @@ cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stage
                                         unsigned *err, cudaStream_t stream);
 cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
                                           cudaStream_t stream);
+cudaError_t launch_probe_nvfp4_mma(int pair, int ctas, int iters, unsigned *err,
+                                   cudaStream_t stream);
 // The LM head's accumulator hand-off without data (probe.cu).
 cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, int iters,
                                    unsigned *err, cudaStream_t stream);
@@ -695,6 +697,15 @@ int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream) {
                                                   static_cast<cudaStream_t>(stream)));
   return map_cuda(launch_probe_fp8_mma_stages(pair ? 1 : 0, ctas, iters, stages, d->err,
                                               static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_probe_nvfp4_mma(int pair, int ctas, int iters, void *stream) {
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20)) return NFQ_ERR_SHAPE;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_probe_nvfp4_mma(pair ? 1 : 0, ctas, iters, d->err,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,

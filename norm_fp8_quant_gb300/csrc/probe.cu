@@ -1,6 +1,7 @@
 // Measurement kernels (not on the hot path): the rate at which tcgen05 FP8
-// MMAs run when nothing else competes for the SM (the FP8 tensor roofline
-// that the LM head's tensor-pipe figures are read against), the rate at
+// and block-scaled NVFP4 MMAs run when nothing else competes for the SM (the
+// tensor rooflines that the LM heads' tensor-pipe figures are read against),
+// the rate at
 // which TMEM accumulators can be read into registers, the time of the
 // LM head's accumulator hand-off between the MMA thread and the epilogue
 // warps through two (or more) TMEM buffers, with no data to stream;
@@ -500,6 +501,111 @@ cudaError_t launch_probe_tmem_ld(int batched, int ctas, int iters, cudaStream_t 
   return cudaGetLastError();
 }
 
+// nvfp4_mma_rate_kernel<kPair>: as fp8_mma_rate_kernel with the LM head's
+// block-scaled NVFP4 MMA (tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X,
+// K = 64 e2m1 elements each, four per 256-element K step) on one operand set:
+// M = 128 x N = 256 per CTA or M = 256 x N = 256 per pair.  The block scales
+// (e4m3 1.0) sit in TMEM columns 256..303 in the LM head's layout.
+__device__ __forceinline__ void probe_mma_fp4_pair(uint32_t d, uint64_t a, uint64_t b,
+                                                   uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                   uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+
+template <bool kPair>
+__global__ void __launch_bounds__(128, 1) nvfp4_mma_rate_kernel(int iters, unsigned *err) {
+  constexpr uint32_t kA = 128 * 128, kB = (kPair ? 128 : 256) * 128;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  __shared__ uint64_t done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+  const int warp = (int)(threadIdx.x / 32), lane = (int)(threadIdx.x % 32);
+  const bool issuer = !kPair || cluster_ctarank() == 0;
+
+  uint4 *z = reinterpret_cast<uint4 *>(smem);
+  for (uint32_t i = threadIdx.x; i < (kA + kB) / 16; i += blockDim.x)
+    z[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&done), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(&tmem_base), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&tmem_base), 512);
+      tmem_relinquish();
+    }
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  {
+    // every warp its own lane quadrant: 48 scale columns of e4m3 1.0
+    uint32_t one[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) one[j] = 0x38383838u;
+    const uint32_t col = tmem_base + ((uint32_t)(32 * warp) << 16) + 256u;
+    tmem_st32(col, one);
+    tmem_st16(col + 32u, *reinterpret_cast<const uint32_t(*)[16]>(one));
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  tc_fence_after();
+
+  if (warp == 0) {
+    if (issuer && lane == 0) {
+      const uint32_t idesc = idesc_nvfp4(kPair ? 256 : 128, 256);
+      const uint64_t ad = sw128_kmajor_desc(smem_u32(smem)), bd = sw128_kmajor_desc(smem_u32(smem + kA));
+      const uint32_t sf = tmem_base + 256u;
+      for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if constexpr (kPair)
+            probe_mma_fp4_pair(tmem_base, ad + 2u * kk, bd + 2u * kk, idesc, sf + 4u * kk,
+                               sf + 16u + 8u * kk, (it | kk) ? 1u : 0u);
+          else
+            mma_fp4_block16(tmem_base, ad + 2u * kk, bd + 2u * kk, idesc, sf + 4u * kk,
+                            sf + 16u + 8u * kk, (it | kk) ? 1u : 0u);
+        }
+      }
+      if constexpr (kPair)
+        mma_commit_pair(smem_u32(&done), (uint16_t)3);
+      else
+        mma_commit(smem_u32(&done));
+    }
+    __syncwarp();
+    if (lane == 0 &&
+        !mbar_wait(smem_u32(&done), 0u, (volatile int *)&abort_flag, err, kProbeErrBit))
+      mbar_wait_drain(smem_u32(&done), 0u);
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) {
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, 512);
+    else
+      tmem_dealloc(tmem_base, 512);
+  }
+}
+
 // `stages` sets of tiles (1..4): each K block reads fresh operands from shared
 // memory, as the LM head's pipeline does, instead of the same tiles again.
 cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stages,
@@ -530,6 +636,28 @@ cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stage
 cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,
                                  cudaStream_t stream) {
   return launch_probe_fp8_mma_stages(pair, ctas, iters, 1, err, stream);
+}
+
+cudaError_t launch_probe_nvfp4_mma(int pair, int ctas, int iters, unsigned *err,
+                                   cudaStream_t stream) {
+  const size_t smem = 120u * 1024u;   // the tiles need 48 KB; 120 KB keeps one CTA per SM
+  auto kern = pair ? nvfp4_mma_rate_kernel<true> : nvfp4_mma_rate_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pair ? 2 * ctas : ctas));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, iters, err);
 }
 
 // The accumulator hand-off probe: `ctas` CTAs (pair: `ctas` CTA pairs) with

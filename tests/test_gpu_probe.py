@@ -30,6 +30,16 @@ def test_probe_fp8_mma_runs(nfq, pair, stages):
         nfq.probe_fp8_mma(pair, 4, 16, 5)
 
 
+@pytest.mark.parametrize("pair", [False, True])
+def test_probe_nvfp4_mma_runs(nfq, pair):
+    flops = nfq.probe_nvfp4_mma(pair, 4, 16)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    assert flops == 2.0 * (256 if pair else 128) * 256 * 256 * 16 * 4
+    with pytest.raises(nfq.NfqError):
+        nfq.probe_nvfp4_mma(pair, 0, 16)
+
+
 def test_probe_mma_with_tmem_readers_runs(nfq):
     flops = nfq.probe_fp8_mma(False, 4, 64, 0)
     torch.cuda.synchronize()
