@@ -191,6 +191,46 @@ def test_nvfp4_lm_head_planted_ties_and_zero_logits(nfq):
           expected={t: a for t, (a, b) in pairs.items()})
 
 
+def test_nvfp4_pair_planted_ties(nfq):
+    """200 tokens on CTA pairs, tokens of both CTAs (0..127 and 128..199), with
+    exact duplicate rows (codes and block scales).  With 256 blocks over 76
+    pairs the first pair holds blocks 0..2: a one-block tile (rows 0..63 in the
+    even CTA, 64..127 in the odd one), then blocks 1 and 2 as one tile (128..255
+    even, 256..383 odd).  The duplicates sit across the halves of a one-block
+    tile (63 | 64) and of a two-block tile (255 | 256), inside one half, across
+    tiles (127 | 128), across pairs (383 | 384), across shards (8191 | 8192) and
+    at the last row.  The lowest index wins, and the pair form matches two token
+    groups byte for byte."""
+    T, H, V, S = 200, 512, 32768, 4
+    w = synth.workload("tiny", T=T, H=H, k=2, V=V, S=S, seed=21)
+    act = oracle_stage1(synth.stage1_inputs(w))
+    qw, sw, gw = (x.copy() if isinstance(x, np.ndarray) else x for x in fp4_weights(w))
+    pairs = {0: (63, 64), 5: (255, 256), 64: (3, 17), 127: (127, 128), 128: (383, 384),
+             150: (8191, 8192), 190: (20000, 32767), 199: (300, 301)}
+    for t, (a, b) in pairs.items():
+        # e2m1 +-6 where the activation is positive / negative, 0 where it is 0;
+        # the largest block scale everywhere: this row wins for token t
+        u = np.stack([act["codes"][t] & 15, act["codes"][t] >> 4], axis=-1).reshape(-1)
+        pat = np.where((u & 7) == 0, 0, np.where(u & 8, 0xF, 0x7)).astype(np.uint8)
+        row = (pat[0::2] | (pat[1::2] << 4)).astype(np.uint8)
+        for v in (a, b):
+            qw[v] = row
+            sw[v] = 0x7E
+    pair = run_lm(nfq, act, qw, sw, gw, S)
+    nfq.lm_head_pair(False)
+    try:
+        groups = run_lm(nfq, act, qw, sw, gw, S)
+    finally:
+        nfq.lm_head_pair(True)
+    for x, y in zip(pair, groups):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    tok = pair[0]
+    for t, (a, b) in pairs.items():
+        assert tok[t] == a
+    check(*pair, act, qw, sw, gw, S, list(range(T)),
+          expected={t: a for t, (a, b) in pairs.items()})
+
+
 def test_nvfp4_gpu_stage1_feeds_the_lm_head(nfq):
     """The two NVFP4 stages chained on the GPU: the LM head on the GPU's own
     activation agrees with the oracle's LM head on that activation."""
