@@ -453,8 +453,9 @@ __global__ void __launch_bounds__(kF4Threads, 1)
 //    CTA's sfready barrier, which therefore completes once both CTAs' bytes
 //    have landed and both CTAs' scales are in TMEM: the MMA thread waits on it
 //    alone;
-//  - the MMA commits arrive, multicast, on both CTAs' empty barriers of the
-//    two rings and on both tfull barriers;
+//  - one MMA commit per step arrives, multicast, on both CTAs' empty barrier
+//    of the step (which frees its weight, TMEM and activation slots), and one
+//    per tile on both tfull barriers;
 //  - both CTAs' epilogue warps arrive on the even CTA's tempty barrier.
 // The remote arrivals carry execution dependencies only (the copies and the
 // MMAs go through the async proxy, TMEM accesses are ordered by the tcgen05
@@ -480,8 +481,7 @@ static_assert(kP4NA <= kP4MaxW, "the activation producer stays within the full-b
 
 struct Fp4PairSmem {
   uint64_t full[kP4MaxW];         // this CTA's weight and activation bytes of a step have landed
-  uint64_t wempty[kP4MaxW];       // the step's MMAs are done: weight slot (and TMEM slot) free
-  uint64_t aempty[kP4NA];
+  uint64_t empty[kP4MaxW];        // the step's MMAs are done: its weight, TMEM and activation slots are free
   uint64_t sfready[kF4MaxStages]; // even CTA: both CTAs' bytes landed, scales in TMEM
   uint64_t tfull;
   uint64_t tempty;                // even CTA: both CTAs' epilogues are done with the tile
@@ -560,9 +560,8 @@ __global__ void __launch_bounds__(kP4Threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < nw; ++s) {
       mbar_init(smem_u32(&sh->full[s]), 2);      // the two producers
-      mbar_init(smem_u32(&sh->wempty[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
     }
-    for (int s = 0; s < kP4NA; ++s) mbar_init(smem_u32(&sh->aempty[s]), 1);
     for (int s = 0; s < nw; ++s) mbar_init(smem_u32(&sh->sfready[s]), 2 * kF4SfWarps);
     mbar_init(smem_u32(&sh->tfull), 1);
     mbar_init(smem_u32(&sh->tempty), 2 * kF4EpiWarps);
@@ -623,7 +622,7 @@ __global__ void __launch_bounds__(kP4Threads, 1)
       if (ti < n_tiles) small_tile(b_begin, b_end, ti, blk0, nb);
       uint32_t it = npre;
       for (; it < total; ++it) {
-        if (!mbar_wait(smem_u32(&sh->wempty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2))
+        if (!mbar_wait(smem_u32(&sh->empty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2))
           break;
         const uint32_t fb = smem_u32(&sh->full[s]);
         mbar_arrive_expect_tx(fb, pair_weight_bytes(nb));
@@ -655,23 +654,28 @@ __global__ void __launch_bounds__(kP4Threads, 1)
     __syncwarp();
   } else if (warp == kP4AProducer) {
     // --------------------------------------------------- activation producer --
-    // The activation boxes hold exactly this CTA's Tc token rows.
+    // The activation boxes hold exactly this CTA's Tc token rows.  Slot s of
+    // step it is free once the MMAs of step it - kP4NA are done: their commit
+    // on empty[(it - kP4NA) % nw] (that barrier cannot have moved on by a
+    // further phase, which needs this producer's arrival for a later step).
     if (lane == 0) {
       const uint64_t pol_a = policy_evict_last();
-      uint32_t s = 0, ph = 0, f = 0, it = 0;   // activation slot, its phase; full barrier
+      uint32_t s = 0, f = 0, e = 0, eph = 0, it = 0;   // activation slot; full barrier; empty barrier of step it - kP4NA
       int ks = 0;
       for (; it < total; ++it) {
-        if (!mbar_wait(smem_u32(&sh->aempty[s]), ph ^ 1u, abort_flag, p.err, kErrBitStage2))
-          break;
+        if (it >= (uint32_t)kP4NA) {
+          if (!mbar_wait(smem_u32(&sh->empty[e]), eph, abort_flag, p.err, kErrBitStage2)) break;
+          if (++e == (uint32_t)nw) {
+            e = 0;
+            eph ^= 1u;
+          }
+        }
         uint8_t *st = aring + (size_t)s * kP4AStage;
         const uint32_t fb = smem_u32(&sh->full[f]);
         mbar_arrive_expect_tx(fb, (uint32_t)Tc * (128u + 16u));
         tma_load_2d(smem_u32(st), tm_a, ks * 128, 0, fb, pol_a);
         tma_load_2d(smem_u32(st + kP4ASfa), tm_sa, ks * 16, 0, fb, pol_a);
-        if (++s == (uint32_t)kP4NA) {
-          s = 0;
-          ph ^= 1u;
-        }
+        if (++s == (uint32_t)kP4NA) s = 0;
         if (++f == (uint32_t)nw) f = 0;
         if (++ks == G) ks = 0;
       }
@@ -679,9 +683,11 @@ __global__ void __launch_bounds__(kP4Threads, 1)
     __syncwarp();
   } else if (warp == kP4Mma) {
     // ------------------------------------------------------------------- MMA --
-    // One thread of the even CTA issues for the pair.  The last commit on a
-    // weight-ring empty barrier covers every MMA issued before it: the thread
-    // waits for it before the teardown, also when it gave up within a tile.
+    // One thread of the even CTA issues for the pair, one commit per step: this
+    // thread's per-step path (wait, fence, four MMAs, commits) is what bounds the
+    // K loop.  The last commit on an empty barrier covers every MMA issued
+    // before it: the thread waits for it before the teardown, also when it gave
+    // up within a tile.
     if (lane == 0 && even) {
       const uint64_t a_desc0 = sw128_kmajor_desc(smem_u32(aring));
       const uint64_t w_desc0 = sw128_kmajor_desc(smem_u32(wring));
@@ -708,8 +714,7 @@ __global__ void __launch_bounds__(kP4Threads, 1)
           for (int kk = 0; kk < 4; ++kk)
             mma_fp4_block16_pair(tmem_base, ad + 2u * kk, wd + 2u * kk, idesc, sf + 4u * kk,
                                  sf + 16u + 8u * kk, (ks > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_pair(smem_u32(&sh->wempty[ws]), (uint16_t)3);
-          mma_commit_pair(smem_u32(&sh->aempty[as]), (uint16_t)3);
+          mma_commit_pair(smem_u32(&sh->empty[ws]), (uint16_t)3);
           if (ks == G - 1) mma_commit_pair(smem_u32(&sh->tfull), (uint16_t)3);
           ++n_issued;
           ws_last = ws;
@@ -721,7 +726,7 @@ __global__ void __launch_bounds__(kP4Threads, 1)
           if (++as == (uint32_t)kP4NA) as = 0;
         }
       }
-      if (n_issued > 0) mbar_wait_drain(smem_u32(&sh->wempty[ws_last]), wph_last);
+      if (n_issued > 0) mbar_wait_drain(smem_u32(&sh->empty[ws_last]), wph_last);
     }
     __syncwarp();
   } else if (warp >= kF4SfWarp0) {
