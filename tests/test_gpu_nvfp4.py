@@ -328,6 +328,28 @@ def test_nvfp4_cta_pairs_equal_two_token_groups(nfq, T, H, V, S):
     check(*pair, act, qw, sw, gw, S, list(range(T)), cache_key=("nvfp4_pair", T, H, V, S))
 
 
+def test_nvfp4_stage_tuning_keeps_the_bytes(nfq):
+    """The pipeline-depth hook: the single-CTA kernel (64 tokens) and the
+    CTA-pair kernel (200 tokens) give the same bytes at every depth they
+    accept, and depths the pair kernel must refuse (a weight ring shallower
+    than its 4-slot activation ring) fall back to the default."""
+    outs = {}
+    for T in (64, 200):
+        w = synth.workload("tiny", T=T, H=1024, k=2, V=40000, S=4, seed=T + 7)
+        act = oracle_stage1(synth.stage1_inputs(w))
+        qw, sw, gw = fp4_weights(w)
+        try:
+            for stages in (0, 2, 3, 4, 5):
+                nfq.lm_head_nvfp4_tune(stages)
+                outs[(T, stages)] = run_lm(nfq, act, qw, sw, gw, w.S)
+        finally:
+            nfq.lm_head_nvfp4_tune(0)
+        for stages in (2, 3, 4, 5):
+            for a, b in zip(outs[(T, 0)], outs[(T, stages)]):
+                assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (T, stages)
+        check(*outs[(T, 0)], act, qw, sw, gw, w.S, list(range(T)))
+
+
 def test_fp4_quotients_match_ieee_division_exhaustively(nfq):
     """The NVFP4 stage 1 forms each block-scale code and each e2m1 code without
     IEEE divisions.  Over every bf16 row maximum and every finite e4m3 block
