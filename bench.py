@@ -676,7 +676,9 @@ def run_ours(args, rank, world, local):
                                               else ncu_traffic("lm_head_nvfp4_tie_stress"
                                                                if fp4 else "lm_head_tie_stress")
                                               if args.workload == "tie_stress" and not unfused
-                                              else None),
+                                              else ncu_traffic("lm_head_decode_c1")
+                                              if args.workload == "decode_c1" and not fp4
+                                              and not unfused else None),
                                   "kernel": ("lm_head_fp4_kernel" if fp4 and T <= 128 else
                                              "lm_head_fp4_pair_kernel (CTA pairs, cta_group::2)"
                                              if fp4 and T <= 256 else
