@@ -116,6 +116,49 @@ def test_nvfp4_chain_matches_oracle(nfq, name, P):
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
+def test_chain_on_cta_pairs(nfq, fmt):
+    """200 tokens a position: every LM head of a three-position chain runs on
+    CTA pairs (cta_group::2), launched programmatically after the stage 1 that
+    writes its activation while its weight stages are already requested.  Every
+    token of every link against the oracle fed the GPU's previous hidden."""
+    from tests._parity import check_stage2_fp4
+    P = 3
+    w = synth.workload("tiny", T=200, H=1024, k=2, V=32768, S=8, seed=41)
+    base = synth.stage1_inputs(w)
+    pos = [synth.stage1_inputs(synth.workload("tiny", T=200, H=1024, k=2, seed=p + 42))["partials"]
+           for p in range(P)]
+    parts = [[to_dev_bf16(x) for x in part] for part in pos]
+    hidden = [torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    if fmt == "fp8":
+        qw, sw = synth.lm_head_weights(w)
+        toks, _ = nfq.mtp_draft_chain(parts, to_dev_bf16(base["residual"]),
+                                      to_dev_bf16(base["norm_w"]),
+                                      nfq.pack_lm_head_weights(to_dev(qw)), to_dev(sw), w.S, w.eps,
+                                      hidden_bufs=hidden)
+    else:
+        qw, sw, gw = synth.lm_head_weights_nvfp4(w)
+        wp = nfq.pack_lm_head_weights_nvfp4(to_dev(qw), to_dev(sw), gw)
+        toks, _ = nfq.mtp_draft_chain_nvfp4(parts, to_dev_bf16(base["residual"]),
+                                            to_dev_bf16(base["norm_w"]), wp, w.S, w.eps,
+                                            hidden_bufs=hidden)
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    toks = toks.cpu().numpy()
+    gh = [bf16_host(h) for h in hidden]
+    sample = list(range(w.T))
+    for p in range(P):
+        res = base["residual"] if p == 0 else gh[p - 1]
+        ref = oracle.reduce_norm_quant(pos[p], res, base["norm_w"], w.eps)
+        _hidden_within_one_ulp(gh[p], ref["hidden"])
+        if fmt == "fp8":
+            check_stage2(toks[p], ref["codes"], ref["scales"], qw, sw, w.S, sample)
+        else:
+            act = oracle.nvfp4_quant(gh[p])
+            check_stage2_fp4(toks[p], act["codes"], act["block_scales"], act["global_scales"], qw,
+                             sw, gw, w.S, sample)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
 def test_chain_under_one_cuda_graph(nfq, fmt):
     """Five chained draft positions captured in one CUDA graph: every replay
     gives the bytes of the eager chain (tokens, every position's hidden, the
