@@ -159,19 +159,22 @@ def test_chain_on_cta_pairs(nfq, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["fp8", "nvfp4"])
-def test_chain_under_one_cuda_graph(nfq, fmt):
+@pytest.mark.parametrize("T", [64, 200])
+def test_chain_under_one_cuda_graph(nfq, fmt, T):
     """Five chained draft positions captured in one CUDA graph: every replay
     gives the bytes of the eager chain (tokens, every position's hidden, the
     activation), the argmax workspace returns to zero, and every link matches
-    the oracle fed the previous link's hidden."""
+    the oracle fed the previous link's hidden.  200 tokens run the LM heads on
+    CTA pairs."""
     from tests._parity import check_stage2_fp4
     P = 5
-    w = synth.workload("decode_c64", V=32768, S=8)
+    w = synth.workload("decode_c64", T=T, V=32768, S=8)
     base = synth.stage1_inputs(w)
-    pos = [synth.stage1_inputs(synth.workload("decode_c64", seed=p + 1))["partials"] for p in range(P)]
+    pos = [synth.stage1_inputs(synth.workload("decode_c64", T=T, seed=p + 1))["partials"]
+           for p in range(P)]
     parts = [[to_dev_bf16(x) for x in part] for part in pos]
     res0, nw = to_dev_bf16(base["residual"]), to_dev_bf16(base["norm_w"])
-    T, H = w.T, w.H
+    H = w.H
     hidden = [torch.empty((T, H), dtype=torch.bfloat16, device="cuda") for _ in range(P)]
     toks = torch.empty((P, T), dtype=torch.int32, device="cuda")
     ws = nfq.lm_head_workspace(T, w.S, "cuda")
