@@ -1049,8 +1049,30 @@ def run_probe_mma(args, local):
                                   2: "none: each group of MMAs waited for before the next"}[mode],
                      "ctas": 2 * ctas if pair else ctas, "launches": n,
                      "ns_per_k_block": round(ms * 1e6 / (n * iters), 1)})
+    latency = []
+    for mode, what in ((0, "two warps of one CTA, local arrivals"),
+                       (1, "the two CTAs of a cluster, remote arrivals at CTA scope"),
+                       (2, "the two CTAs of a cluster, remote arrivals with cluster-scope release"),
+                       (3, "the two CTAs of a cluster, st.async counted on the peer's barrier")):
+        iters = 20000
+        for _ in range(2):
+            nfq.probe_handoff(mode, iters)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n = 5
+        e0.record()
+        hops = 0
+        for _ in range(n):
+            hops += nfq.probe_handoff(mode, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        if nfq.device_error() != nfq.NFQ_OK:
+            raise RuntimeError("the hand-off latency probe reported an expired wait")
+        latency.append({"between": what, "launches": n,
+                        "ns_one_way": round(e0.elapsed_time(e1) * 1e6 / hops, 1)})
     return {"metric": "FP8 dense tensor rate (tcgen05.mma kind::f8f6f4 from shared memory)",
-            "unit": "TFLOP/s", "rows": rows, "tmem_read": tmem,
+            "unit": "TFLOP/s", "rows": rows, "tmem_read": tmem, "handoff_latency": latency,
             "handshake": {"rows": hand,
                           "what": "the LM head's accumulator hand-off without data: per K block "
                                   "(128 deep, 256 weight columns) four MMAs per N-column group, "

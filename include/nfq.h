@@ -433,6 +433,14 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   of 1.0 in TMEM; 2 * M * 256 * 256 * iters flops per CTA (per pair).
  *   Asynchronous on `stream`; NFQ_ERR_SHAPE for ctas outside 1..4096 or iters
  *   outside 1..2^20.
+ * nfq_probe_handoff: a measurement kernel, not part of the path: `iters`
+ *   round trips of a barrier hand-off between two threads, each waiting
+ *   (bounded) on its own mbarrier for the other's signal.  mode 0: two warps
+ *   of one CTA, local arrivals; 1: the two CTAs of a cluster, remote arrivals
+ *   at CTA scope; 2: the same with release at cluster scope; 3: the same by
+ *   st.async of one word counted on the peer's barrier.  Asynchronous on
+ *   `stream`; time it with events.  NFQ_ERR_SHAPE for mode outside 0..3 or
+ *   iters outside 1..2^20.
  * nfq_probe_tmem_ld: a measurement kernel, not part of the path.  `ctas` CTAs
  *   of 16 warps each read a 128-lane x 256-column TMEM accumulator into
  *   registers `iters` times, in the LM head epilogue's pattern (each warp 32
@@ -507,6 +515,7 @@ void nfq_stage1_grid(int max_ctas);
 void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma);
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
 int nfq_probe_nvfp4_mma(int pair, int ctas, int iters, void *stream);
+int nfq_probe_handoff(int mode, int iters, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream);
 int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, void *stream);

@@ -106,6 +106,8 @@ def load(path: str = LIB_PATH):
     lib.nfq_probe_fp8_mma.restype = ctypes.c_int
     lib.nfq_probe_nvfp4_mma.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_nvfp4_mma.restype = ctypes.c_int
+    lib.nfq_probe_handoff.argtypes = [ctypes.c_int, ctypes.c_int, _P]
+    lib.nfq_probe_handoff.restype = ctypes.c_int
     lib.nfq_probe_tmem_ld.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_tmem_ld.restype = ctypes.c_int
     lib.nfq_probe_handshake.argtypes = [ctypes.c_int] * 5 + [_P]
@@ -424,6 +426,18 @@ def probe_nvfp4_mma(pair: bool, ctas: int, iters: int, stream=None):
                       _raw_stream(dev, stream)), "nfq_probe_nvfp4_mma")
     M = 256 if pair else 128
     return 2.0 * M * 256 * 256 * iters * ctas
+
+
+def probe_handoff(mode: int, iters: int, stream=None):
+    """Launch the barrier hand-off latency kernel (not part of the path):
+    `iters` round trips; mode 0 within a CTA, 1..3 between the CTAs of a
+    cluster (remote arrival at CTA scope, with cluster-scope release, by
+    st.async).  Returns the number of one-way hand-offs."""
+    import torch
+    dev = torch.cuda.current_device()
+    _check(_on_device(dev, load().nfq_probe_handoff, mode, iters, _raw_stream(dev, stream)),
+           "nfq_probe_handoff")
+    return 2 * iters
 
 
 def probe_tmem_ld(batched: bool, ctas: int, iters: int, stream=None):

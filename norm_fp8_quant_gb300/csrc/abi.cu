@@ -200,6 +200,7 @@ cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
                                           cudaStream_t stream);
 cudaError_t launch_probe_nvfp4_mma(int pair, int ctas, int iters, unsigned *err,
                                    cudaStream_t stream);
+cudaError_t launch_probe_handoff(int mode, int iters, unsigned *err, cudaStream_t stream);
 // The LM head's accumulator hand-off without data (probe.cu).
 cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, int iters,
                                    unsigned *err, cudaStream_t stream);
@@ -706,6 +707,14 @@ int nfq_probe_nvfp4_mma(int pair, int ctas, int iters, void *stream) {
   if (st != NFQ_OK) return st;
   return map_cuda(launch_probe_nvfp4_mma(pair ? 1 : 0, ctas, iters, d->err,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_probe_handoff(int mode, int iters, void *stream) {
+  if (mode < 0 || mode > 3 || iters < 1 || iters > (1 << 20)) return NFQ_ERR_SHAPE;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_probe_handoff(mode, iters, d->err, static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_stage1_reads(const void *const *partials, int k, const void *residual, int T,

@@ -1,7 +1,8 @@
 // Measurement kernels (not on the hot path): the rate at which tcgen05 FP8
 // and block-scaled NVFP4 MMAs run when nothing else competes for the SM (the
 // tensor rooflines that the LM heads' tensor-pipe figures are read against),
-// the rate at
+// the latency of the barrier hand-offs (within a CTA and between the CTAs of
+// a pair), the rate at
 // which TMEM accumulators can be read into registers, the time of the
 // LM head's accumulator hand-off between the MMA thread and the epilogue
 // warps through two (or more) TMEM buffers, with no data to stream;
@@ -606,6 +607,61 @@ __global__ void __launch_bounds__(128, 1) nvfp4_mma_rate_kernel(int iters, unsig
   }
 }
 
+// handoff_kernel<MODE>: the latency of the barrier hand-offs the LM heads'
+// pipelines are built from, as a ping-pong of `iters` round trips between two
+// threads, each waiting (bounded) on its own mbarrier for the other's signal:
+//   0: two warps of one CTA, local arrivals;
+//   1: the two CTAs of a cluster, remote arrivals at CTA scope (the form the
+//      CTA-pair kernels use);
+//   2: the same with release at cluster scope;
+//   3: the same by st.async of one word, counted (complete_tx) on the peer's
+//      barrier.
+template <int MODE>
+__global__ void __launch_bounds__(64, 1) handoff_kernel(int iters, unsigned *err) {
+  constexpr bool kPair = MODE != 0;
+  __shared__ uint64_t bar[2];   // MODE 0: one per thread; pairs: bar[0] in each CTA
+  __shared__ int abort_flag;
+  __shared__ float box;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int warp = (int)(threadIdx.x / 32), lane = (int)(threadIdx.x % 32);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar[0]), 1);
+    mbar_init(smem_u32(&bar[1]), 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();
+  const bool ping = lane == 0 && (kPair ? (rank == 0 && warp == 0) : warp == 0);
+  const bool pong = lane == 0 && (kPair ? (rank == 1 && warp == 0) : warp == 1);
+  if (ping || pong) {
+    // own barrier to wait on, and where the signal goes
+    const uint32_t mine = smem_u32(&bar[kPair ? 0 : (ping ? 0 : 1)]);
+    const uint32_t theirs = smem_u32(&bar[kPair ? 0 : (ping ? 1 : 0)]);
+    const uint32_t peer = rank ^ 1u;
+    for (int i = 0; i < iters; ++i) {
+      const bool first = ping;   // ping signals, then waits; pong waits, then signals
+      for (int step = 0; step < 2; ++step) {
+        if ((step == 0) == first) {
+          if constexpr (MODE == 0) mbar_arrive(theirs);
+          else if constexpr (MODE == 1) mbar_arrive_remote_cta(theirs, peer);
+          else if constexpr (MODE == 2) mbar_arrive_remote(theirs, peer);
+          else st_async_remote_f32(smem_u32(&box), theirs, peer, 1.0f);
+        } else {
+          if constexpr (MODE == 3) mbar_arrive_expect_tx(mine, 4u);
+          if (!mbar_wait(mine, (uint32_t)(i & 1), (volatile int *)&abort_flag, err, kProbeErrBit)) {
+            i = iters;
+            break;
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync_all();   // no CTA leaves while its peer may signal it
+}
+
 // `stages` sets of tiles (1..4): each K block reads fresh operands from shared
 // memory, as the LM head's pipeline does, instead of the same tiles again.
 cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stages,
@@ -636,6 +692,27 @@ cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stage
 cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,
                                  cudaStream_t stream) {
   return launch_probe_fp8_mma_stages(pair, ctas, iters, 1, err, stream);
+}
+
+cudaError_t launch_probe_handoff(int mode, int iters, unsigned *err, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(mode == 0 ? 1u : 2u);
+  cfg.blockDim = dim3(64);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = mode == 0 ? 1 : 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  switch (mode) {
+    case 0: return cudaLaunchKernelEx(&cfg, handoff_kernel<0>, iters, err);
+    case 1: return cudaLaunchKernelEx(&cfg, handoff_kernel<1>, iters, err);
+    case 2: return cudaLaunchKernelEx(&cfg, handoff_kernel<2>, iters, err);
+    case 3: return cudaLaunchKernelEx(&cfg, handoff_kernel<3>, iters, err);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_probe_nvfp4_mma(int pair, int ctas, int iters, unsigned *err,

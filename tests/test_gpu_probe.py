@@ -40,6 +40,15 @@ def test_probe_nvfp4_mma_runs(nfq, pair):
         nfq.probe_nvfp4_mma(pair, 0, 16)
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+def test_probe_handoff_runs(nfq, mode):
+    assert nfq.probe_handoff(mode, 64) == 128
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    with pytest.raises(nfq.NfqError):
+        nfq.probe_handoff(4, 64)
+
+
 def test_probe_mma_with_tmem_readers_runs(nfq):
     flops = nfq.probe_fp8_mma(False, 4, 64, 0)
     torch.cuda.synchronize()
