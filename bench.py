@@ -1049,6 +1049,25 @@ def run_probe_mma(args, local):
                                   2: "none: each group of MMAs waited for before the next"}[mode],
                      "ctas": 2 * ctas if pair else ctas, "launches": n,
                      "ns_per_k_block": round(ms * 1e6 / (n * iters), 1)})
+    shapes = []
+    for m, n in ((128, 256), (128, 128), (128, 64), (128, 16), (64, 256), (64, 64)):
+        # the time of one K = 32 FP8 MMA by shape: why the weight is the N = 256 operand
+        iters = 2048
+        for _ in range(2):
+            nfq.probe_fp8_mma_shape(m, n, sms, iters)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_l = max(5, min(50, args.steps))
+        e0.record()
+        for _ in range(n_l):
+            nfq.probe_fp8_mma_shape(m, n, sms, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        if nfq.device_error() != nfq.NFQ_OK:
+            raise RuntimeError("the MMA shape probe reported an expired wait")
+        shapes.append({"M": m, "N": n, "ctas": sms, "launches": n_l,
+                       "ns_per_mma": round(e0.elapsed_time(e1) * 1e6 / (n_l * iters * 4), 2)})
     latency = []
     for mode, what in ((0, "two warps of one CTA, local arrivals"),
                        (1, "the two CTAs of a cluster, remote arrivals at CTA scope"),
@@ -1072,7 +1091,8 @@ def run_probe_mma(args, local):
         latency.append({"between": what, "launches": n,
                         "ns_one_way": round(e0.elapsed_time(e1) * 1e6 / hops, 1)})
     return {"metric": "FP8 dense tensor rate (tcgen05.mma kind::f8f6f4 from shared memory)",
-            "unit": "TFLOP/s", "rows": rows, "tmem_read": tmem, "handoff_latency": latency,
+            "unit": "TFLOP/s", "rows": rows, "mma_shapes": shapes, "tmem_read": tmem,
+            "handoff_latency": latency,
             "handshake": {"rows": hand,
                           "what": "the LM head's accumulator hand-off without data: per K block "
                                   "(128 deep, 256 weight columns) four MMAs per N-column group, "

@@ -433,6 +433,12 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   of 1.0 in TMEM; 2 * M * 256 * 256 * iters flops per CTA (per pair).
  *   Asynchronous on `stream`; NFQ_ERR_SHAPE for ctas outside 1..4096 or iters
  *   outside 1..2^20.
+ * nfq_probe_fp8_mma_shape: a measurement kernel, not part of the path.  As
+ *   nfq_probe_fp8_mma with one operand set and single CTAs, for MMAs of
+ *   M = m x N = n x K = 32 (m 64 or 128; n in 16..256, a multiple of 8 for
+ *   m = 64 and of 16 for m = 128): 2 * m * n * 128 * iters flops per CTA.
+ *   NFQ_ERR_SHAPE for other shapes, ctas outside 1..4096 or iters outside
+ *   1..2^20.
  * nfq_probe_handoff: a measurement kernel, not part of the path: `iters`
  *   round trips of a barrier hand-off between two threads, each waiting
  *   (bounded) on its own mbarrier for the other's signal.  mode 0: two warps
@@ -516,6 +522,7 @@ void nfq_stage1_split(int max_tokens, int ctas_per_row, int vpt, int tma);
 int nfq_probe_fp8_mma(int pair, int ctas, int iters, int stages, void *stream);
 int nfq_probe_nvfp4_mma(int pair, int ctas, int iters, void *stream);
 int nfq_probe_handoff(int mode, int iters, void *stream);
+int nfq_probe_fp8_mma_shape(int m, int n, int ctas, int iters, void *stream);
 int nfq_probe_tmem_ld(int batched, int ctas, int iters, void *stream);
 int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream);
 int nfq_check_fp8_quotient(unsigned long long *mismatches, unsigned *first_bad, void *stream);

@@ -108,6 +108,9 @@ def load(path: str = LIB_PATH):
     lib.nfq_probe_nvfp4_mma.restype = ctypes.c_int
     lib.nfq_probe_handoff.argtypes = [ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_handoff.restype = ctypes.c_int
+    lib.nfq_probe_fp8_mma_shape.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             _P]
+    lib.nfq_probe_fp8_mma_shape.restype = ctypes.c_int
     lib.nfq_probe_tmem_ld.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]
     lib.nfq_probe_tmem_ld.restype = ctypes.c_int
     lib.nfq_probe_handshake.argtypes = [ctypes.c_int] * 5 + [_P]
@@ -426,6 +429,17 @@ def probe_nvfp4_mma(pair: bool, ctas: int, iters: int, stream=None):
                       _raw_stream(dev, stream)), "nfq_probe_nvfp4_mma")
     M = 256 if pair else 128
     return 2.0 * M * 256 * 256 * iters * ctas
+
+
+def probe_fp8_mma_shape(m: int, n: int, ctas: int, iters: int, stream=None):
+    """Launch the FP8 MMA-rate kernel (not part of the path) with MMAs of
+    M = m x N = n x K = 32 on single CTAs.  Returns the flops the launch
+    performs."""
+    import torch
+    dev = torch.cuda.current_device()
+    _check(_on_device(dev, load().nfq_probe_fp8_mma_shape, m, n, ctas, iters,
+                      _raw_stream(dev, stream)), "nfq_probe_fp8_mma_shape")
+    return 2.0 * m * n * 128 * iters * ctas
 
 
 def probe_handoff(mode: int, iters: int, stream=None):

@@ -201,6 +201,8 @@ cudaError_t launch_probe_mma_with_readers(int ctas, int iters, unsigned *err,
 cudaError_t launch_probe_nvfp4_mma(int pair, int ctas, int iters, unsigned *err,
                                    cudaStream_t stream);
 cudaError_t launch_probe_handoff(int mode, int iters, unsigned *err, cudaStream_t stream);
+cudaError_t launch_probe_fp8_mma_shape(int m, int n, int ctas, int iters, unsigned *err,
+                                       cudaStream_t stream);
 // The LM head's accumulator hand-off without data (probe.cu).
 cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, int iters,
                                    unsigned *err, cudaStream_t stream);
@@ -707,6 +709,17 @@ int nfq_probe_nvfp4_mma(int pair, int ctas, int iters, void *stream) {
   if (st != NFQ_OK) return st;
   return map_cuda(launch_probe_nvfp4_mma(pair ? 1 : 0, ctas, iters, d->err,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+int nfq_probe_fp8_mma_shape(int m, int n, int ctas, int iters, void *stream) {
+  if (!((m == 64 && n % 8 == 0) || (m == 128 && n % 16 == 0)) || n < 16 || n > 256 || ctas < 1 ||
+      ctas > 4096 || iters < 1 || iters > (1 << 20))
+    return NFQ_ERR_SHAPE;
+  DeviceInfo *d = nullptr;
+  const int st = device_info(&d);
+  if (st != NFQ_OK) return st;
+  return map_cuda(launch_probe_fp8_mma_shape(m, n, ctas, iters, d->err,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int nfq_probe_handoff(int mode, int iters, void *stream) {

@@ -33,7 +33,7 @@ constexpr int kProbeErrBit = 4;
 
 template <bool kPair>
 __global__ void __launch_bounds__(128, 1)
-    fp8_mma_rate_kernel(int iters, int stages, unsigned *err) {
+    fp8_mma_rate_kernel(int iters, int stages, int m, int n, unsigned *err) {
   // A: 128 rows x 128 bytes; B: 256 rows (one CTA) or 128 rows (each CTA of a pair)
   constexpr uint32_t kA = 128 * 128, kB = (kPair ? 128 : 256) * 128;
   extern __shared__ uint8_t smem_raw[];
@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(128, 1)
 
   if (warp == 0) {
     if (issuer && lane == 0) {
-      const uint32_t idesc = idesc_e4m3_f32(kPair ? 256 : 128, 256);
+      // m x n per CTA (pairs: 256 x 256); the tiles hold the largest shape
+      const uint32_t idesc = idesc_e4m3_f32(kPair ? 256u : (uint32_t)m, kPair ? 256u : (uint32_t)n);
       int st = 0;
       for (int it = 0; it < iters; ++it) {
         const uint32_t a = smem_u32(smem + (size_t)st * (kA + kB)), b = a + kA;
@@ -686,7 +687,22 @@ cudaError_t launch_probe_fp8_mma_stages(int pair, int ctas, int iters, int stage
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, iters, stages, err);
+  return cudaLaunchKernelEx(&cfg, kern, iters, stages, 128, 256, err);
+}
+
+// One operand set, one CTA per SM, MMAs of M = m x N = n (cta_group::1):
+// m 64 or 128, n a multiple of 8 (m = 64) or 16 (m = 128) in 16..256.
+cudaError_t launch_probe_fp8_mma_shape(int m, int n, int ctas, int iters, unsigned *err,
+                                       cudaStream_t stream) {
+  if (!((m == 64 && n % 8 == 0) || (m == 128 && n % 16 == 0)) || n < 16 || n > 256)
+    return cudaErrorInvalidValue;
+  const size_t smem = 120u * 1024u;
+  auto kern = fp8_mma_rate_kernel<false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)ctas, 128, smem, stream>>>(iters, 1, m, n, err);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_probe_fp8_mma(int pair, int ctas, int iters, unsigned *err,

@@ -262,6 +262,9 @@ def test_probe_argument_validation(lib):
     assert lib.nfq_probe_nvfp4_mma(1, 0, 16, None) == shape
     assert lib.nfq_probe_nvfp4_mma(0, 4, 0, None) == shape
     assert lib.nfq_probe_handoff(4, 16, None) == shape
+    assert lib.nfq_probe_fp8_mma_shape(96, 256, 4, 16, None) == shape
+    assert lib.nfq_probe_fp8_mma_shape(128, 264, 4, 16, None) == shape
+    assert lib.nfq_probe_fp8_mma_shape(64, 12, 4, 16, None) == shape
     assert lib.nfq_probe_handoff(1, 0, None) == shape
     assert lib.nfq_probe_tmem_ld(0, 0, 8, None) == shape
     assert lib.nfq_check_fp8_quotient(None, None, None) == nfq.NFQ_ERR_NULL

@@ -40,6 +40,15 @@ def test_probe_nvfp4_mma_runs(nfq, pair):
         nfq.probe_nvfp4_mma(pair, 0, 16)
 
 
+@pytest.mark.parametrize("m,n", [(128, 256), (128, 16), (64, 256), (64, 8 * 3 + 16)])
+def test_probe_fp8_mma_shape_runs(nfq, m, n):
+    assert nfq.probe_fp8_mma_shape(m, n, 4, 16) == 2.0 * m * n * 128 * 16 * 4
+    torch.cuda.synchronize()
+    assert nfq.device_error() == 0
+    with pytest.raises(nfq.NfqError):
+        nfq.probe_fp8_mma_shape(128, 24, 4, 16)      # N not a multiple of 16 for M = 128
+
+
 @pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_probe_handoff_runs(nfq, mode):
     assert nfq.probe_handoff(mode, 64) == 128
