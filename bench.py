@@ -1025,7 +1025,8 @@ def run_probe_mma(args, local):
                      "TB/s": round(nbytes / (ms * 1e-3) / 1e12, 2)})
     hand = []
     for pair, buffers, mode in ((False, 2, 2), (False, 2, 0), (False, 2, 1), (True, 2, 2),
-                                (True, 2, 0), (True, 2, 1), (False, 4, 1), (False, 8, 1)):
+                                (True, 2, 0), (True, 2, 1), (False, 4, 1), (False, 8, 1),
+                                (False, 4, 3), (True, 4, 1), (True, 4, 3)):
         ctas = sms // 2 if pair else sms
         iters = 2048
         for _ in range(3):
@@ -1046,7 +1047,8 @@ def run_probe_mma(args, local):
                      "buffers": buffers, "N": 512 // buffers,
                      "epilogue": {0: "16 warps release each buffer unread",
                                   1: "16 warps read their columns (16 at a time), then release",
-                                  2: "none: each group of MMAs waited for before the next"}[mode],
+                                  2: "none: each group of MMAs waited for before the next",
+                                  3: "each buffer its own 8 warps, 64 columns each, then release"}[mode],
                      "ctas": 2 * ctas if pair else ctas, "launches": n,
                      "ns_per_k_block": round(ms * 1e6 / (n * iters), 1)})
     shapes = []

@@ -458,14 +458,17 @@ int nfq_unfused_argmax_bf16(const void *logits, int T, int V, int32_t *tokens_ou
  *   (pair != 0: `ctas` CTA pairs, cta_group::2, M = 256) run `iters` K blocks;
  *   one thread issues each K block as buffers / 2 groups of four MMAs of
  *   M = 128 x N = 512 / buffers x K = 32, each group into its own TMEM buffer
- *   (buffers = 2, 4 or 8 fill the 512 columns; pairs: 2), and 16 epilogue
- *   warps per CTA wait for each buffer and release it, after reading their
- *   N / 4 columns 16 at a time (mode 1) or at once (mode 0); mode 2: no
- *   epilogue, the issuing thread waits for each group to complete before the
- *   next.  Asynchronous on `stream`; time it with events: the time per K block
- *   is what one K block of the LM head's K loop costs before any data moves.
- *   NFQ_ERR_SHAPE for ctas outside 1..4096, iters outside 1..2^20, mode
- *   outside 0..2, buffers other than 2, 4, 8, or pairs with buffers != 2.
+ *   (buffers = 2, 4 or 8 fill the 512 columns; pairs: 2 or 4), and 16
+ *   epilogue warps per CTA wait for each buffer and release it, after
+ *   reading their N / 4 columns 16 at a time (mode 1) or without reading
+ *   (mode 0); mode 2: no epilogue, the issuing thread waits for each group to
+ *   complete before the next; mode 3 (buffers = 4): each 128-column buffer
+ *   has its own half of the epilogue warps, which read 64 columns each, so
+ *   the two halves of a K block are handed off independently.  Asynchronous
+ *   on `stream`; time it with events: the time per K block is what one K
+ *   block of the LM head's K loop costs before any data moves.  NFQ_ERR_SHAPE
+ *   for ctas outside 1..4096, iters outside 1..2^20, mode outside 0..3,
+ *   buffers other than 2, 4, 8, pairs with 8 buffers, or mode 3 without 4.
  * nfq_check_fp8_quotient: a verification kernel, not part of the path.  Stage
  *   1 forms each group's FP8 scale RN(amax / 448) and codes e4m3(RN(hidden /
  *   scale)) without IEEE divisions: the scale from the constant RN(1 / 448)

@@ -756,9 +756,10 @@ int nfq_probe_stage1_reads(const void *const *partials, int k, const void *resid
 }
 
 int nfq_probe_handshake(int pair, int buffers, int mode, int ctas, int iters, void *stream) {
-  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || mode < 0 || mode > 2)
+  if (ctas < 1 || ctas > 4096 || iters < 1 || iters > (1 << 20) || mode < 0 || mode > 3)
     return NFQ_ERR_SHAPE;
-  if (!(buffers == 2 || (!pair && (buffers == 4 || buffers == 8)))) return NFQ_ERR_SHAPE;
+  if (!(buffers == 2 || buffers == 4 || (!pair && buffers == 8))) return NFQ_ERR_SHAPE;
+  if (mode == 3 && buffers != 4) return NFQ_ERR_SHAPE;
   DeviceInfo *d = nullptr;
   const int st = device_info(&d);
   if (st != NFQ_OK) return st;

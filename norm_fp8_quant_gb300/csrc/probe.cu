@@ -247,12 +247,17 @@ __global__ void __launch_bounds__(17 * 32, 1) mma_with_readers_kernel(int iters,
 // remote arrivals on the even CTA's barrier), which the issuing thread waits
 // for before it reuses the buffer.  mode 2: no epilogue; the issuing thread
 // waits for each group to complete before it issues the next (the MMAs'
-// issue-to-completion latency).
+// issue-to-completion latency).  mode 3 (NB = 4): each 128-column buffer has
+// its own half of the epilogue: warps 4h + 2j + q' with column group
+// g = warp / 4, half h = g / 2, read 64 columns of the buffers of group h only
+// (8 warps per buffer, 16 on CTA pairs), so the two halves of a K block are
+// handed off independently.
 template <bool kPair, int NB>
 __global__ void __launch_bounds__(17 * 32, 1) handshake_kernel(int iters, int mode, unsigned *err) {
   constexpr int N = 512 / NB, GROUPS = NB / 2, C = N / 4;
-  static_assert(!kPair || NB == 2, "CTA pairs: two 256-column buffers only");
+  static_assert(!kPair || NB == 2 || NB == 4, "CTA pairs: two or four buffers");
   constexpr uint32_t kA = 128 * 128, kB = (kPair ? 128 : 256) * 128;
+  constexpr int kRowsPerGroup = kPair ? N / 2 : N;   // B rows per CTA per group
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -267,9 +272,10 @@ __global__ void __launch_bounds__(17 * 32, 1) handshake_kernel(int iters, int mo
   for (uint32_t i = threadIdx.x; i < (kA + kB) / 16; i += blockDim.x)
     z[i] = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
+    const uint32_t readers = mode == 3 ? 8u : 16u;
     for (int b = 0; b < NB; ++b) {
       mbar_init(smem_u32(&full[b]), 1);
-      mbar_init(smem_u32(&empty[b]), kPair ? 32 : 16);
+      mbar_init(smem_u32(&empty[b]), kPair ? 2u * readers : readers);
     }
     mbar_init(smem_u32(&fin), 1);
     abort_flag = 0;
@@ -304,8 +310,8 @@ __global__ void __launch_bounds__(17 * 32, 1) handshake_kernel(int iters, int mo
             break;
           tc_fence_after();
         }
-        // group grp multiplies B rows grp * N .. + N - 1 (128 bytes each)
-        const uint64_t bd = b_desc + (uint64_t)((grp * N * 128) >> 4);
+        // group grp multiplies this CTA's B rows grp * kRowsPerGroup .. (128 bytes each)
+        const uint64_t bd = b_desc + (uint64_t)((grp * kRowsPerGroup * 128) >> 4);
         const uint32_t d = tmem_base + (uint32_t)(buf * N);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -336,17 +342,20 @@ __global__ void __launch_bounds__(17 * 32, 1) handshake_kernel(int iters, int mo
     }
     __syncwarp();
   } else if (mode != 2) {
-    const uint32_t t0 =
-        tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(C * (warp >> 2));
+    // mode 3: this warp's half (group) and its 64 columns of that half's buffers
+    const int g = warp >> 2;
+    const int cols = mode == 3 ? 64 : C;
+    const uint32_t t0 = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) +
+                        (uint32_t)(mode == 3 ? 64 * (g & 1) : C * g);
     uint32_t x = 0;
     for (int i = 0; i < total; ++i) {
       const int buf = i % NB, use = i / NB;
+      if (mode == 3 && (i % GROUPS) != (g >> 1)) continue;
       const bool got = mbar_wait(smem_u32(&full[buf]), (uint32_t)(use & 1), ab, err, kProbeErrBit);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      if (mode == 1) {
-#pragma unroll
-        for (int c = 0; c < C; c += 16) {
+      if (mode == 1 || mode == 3) {
+        for (int c = 0; c < cols; c += 16) {
           uint32_t r[16];
           tmem_ld16(t0 + (uint32_t)(buf * N + c), r);
           tmem_wait_ld();
@@ -759,10 +768,11 @@ cudaError_t launch_probe_handshake(int pair, int buffers, int mode, int ctas, in
                                    unsigned *err, cudaStream_t stream) {
   void (*kern)(int, int, unsigned *) = nullptr;
   if (pair && buffers == 2) kern = handshake_kernel<true, 2>;
+  else if (pair && buffers == 4) kern = handshake_kernel<true, 4>;
   else if (!pair && buffers == 2) kern = handshake_kernel<false, 2>;
   else if (!pair && buffers == 4) kern = handshake_kernel<false, 4>;
   else if (!pair && buffers == 8) kern = handshake_kernel<false, 8>;
-  if (!kern || mode < 0 || mode > 2) return cudaErrorInvalidValue;
+  if (!kern || mode < 0 || mode > 3 || (mode == 3 && buffers != 4)) return cudaErrorInvalidValue;
   // 48 KB of tiles; 120 KB keeps one CTA per SM
   const size_t smem = 120u * 1024u;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

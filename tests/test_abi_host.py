@@ -253,8 +253,9 @@ def test_probe_argument_validation(lib):
     device call (so these run without a GPU)."""
     shape = nfq.NFQ_ERR_SHAPE
     assert lib.nfq_probe_handshake(0, 3, 1, 4, 16, None) == shape     # 3 buffers
-    assert lib.nfq_probe_handshake(1, 4, 1, 4, 16, None) == shape     # pairs: 2 buffers only
-    assert lib.nfq_probe_handshake(0, 2, 3, 4, 16, None) == shape     # mode 3
+    assert lib.nfq_probe_handshake(1, 8, 1, 4, 16, None) == shape     # pairs: 2 or 4 buffers
+    assert lib.nfq_probe_handshake(0, 2, 4, 4, 16, None) == shape     # mode 4
+    assert lib.nfq_probe_handshake(0, 2, 3, 4, 16, None) == shape     # mode 3: 4 buffers only
     assert lib.nfq_probe_handshake(0, 2, 1, 0, 16, None) == shape     # no CTAs
     assert lib.nfq_probe_handshake(0, 2, 1, 4, 0, None) == shape      # no K blocks
     assert lib.nfq_probe_fp8_mma(1, 4, 16, 0, None) == shape          # readers: one CTA only

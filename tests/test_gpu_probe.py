@@ -84,8 +84,10 @@ def test_probe_stage1_reads_runs(nfq, T, H, k):
     assert nfq.device_error() == 0
 
 
-@pytest.mark.parametrize("pair,buffers", [(False, 2), (False, 4), (False, 8), (True, 2)])
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("pair,buffers,mode",
+                         [(p, b, m) for p, b in ((False, 2), (False, 4), (False, 8), (True, 2),
+                                                 (True, 4)) for m in (0, 1, 2)]
+                         + [(False, 4, 3), (True, 4, 3)])
 def test_probe_handshake_runs(nfq, pair, buffers, mode):
     """The accumulator hand-off probe runs every K block through its buffers and
     leaves no expired wait, with and without an epilogue."""
